@@ -1,0 +1,221 @@
+/*
+ * mxmoe.h -- C ABI of the MXFP8 (OCP MX, W8A8) block-scaled fused-MoE
+ * expert forward for NVIDIA GB300 (sm_103a).
+ *
+ * The forward, as "Quantization on Ascend" (sglang docs, section "MXFP8 for
+ * LLM MoE models", implementation notes "Forward", "Online path", "Offline
+ * path") and sglang PR #32266 (commit note adding the fused experts kernel:
+ * routing -> act quant -> swiglu_quant -> grouped_matmul -> finalize_routing)
+ * describe it:
+ *
+ *   moe_route_quant_mxfp8           top-k routing + expert permutation with the
+ *                                   per-token MX activation quant fused in
+ *                                   (init_routing quant_mode=3)
+ *   grouped_gemm_swiglu_quant_mxfp8 grouped GEMM over w13 (gate+up) + SwiGLU +
+ *                                   MXFP8 requant (payload + block scale)
+ *   grouped_gemm_mxfp8              grouped GEMM over w2, bf16 output
+ *   moe_finalize_routing            weighted top-k combine back to token order
+ *   moe_forward_mxfp8               the four above on one stream
+ *   mx_quantize_3d                  load-time MX quant of [E, N, K] weights
+ *
+ * Formats.  An MX block is 32 consecutive elements along the contraction
+ * axis K.  Payload: one float8_e4m3fn byte per element.  Scale: one UE8M0
+ * (e8m0) byte per block, value 2^(byte - 127), chosen as
+ * floor(log2(block amax)) - 8 clamped to [-127, 127] (all-zero block -> 0);
+ * elements round to nearest-even and saturate at +-448 (OCP MX v1.0).
+ * Scales are stored [rows, K/32] row-major; for K % 64 == 0 these are the
+ * same bytes as the pair-split [rows, K/64, 2] view the pages use.
+ *
+ * Conventions (all entry points):
+ *   - Every data pointer is a DEVICE pointer owned by the caller; the
+ *     library never allocates, frees or keeps device memory it was given.
+ *   - bf16 tensors are passed as uint16_t bit patterns.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  All work
+ *     is enqueued asynchronously on it; no call synchronizes the host.
+ *   - Arguments are validated before anything is launched; on a non-OK
+ *     status nothing was enqueued.  Pointers must be 16-byte aligned.
+ *   - Kernels that wait on on-chip barriers give every wait a time limit;
+ *     when one runs out the kernel records MXMOE_ERR_DEVICE_TIMEOUT in a
+ *     device status word and returns.  mxmoe_get_device_status() reads it.
+ *   - Not thread-safe across concurrent calls that share output buffers.
+ */
+#ifndef MXMOE_H_
+#define MXMOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MXMOE_OK = 0,
+  MXMOE_ERR_NULL = 1,            /* a required pointer is NULL              */
+  MXMOE_ERR_ALIGN = 2,           /* a pointer is not 16-byte aligned        */
+  MXMOE_ERR_SHAPE = 3,           /* a size is out of range or inconsistent  */
+  MXMOE_ERR_UNSUPPORTED = 4,     /* valid but not supported by this build   */
+  MXMOE_ERR_WORKSPACE = 5,       /* workspace missing or too small          */
+  MXMOE_ERR_CUDA = 6,            /* a CUDA runtime call or launch failed    */
+  MXMOE_ERR_DEVICE_TIMEOUT = 7,  /* a device-side wait ran out of time      */
+  MXMOE_ERR_DEVICE_CHECK = 8     /* a device-side consistency check failed  */
+} mxmoe_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* mxmoe_status_string(mxmoe_status status);
+
+/*
+ * Load-time MX quantization of a 3D weight tensor (also any 2D tensor with
+ * E = 1).  "Quantization on Ascend", MoE MXFP8 online path: bf16 expert
+ * weights are quantized once at load, a 3D [E, N, K] input accepted directly.
+ *
+ *   w      bf16 [E, N, K] row-major (K contiguous)
+ *   q      e4m3 [E, N, K]            (output)
+ *   scale  e8m0 [E, N, K/32]         (output)
+ * Requires K % 32 == 0, E, N >= 1.  Empty (E*N == 0) is a no-op.
+ */
+mxmoe_status mx_quantize_3d(const uint16_t* w, int64_t E, int64_t N, int64_t K,
+                            uint8_t* q, uint8_t* scale, void* stream);
+
+/*
+ * Workspace bytes moe_route_quant_mxfp8 / moe_route_permute_bf16 need for
+ * T tokens and E experts (per-block expert histograms).
+ */
+size_t moe_route_quant_mxfp8_workspace_size(int T, int E);
+
+/*
+ * Top-k routing with the per-token MX activation quant fused into the expert
+ * permutation: init_routing with quant_mode=3 ("Quantization on Ascend",
+ * MoE MXFP8 "Forward" note; PR #32266 commit note on quant_mode=3, whose
+ * output is byte-identical to routing followed by a separate quant pass).
+ *
+ *   x              bf16 [T, H] hidden states
+ *   logits         fp32 [T, E] router logits
+ *   renormalize    nonzero: the k softmax weights are divided by their sum
+ *   xq             e4m3 [M, H], M = T*k   expanded rows, grouped by expert
+ *   xs             e8m0 [M, H/32]
+ *   topk_ids       int32 [T, k]   experts of each token, descending logit,
+ *                                 ties to the lower expert id
+ *   topk_w         fp32 [T, k]    routing weights (softmax, optionally renormed)
+ *   sorted_to_src  int32 [M]      expanded row p holds flat assignment
+ *                                 sorted_to_src[p] = t*k + j (token t = /k)
+ *   src_to_sorted  int32 [M]      inverse permutation
+ *   expert_counts  int64 [E]      rows per expert (the COUNT group list)
+ *   expert_offsets int64 [E+1]    exclusive prefix of counts, offsets[E] = M
+ *                                 (the CUMULATIVE group list, leading 0)
+ * Rows of one expert are in flat-index order (deterministic).
+ * Requires 1 <= k <= min(E, 32), E <= 1024, H % 32 == 0, T >= 0.
+ * T == 0 writes only counts/offsets (all zero).
+ */
+mxmoe_status moe_route_quant_mxfp8(const uint16_t* x, const float* logits, int T, int H,
+                                   int E, int k, int renormalize, uint8_t* xq, uint8_t* xs,
+                                   int32_t* topk_ids, float* topk_w, int32_t* sorted_to_src,
+                                   int32_t* src_to_sorted, int64_t* expert_counts,
+                                   int64_t* expert_offsets, void* ws, size_t ws_bytes,
+                                   void* stream);
+
+/*
+ * The two-step comparator of moe_route_quant_mxfp8: the same routing and
+ * permutation, but the expanded rows are written as bf16 (init_routing
+ * without quant); a separate mx_quantize_3d(xp, 1, M, H) pass then gives the
+ * same bytes as the fused call.  Arguments as above, xp bf16 [M, H].
+ */
+mxmoe_status moe_route_permute_bf16(const uint16_t* x, const float* logits, int T, int H,
+                                    int E, int k, int renormalize, uint16_t* xp,
+                                    int32_t* topk_ids, float* topk_w, int32_t* sorted_to_src,
+                                    int32_t* src_to_sorted, int64_t* expert_counts,
+                                    int64_t* expert_offsets, void* ws, size_t ws_bytes,
+                                    void* stream);
+
+/*
+ * gmm1: grouped GEMM over w13 fused with SwiGLU and the MXFP8 requant
+ * (PR #30768 report, GroupedMatmulSwigluQuant: returns quantized activations
+ * and their block scale; "Quantization on Ascend": gmm1 fuses gate/up +
+ * swiglu + requant and takes the cumulative group list).
+ *
+ * For expert e and rows r in [offsets[e], offsets[e+1]):
+ *   h   = deq(xq[r]) . deq(w13[e])^T          fp32 accumulate, [2I]
+ *   a   = silu(h[0:I]) * h[I:2I]              gate rows first, then up
+ *   aq[r], as[r] = MX-quant(a) along I
+ *
+ *   xq, xs          e4m3 [M, H], e8m0 [M, H/32]
+ *   w13q, w13s      e4m3 [E, 2I, H], e8m0 [E, 2I, H/32]
+ *   expert_offsets  int64 [E+1] on the device, offsets[E] == M
+ *   aq, as          e4m3 [M, I], e8m0 [M, I/32]   (outputs)
+ * Requires H % 128 == 0, I % 128 == 0, 1 <= E <= 256, M >= 0.
+ */
+mxmoe_status grouped_gemm_swiglu_quant_mxfp8(const uint8_t* xq, const uint8_t* xs,
+                                             const uint8_t* w13q, const uint8_t* w13s,
+                                             const int64_t* expert_offsets, int64_t M, int E,
+                                             int H, int I, uint8_t* aq, uint8_t* as,
+                                             void* stream);
+
+/*
+ * gmm2: grouped GEMM over w2 ("Quantization on Ascend", MoE MXFP8 "Forward":
+ * npu_grouped_matmul with the count group list; the offsets here carry the
+ * same information in cumulative form).
+ *
+ *   y[r] = deq(aq[r]) . deq(w2[e])^T, fp32 accumulate, rounded to bf16
+ *
+ *   aq, as      e4m3 [M, I], e8m0 [M, I/32]
+ *   w2q, w2s    e4m3 [E, H, I], e8m0 [E, H, I/32]
+ *   y           bf16 [M, H]   (output)
+ * Requires I % 128 == 0, H % 128 == 0, 1 <= E <= 256, M >= 0.
+ */
+mxmoe_status grouped_gemm_mxfp8(const uint8_t* aq, const uint8_t* as, const uint8_t* w2q,
+                                const uint8_t* w2s, const int64_t* expert_offsets, int64_t M,
+                                int E, int I, int H, uint16_t* y, void* stream);
+
+/*
+ * Finalize routing: weighted top-k combine back to token order
+ * ("Quantization on Ascend", MoE layers use init_routing / finalize_routing;
+ * PR #32266 fused experts note).
+ *
+ *   out[t] = sum_{j<k} topk_w[t, j] * y[src_to_sorted[t*k + j]]
+ *
+ * fp32 accumulation in slot order j = 0..k-1, rounded once to bf16.
+ *   y bf16 [M, H], topk_w fp32 [T, k], src_to_sorted int32 [T*k],
+ *   out bf16 [T, H].  Requires H % 8 == 0, 1 <= k <= 32.
+ */
+mxmoe_status moe_finalize_routing(const uint16_t* y, const float* topk_w,
+                                  const int32_t* src_to_sorted, int T, int k, int H,
+                                  uint16_t* out, void* stream);
+
+/* Workspace bytes moe_forward_mxfp8 needs (all intermediates of the layer). */
+size_t moe_forward_mxfp8_workspace_size(int T, int H, int E, int k, int I);
+
+/*
+ * The whole MXFP8 expert forward on one stream: route+quant, gmm1 (+SwiGLU
+ * +requant), gmm2, finalize.  Weights are the MX-quantized w13 [E, 2I, H]
+ * and w2 [E, H, I] with their [.., K/32] scales (from mx_quantize_3d, or an
+ * offline checkpoint's float8_e4m3fn payload + uint8 e8m0 scales).
+ *   out bf16 [T, H].  ws: moe_forward_mxfp8_workspace_size() bytes, 256-byte
+ *   aligned; it holds every intermediate and may be reused between calls.
+ */
+mxmoe_status moe_forward_mxfp8(const uint16_t* x, const float* logits, const uint8_t* w13q,
+                               const uint8_t* w13s, const uint8_t* w2q, const uint8_t* w2s,
+                               int T, int H, int E, int k, int I, int renormalize,
+                               uint16_t* out, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Device status word of the current device: 0 or the first error a kernel
+ * recorded (MXMOE_ERR_DEVICE_TIMEOUT / MXMOE_ERR_DEVICE_CHECK).  Synchronizes
+ * the device.  clear != 0 resets the word to 0 afterwards.
+ */
+mxmoe_status mxmoe_get_device_status(int32_t* status_out, int clear);
+
+/*
+ * Time limit, in SM clock cycles, of every bounded device-side wait that a
+ * kernel launched afterwards uses (default about 2^32 cycles, ~2 s).
+ * Values < 1 restore the default.  Meant for tests of the timeout path.
+ */
+void mxmoe_set_wait_limit_cycles(long long cycles);
+
+/* Library version string. */
+const char* mxmoe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXMOE_H_ */

@@ -1,0 +1,13 @@
+"""MXFP8 (OCP MX, W8A8) block-scaled fused-MoE expert forward for GB300 (sm_103a).
+
+The compute path is the C-ABI library ``libmxmoe.so`` (hand-written CUDA,
+tcgen05 tensor cores); ``api`` is its thin Python binding and ``workloads``
+the seeded synthetic inputs.  Importing ``api`` functions loads the library
+lazily and raises if it has not been built.
+"""
+
+from .api import (  # noqa: F401
+    MXFP8MoELayer, device_status, grouped_gemm_mxfp8, grouped_gemm_swiglu_quant_mxfp8,
+    moe_finalize_routing, moe_forward_mxfp8, moe_forward_mxfp8_workspace_size,
+    moe_route_permute_bf16, moe_route_quant_mxfp8, mx_quantize_3d, set_wait_limit_cycles,
+)

@@ -1,0 +1,230 @@
+"""Thin Python binding of libmxmoe.so: argument marshalling only.
+
+Each function has the name of the C entry point it calls, takes CUDA torch
+tensors, allocates its outputs with torch (device memory is PyTorch's job),
+checks dtypes/shapes/contiguity, and passes raw pointers plus the current
+CUDA stream.  Every step of the computation runs in the library's kernels.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+
+import torch
+
+from . import _lib
+
+
+def _ptr(t):
+    return C.c_void_p(t.data_ptr()) if t is not None else C.c_void_p(0)
+
+
+def _stream():
+    return C.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _need(t, name, dtype, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name}: expected {ndim} dims, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _u8(t):
+    return t.view(torch.uint8) if t.dtype in (torch.float8_e4m3fn, torch.int8) else t
+
+
+def mx_quantize_3d(w: torch.Tensor):
+    """bf16 [E, N, K] (or [N, K]) -> (e4m3 payload uint8 same shape, e8m0 scales uint8 [.., K/32])."""
+    _need(w, "w", torch.bfloat16)
+    shape = tuple(w.shape)
+    if w.dim() == 2:
+        E, (N, K) = 1, shape
+    elif w.dim() == 3:
+        E, N, K = shape
+    else:
+        raise ValueError("w must be 2D or 3D")
+    q = torch.empty(shape, dtype=torch.uint8, device=w.device)
+    s = torch.empty(shape[:-1] + (K // 32 if K % 32 == 0 else 0,), dtype=torch.uint8,
+                    device=w.device)
+    _lib.check("mx_quantize_3d", _lib.load().mx_quantize_3d(
+        _ptr(w), E, N, K, _ptr(q), _ptr(s), _stream()))
+    return q, s
+
+
+def _route(x, logits, k, renormalize, quant):
+    _need(x, "x", torch.bfloat16, 2)
+    _need(logits, "logits", torch.float32, 2)
+    T, H = x.shape
+    E = logits.shape[1]
+    if logits.shape[0] != T:
+        raise ValueError("x and logits disagree on T")
+    dev = x.device
+    M = T * k
+    L = _lib.load()
+    ws_bytes = L.moe_route_quant_mxfp8_workspace_size(T, E)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    out = dict(
+        topk_ids=torch.empty(T, k, dtype=torch.int32, device=dev),
+        topk_w=torch.empty(T, k, dtype=torch.float32, device=dev),
+        sorted_to_src=torch.empty(M, dtype=torch.int32, device=dev),
+        src_to_sorted=torch.empty(M, dtype=torch.int32, device=dev),
+        expert_counts=torch.empty(E, dtype=torch.int64, device=dev),
+        expert_offsets=torch.empty(E + 1, dtype=torch.int64, device=dev),
+    )
+    common = (_ptr(out["topk_ids"]), _ptr(out["topk_w"]), _ptr(out["sorted_to_src"]),
+              _ptr(out["src_to_sorted"]), _ptr(out["expert_counts"]),
+              _ptr(out["expert_offsets"]), _ptr(ws), ws.numel(), _stream())
+    if quant:
+        out["xq"] = torch.empty(M, H, dtype=torch.uint8, device=dev)
+        out["xs"] = torch.empty(M, H // 32, dtype=torch.uint8, device=dev)
+        _lib.check("moe_route_quant_mxfp8", L.moe_route_quant_mxfp8(
+            _ptr(x), _ptr(logits), T, H, E, k, int(bool(renormalize)), _ptr(out["xq"]),
+            _ptr(out["xs"]), *common))
+    else:
+        out["xp"] = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+        _lib.check("moe_route_permute_bf16", L.moe_route_permute_bf16(
+            _ptr(x), _ptr(logits), T, H, E, k, int(bool(renormalize)), _ptr(out["xp"]), *common))
+    return out
+
+
+def moe_route_quant_mxfp8(x, logits, k: int, renormalize: bool = True) -> dict:
+    """Routing + permutation with the MX activation quant fused (quant_mode=3)."""
+    return _route(x, logits, k, renormalize, True)
+
+
+def moe_route_permute_bf16(x, logits, k: int, renormalize: bool = True) -> dict:
+    """Routing + permutation writing bf16 expanded rows (two-step comparator)."""
+    return _route(x, logits, k, renormalize, False)
+
+
+def grouped_gemm_swiglu_quant_mxfp8(xq, xs, w13q, w13s, expert_offsets):
+    """gmm1 + SwiGLU + requant -> (aq uint8 [M, I], as uint8 [M, I/32])."""
+    xq, w13q = _u8(xq), _u8(w13q)
+    _need(xq, "xq", torch.uint8, 2)
+    _need(xs, "xs", torch.uint8, 2)
+    _need(w13q, "w13q", torch.uint8, 3)
+    _need(w13s, "w13s", torch.uint8, 3)
+    _need(expert_offsets, "expert_offsets", torch.int64, 1)
+    M, H = xq.shape
+    E, N2, _ = w13q.shape
+    I = N2 // 2
+    if expert_offsets.numel() != E + 1:
+        raise ValueError("expert_offsets must have E+1 entries")
+    aq = torch.empty(M, I, dtype=torch.uint8, device=xq.device)
+    as_ = torch.empty(M, I // 32, dtype=torch.uint8, device=xq.device)
+    _lib.check("grouped_gemm_swiglu_quant_mxfp8", _lib.load().grouped_gemm_swiglu_quant_mxfp8(
+        _ptr(xq), _ptr(xs), _ptr(w13q), _ptr(w13s), _ptr(expert_offsets), M, E, H, I,
+        _ptr(aq), _ptr(as_), _stream()))
+    return aq, as_
+
+
+def grouped_gemm_mxfp8(aq, as_, w2q, w2s, expert_offsets):
+    """gmm2 -> y bf16 [M, H]."""
+    aq, w2q = _u8(aq), _u8(w2q)
+    _need(aq, "aq", torch.uint8, 2)
+    _need(as_, "as", torch.uint8, 2)
+    _need(w2q, "w2q", torch.uint8, 3)
+    _need(w2s, "w2s", torch.uint8, 3)
+    _need(expert_offsets, "expert_offsets", torch.int64, 1)
+    M, I = aq.shape
+    E, H, _ = w2q.shape
+    y = torch.empty(M, H, dtype=torch.bfloat16, device=aq.device)
+    _lib.check("grouped_gemm_mxfp8", _lib.load().grouped_gemm_mxfp8(
+        _ptr(aq), _ptr(as_), _ptr(w2q), _ptr(w2s), _ptr(expert_offsets), M, E, I, H, _ptr(y),
+        _stream()))
+    return y
+
+
+def moe_finalize_routing(y, topk_w, src_to_sorted, k: int):
+    """Weighted top-k combine -> out bf16 [T, H]."""
+    _need(y, "y", torch.bfloat16, 2)
+    _need(topk_w, "topk_w", torch.float32, 2)
+    _need(src_to_sorted, "src_to_sorted", torch.int32, 1)
+    T = topk_w.shape[0]
+    H = y.shape[1]
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=y.device)
+    _lib.check("moe_finalize_routing", _lib.load().moe_finalize_routing(
+        _ptr(y), _ptr(topk_w), _ptr(src_to_sorted), T, k, H, _ptr(out), _stream()))
+    return out
+
+
+def moe_forward_mxfp8_workspace_size(T: int, H: int, E: int, k: int, I: int) -> int:
+    return int(_lib.load().moe_forward_mxfp8_workspace_size(T, H, E, k, I))
+
+
+def moe_forward_mxfp8(x, logits, w13q, w13s, w2q, w2s, k: int, renormalize: bool = True,
+                      out=None, workspace=None):
+    """The whole expert forward on the current stream -> out bf16 [T, H]."""
+    w13q, w2q = _u8(w13q), _u8(w2q)
+    _need(x, "x", torch.bfloat16, 2)
+    _need(logits, "logits", torch.float32, 2)
+    for t, n in ((w13q, "w13q"), (w13s, "w13s"), (w2q, "w2q"), (w2s, "w2s")):
+        _need(t, n, torch.uint8, 3)
+    T, H = x.shape
+    E, N2, _ = w13q.shape
+    I = N2 // 2
+    ws_bytes = moe_forward_mxfp8_workspace_size(T, H, E, k, I)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=x.device)
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=x.device)
+    _lib.check("moe_forward_mxfp8", _lib.load().moe_forward_mxfp8(
+        _ptr(x), _ptr(logits), _ptr(w13q), _ptr(w13s), _ptr(w2q), _ptr(w2s), T, H, E, k, I,
+        int(bool(renormalize)), _ptr(out), _ptr(workspace), workspace.numel(), _stream()))
+    return out
+
+
+def device_status(clear: bool = True) -> int:
+    """The library's device status word (synchronizes the device)."""
+    v = C.c_int32(0)
+    _lib.check("mxmoe_get_device_status", _lib.load().mxmoe_get_device_status(C.byref(v), int(clear)))
+    return int(v.value)
+
+
+def set_wait_limit_cycles(cycles: int) -> None:
+    _lib.load().mxmoe_set_wait_limit_cycles(int(cycles))
+
+
+class MXFP8MoELayer:
+    """MX-quantized expert weights plus a reusable workspace for one layer shape.
+
+    ``from_bf16`` quantizes bf16 w13 [E, 2I, H] / w2 [E, H, I] on the device
+    (the online, load-time path); ``from_quantized`` takes an offline
+    checkpoint's e4m3 payload and e8m0 scales as they are.
+    """
+
+    def __init__(self, w13q, w13s, w2q, w2s, k: int, renormalize: bool = True):
+        self.w13q, self.w13s, self.w2q, self.w2s = _u8(w13q), w13s, _u8(w2q), w2s
+        self.k = k
+        self.renormalize = renormalize
+        self.E, n2, self.H = self.w13q.shape
+        self.I = n2 // 2
+        self._ws = None
+
+    @classmethod
+    def from_bf16(cls, w13, w2, k: int, renormalize: bool = True):
+        w13q, w13s = mx_quantize_3d(w13)
+        w2q, w2s = mx_quantize_3d(w2)
+        return cls(w13q, w13s, w2q, w2s, k, renormalize)
+
+    @classmethod
+    def from_quantized(cls, w13q, w13s, w2q, w2s, k: int, renormalize: bool = True):
+        return cls(w13q, w13s, w2q, w2s, k, renormalize)
+
+    def workspace(self, T: int, device):
+        need = moe_forward_mxfp8_workspace_size(T, self.H, self.E, self.k, self.I)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+        return self._ws
+
+    def __call__(self, x, logits, out=None):
+        return moe_forward_mxfp8(x, logits, self.w13q, self.w13s, self.w2q, self.w2s, self.k,
+                                 self.renormalize, out=out,
+                                 workspace=self.workspace(x.shape[0], x.device))

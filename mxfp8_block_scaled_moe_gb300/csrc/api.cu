@@ -1,0 +1,303 @@
+// C ABI of the MXFP8 MoE library: argument validation, the device status
+// word, workspace carving and the layer orchestration (moe_forward_mxfp8).
+// The declarations and their contracts are in include/mxmoe.h.
+#include <atomic>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "mxmoe.h"
+
+namespace mxmoe {
+
+// Library status word (one per device the library is loaded on).  Kernels get
+// its device address as a parameter; they only ever write a non-zero error.
+__device__ int g_device_status = 0;
+
+static std::atomic<long long> g_wait_limit{0};
+constexpr long long kDefaultWaitLimit = 1ll << 32;  // ~2 s at 2 GHz
+
+long long wait_limit_cycles() {
+  const long long v = g_wait_limit.load();
+  return v > 0 ? v : kDefaultWaitLimit;
+}
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int g_sms[kMaxDevices] = {0};
+int* g_status_ptr[kMaxDevices] = {nullptr};
+}  // namespace
+
+int num_sms() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= kMaxDevices) return 1;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_sms[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    g_sms[dev] = n > 0 ? n : 1;
+  }
+  return g_sms[dev];
+}
+
+int* device_status_ptr() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) == cudaSuccess) g_status_ptr[dev] = (int*)p;
+  }
+  return g_status_ptr[dev];
+}
+
+static inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+static inline size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+}  // namespace mxmoe
+
+using namespace mxmoe;
+
+#define MXMOE_CHECK_PTR(p)                 \
+  do {                                     \
+    if ((p) == nullptr) return MXMOE_ERR_NULL; \
+    if (!aligned16(p)) return MXMOE_ERR_ALIGN; \
+  } while (0)
+
+static mxmoe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MXMOE_OK : MXMOE_ERR_CUDA; }
+
+extern "C" {
+
+const char* mxmoe_status_string(mxmoe_status s) {
+  switch (s) {
+    case MXMOE_OK: return "MXMOE_OK";
+    case MXMOE_ERR_NULL: return "MXMOE_ERR_NULL: a required pointer is NULL";
+    case MXMOE_ERR_ALIGN: return "MXMOE_ERR_ALIGN: a pointer is not 16-byte aligned";
+    case MXMOE_ERR_SHAPE: return "MXMOE_ERR_SHAPE: a size is out of range or inconsistent";
+    case MXMOE_ERR_UNSUPPORTED: return "MXMOE_ERR_UNSUPPORTED: not supported by this build";
+    case MXMOE_ERR_WORKSPACE: return "MXMOE_ERR_WORKSPACE: workspace missing or too small";
+    case MXMOE_ERR_CUDA: return "MXMOE_ERR_CUDA: a CUDA call or kernel launch failed";
+    case MXMOE_ERR_DEVICE_TIMEOUT: return "MXMOE_ERR_DEVICE_TIMEOUT: a device-side wait timed out";
+    case MXMOE_ERR_DEVICE_CHECK: return "MXMOE_ERR_DEVICE_CHECK: a device-side check failed";
+  }
+  return "MXMOE_ERR_UNKNOWN";
+}
+
+const char* mxmoe_version(void) { return "mxmoe 0.1.0 (sm_103a)"; }
+
+void mxmoe_set_wait_limit_cycles(long long cycles) { g_wait_limit.store(cycles > 0 ? cycles : 0); }
+
+mxmoe_status mxmoe_get_device_status(int32_t* status_out, int clear) {
+  if (!status_out) return MXMOE_ERR_NULL;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MXMOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return MXMOE_ERR_CUDA;
+  *status_out = v;
+  if (clear) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return MXMOE_ERR_CUDA;
+  }
+  return MXMOE_OK;
+}
+
+mxmoe_status mx_quantize_3d(const uint16_t* w, int64_t E, int64_t N, int64_t K, uint8_t* q,
+                            uint8_t* scale, void* stream) {
+  if (E < 0 || N < 0 || K <= 0 || K % 32 != 0) return MXMOE_ERR_SHAPE;
+  if (E == 0 || N == 0) return MXMOE_OK;
+  MXMOE_CHECK_PTR(w);
+  MXMOE_CHECK_PTR(q);
+  if (!scale) return MXMOE_ERR_NULL;
+  return from_cuda(launch_mx_quantize(w, E * N, K, q, scale, (cudaStream_t)stream));
+}
+
+size_t moe_route_quant_mxfp8_workspace_size(int T, int E) {
+  if (T < 0 || E <= 0) return 0;
+  return route_workspace_bytes(T, E);
+}
+
+static mxmoe_status check_route(const uint16_t* x, const float* logits, int T, int H, int E, int k,
+                                int32_t* topk_ids, float* topk_w, int32_t* sorted_to_src,
+                                int32_t* src_to_sorted, int64_t* counts, int64_t* offsets,
+                                void* ws, size_t ws_bytes) {
+  if (T < 0 || H <= 0 || H % 32 != 0 || E <= 0 || E > 1024 || k < 1 || k > 32 || k > E)
+    return MXMOE_ERR_SHAPE;
+  if ((int64_t)T * k >= (1ll << 31)) return MXMOE_ERR_SHAPE;
+  MXMOE_CHECK_PTR(counts);
+  MXMOE_CHECK_PTR(offsets);
+  if (T == 0) return MXMOE_OK;
+  MXMOE_CHECK_PTR(x);
+  MXMOE_CHECK_PTR(logits);
+  MXMOE_CHECK_PTR(topk_ids);
+  MXMOE_CHECK_PTR(topk_w);
+  MXMOE_CHECK_PTR(sorted_to_src);
+  MXMOE_CHECK_PTR(src_to_sorted);
+  if (!ws) return MXMOE_ERR_WORKSPACE;
+  if (!aligned16(ws)) return MXMOE_ERR_ALIGN;
+  if (ws_bytes < route_workspace_bytes(T, E)) return MXMOE_ERR_WORKSPACE;
+  return MXMOE_OK;
+}
+
+mxmoe_status moe_route_quant_mxfp8(const uint16_t* x, const float* logits, int T, int H, int E,
+                                   int k, int renormalize, uint8_t* xq, uint8_t* xs,
+                                   int32_t* topk_ids, float* topk_w, int32_t* sorted_to_src,
+                                   int32_t* src_to_sorted, int64_t* expert_counts,
+                                   int64_t* expert_offsets, void* ws, size_t ws_bytes,
+                                   void* stream) {
+  mxmoe_status st = check_route(x, logits, T, H, E, k, topk_ids, topk_w, sorted_to_src,
+                                src_to_sorted, expert_counts, expert_offsets, ws, ws_bytes);
+  if (st != MXMOE_OK) return st;
+  if (T > 0) {
+    MXMOE_CHECK_PTR(xq);
+    if (!xs) return MXMOE_ERR_NULL;
+  }
+  return from_cuda(launch_route(x, logits, T, H, E, k, renormalize != 0, true, xq, xs, nullptr,
+                                topk_ids, topk_w, sorted_to_src, src_to_sorted, expert_counts,
+                                expert_offsets, (int32_t*)ws, (cudaStream_t)stream));
+}
+
+mxmoe_status moe_route_permute_bf16(const uint16_t* x, const float* logits, int T, int H, int E,
+                                    int k, int renormalize, uint16_t* xp, int32_t* topk_ids,
+                                    float* topk_w, int32_t* sorted_to_src, int32_t* src_to_sorted,
+                                    int64_t* expert_counts, int64_t* expert_offsets, void* ws,
+                                    size_t ws_bytes, void* stream) {
+  mxmoe_status st = check_route(x, logits, T, H, E, k, topk_ids, topk_w, sorted_to_src,
+                                src_to_sorted, expert_counts, expert_offsets, ws, ws_bytes);
+  if (st != MXMOE_OK) return st;
+  if (T > 0) MXMOE_CHECK_PTR(xp);
+  return from_cuda(launch_route(x, logits, T, H, E, k, renormalize != 0, false, nullptr, nullptr,
+                                xp, topk_ids, topk_w, sorted_to_src, src_to_sorted, expert_counts,
+                                expert_offsets, (int32_t*)ws, (cudaStream_t)stream));
+}
+
+static mxmoe_status check_gemm(const uint8_t* a, const uint8_t* sa, const uint8_t* w,
+                               const uint8_t* sw, const int64_t* offsets, int64_t M, int E, int K,
+                               int N, const void* out) {
+  if (M < 0 || M >= (1ll << 31) || E < 1 || K <= 0 || N <= 0) return MXMOE_ERR_SHAPE;
+  if (E > 256) return MXMOE_ERR_UNSUPPORTED;
+  if (K % 128 != 0 || N % 128 != 0) return MXMOE_ERR_UNSUPPORTED;
+  MXMOE_CHECK_PTR(offsets);
+  if (M == 0) return MXMOE_OK;
+  MXMOE_CHECK_PTR(a);
+  MXMOE_CHECK_PTR(w);
+  MXMOE_CHECK_PTR(out);
+  if (!sa || !sw) return MXMOE_ERR_NULL;
+  if (((uintptr_t)sa & 3u) || ((uintptr_t)sw & 3u)) return MXMOE_ERR_ALIGN;
+  return MXMOE_OK;
+}
+
+mxmoe_status grouped_gemm_swiglu_quant_mxfp8(const uint8_t* xq, const uint8_t* xs,
+                                             const uint8_t* w13q, const uint8_t* w13s,
+                                             const int64_t* expert_offsets, int64_t M, int E,
+                                             int H, int I, uint8_t* aq, uint8_t* as,
+                                             void* stream) {
+  mxmoe_status st = check_gemm(xq, xs, w13q, w13s, expert_offsets, M, E, H, I, aq);
+  if (st != MXMOE_OK) return st;
+  if (M > 0 && !as) return MXMOE_ERR_NULL;
+  if ((int64_t)E * 2 * I >= (1ll << 31)) return MXMOE_ERR_SHAPE;
+  return from_cuda(launch_gemm_swiglu_quant(xq, xs, w13q, w13s, expert_offsets, M, E, H, I, aq, as,
+                                            (cudaStream_t)stream));
+}
+
+mxmoe_status grouped_gemm_mxfp8(const uint8_t* aq, const uint8_t* as, const uint8_t* w2q,
+                                const uint8_t* w2s, const int64_t* expert_offsets, int64_t M,
+                                int E, int I, int H, uint16_t* y, void* stream) {
+  mxmoe_status st = check_gemm(aq, as, w2q, w2s, expert_offsets, M, E, I, H, y);
+  if (st != MXMOE_OK) return st;
+  if ((int64_t)E * H >= (1ll << 31)) return MXMOE_ERR_SHAPE;
+  return from_cuda(
+      launch_gemm_bf16(aq, as, w2q, w2s, expert_offsets, M, E, I, H, y, (cudaStream_t)stream));
+}
+
+mxmoe_status moe_finalize_routing(const uint16_t* y, const float* topk_w,
+                                  const int32_t* src_to_sorted, int T, int k, int H,
+                                  uint16_t* out, void* stream) {
+  if (T < 0 || k < 1 || k > 32 || H <= 0 || H % 8 != 0) return MXMOE_ERR_SHAPE;
+  if (T == 0) return MXMOE_OK;
+  MXMOE_CHECK_PTR(y);
+  MXMOE_CHECK_PTR(topk_w);
+  MXMOE_CHECK_PTR(src_to_sorted);
+  MXMOE_CHECK_PTR(out);
+  return from_cuda(launch_finalize(y, topk_w, src_to_sorted, T, k, H, out, (cudaStream_t)stream));
+}
+
+// Workspace of the whole layer, in this order (each 256-byte aligned):
+// xq [M,H] | xs [M,H/32] | topk_ids [T,k] | topk_w [T,k] | sorted_to_src [M] |
+// src_to_sorted [M] | counts [E] | offsets [E+1] | route histograms |
+// aq [M,I] | as [M,I/32] | y [M,H] bf16
+struct FwdLayout {
+  size_t xq, xs, ids, w, s2s, src2s, counts, offs, hist, aq, as, y, total;
+};
+
+static FwdLayout fwd_layout(int T, int H, int E, int k, int I) {
+  FwdLayout L;
+  const size_t M = (size_t)T * k;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o += align256(bytes); return at; };
+  L.xq = take(M * H);
+  L.xs = take(M * (H / 32));
+  L.ids = take(M * 4);
+  L.w = take(M * 4);
+  L.s2s = take(M * 4);
+  L.src2s = take(M * 4);
+  L.counts = take((size_t)E * 8);
+  L.offs = take((size_t)(E + 1) * 8);
+  L.hist = take(route_workspace_bytes(T, E));
+  L.aq = take(M * I);
+  L.as = take(M * (I / 32));
+  L.y = take(M * H * 2);
+  L.total = o;
+  return L;
+}
+
+size_t moe_forward_mxfp8_workspace_size(int T, int H, int E, int k, int I) {
+  if (T < 0 || H <= 0 || E <= 0 || k <= 0 || I <= 0) return 0;
+  return fwd_layout(T, H, E, k, I).total;
+}
+
+mxmoe_status moe_forward_mxfp8(const uint16_t* x, const float* logits, const uint8_t* w13q,
+                               const uint8_t* w13s, const uint8_t* w2q, const uint8_t* w2s,
+                               int T, int H, int E, int k, int I, int renormalize,
+                               uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+  if (T < 0 || H <= 0 || E <= 0 || k < 1 || k > 32 || k > E || I <= 0) return MXMOE_ERR_SHAPE;
+  if (E > 256 || H % 128 != 0 || I % 128 != 0) return MXMOE_ERR_UNSUPPORTED;
+  if ((int64_t)T * k >= (1ll << 31)) return MXMOE_ERR_SHAPE;
+  if (T == 0) return MXMOE_OK;
+  MXMOE_CHECK_PTR(x);
+  MXMOE_CHECK_PTR(logits);
+  MXMOE_CHECK_PTR(w13q);
+  MXMOE_CHECK_PTR(w2q);
+  MXMOE_CHECK_PTR(out);
+  if (!w13s || !w2s) return MXMOE_ERR_NULL;
+  if (!ws) return MXMOE_ERR_WORKSPACE;
+  if ((uintptr_t)ws & 255u) return MXMOE_ERR_ALIGN;
+  const FwdLayout L = fwd_layout(T, H, E, k, I);
+  if (ws_bytes < L.total) return MXMOE_ERR_WORKSPACE;
+  uint8_t* b = (uint8_t*)ws;
+  const int64_t M = (int64_t)T * k;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint8_t* xq = b + L.xq;
+  uint8_t* xs = b + L.xs;
+  int32_t* ids = (int32_t*)(b + L.ids);
+  float* w = (float*)(b + L.w);
+  int32_t* s2s = (int32_t*)(b + L.s2s);
+  int32_t* src2s = (int32_t*)(b + L.src2s);
+  int64_t* counts = (int64_t*)(b + L.counts);
+  int64_t* offs = (int64_t*)(b + L.offs);
+  uint8_t* aq = b + L.aq;
+  uint8_t* as = b + L.as;
+  uint16_t* y = (uint16_t*)(b + L.y);
+  cudaError_t e = launch_route(x, logits, T, H, E, k, renormalize != 0, true, xq, xs, nullptr,
+                               ids, w, s2s, src2s, counts, offs, (int32_t*)(b + L.hist), s);
+  if (e != cudaSuccess) return MXMOE_ERR_CUDA;
+  e = launch_gemm_swiglu_quant(xq, xs, w13q, w13s, offs, M, E, H, I, aq, as, s);
+  if (e != cudaSuccess) return MXMOE_ERR_CUDA;
+  e = launch_gemm_bf16(aq, as, w2q, w2s, offs, M, E, I, H, y, s);
+  if (e != cudaSuccess) return MXMOE_ERR_CUDA;
+  e = launch_finalize(y, w, src2s, T, k, H, out, s);
+  return from_cuda(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,85 @@
+// Device helpers shared by the MXFP8 MoE kernels (sm_103a).
+//
+// MX element/scale arithmetic (OCP MX v1.0, the format named on
+// "Quantization on Ascend", MoE MXFP8 notes):
+//   block scale byte  b = clamp(floor(log2(amax)) - 8, -127, 127) + 127
+//   element           q = e4m3_rn_satfinite(x * 2^(127 - b))
+// For a finite fp32/bf16 amax with biased exponent field ef (0 for zero and
+// subnormals), floor(log2(amax)) - 8 + 127 = ef - 8 for normal values, and
+// every subnormal or zero amax clamps to -127, so b = max(ef - 8, 0).  The
+// largest b any bf16/fp32 input reaches is 254 - 8 = 246, so 2^(127 - b) is
+// always a normal fp32 and the product x * 2^(127 - b) is exact (|x|/2^s <
+// 512; values below 2^-126 after scaling round to zero in e4m3 anyway).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mxmoe {
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) {
+  return __uint_as_float(b16 << 16);
+}
+
+// fp32 -> bf16 bits, round to nearest even (finite inputs).
+__device__ __forceinline__ uint32_t float_to_bf16_bits(float f) {
+  uint32_t u = __float_as_uint(f);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return u >> 16;
+}
+
+// Scale byte from the bit pattern of |amax| as fp32 (sign cleared).
+__device__ __forceinline__ uint32_t e8m0_from_amax_bits(uint32_t amax_bits) {
+  int ef = (int)(amax_bits >> 23);
+  int b = ef - 8;
+  return (uint32_t)(b < 0 ? 0 : b);
+}
+
+// 2^(127 - b) as an fp32 multiplier.
+__device__ __forceinline__ float inv_scale_from_e8m0(uint32_t b) {
+  return __uint_as_float((254u - b) << 23);
+}
+
+// Two fp32 -> two e4m3 bytes (lo -> bits 0..7, hi -> bits 8..15), RNE, saturating.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return (uint32_t)r;
+}
+
+// Four fp32 -> packed 4 e4m3 bytes (v0 in the lowest byte).
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float v0, float v1, float v2, float v3) {
+  return cvt_e4m3x2(v0, v1) | (cvt_e4m3x2(v2, v3) << 16);
+}
+
+__device__ __forceinline__ uint32_t umax(uint32_t a, uint32_t b) { return a > b ? a : b; }
+
+// |x| bit pattern of a bf16 pair packed in a 32-bit word, as two fp32 patterns' max.
+__device__ __forceinline__ uint32_t bf16x2_absmax_bits(uint32_t w) {
+  uint32_t lo = (w & 0x7FFFu) << 16;
+  uint32_t hi = (w & 0x7FFF0000u);
+  return umax(lo, hi);
+}
+
+// Streaming 16-byte global accesses.
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ void st_v4(void* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" :: "l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w) : "memory");
+}
+__device__ __forceinline__ void st_cs_v4(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" :: "l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w) : "memory");
+}
+
+// Record the first device-side error in the library's status word.
+__device__ __forceinline__ void report_error(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+}  // namespace mxmoe

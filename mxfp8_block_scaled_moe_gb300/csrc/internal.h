@@ -1,0 +1,43 @@
+// Internal launchers of the MXFP8 MoE library (host side, not exported).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mxmoe {
+
+// Routing: tokens handled by one block of the top-k / rank kernel.
+constexpr int kRouteTokensPerBlock = 64;
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int num_sms();                       // of the current device (cached)
+int* device_status_ptr();            // library status word on the current device
+long long wait_limit_cycles();
+
+cudaError_t launch_mx_quantize(const uint16_t* x, int64_t rows, int64_t K, uint8_t* q,
+                               uint8_t* scale, cudaStream_t stream);
+
+// Routing + permutation.  quant == true: xq/xs outputs; false: bf16 xp output.
+cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, int E, int k,
+                         bool renormalize, bool quant, uint8_t* xq, uint8_t* xs, uint16_t* xp,
+                         int32_t* topk_ids, float* topk_w, int32_t* sorted_to_src,
+                         int32_t* src_to_sorted, int64_t* counts, int64_t* offsets,
+                         int32_t* block_hist, cudaStream_t stream);
+
+size_t route_workspace_bytes(int T, int E);
+
+cudaError_t launch_finalize(const uint16_t* y, const float* topk_w, const int32_t* src_to_sorted,
+                            int T, int k, int H, uint16_t* out, cudaStream_t stream);
+
+// Grouped GEMMs.  Return cudaErrorInvalidValue when a tensor map can't be built.
+cudaError_t launch_gemm_swiglu_quant(const uint8_t* xq, const uint8_t* xs, const uint8_t* w13q,
+                                     const uint8_t* w13s, const int64_t* offsets, int64_t M,
+                                     int E, int H, int I, uint8_t* aq, uint8_t* as,
+                                     cudaStream_t stream);
+cudaError_t launch_gemm_bf16(const uint8_t* aq, const uint8_t* as, const uint8_t* w2q,
+                             const uint8_t* w2s, const int64_t* offsets, int64_t M, int E,
+                             int I, int H, uint16_t* y, cudaStream_t stream);
+
+}  // namespace mxmoe

@@ -1,0 +1,320 @@
+// Top-k routing, expert permutation and the fused per-token MX activation
+// quant (init_routing with quant_mode=3).
+//
+// "Quantization on Ascend", MoE MXFP8 "Forward": the dispatcher runs
+// init_routing with quant_mode=3, which fuses the per-token MX activation
+// quant into routing and emits the e4m3 payload, the e8m0 block scale and the
+// per-expert token counts.  sglang PR #32266 (commit note on quant_mode=3):
+// the fused output is byte-identical to routing followed by a separate quant.
+//
+// Three kernels, one stream:
+//   1. route_topk_rank: one warp per token picks the top-k experts (descending
+//      logit, ties -> lower id) and their softmax weights; then one warp per
+//      block ranks the block's assignments within each expert in flat order
+//      (warp match + popcount) and stores the block's per-expert histogram.
+//   2. route_scan: per-expert exclusive prefix of the block histograms (the
+//      block's base row inside each expert) and of the expert totals (offsets).
+//   3. route_permute_quant: one warp per token computes its k destination rows
+//      (offset + block base + rank), quantizes its hidden row once and writes
+//      the payload/scale to all k rows (or copies bf16 rows, two-step mode).
+// The permutation is deterministic: rows of one expert are in flat-index
+// (token) order.
+//
+// Roofline (kernel 3 dominates): x read once (2 B/elem) + k copies of the
+// payload (1 B) and scales (1/32 B) written; ids/weights/indices are small.
+#include "common.cuh"
+#include "internal.h"
+
+namespace mxmoe {
+
+constexpr int kRouteThreads = 256;
+constexpr int kRouteWarps = kRouteThreads / 32;
+
+// Is (v, id) a better pick than (bv, bid)?  Larger logit, then lower id.
+__device__ __forceinline__ bool better(float v, int id, float bv, int bid) {
+  return v > bv || (v == bv && id < bid);
+}
+
+template <int EPL>  // logits per lane: E <= 32 * EPL
+__global__ void __launch_bounds__(kRouteThreads) route_topk_rank_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int renormalize,
+    int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
+    int32_t* __restrict__ local_rank, int32_t* __restrict__ block_hist) {
+  extern __shared__ int smem_i[];
+  int* s_cnt = smem_i;                           // [E]
+  int* s_ids = smem_i + E;                       // [kRouteTokensPerBlock * k]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t0 = blockIdx.x * kRouteTokensPerBlock;
+  const int nt = min(kRouteTokensPerBlock, T - t0);
+
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+
+  for (int tl = warp; tl < nt; tl += kRouteWarps) {
+    const int t = t0 + tl;
+    const float* row = logits + (int64_t)t * E;
+    float v[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = e < E ? row[e] : -INFINITY;
+    }
+    uint32_t taken = 0;
+    int my_id = 0;
+    float my_val = 0.f;
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int bid = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((taken >> i) & 1u) && better(v[i], e, bv, bid)) { bv = v[i]; bid = e; }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oid = __shfl_xor_sync(0xffffffffu, bid, off);
+        if (better(ov, oid, bv, bid)) { bv = ov; bid = oid; }
+      }
+      if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
+      if (lane == j) { my_id = bid; my_val = bv; }
+    }
+    // softmax weights of the chosen experts
+    const float vmax = __shfl_sync(0xffffffffu, my_val, 0);
+    float denom;
+    if (renormalize) {
+      float ej = lane < k ? expf(my_val - vmax) : 0.f;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) ej += __shfl_xor_sync(0xffffffffu, ej, off);
+      denom = ej;
+    } else {
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E) s += expf(v[i] - vmax);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      denom = s;
+    }
+    if (lane < k) {
+      topk_ids[(int64_t)t * k + lane] = my_id;
+      topk_w[(int64_t)t * k + lane] = expf(my_val - vmax) / denom;
+      s_ids[tl * k + lane] = my_id;
+    }
+  }
+  __syncthreads();
+
+  // stable per-expert rank of the block's assignments, in flat order
+  if (warp == 0) {
+    const int na = nt * k;
+    for (int c = 0; c < na; c += 32) {
+      const int f = c + lane;
+      const bool valid = f < na;
+      const int e = valid ? s_ids[f] : -1;
+      const uint32_t peers = __match_any_sync(0xffffffffu, e);
+      const int leader = __ffs(peers) - 1;
+      const int base = valid ? s_cnt[e] : 0;
+      const int rank = base + __popc(peers & ((1u << lane) - 1u));
+      __syncwarp();
+      if (valid && lane == leader) s_cnt[e] = base + __popc(peers);
+      __syncwarp();
+      if (valid) local_rank[(int64_t)t0 * k + f] = rank;
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    block_hist[(int64_t)blockIdx.x * E + e] = s_cnt[e];
+}
+
+// One block of 1024 threads.  G = 1024 / E thread groups split the routing
+// blocks; hist[b][e] becomes the exclusive prefix over blocks of expert e.
+__global__ void __launch_bounds__(1024) route_scan_kernel(int32_t* __restrict__ hist, int nb,
+                                                          int E, int64_t* __restrict__ counts,
+                                                          int64_t* __restrict__ offsets) {
+  extern __shared__ int smem_i[];
+  const int G = max(1, (int)(blockDim.x / E));
+  int* s_part = smem_i;          // [G][E]
+  int* s_tot = smem_i + G * E;   // [E]
+  const int g = threadIdx.x / E, e = threadIdx.x % E;
+  const int per = (nb + G - 1) / G;
+  const int b0 = g * per, b1 = min(nb, b0 + per);
+  const bool active = g < G;
+  if (active) {
+    int s = 0;
+    for (int b = b0; b < b1; ++b) s += hist[(int64_t)b * E + e];
+    s_part[g * E + e] = s;
+  }
+  __syncthreads();
+  if (threadIdx.x < E) {
+    int run = 0;
+    for (int gg = 0; gg < G; ++gg) {
+      const int v = s_part[gg * E + threadIdx.x];
+      s_part[gg * E + threadIdx.x] = run;
+      run += v;
+    }
+    s_tot[threadIdx.x] = run;
+  }
+  __syncthreads();
+  if (active) {
+    int run = s_part[g * E + e];
+    for (int b = b0; b < b1; ++b) {
+      const int v = hist[(int64_t)b * E + e];
+      hist[(int64_t)b * E + e] = run;
+      run += v;
+    }
+  }
+  // exclusive scan of the expert totals (E <= 1024), warp-shuffle based
+  __shared__ int s_warp[32];
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  int v = tid < E ? s_tot[tid] : 0;
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) s_warp[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int x = s_warp[lane];
+    int xi = x;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, xi, off);
+      if (lane >= off) xi += o;
+    }
+    s_warp[lane] = xi - x;  // exclusive prefix of warp totals
+  }
+  __syncthreads();
+  const int excl = incl - v + s_warp[w];
+  if (tid < E) {
+    counts[tid] = v;
+    offsets[tid] = excl;
+    if (tid == E - 1) offsets[E] = excl + v;
+  }
+}
+
+template <bool kQuant>
+__global__ void __launch_bounds__(kRouteThreads) route_permute_kernel(
+    const uint16_t* __restrict__ x, int T, int H, int E, int k,
+    const int32_t* __restrict__ topk_ids, const int32_t* __restrict__ block_base,
+    const int64_t* __restrict__ offsets, int32_t* __restrict__ src_to_sorted,
+    int32_t* __restrict__ sorted_to_src, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
+    uint16_t* __restrict__ xp) {
+  __shared__ int64_t s_dest[kRouteWarps][32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t = blockIdx.x * kRouteWarps + warp;
+  if (t >= T) return;  // warp-uniform
+  const int b = t / kRouteTokensPerBlock;
+  if (lane < k) {
+    const int64_t f = (int64_t)t * k + lane;
+    const int e = topk_ids[f];
+    const int64_t dest = offsets[e] + block_base[(int64_t)b * E + e] + src_to_sorted[f];
+    src_to_sorted[f] = (int32_t)dest;
+    sorted_to_src[dest] = (int32_t)f;
+    s_dest[warp][lane] = dest;
+  }
+  __syncwarp();
+  const uint16_t* xr = x + (int64_t)t * H;
+  const int H32 = H / 32;
+  for (int c0 = 0; c0 < H; c0 += 512) {  // 16 elements per lane per step
+    const int c = c0 + lane * 16;
+    const bool ok = c < H;
+    uint4 a = make_uint4(0, 0, 0, 0), bb = make_uint4(0, 0, 0, 0);
+    if (ok) {
+      a = ld_nc_v4(xr + c);
+      bb = ld_nc_v4(xr + c + 8);
+    }
+    if (kQuant) {
+      uint32_t m = umax(umax(bf16x2_absmax_bits(a.x), bf16x2_absmax_bits(a.y)),
+                        umax(bf16x2_absmax_bits(a.z), bf16x2_absmax_bits(a.w)));
+      m = umax(m, umax(umax(bf16x2_absmax_bits(bb.x), bf16x2_absmax_bits(bb.y)),
+                       umax(bf16x2_absmax_bits(bb.z), bf16x2_absmax_bits(bb.w))));
+      m = umax(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      const uint32_t sb = e8m0_from_amax_bits(m);
+      const float inv = inv_scale_from_e8m0(sb);
+      const uint32_t w[8] = {a.x, a.y, a.z, a.w, bb.x, bb.y, bb.z, bb.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t w0 = w[2 * i], w1 = w[2 * i + 1];
+        o[i] = cvt_e4m3x4(bf16_bits_to_float(w0 & 0xFFFFu) * inv,
+                          bf16_bits_to_float(w0 >> 16) * inv,
+                          bf16_bits_to_float(w1 & 0xFFFFu) * inv,
+                          bf16_bits_to_float(w1 >> 16) * inv);
+      }
+      if (ok) {
+        const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
+        for (int j = 0; j < k; ++j) {
+          const int64_t d = s_dest[warp][j];
+          st_cs_v4(xq + d * H + c, ov);
+          if ((lane & 1) == 0) xs[d * H32 + (c >> 5)] = (uint8_t)sb;
+        }
+      }
+    } else if (ok) {
+      for (int j = 0; j < k; ++j) {
+        const int64_t d = s_dest[warp][j];
+        st_cs_v4(xp + d * H + c, a);
+        st_cs_v4(xp + d * H + c + 8, bb);
+      }
+    }
+  }
+}
+
+size_t route_workspace_bytes(int T, int E) {
+  const int64_t nb = ceil_div(T, kRouteTokensPerBlock);
+  const size_t b = (size_t)(nb > 0 ? nb : 1) * (size_t)E * sizeof(int32_t);
+  return (b + 255) & ~(size_t)255;
+}
+
+template <int EPL>
+static void launch_topk(int nb, size_t smem, cudaStream_t stream, const float* logits, int T,
+                        int E, int k, int renorm, int32_t* ids, float* w, int32_t* rank,
+                        int32_t* hist) {
+  route_topk_rank_kernel<EPL><<<nb, kRouteThreads, smem, stream>>>(logits, T, E, k, renorm, ids,
+                                                                    w, rank, hist);
+}
+
+cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, int E, int k,
+                         bool renormalize, bool quant, uint8_t* xq, uint8_t* xs, uint16_t* xp,
+                         int32_t* topk_ids, float* topk_w, int32_t* sorted_to_src,
+                         int32_t* src_to_sorted, int64_t* counts, int64_t* offsets,
+                         int32_t* block_hist, cudaStream_t stream) {
+  if (T == 0) {
+    cudaError_t err = cudaMemsetAsync(counts, 0, sizeof(int64_t) * E, stream);
+    if (err != cudaSuccess) return err;
+    return cudaMemsetAsync(offsets, 0, sizeof(int64_t) * (E + 1), stream);
+  }
+  const int nb = (int)ceil_div(T, kRouteTokensPerBlock);
+  const size_t smem1 = sizeof(int) * ((size_t)E + (size_t)kRouteTokensPerBlock * k);
+  const int epl = (E + 31) / 32;
+  const int rn = renormalize ? 1 : 0;
+  // src_to_sorted holds the in-block rank between kernels 1 and 3
+  if (epl <= 1)       launch_topk<1>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist);
+  else if (epl <= 2)  launch_topk<2>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist);
+  else if (epl <= 4)  launch_topk<4>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist);
+  else if (epl <= 8)  launch_topk<8>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist);
+  else if (epl <= 16) launch_topk<16>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist);
+  else                launch_topk<32>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+
+  const int G = E >= 1024 ? 1 : 1024 / E;
+  const size_t smem2 = sizeof(int) * ((size_t)G * E + E);
+  route_scan_kernel<<<1, 1024, smem2, stream>>>(block_hist, nb, E, counts, offsets);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+
+  const int nb3 = (int)ceil_div(T, kRouteWarps);
+  if (quant)
+    route_permute_kernel<true><<<nb3, kRouteThreads, 0, stream>>>(
+        x, T, H, E, k, topk_ids, block_hist, offsets, src_to_sorted, sorted_to_src, xq, xs, nullptr);
+  else
+    route_permute_kernel<false><<<nb3, kRouteThreads, 0, stream>>>(
+        x, T, H, E, k, topk_ids, block_hist, offsets, src_to_sorted, sorted_to_src, nullptr,
+        nullptr, xp);
+  return cudaGetLastError();
+}
+
+}  // namespace mxmoe

@@ -1,0 +1,86 @@
+"""The C-ABI library builds, loads and exports every declared symbol; host-side
+argument validation rejects bad calls before any launch (no GPU needed)."""
+
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mxfp8_block_scaled_moe_gb300 import _lib, build
+    build.build()
+    return _lib.load()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "mxmoe.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, re.M)
+    return sorted(set(n for n in names if n not in ("if", "defined")))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from mxfp8_block_scaled_moe_gb300 import _lib
+    declared = _declared_functions()
+    assert len(declared) >= 13
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(declared) == set(_lib.EXPORTS)
+
+
+def test_status_strings(lib):
+    for code in range(9):
+        assert lib.mxmoe_status_string(code).decode().startswith("MXMOE_")
+    assert b"sm_103a" in lib.mxmoe_version()
+
+
+def test_workspace_sizes(lib):
+    assert lib.moe_route_quant_mxfp8_workspace_size(16384, 128) >= 256 * 128 * 4
+    ws = lib.moe_forward_mxfp8_workspace_size(16384, 2048, 128, 8, 768)
+    M = 16384 * 8
+    assert ws >= M * 2048 * 3 + M * 768
+    assert lib.moe_forward_mxfp8_workspace_size(-1, 2048, 128, 8, 768) == 0
+
+
+def test_host_validation_rejects_bad_arguments(lib):
+    p = C.c_void_p(4096)        # never dereferenced: validation fails first
+    odd = C.c_void_p(4097)
+    nul = C.c_void_p(0)
+    # K not a multiple of 32
+    assert lib.mx_quantize_3d(p, 1, 4, 33, p, p, nul) == 3
+    # misaligned payload pointer
+    assert lib.mx_quantize_3d(odd, 1, 4, 64, p, p, nul) == 2
+    # null weight pointer
+    assert lib.mx_quantize_3d(nul, 1, 4, 64, p, p, nul) == 1
+    # empty tensor is a no-op
+    assert lib.mx_quantize_3d(nul, 0, 4, 64, nul, nul, nul) == 0
+    # k > E
+    assert lib.moe_route_quant_mxfp8(p, p, 4, 64, 4, 5, 1, p, p, p, p, p, p, p, p, p, 1 << 20, nul) == 3
+    # workspace too small
+    assert lib.moe_route_quant_mxfp8(p, p, 4096, 64, 8, 2, 1, p, p, p, p, p, p, p, p, p, 16, nul) == 5
+    # GEMM with K % 128 != 0 -> unsupported; E > 256 -> unsupported
+    assert lib.grouped_gemm_mxfp8(p, p, p, p, p, 128, 8, 96, 256, p, nul) == 4
+    assert lib.grouped_gemm_mxfp8(p, p, p, p, p, 128, 300, 128, 256, p, nul) == 4
+    # negative M
+    assert lib.grouped_gemm_swiglu_quant_mxfp8(p, p, p, p, p, -1, 8, 256, 128, p, p, nul) == 3
+    # finalize: H % 8 != 0
+    assert lib.moe_finalize_routing(p, p, p, 4, 2, 12, p, nul) == 3
+    # forward: workspace not 256-aligned / too small
+    assert lib.moe_forward_mxfp8(p, p, p, p, p, p, 64, 256, 8, 2, 128, 1, p, C.c_void_p(4096 + 16),
+                                 1 << 30, nul) == 2
+    assert lib.moe_forward_mxfp8(p, p, p, p, p, p, 64, 256, 8, 2, 128, 1, p, p, 1024, nul) == 5
+    # T == 0 is a no-op
+    assert lib.moe_forward_mxfp8(nul, nul, nul, nul, nul, nul, 0, 256, 8, 2, 128, 1, nul, nul, 0,
+                                 nul) == 0
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+    import mxfp8_block_scaled_moe_gb300 as mm
+    with pytest.raises(ValueError, match="CUDA"):
+        mm.mx_quantize_3d(torch.zeros(2, 64, dtype=torch.bfloat16))
