@@ -40,7 +40,7 @@ FP8_OVER_BF16 = 2.0   # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 
 # DRAM traffic of one gmm1 launch from an ncu capture, keyed by the hash of the
 # GEMM source it was taken on (profiles/gemm1_swiglu_quant_qwen3_30b_prefill.md).
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {"0a79c3073112a1c8": 786962176}
 
 
 def parse():
