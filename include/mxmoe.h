@@ -115,6 +115,35 @@ mxmoe_status moe_route_quant_mxfp8(const uint16_t* x, const float* logits, int T
                                    void* stream);
 
 /*
+ * moe_route_quant_mxfp8 for callers that cannot allocate device memory.
+ * The pages have no counterpart of this entry point; it exists for callers
+ * such as serving runtimes that pre-partition all device memory into their
+ * own pool and forbid cudaMalloc while serving (an allocation there can
+ * synchronize the device and fragments the pool), or plug-ins whose host
+ * framework owns device memory and offers no workspace hook.
+ *
+ * Same arguments, results and layouts as moe_route_quant_mxfp8, minus the
+ * workspace: the routing scratch (per-block expert histograms) lives in a
+ * 1 MiB array inside the library that every GPU loading the library keeps
+ * until the process exits.  Inputs and outputs remain the caller's.
+ *   - Limit: ceil(T / 64) * E <= 262144 (e.g. T = 131072 tokens at E = 128);
+ *     larger calls return MXMOE_ERR_WORKSPACE and launch nothing.
+ *   - The call allocates nothing (no cudaMalloc / cudaFree, no allocating
+ *     library routine).  Its first call on a device looks up the array's
+ *     device address with that device current; make that first call before
+ *     any stream capture.
+ *   - Every call shares the one array.  Each call writes every scratch entry
+ *     it later reads, so nothing has to start at zero, but calls that
+ *     overlap on the GPU (other streams, other threads) race on it.
+ */
+mxmoe_status moe_route_quant_mxfp8_noalloc(const uint16_t* x, const float* logits, int T, int H,
+                                           int E, int k, int renormalize, uint8_t* xq,
+                                           uint8_t* xs, int32_t* topk_ids, float* topk_w,
+                                           int32_t* sorted_to_src, int32_t* src_to_sorted,
+                                           int64_t* expert_counts, int64_t* expert_offsets,
+                                           void* stream);
+
+/*
  * The two-step comparator of moe_route_quant_mxfp8: the same routing and
  * permutation, but the expanded rows are written as bf16 (init_routing
  * without quant); a separate mx_quantize_3d(xp, 1, M, H) pass then gives the

@@ -18,7 +18,7 @@ EXPORTS = (
     "mxmoe_set_wait_limit_cycles", "mx_quantize_3d", "moe_route_quant_mxfp8_workspace_size",
     "moe_route_quant_mxfp8", "moe_route_permute_bf16", "grouped_gemm_swiglu_quant_mxfp8",
     "grouped_gemm_mxfp8", "moe_finalize_routing", "moe_forward_mxfp8_workspace_size",
-    "moe_forward_mxfp8",
+    "moe_forward_mxfp8", "moe_route_quant_mxfp8_noalloc",
 )
 
 _P = C.c_void_p
@@ -35,6 +35,8 @@ _PROTOS = {
     "moe_route_quant_mxfp8_workspace_size": (_SZ, [_I, _I]),
     "moe_route_quant_mxfp8": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P,
                                    _P, _SZ, _P]),
+    "moe_route_quant_mxfp8_noalloc": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
+                                           _P, _P, _P]),
     "moe_route_permute_bf16": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P,
                                     _P, _SZ, _P]),
     "grouped_gemm_swiglu_quant_mxfp8": (_I, [_P, _P, _P, _P, _P, _I64, _I, _I, _I, _P, _P, _P]),

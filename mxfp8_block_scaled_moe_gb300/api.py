@@ -228,3 +228,34 @@ class MXFP8MoELayer:
         return moe_forward_mxfp8(x, logits, self.w13q, self.w13s, self.w2q, self.w2s, self.k,
                                  self.renormalize, out=out,
                                  workspace=self.workspace(x.shape[0], x.device))
+
+
+def moe_route_quant_mxfp8_noalloc(x, logits, k: int, renormalize: bool = True) -> dict:
+    """moe_route_quant_mxfp8 through the entry point that takes no workspace.
+
+    For callers that cannot allocate device scratch: the library keeps the
+    routing scratch in a fixed 1 MiB device array (ceil(T/64)*E <= 262144).
+    The outputs are still allocated here, by torch, like every other binding.
+    """
+    _need(x, "x", torch.bfloat16, 2)
+    _need(logits, "logits", torch.float32, 2)
+    T, H = x.shape
+    E = logits.shape[1]
+    dev = x.device
+    M = T * k
+    out = dict(
+        topk_ids=torch.empty(T, k, dtype=torch.int32, device=dev),
+        topk_w=torch.empty(T, k, dtype=torch.float32, device=dev),
+        sorted_to_src=torch.empty(M, dtype=torch.int32, device=dev),
+        src_to_sorted=torch.empty(M, dtype=torch.int32, device=dev),
+        expert_counts=torch.empty(E, dtype=torch.int64, device=dev),
+        expert_offsets=torch.empty(E + 1, dtype=torch.int64, device=dev),
+        xq=torch.empty(M, H, dtype=torch.uint8, device=dev),
+        xs=torch.empty(M, H // 32, dtype=torch.uint8, device=dev),
+    )
+    _lib.check("moe_route_quant_mxfp8_noalloc", _lib.load().moe_route_quant_mxfp8_noalloc(
+        _ptr(x), _ptr(logits), T, H, E, k, int(bool(renormalize)), _ptr(out["xq"]),
+        _ptr(out["xs"]), _ptr(out["topk_ids"]), _ptr(out["topk_w"]), _ptr(out["sorted_to_src"]),
+        _ptr(out["src_to_sorted"]), _ptr(out["expert_counts"]), _ptr(out["expert_offsets"]),
+        _stream()))
+    return out
