@@ -316,9 +316,21 @@ def main():
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    mm.api.layer_profile_enable(True)   # CUDA events between the layer's kernels
+    step_ms, prof = [], []
     with ClockSampler(local_rank, enabled=not args.no_clocks) as clk:
-        step_ms = time_fn(torch, step, args.steps, flush, stream)
+        for _ in range(args.steps):
+            flush.fill_(1)
+            ev_a = torch.cuda.Event(enable_timing=True)
+            ev_b = torch.cuda.Event(enable_timing=True)
+            ev_a.record(stream)
+            step()
+            ev_b.record(stream)
+            ev_b.synchronize()
+            step_ms.append(ev_a.elapsed_time(ev_b))
+            prof.append(mm.api.layer_profile_read())
         torch.cuda.synchronize()
+    mm.api.layer_profile_enable(False)
     if world > 1:
         dist.barrier()
     total_ms = sum(step_ms)
@@ -328,26 +340,18 @@ def main():
     total_ms = float(t_max.item())
     value = world * T * args.steps / (total_ms / 1e3)
 
-    # ---- per-kernel breakdown (same inputs, CUDA events, L2 flushed)
+    # ---- per-kernel times inside the timed steps (library events on the stream)
+    def kmean(key):
+        return statistics.mean(p_[key] for p_ in prof)
+    route_ms, gemm1_ms = kmean("route_quant"), kmean("gemm1_swiglu_quant")
+    gemm2_ms, fin_ms = kmean("gemm2"), kmean("finalize")
+    # the two-step comparator (bf16 permute, then a separate quant pass)
     reps = max(5, min(args.steps, 20))
-    r = mm.moe_route_quant_mxfp8(x, logits, k)
-    route_ms = statistics.median(time_fn(torch, lambda: mm.moe_route_quant_mxfp8(x, logits, k),
-                                         reps, flush, stream))
 
     def twostep():
         rr = mm.moe_route_permute_bf16(x, logits, k)
         mm.mx_quantize_3d(rr["xp"])
     twostep_ms = statistics.median(time_fn(torch, twostep, reps, flush, stream))
-    g1 = lambda: mm.grouped_gemm_swiglu_quant_mxfp8(r["xq"], r["xs"], layer.w13q, layer.w13s,
-                                                   r["expert_offsets"])
-    aq, as_ = g1()
-    gemm1_t = time_fn(torch, g1, reps, flush, stream)
-    gemm1_ms = statistics.mean(gemm1_t)
-    g2 = lambda: mm.grouped_gemm_mxfp8(aq, as_, layer.w2q, layer.w2s, r["expert_offsets"])
-    y = g2()
-    gemm2_ms = statistics.mean(time_fn(torch, g2, reps, flush, stream))
-    fin = lambda: mm.moe_finalize_routing(y, r["topk_w"], r["src_to_sorted"], k)
-    fin_ms = statistics.median(time_fn(torch, fin, reps, flush, stream))
     torch.cuda.synchronize()
     if mm.device_status() != 0:
         raise RuntimeError("device status error during timing")
@@ -365,7 +369,9 @@ def main():
                 "frac": round(gemm1_tflops / fp8_peak, 4), "traffic": traffic,
                 "peak_source": f"{peaks['source']}: bf16 dense burst {peaks['bf16_tflops']} TFLOP/s "
                                f"x {FP8_OVER_BF16} (nominal fp8/bf16 ratio)",
-                "flops_per_launch": gemm1_flops, "launch_ms": round(gemm1_ms, 4)}
+                "flops_per_launch": gemm1_flops, "launch_ms": round(gemm1_ms, 4),
+                "timing": "mean over the timed steps, CUDA events recorded by the library "
+                          "around this kernel on the launching stream"}
     kernels = {
         "route_quant": {"ms": route_ms, "GB/s": ab["route"] / route_ms / 1e6,
                         "frac_hbm": ab["route"] / route_ms / 1e6 / hbm},

@@ -170,7 +170,7 @@ mxmoe_status moe_route_permute_bf16(const uint16_t* x, const float* logits, int 
  *   xq, xs          e4m3 [M, H], e8m0 [M, H/32]
  *   w13q, w13s      e4m3 [E, 2I, H], e8m0 [E, 2I, H/32]
  *   expert_offsets  int64 [E+1] on the device, offsets[E] == M
- *   aq, as          e4m3 [M, I], e8m0 [M, I/32]   (outputs)
+ *   aq, as          e4m3 [M, I], e8m0 [M, I/32]   (outputs; aq 32-byte aligned)
  * Requires H % 128 == 0, I % 128 == 0, 1 <= E <= 256, M >= 0.
  */
 mxmoe_status grouped_gemm_swiglu_quant_mxfp8(const uint8_t* xq, const uint8_t* xs,
@@ -188,7 +188,7 @@ mxmoe_status grouped_gemm_swiglu_quant_mxfp8(const uint8_t* xq, const uint8_t* x
  *
  *   aq, as      e4m3 [M, I], e8m0 [M, I/32]
  *   w2q, w2s    e4m3 [E, H, I], e8m0 [E, H, I/32]
- *   y           bf16 [M, H]   (output)
+ *   y           bf16 [M, H]   (output, 32-byte aligned)
  * Requires I % 128 == 0, H % 128 == 0, 1 <= E <= 256, M >= 0.
  */
 mxmoe_status grouped_gemm_mxfp8(const uint8_t* aq, const uint8_t* as, const uint8_t* w2q,
@@ -220,11 +220,51 @@ size_t moe_forward_mxfp8_workspace_size(int T, int H, int E, int k, int I);
  * offline checkpoint's float8_e4m3fn payload + uint8 e8m0 scales).
  *   out bf16 [T, H].  ws: moe_forward_mxfp8_workspace_size() bytes, 256-byte
  *   aligned; it holds every intermediate and may be reused between calls.
+ *   Inside the call the activation scales and a copy of the weight scales
+ *   live in the MMA layout (see mx_scales_to_mma_layout).
  */
 mxmoe_status moe_forward_mxfp8(const uint16_t* x, const float* logits, const uint8_t* w13q,
                                const uint8_t* w13s, const uint8_t* w2q, const uint8_t* w2s,
                                int T, int H, int E, int k, int I, int renormalize,
                                uint16_t* out, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Load-time re-layout of weight scales into the tensor-core ("MMA") layout
+ * that moe_forward_mxfp8_mma_scales consumes.  Not an operation of the
+ * pages (their FRACTAL_NZ re-tiling plays the same role for Ascend): the
+ * GB300 tensor cores read each 128-row x 128-K block's 512 scale bytes as
+ * one chunk, byte (r % 32) * 16 + (r / 32) * 4 + kb for row r of the block
+ * and 32-element block kb, chunks ordered (row block, K slice).
+ *   scale  e8m0 [E, N, K/32]   ->   out  e8m0, E*N*K/32 bytes (same size)
+ * Requires N % 128 == 0, K % 128 == 0.
+ */
+mxmoe_status mx_scales_to_mma_layout(const uint8_t* scale, int64_t E, int64_t N, int64_t K,
+                                     uint8_t* out, void* stream);
+
+/*
+ * moe_forward_mxfp8 with the weight scales already in the MMA layout
+ * (mx_scales_to_mma_layout, done once at load); saves re-laying them out on
+ * every call.  All other arguments and results as moe_forward_mxfp8.
+ */
+mxmoe_status moe_forward_mxfp8_mma_scales(const uint16_t* x, const float* logits,
+                                          const uint8_t* w13q, const uint8_t* w13s_mma,
+                                          const uint8_t* w2q, const uint8_t* w2s_mma, int T,
+                                          int H, int E, int k, int I, int renormalize,
+                                          uint16_t* out, void* ws, size_t ws_bytes,
+                                          void* stream);
+
+/*
+ * Per-kernel timing of moe_forward_mxfp8 / moe_forward_mxfp8_mma_scales
+ * (instrumentation, off by default; not part of the method).  While
+ * enabled, each layer call records CUDA events on its stream between its
+ * kernels; mxmoe_layer_profile_read then returns, for the last such call on
+ * the current device, n <= 5 segment times in milliseconds:
+ *   [0] weight-scale re-layout (0 for the _mma_scales entry point),
+ *   [1] route + fused quant, [2] gmm1, [3] gmm2, [4] finalize.
+ * The read synchronizes on the call's last event.  Not thread-safe.
+ */
+mxmoe_status mxmoe_layer_profile_enable(int enable);
+mxmoe_status mxmoe_layer_profile_read(float* ms, int n);
 
 /*
  * Device status word of the current device: 0 or the first error a kernel

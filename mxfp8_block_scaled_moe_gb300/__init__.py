@@ -9,5 +9,6 @@ lazily and raises if it has not been built.
 from .api import (  # noqa: F401
     MXFP8MoELayer, device_status, grouped_gemm_mxfp8, grouped_gemm_swiglu_quant_mxfp8,
     moe_finalize_routing, moe_forward_mxfp8, moe_forward_mxfp8_workspace_size,
-    moe_route_permute_bf16, moe_route_quant_mxfp8, mx_quantize_3d, set_wait_limit_cycles,
+    moe_forward_mxfp8_mma_scales, moe_route_permute_bf16, moe_route_quant_mxfp8, mx_quantize_3d,
+    mx_scales_to_mma_layout, set_wait_limit_cycles,
 )

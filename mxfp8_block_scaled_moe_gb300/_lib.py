@@ -18,7 +18,8 @@ EXPORTS = (
     "mxmoe_set_wait_limit_cycles", "mx_quantize_3d", "moe_route_quant_mxfp8_workspace_size",
     "moe_route_quant_mxfp8", "moe_route_permute_bf16", "grouped_gemm_swiglu_quant_mxfp8",
     "grouped_gemm_mxfp8", "moe_finalize_routing", "moe_forward_mxfp8_workspace_size",
-    "moe_forward_mxfp8", "moe_route_quant_mxfp8_noalloc",
+    "moe_forward_mxfp8", "moe_route_quant_mxfp8_noalloc", "mx_scales_to_mma_layout",
+    "moe_forward_mxfp8_mma_scales", "mxmoe_layer_profile_enable", "mxmoe_layer_profile_read",
 )
 
 _P = C.c_void_p
@@ -44,6 +45,11 @@ _PROTOS = {
     "moe_finalize_routing": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "moe_forward_mxfp8_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "moe_forward_mxfp8": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "moe_forward_mxfp8_mma_scales": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P,
+                                          _SZ, _P]),
+    "mx_scales_to_mma_layout": (_I, [_P, _I64, _I64, _I64, _P, _P]),
+    "mxmoe_layer_profile_enable": (_I, [_I]),
+    "mxmoe_layer_profile_read": (_I, [C.POINTER(C.c_float), _I]),
 }
 
 _lib = None

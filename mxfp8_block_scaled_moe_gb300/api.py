@@ -181,11 +181,61 @@ def moe_forward_mxfp8(x, logits, w13q, w13s, w2q, w2s, k: int, renormalize: bool
     return out
 
 
+def mx_scales_to_mma_layout(scale, K: int):
+    """e8m0 scales [E, N, K/32] (or [N, K/32]) -> the tensor-core layout (same byte count)."""
+    _need(scale, "scale", torch.uint8)
+    if scale.dim() == 2:
+        E, N = 1, scale.shape[0]
+    elif scale.dim() == 3:
+        E, N = scale.shape[0], scale.shape[1]
+    else:
+        raise ValueError("scale must be 2D or 3D")
+    out = torch.empty_like(scale)
+    _lib.check("mx_scales_to_mma_layout", _lib.load().mx_scales_to_mma_layout(
+        _ptr(scale), E, N, K, _ptr(out), _stream()))
+    return out
+
+
+def moe_forward_mxfp8_mma_scales(x, logits, w13q, w13s_mma, w2q, w2s_mma, k: int,
+                                 renormalize: bool = True, out=None, workspace=None):
+    """moe_forward_mxfp8 with weight scales already in the tensor-core layout."""
+    w13q, w2q = _u8(w13q), _u8(w2q)
+    _need(x, "x", torch.bfloat16, 2)
+    _need(logits, "logits", torch.float32, 2)
+    for t, n in ((w13q, "w13q"), (w13s_mma, "w13s_mma"), (w2q, "w2q"), (w2s_mma, "w2s_mma")):
+        _need(t, n, torch.uint8, 3)
+    T, H = x.shape
+    E, N2, _ = w13q.shape
+    I = N2 // 2
+    ws_bytes = moe_forward_mxfp8_workspace_size(T, H, E, k, I)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=x.device)
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=x.device)
+    _lib.check("moe_forward_mxfp8_mma_scales", _lib.load().moe_forward_mxfp8_mma_scales(
+        _ptr(x), _ptr(logits), _ptr(w13q), _ptr(w13s_mma), _ptr(w2q), _ptr(w2s_mma), T, H, E, k, I,
+        int(bool(renormalize)), _ptr(out), _ptr(workspace), workspace.numel(), _stream()))
+    return out
+
+
 def device_status(clear: bool = True) -> int:
     """The library's device status word (synchronizes the device)."""
     v = C.c_int32(0)
     _lib.check("mxmoe_get_device_status", _lib.load().mxmoe_get_device_status(C.byref(v), int(clear)))
     return int(v.value)
+
+
+def layer_profile_enable(enable: bool = True) -> None:
+    """Record CUDA events between the layer call's kernels (instrumentation)."""
+    _lib.check("mxmoe_layer_profile_enable", _lib.load().mxmoe_layer_profile_enable(int(enable)))
+
+
+def layer_profile_read() -> dict:
+    """Per-kernel milliseconds of the last profiled layer call (synchronizes)."""
+    arr = (C.c_float * 5)()
+    _lib.check("mxmoe_layer_profile_read", _lib.load().mxmoe_layer_profile_read(arr, 5))
+    keys = ("weight_scale_layout", "route_quant", "gemm1_swiglu_quant", "gemm2", "finalize")
+    return dict(zip(keys, (float(v) for v in arr)))
 
 
 def set_wait_limit_cycles(cycles: int) -> None:
@@ -194,6 +244,10 @@ def set_wait_limit_cycles(cycles: int) -> None:
 
 class MXFP8MoELayer:
     """MX-quantized expert weights plus a reusable workspace for one layer shape.
+
+    At construction the weight scales are also re-laid out once into the
+    tensor-core layout (``mx_scales_to_mma_layout``); calls go through
+    ``moe_forward_mxfp8_mma_scales``.
 
     ``from_bf16`` quantizes bf16 w13 [E, 2I, H] / w2 [E, H, I] on the device
     (the online, load-time path); ``from_quantized`` takes an offline
@@ -206,6 +260,9 @@ class MXFP8MoELayer:
         self.renormalize = renormalize
         self.E, n2, self.H = self.w13q.shape
         self.I = n2 // 2
+        # load time: the scales in the tensor-core layout the layer call reads
+        self.w13s_mma = mx_scales_to_mma_layout(self.w13s, self.H)
+        self.w2s_mma = mx_scales_to_mma_layout(self.w2s, self.I)
         self._ws = None
 
     @classmethod
@@ -225,9 +282,9 @@ class MXFP8MoELayer:
         return self._ws
 
     def __call__(self, x, logits, out=None):
-        return moe_forward_mxfp8(x, logits, self.w13q, self.w13s, self.w2q, self.w2s, self.k,
-                                 self.renormalize, out=out,
-                                 workspace=self.workspace(x.shape[0], x.device))
+        return moe_forward_mxfp8_mma_scales(x, logits, self.w13q, self.w13s_mma, self.w2q,
+                                            self.w2s_mma, self.k, self.renormalize, out=out,
+                                            workspace=self.workspace(x.shape[0], x.device))
 
 
 def moe_route_quant_mxfp8_noalloc(x, logits, k: int, renormalize: bool = True) -> dict:

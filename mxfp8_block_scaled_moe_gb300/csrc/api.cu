@@ -75,7 +75,7 @@ const char* mxmoe_status_string(mxmoe_status s) {
   switch (s) {
     case MXMOE_OK: return "MXMOE_OK";
     case MXMOE_ERR_NULL: return "MXMOE_ERR_NULL: a required pointer is NULL";
-    case MXMOE_ERR_ALIGN: return "MXMOE_ERR_ALIGN: a pointer is not 16-byte aligned";
+    case MXMOE_ERR_ALIGN: return "MXMOE_ERR_ALIGN: a pointer is misaligned (16 bytes; 32 for GEMM outputs)";
     case MXMOE_ERR_SHAPE: return "MXMOE_ERR_SHAPE: a size is out of range or inconsistent";
     case MXMOE_ERR_UNSUPPORTED: return "MXMOE_ERR_UNSUPPORTED: not supported by this build";
     case MXMOE_ERR_WORKSPACE: return "MXMOE_ERR_WORKSPACE: workspace missing or too small";
@@ -183,6 +183,7 @@ static mxmoe_status check_gemm(const uint8_t* a, const uint8_t* sa, const uint8_
   MXMOE_CHECK_PTR(a);
   MXMOE_CHECK_PTR(w);
   MXMOE_CHECK_PTR(out);
+  if ((uintptr_t)out & 31u) return MXMOE_ERR_ALIGN;  // 32-byte sector stores
   if (!sa || !sw) return MXMOE_ERR_NULL;
   if (((uintptr_t)sa & 3u) || ((uintptr_t)sw & 3u)) return MXMOE_ERR_ALIGN;
   return MXMOE_OK;
@@ -224,30 +225,35 @@ mxmoe_status moe_finalize_routing(const uint16_t* y, const float* topk_w,
 }
 
 // Workspace of the whole layer, in this order (each 256-byte aligned):
-// xq [M,H] | xs [M,H/32] | topk_ids [T,k] | topk_w [T,k] | sorted_to_src [M] |
-// src_to_sorted [M] | counts [E] | offsets [E+1] | route histograms |
-// aq [M,I] | as [M,I/32] | y [M,H] bf16
+// xq [M,H] | xs tiled | topk_ids [T,k] | topk_w [T,k] | sorted_to_src [M] |
+// src_to_sorted [M] | counts [E] | offsets [E+1] | tile bases [E+1] |
+// route histograms | aq [M,I] | as tiled | y [M,H] bf16 | w13s tiled | w2s tiled.
+// Tiled activation scales hold at most ceil(M/128) + E row blocks.
 struct FwdLayout {
-  size_t xq, xs, ids, w, s2s, src2s, counts, offs, hist, aq, as, y, total;
+  size_t xq, xs, ids, w, s2s, src2s, counts, offs, tbase, hist, aq, as, y, w13s, w2s, total;
 };
 
 static FwdLayout fwd_layout(int T, int H, int E, int k, int I) {
   FwdLayout L;
   const size_t M = (size_t)T * k;
+  const size_t blocks = (M + 127) / 128 + (size_t)E;
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o += align256(bytes); return at; };
   L.xq = take(M * H);
-  L.xs = take(M * (H / 32));
+  L.xs = take(blocks * 128 * (H / 32));
   L.ids = take(M * 4);
   L.w = take(M * 4);
   L.s2s = take(M * 4);
   L.src2s = take(M * 4);
   L.counts = take((size_t)E * 8);
   L.offs = take((size_t)(E + 1) * 8);
+  L.tbase = take((size_t)(E + 1) * 4);
   L.hist = take(route_workspace_bytes(T, E));
   L.aq = take(M * I);
-  L.as = take(M * (I / 32));
+  L.as = take(blocks * 128 * (I / 32));
   L.y = take(M * H * 2);
+  L.w13s = take((size_t)E * 2 * I * (H / 32));
+  L.w2s = take((size_t)E * H * (I / 32));
   L.total = o;
   return L;
 }
@@ -257,10 +263,71 @@ size_t moe_forward_mxfp8_workspace_size(int T, int H, int E, int k, int I) {
   return fwd_layout(T, H, E, k, I).total;
 }
 
-mxmoe_status moe_forward_mxfp8(const uint16_t* x, const float* logits, const uint8_t* w13q,
-                               const uint8_t* w13s, const uint8_t* w2q, const uint8_t* w2s,
-                               int T, int H, int E, int k, int I, int renormalize,
-                               uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+mxmoe_status mx_scales_to_mma_layout(const uint8_t* scale, int64_t E, int64_t N, int64_t K,
+                                     uint8_t* out, void* stream) {
+  if (E < 0 || N < 0 || K <= 0) return MXMOE_ERR_SHAPE;
+  if (N % 128 != 0 || K % 128 != 0) return MXMOE_ERR_UNSUPPORTED;
+  if (E == 0 || N == 0) return MXMOE_OK;
+  MXMOE_CHECK_PTR(scale);
+  MXMOE_CHECK_PTR(out);
+  return from_cuda(launch_scales_to_tiled(scale, E * N, K, out, (cudaStream_t)stream));
+}
+
+// Opt-in per-kernel timing of the layer call: events recorded on the call's
+// stream between its kernels (one set per device, reused by every call).
+namespace {
+constexpr int kProfEvents = 6;
+std::atomic<int> g_prof_enabled{0};
+cudaEvent_t g_prof_ev[kMaxDevices][kProfEvents] = {};
+bool g_prof_valid[kMaxDevices] = {false};
+
+struct LayerProfiler {
+  int dev = -1;
+  bool on = false;
+  cudaStream_t s;
+  explicit LayerProfiler(cudaStream_t st) : s(st) {
+    if (!g_prof_enabled.load()) return;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return;
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int i = 0; i < kProfEvents; ++i)
+      if (!g_prof_ev[dev][i] && cudaEventCreate(&g_prof_ev[dev][i]) != cudaSuccess) return;
+    g_prof_valid[dev] = false;
+    on = true;
+  }
+  void mark(int i) {
+    if (on) cudaEventRecord(g_prof_ev[dev][i], s);
+  }
+  void done() {
+    if (on) g_prof_valid[dev] = true;
+  }
+};
+}  // namespace
+
+mxmoe_status mxmoe_layer_profile_enable(int enable) {
+  g_prof_enabled.store(enable ? 1 : 0);
+  return MXMOE_OK;
+}
+
+mxmoe_status mxmoe_layer_profile_read(float* ms, int n) {
+  if (!ms || n < 1) return MXMOE_ERR_NULL;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MXMOE_ERR_CUDA;
+  if (!g_prof_valid[dev]) return MXMOE_ERR_UNSUPPORTED;
+  if (cudaEventSynchronize(g_prof_ev[dev][kProfEvents - 1]) != cudaSuccess) return MXMOE_ERR_CUDA;
+  for (int i = 0; i < n && i < kProfEvents - 1; ++i) {
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, g_prof_ev[dev][i], g_prof_ev[dev][i + 1]) != cudaSuccess)
+      return MXMOE_ERR_CUDA;
+    ms[i] = t;
+  }
+  return MXMOE_OK;
+}
+
+static mxmoe_status forward_impl(const uint16_t* x, const float* logits, const uint8_t* w13q,
+                                 const uint8_t* w13s, const uint8_t* w2q, const uint8_t* w2s,
+                                 bool mma_scales, int T, int H, int E, int k, int I,
+                                 int renormalize, uint16_t* out, void* ws, size_t ws_bytes,
+                                 void* stream) {
   if (T < 0 || H <= 0 || E <= 0 || k < 1 || k > 32 || k > E || I <= 0) return MXMOE_ERR_SHAPE;
   if (E > 256 || H % 128 != 0 || I % 128 != 0) return MXMOE_ERR_UNSUPPORTED;
   if ((int64_t)T * k >= (1ll << 31)) return MXMOE_ERR_SHAPE;
@@ -271,6 +338,8 @@ mxmoe_status moe_forward_mxfp8(const uint16_t* x, const float* logits, const uin
   MXMOE_CHECK_PTR(w2q);
   MXMOE_CHECK_PTR(out);
   if (!w13s || !w2s) return MXMOE_ERR_NULL;
+  if (mma_scales && (!aligned16(w13s) || !aligned16(w2s))) return MXMOE_ERR_ALIGN;
+  if (!mma_scales && (((uintptr_t)w13s & 3u) || ((uintptr_t)w2s & 3u))) return MXMOE_ERR_ALIGN;
   if (!ws) return MXMOE_ERR_WORKSPACE;
   if ((uintptr_t)ws & 255u) return MXMOE_ERR_ALIGN;
   const FwdLayout L = fwd_layout(T, H, E, k, I);
@@ -286,18 +355,57 @@ mxmoe_status moe_forward_mxfp8(const uint16_t* x, const float* logits, const uin
   int32_t* src2s = (int32_t*)(b + L.src2s);
   int64_t* counts = (int64_t*)(b + L.counts);
   int64_t* offs = (int64_t*)(b + L.offs);
+  int32_t* tbase = (int32_t*)(b + L.tbase);
   uint8_t* aq = b + L.aq;
   uint8_t* as = b + L.as;
   uint16_t* y = (uint16_t*)(b + L.y);
-  cudaError_t e = launch_route(x, logits, T, H, E, k, renormalize != 0, true, xq, xs, nullptr,
-                               ids, w, s2s, src2s, counts, offs, (int32_t*)(b + L.hist), s);
+  const uint8_t* w13s_t = w13s;
+  const uint8_t* w2s_t = w2s;
+  cudaError_t e;
+  LayerProfiler prof(s);
+  prof.mark(0);
+  if (!mma_scales) {
+    e = launch_scales_to_tiled(w13s, (int64_t)E * 2 * I, H, b + L.w13s, s);
+    if (e != cudaSuccess) return MXMOE_ERR_CUDA;
+    e = launch_scales_to_tiled(w2s, (int64_t)E * H, I, b + L.w2s, s);
+    if (e != cudaSuccess) return MXMOE_ERR_CUDA;
+    w13s_t = b + L.w13s;
+    w2s_t = b + L.w2s;
+  }
+  prof.mark(1);
+  e = launch_route(x, logits, T, H, E, k, renormalize != 0, true, xq, xs, nullptr, ids, w, s2s,
+                   src2s, counts, offs, (int32_t*)(b + L.hist), s, tbase);
   if (e != cudaSuccess) return MXMOE_ERR_CUDA;
-  e = launch_gemm_swiglu_quant(xq, xs, w13q, w13s, offs, M, E, H, I, aq, as, s);
+  prof.mark(2);
+  e = launch_gemm_swiglu_quant(xq, xs, w13q, w13s_t, offs, M, E, H, I, aq, as, s, true);
   if (e != cudaSuccess) return MXMOE_ERR_CUDA;
-  e = launch_gemm_bf16(aq, as, w2q, w2s, offs, M, E, I, H, y, s);
+  prof.mark(3);
+  e = launch_gemm_bf16(aq, as, w2q, w2s_t, offs, M, E, I, H, y, s, true);
   if (e != cudaSuccess) return MXMOE_ERR_CUDA;
+  prof.mark(4);
   e = launch_finalize(y, w, src2s, T, k, H, out, s);
-  return from_cuda(e);
+  if (e != cudaSuccess) return MXMOE_ERR_CUDA;
+  prof.mark(5);
+  prof.done();
+  return MXMOE_OK;
+}
+
+mxmoe_status moe_forward_mxfp8(const uint16_t* x, const float* logits, const uint8_t* w13q,
+                               const uint8_t* w13s, const uint8_t* w2q, const uint8_t* w2s,
+                               int T, int H, int E, int k, int I, int renormalize,
+                               uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+  return forward_impl(x, logits, w13q, w13s, w2q, w2s, false, T, H, E, k, I, renormalize, out, ws,
+                      ws_bytes, stream);
+}
+
+mxmoe_status moe_forward_mxfp8_mma_scales(const uint16_t* x, const float* logits,
+                                          const uint8_t* w13q, const uint8_t* w13s_mma,
+                                          const uint8_t* w2q, const uint8_t* w2s_mma, int T,
+                                          int H, int E, int k, int I, int renormalize,
+                                          uint16_t* out, void* ws, size_t ws_bytes,
+                                          void* stream) {
+  return forward_impl(x, logits, w13q, w13s_mma, w2q, w2s_mma, true, T, H, E, k, I, renormalize,
+                      out, ws, ws_bytes, stream);
 }
 
 }  // extern "C"

@@ -52,6 +52,13 @@ __device__ __forceinline__ uint32_t cvt_e4m3x4(float v0, float v1, float v2, flo
   return cvt_e4m3x2(v0, v1) | (cvt_e4m3x2(v2, v3) << 16);
 }
 
+// Two fp32 -> packed bf16x2 (lo in bits 0..15), round to nearest even.
+__device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t umax(uint32_t a, uint32_t b) { return a > b ? a : b; }
 
 // |x| bit pattern of a bf16 pair packed in a 32-bit word, as two fp32 patterns' max.
@@ -75,6 +82,13 @@ __device__ __forceinline__ void st_v4(void* p, uint4 v) {
 __device__ __forceinline__ void st_cs_v4(void* p, uint4 v) {
   asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" :: "l"(p), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w) : "memory");
+}
+
+// 32-byte (one full sector) global store; the address must be 32-byte aligned.
+__device__ __forceinline__ void st_v8(void* p, const uint32_t (&v)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
 }
 
 // Record the first device-side error in the library's status word.

@@ -7,7 +7,7 @@
 //        GroupedMatmulSwigluQuant; "Quantization on Ascend", MoE "Forward").
 //   gmm2 (grouped_gemm_mxfp8): y[r] = aq[r] . w2[e]^T, bf16 out.
 //
-// Design (one persistent CTA per SM, 192 threads, warp-specialized):
+// Design (one persistent CTA per SM, 576 threads, warp-specialized):
 //   warp 0      producer: TMA (128B swizzle) loads of the A tile [128 x 128]
 //               and the B tile [BN x 128] e4m3, plus cp.async of the e8m0
 //               scales into the tensor-core scale-factor staging layout;
@@ -17,8 +17,10 @@
 //               tcgen05.mma.kind::mxf8f6f4.block_scale (M=128, N=BN, K=32,
 //               UE8M0 scales, one scale per 32 K-elements) accumulate the
 //               fp32 tile in tensor memory; tcgen05.commit frees the stage.
-//   warps 2-5   epilogue: tcgen05.ld the accumulator (one thread per row),
-//               SwiGLU + MX requant (gmm1) or bf16 rounding (gmm2), store.
+//   warps 2-17  epilogue: tcgen05.ld the accumulator into registers (one
+//               thread per row and a quarter of the columns), release it to the
+//               MMA warp, then SwiGLU + MX requant (gmm1) or bf16 rounding
+//               (gmm2) and the stores, overlapping the next tile's mainloop.
 // Tiles are scheduled per expert from the device-side offsets: the CTA reads
 // offsets[0..E], builds the prefix of per-expert tile counts in shared
 // memory and walks tiles blockIdx.x, blockIdx.x + gridDim.x, ...  A tile that
@@ -40,6 +42,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tiled_scales.h"
 
 namespace mxmoe {
 namespace gemm {
@@ -47,7 +50,9 @@ namespace gemm {
 constexpr int BM = 128;         // rows of A per tile (tokens)
 constexpr int BK = 128;         // K elements (= bytes) per stage
 constexpr int STAGES = 4;
-constexpr int THREADS = 192;
+constexpr int EPI_WARPS = 16;  // epilogue warps (a multiple of 4)
+constexpr int EPI_GROUPS = EPI_WARPS / 4;
+constexpr int THREADS = 64 + 32 * EPI_WARPS;  // producer, MMA, epilogue
 constexpr int MAX_E = 256;
 constexpr int TMEM_COLS = 512;
 constexpr int SF_COL0 = 256;    // scale factors after the accumulator
@@ -71,16 +76,17 @@ struct Layout {
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;   // tmem addr, abort flag
   static constexpr int OFF_OFFS = OFF_MISC + 16;            // int64 offsets [E+1]
   static constexpr int OFF_TS = OFF_OFFS + (MAX_E + 1) * 8; // int tile_start [E+1]
-  static constexpr int BYTES = OFF_TS + (MAX_E + 1) * 4;
+  static constexpr int OFF_MTB = OFF_TS + (MAX_E + 1) * 4;  // int m-tile base [E+1]
+  static constexpr int BYTES = OFF_MTB + (MAX_E + 1) * 4;
   static constexpr int ALLOC = BYTES + 1024;                // 1 KB alignment slack
 };
 
 struct Params {
-  const uint8_t* sfa;        // [M, K/32]
-  const uint8_t* sfb;        // [E * Nw, K/32]
+  const uint8_t* sfa;        // [M, K/32], or tiled (tiled_scales.h)
+  const uint8_t* sfb;        // [E * Nw, K/32], or tiled
   const int64_t* offsets;    // [E+1]
   void* out;                 // aq [M, n_out] e4m3 or y [M, n_out] bf16
-  uint8_t* out_scale;        // as [M, n_out/32] (gmm1)
+  uint8_t* out_scale;        // as [M, n_out/32] (gmm1), or tiled
   int64_t M;
   int E, K, Nw, n_out, n_tiles_n;
   int* status;
@@ -119,6 +125,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
@@ -229,9 +243,28 @@ __device__ __forceinline__ void decode_tile(int tile, const int* ts, int E, int 
   nt = local - mt * n_tiles_n;
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+// silu(g) * u = g * u / (1 + e^-g), with e^-g = 2^(-g * log2 e) on the
+// hardware ex2 unit and the reciprocal on rcp.approx (relative error of a few
+// fp32 ulp; e^-g -> inf gives 0, e^-g -> 0 gives g * u).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float swiglu(float g, float u) {
+  const float e = ex2_approx(-1.4426950408889634f * g);
+  return (g * u) * rcp_approx(1.0f + e);
+}
 
-template <int BN, bool kSwiglu>
+// kTiledSF: all scales (A, B and gmm1's output scales) use the tiled layout
+// of tiled_scales.h and each stage's scale chunks arrive by bulk copy;
+// otherwise they are the row-major [rows, K/32] arrays, staged by cp.async.
+template <int BN, bool kSwiglu, bool kTiledSF>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const Params p) {
@@ -246,6 +279,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
   int64_t* s_off = reinterpret_cast<int64_t*>(smem + L::OFF_OFFS);
   int* s_ts = reinterpret_cast<int*>(smem + L::OFF_TS);
+  int* s_mtb = reinterpret_cast<int*>(smem + L::OFF_MTB);
   auto bar_full = [&](int s) { return sbase + L::OFF_BAR + 8u * s; };
   auto bar_empty = [&](int s) { return sbase + L::OFF_BAR + 8u * (STAGES + s); };
   const uint32_t bar_acc_full = sbase + L::OFF_BAR + 8u * (2 * STAGES);
@@ -256,11 +290,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   // ---- set-up: barriers, TMEM, tile schedule
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar_full(s), 1 + 32);  // producer expect_tx + 32 cp.async arrivals
+      // producer expect_tx (+ 32 cp.async arrivals when scales come by cp.async)
+      mbar_init(bar_full(s), kTiledSF ? 1 : 1 + 32);
       mbar_init(bar_empty(s), 1);      // tcgen05.commit
     }
     mbar_init(bar_acc_full, 1);
-    mbar_init(bar_acc_empty, 4);       // one arrive per epilogue warp
+    mbar_init(bar_acc_empty, EPI_WARPS);  // one arrive per epilogue warp
     mbar_init(bar_drain, 1);
     *s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -275,9 +310,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   if (warp == 2) {
     // per-expert tile counts -> exclusive prefix (E <= 256: 8 experts per lane)
+    // and of m-tile counts (the tiled scale layout's per-expert block base)
     constexpr int PER = MAX_E / 32;
-    int cnt[PER];
-    int run = 0;
+    int cnt[PER], mcnt[PER];
+    int run = 0, mrun = 0;
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
       const int e = lane * PER + i;
@@ -286,24 +322,27 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int64_t o0 = p.offsets[e], o1 = p.offsets[e + 1];
         s_off[e] = o0;
         if (e == E - 1) s_off[E] = o1;
-        c = (int)((o1 - o0 + BM - 1) / BM) * p.n_tiles_n;
+        c = (int)((o1 - o0 + BM - 1) / BM);
       }
       cnt[i] = run;
-      run += c;
+      mcnt[i] = mrun;
+      run += c * p.n_tiles_n;
+      mrun += c;
     }
-    int incl = run;
+    int incl = run, mincl = mrun;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const int o = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += o;
+      const int mo = __shfl_up_sync(0xffffffffu, mincl, off);
+      if (lane >= off) { incl += o; mincl += mo; }
     }
-    const int excl = incl - run;
+    const int excl = incl - run, mexcl = mincl - mrun;
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
       const int e = lane * PER + i;
-      if (e < E) s_ts[e] = excl + cnt[i];
+      if (e < E) { s_ts[e] = excl + cnt[i]; s_mtb[e] = mexcl + mcnt[i]; }
     }
-    if (lane == 31) s_ts[E] = incl;
+    if (lane == 31) { s_ts[E] = incl; s_mtb[E] = mincl; }
   }
   tc_fence_before();
   __syncthreads();
@@ -332,8 +371,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         const uint32_t sA = sbase + L::OFF_A + stage * L::A_BYTES;
         const uint32_t sB = sbase + L::OFF_B + stage * L::B_BYTES;
+        const uint32_t sSFA = sbase + L::OFF_SFA + stage * L::SFA_BYTES;
+        const uint32_t sSFB = sbase + L::OFF_SFB + stage * L::SFB_BYTES;
         if (lane == 0) {
-          mbar_arrive_expect_tx(bar_full(stage), L::A_BYTES + L::B_BYTES);
+          mbar_arrive_expect_tx(bar_full(stage), L::A_BYTES + L::B_BYTES +
+                                                     (kTiledSF ? L::SFA_BYTES + L::SFB_BYTES : 0));
           tma_load_2d(sA, &tmA, kt * BK, (int)row0, bar_full(stage));
           if (kSwiglu) {
             tma_load_2d(sB, &tmB, kt * BK, (int)(brow + (int64_t)nt * (BN / 2)), bar_full(stage));
@@ -342,11 +384,25 @@ __global__ void __launch_bounds__(THREADS, 1)
           } else {
             tma_load_2d(sB, &tmB, kt * BK, (int)(brow + (int64_t)nt * BN), bar_full(stage));
           }
+          if (kTiledSF) {
+            // one 512-byte chunk per 128 rows: A's m-tile block, B's row blocks
+            bulk_copy_g2s(sSFA, p.sfa + ((int64_t)(s_mtb[e] + mt) * KT + kt) * 512, 512,
+                          bar_full(stage));
+#pragma unroll
+            for (int c = 0; c < BN / 128; ++c) {
+              int64_t wrow;
+              if (kSwiglu)
+                wrow = c == 0 ? brow + (int64_t)nt * (BN / 2) : brow + p.n_out + (int64_t)nt * (BN / 2);
+              else
+                wrow = brow + (int64_t)nt * BN + 128 * c;
+              bulk_copy_g2s(sSFB + 512 * c, p.sfb + ((wrow >> 7) * KT + kt) * 512, 512,
+                            bar_full(stage));
+            }
+          }
         }
         // scale factors: 4 bytes (4 K-blocks) per row, staged as
         // byte(r, kb) = (r % 32) * 16 + (r / 32) * 4 + kb per 128-row chunk
-        const uint32_t sSFA = sbase + L::OFF_SFA + stage * L::SFA_BYTES;
-        const uint32_t sSFB = sbase + L::OFF_SFB + stage * L::SFB_BYTES;
+        if (!kTiledSF) {
 #pragma unroll
         for (int i = 0; i < BM / 32; ++i) {
           const int r = lane + 32 * i;
@@ -369,6 +425,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                      p.sfb + wrow * K32 + kt * 4, 4u);
         }
         cp_async_mbar_arrive_noinc(bar_full(stage));
+        }
         armed |= 1u << stage;
         if (phase) armed_parity |= 1u << stage; else armed_parity &= ~(1u << stage);
         if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -402,7 +459,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             ok = false;
             break;
           }
-          fence_proxy_async_smem();  // cp.async-written scales -> async proxy
+          if (!kTiledSF) fence_proxy_async_smem();  // cp.async-written scales -> async proxy
           tc_fence_after();
           const uint32_t sA = sbase + L::OFF_A + stage * L::A_BYTES;
           const uint32_t sB = sbase + L::OFF_B + stage * L::B_BYTES;
@@ -438,10 +495,21 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     __syncwarp();
   } else {
-    // ================= epilogue (warps 2..5 -> TMEM lane quarters 2,3,0,1)
+    // ================= epilogue: EPI_WARPS warps, EPI_GROUPS per TMEM lane
+    // quarter (warp & 3 = quarter; group g takes the g-th slice of the
+    // columns).  Each thread drains its row's slice of the accumulator into
+    // registers, releases the accumulator to the MMA warp at once, and only
+    // then does the math and the stores, so the epilogue of tile i overlaps
+    // the mainloop of tile i+1.
     const int q = warp & 3;
+    const int grp = (warp - 2) >> 2;
     const int row = q * 32 + lane;
     const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
+    // columns per thread: SwiGLU -> GC gate + GC up columns; plain -> PC
+    constexpr int GC = BN / 2 / EPI_GROUPS;
+    constexpr int PC = BN / EPI_GROUPS;
+    constexpr int CH = kSwiglu ? 2 * (GC / 32) : PC / 32;  // 32-column chunks
+    static_assert(kSwiglu ? GC % 32 == 0 : PC % 32 == 0, "epilogue slices are whole 32-column chunks");
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
       int e, mt, nt;
@@ -451,20 +519,32 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool got = wait_bar(bar_acc_full, acc_phase, p.wait_limit, p.status, s_abort);
       if (!__all_sync(0xffffffffu, got)) break;  // keep the warp converged
       tc_fence_after();
+      uint32_t v[CH][32];
       if (kSwiglu) {
-        constexpr int HALF = BN / 2;
+        // gate columns [grp*GC, +GC), up columns BN/2 + the same
+#pragma unroll
+        for (int c = 0; c < CH / 2; ++c) {
+          tmem_ld_32(t_row + grp * GC + c * 32, v[c]);
+          tmem_ld_32(t_row + BN / 2 + grp * GC + c * 32, v[CH / 2 + c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < CH; ++c) tmem_ld_32(t_row + grp * PC + c * 32, v[c]);
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_acc_empty);
+      acc_phase ^= 1;
+      if (kSwiglu) {
         uint8_t* aq = reinterpret_cast<uint8_t*>(p.out);
-#pragma unroll 1
-        for (int c = 0; c < HALF / 32; ++c) {
-          uint32_t g[32], u[32];
-          tmem_ld_32(t_row + c * 32, g);
-          tmem_ld_32(t_row + HALF + c * 32, u);
-          tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < CH / 2; ++c) {
           float a[32];
           uint32_t m = 0;
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            a[i] = silu_f(__uint_as_float(g[i])) * __uint_as_float(u[i]);
+            a[i] = swiglu(__uint_as_float(v[c][i]), __uint_as_float(v[CH / 2 + c][i]));
             m = umax(m, __float_as_uint(a[i]) & 0x7FFFFFFFu);
           }
           const uint32_t sb = e8m0_from_amax_bits(m);
@@ -475,36 +555,30 @@ __global__ void __launch_bounds__(THREADS, 1)
             o[i] = cvt_e4m3x4(a[4 * i] * inv, a[4 * i + 1] * inv, a[4 * i + 2] * inv,
                               a[4 * i + 3] * inv);
           if (valid) {
-            uint8_t* dst = aq + grow * p.n_out + (int64_t)nt * HALF + c * 32;
-            st_v4(dst, make_uint4(o[0], o[1], o[2], o[3]));
-            st_v4(dst + 16, make_uint4(o[4], o[5], o[6], o[7]));
-            p.out_scale[grow * (p.n_out / 32) + (int64_t)nt * (HALF / 32) + c] = (uint8_t)sb;
+            const int64_t col = (int64_t)nt * (BN / 2) + grp * GC + c * 32;
+            st_v8(aq + grow * p.n_out + col, o);
+            if (kTiledSF)
+              p.out_scale[tiled_scale_offset((int64_t)(s_mtb[e] + mt) * BM + row, (int)(col >> 5),
+                                             p.n_out / 128)] = (uint8_t)sb;
+            else
+              p.out_scale[grow * (p.n_out / 32) + (col >> 5)] = (uint8_t)sb;
           }
         }
       } else {
         uint16_t* y = reinterpret_cast<uint16_t*>(p.out);
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld_32(t_row + c * 32, v);
-          tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
           uint32_t o[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            o[i] = float_to_bf16_bits(__uint_as_float(v[2 * i])) |
-                   (float_to_bf16_bits(__uint_as_float(v[2 * i + 1])) << 16);
+            o[i] = cvt_bf16x2(__uint_as_float(v[c][2 * i]), __uint_as_float(v[c][2 * i + 1]));
           if (valid) {
-            uint16_t* dst = y + grow * p.n_out + (int64_t)nt * BN + c * 32;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              st_v4(dst + 8 * i, make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]));
+            uint16_t* dst = y + grow * p.n_out + (int64_t)nt * BN + grp * PC + c * 32;
+            st_v8(dst, *reinterpret_cast<const uint32_t(*)[8]>(&o[0]));
+            st_v8(dst + 16, *reinterpret_cast<const uint32_t(*)[8]>(&o[8]));
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_acc_empty);
-      acc_phase ^= 1;
     }
   }
 
@@ -550,7 +624,7 @@ static bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t 
   return r == CUDA_SUCCESS;
 }
 
-template <int BN, bool kSwiglu>
+template <int BN, bool kSwiglu, bool kTiledSF>
 static cudaError_t launch(const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
                           const uint8_t* sfb, const int64_t* offsets, int64_t M, int E, int K,
                           int Nw, int n_out, void* out, uint8_t* out_scale, cudaStream_t stream) {
@@ -575,7 +649,7 @@ static cudaError_t launch(const uint8_t* a, const uint8_t* sfa, const uint8_t* b
   p.n_tiles_n = kSwiglu ? n_out / (BN / 2) : n_out / BN;
   p.status = device_status_ptr();
   p.wait_limit = wait_limit_cycles();
-  auto kern = grouped_gemm_kernel<BN, kSwiglu>;
+  auto kern = grouped_gemm_kernel<BN, kSwiglu, kTiledSF>;
   static int configured_dev = -1;  // smem attribute is per device
   int dev = 0;
   cudaGetDevice(&dev);
@@ -596,16 +670,29 @@ static cudaError_t launch(const uint8_t* a, const uint8_t* sfa, const uint8_t* b
 cudaError_t launch_gemm_swiglu_quant(const uint8_t* xq, const uint8_t* xs, const uint8_t* w13q,
                                      const uint8_t* w13s, const int64_t* offsets, int64_t M,
                                      int E, int H, int I, uint8_t* aq, uint8_t* as,
-                                     cudaStream_t stream) {
-  return gemm::launch<256, true>(xq, xs, w13q, w13s, offsets, M, E, H, 2 * I, I, aq, as, stream);
+                                     cudaStream_t stream, bool tiled_scales) {
+  if (tiled_scales)
+    return gemm::launch<256, true, true>(xq, xs, w13q, w13s, offsets, M, E, H, 2 * I, I, aq, as,
+                                         stream);
+  return gemm::launch<256, true, false>(xq, xs, w13q, w13s, offsets, M, E, H, 2 * I, I, aq, as,
+                                        stream);
 }
 
 cudaError_t launch_gemm_bf16(const uint8_t* aq, const uint8_t* as, const uint8_t* w2q,
                              const uint8_t* w2s, const int64_t* offsets, int64_t M, int E,
-                             int I, int H, uint16_t* y, cudaStream_t stream) {
-  if (H % 256 == 0)
-    return gemm::launch<256, false>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y, nullptr, stream);
-  return gemm::launch<128, false>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y, nullptr, stream);
+                             int I, int H, uint16_t* y, cudaStream_t stream, bool tiled_scales) {
+  if (H % 256 == 0) {
+    if (tiled_scales)
+      return gemm::launch<256, false, true>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y, nullptr,
+                                            stream);
+    return gemm::launch<256, false, false>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y, nullptr,
+                                           stream);
+  }
+  if (tiled_scales)
+    return gemm::launch<128, false, true>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y, nullptr,
+                                          stream);
+  return gemm::launch<128, false, false>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y, nullptr,
+                                         stream);
 }
 
 }  // namespace mxmoe

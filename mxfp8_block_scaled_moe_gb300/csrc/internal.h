@@ -24,7 +24,8 @@ cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, i
                          bool renormalize, bool quant, uint8_t* xq, uint8_t* xs, uint16_t* xp,
                          int32_t* topk_ids, float* topk_w, int32_t* sorted_to_src,
                          int32_t* src_to_sorted, int64_t* counts, int64_t* offsets,
-                         int32_t* block_hist, cudaStream_t stream);
+                         int32_t* block_hist, cudaStream_t stream,
+                         int32_t* tile_base = nullptr);
 
 size_t route_workspace_bytes(int T, int E);
 
@@ -32,12 +33,19 @@ cudaError_t launch_finalize(const uint16_t* y, const float* topk_w, const int32_
                             int T, int k, int H, uint16_t* out, cudaStream_t stream);
 
 // Grouped GEMMs.  Return cudaErrorInvalidValue when a tensor map can't be built.
+// tiled_scales: every scale array (inputs and gmm1's output scales) is in the
+// tiled layout of tiled_scales.h instead of [rows, K/32].
 cudaError_t launch_gemm_swiglu_quant(const uint8_t* xq, const uint8_t* xs, const uint8_t* w13q,
                                      const uint8_t* w13s, const int64_t* offsets, int64_t M,
                                      int E, int H, int I, uint8_t* aq, uint8_t* as,
-                                     cudaStream_t stream);
+                                     cudaStream_t stream, bool tiled_scales = false);
 cudaError_t launch_gemm_bf16(const uint8_t* aq, const uint8_t* as, const uint8_t* w2q,
                              const uint8_t* w2s, const int64_t* offsets, int64_t M, int E,
-                             int I, int H, uint16_t* y, cudaStream_t stream);
+                             int I, int H, uint16_t* y, cudaStream_t stream,
+                             bool tiled_scales = false);
+
+// [rows, K/32] scales -> tiled layout (rows % 128 == 0, K % 128 == 0).
+cudaError_t launch_scales_to_tiled(const uint8_t* scale, int64_t rows, int64_t K, uint8_t* out,
+                                   cudaStream_t stream);
 
 }  // namespace mxmoe

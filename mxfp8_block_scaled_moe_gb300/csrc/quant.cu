@@ -12,6 +12,7 @@
 // the partner lane holds the other half, so the block amax is one shuffle.
 #include "common.cuh"
 #include "internal.h"
+#include "tiled_scales.h"
 
 namespace mxmoe {
 
@@ -61,6 +62,34 @@ cudaError_t launch_mx_quantize(const uint16_t* x, int64_t rows, int64_t K, uint8
   const int64_t cap = (int64_t)num_sms() * 8;  // 2048 resident threads per SM
   if (blocks > cap) blocks = cap;
   mx_quantize_kernel<<<(unsigned)blocks, threads, 0, stream>>>(x, n_units, q, scale);
+  return cudaGetLastError();
+}
+
+// [rows, K/32] e8m0 scales -> the tiled layout of tiled_scales.h.  One thread
+// moves one row's 4 scale bytes of one 128-element K slice (a 4-byte word:
+// K/32 is a multiple of 4, so every word is aligned).
+__global__ void __launch_bounds__(256) scales_to_tiled_kernel(const uint32_t* __restrict__ in,
+                                                              int64_t rows, int KT,
+                                                              uint32_t* __restrict__ out) {
+  const int64_t n = rows * KT;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = i / KT;
+    const int kt = (int)(i - row * KT);
+    out[tiled_scale_offset(row, kt * 4, KT) >> 2] = in[i];
+  }
+}
+
+cudaError_t launch_scales_to_tiled(const uint8_t* scale, int64_t rows, int64_t K, uint8_t* out,
+                                   cudaStream_t stream) {
+  const int KT = (int)(K / 128);
+  const int64_t n = rows * KT;
+  if (n == 0) return cudaSuccess;
+  int64_t blocks = ceil_div(n, 256);
+  const int64_t cap = (int64_t)num_sms() * 8;
+  if (blocks > cap) blocks = cap;
+  scales_to_tiled_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+      reinterpret_cast<const uint32_t*>(scale), rows, KT, reinterpret_cast<uint32_t*>(out));
   return cudaGetLastError();
 }
 

@@ -9,9 +9,10 @@
 //
 // Three kernels, one stream:
 //   1. route_topk_rank: one warp per token picks the top-k experts (descending
-//      logit, ties -> lower id) and their softmax weights; then one warp per
-//      block ranks the block's assignments within each expert in flat order
-//      (warp match + popcount) and stores the block's per-expert histogram.
+//      logit, ties -> lower id) and their softmax weights; each 64-token block
+//      marks its tokens in a per-expert 64-bit mask, from which every
+//      assignment's rank inside the block (flat order) and the block's
+//      per-expert histogram are popcounts.
 //   2. route_scan: per-expert exclusive prefix of the block histograms (the
 //      block's base row inside each expert) and of the expert totals (offsets).
 //   3. route_permute_quant: one warp per token computes its k destination rows
@@ -24,6 +25,7 @@
 // payload (1 B) and scales (1/32 B) written; ids/weights/indices are small.
 #include "common.cuh"
 #include "internal.h"
+#include "tiled_scales.h"
 
 namespace mxmoe {
 
@@ -35,21 +37,31 @@ __device__ __forceinline__ bool better(float v, int id, float bv, int bid) {
   return v > bv || (v == bv && id < bid);
 }
 
+constexpr int kTopkThreads = 1024;
+constexpr int kTopkWarps = kTopkThreads / 32;
+static_assert(kRouteTokensPerBlock == 2 * kTopkWarps, "two tokens per warp");
+
 template <int EPL>  // logits per lane: E <= 32 * EPL
-__global__ void __launch_bounds__(kRouteThreads) route_topk_rank_kernel(
+__global__ void __launch_bounds__(kTopkThreads) route_topk_rank_kernel(
     const float* __restrict__ logits, int T, int E, int k, int renormalize,
     int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
     int32_t* __restrict__ local_rank, int32_t* __restrict__ block_hist) {
-  extern __shared__ int smem_i[];
-  int* s_cnt = smem_i;                           // [E]
-  int* s_ids = smem_i + E;                       // [kRouteTokensPerBlock * k]
+  // s_mask[e] bit tl: token tl of this block chose expert e.  A token's k
+  // experts are distinct, so its rank among the block's rows of expert e in
+  // flat (token) order is the number of earlier tokens with that bit set.
+  extern __shared__ unsigned long long s_mask[];  // [E]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t0 = blockIdx.x * kRouteTokensPerBlock;
   const int nt = min(kRouteTokensPerBlock, T - t0);
 
-  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_mask[e] = 0ull;
+  __syncthreads();
 
-  for (int tl = warp; tl < nt; tl += kRouteWarps) {
+  int chosen[2] = {0, 0};
+#pragma unroll
+  for (int it = 0; it < 2; ++it) {
+    const int tl = warp + kTopkWarps * it;
+    if (tl >= nt) break;  // warp-uniform
     const int t = t0 + tl;
     const float* row = logits + (int64_t)t * E;
     float v[EPL];
@@ -87,51 +99,41 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_rank_kernel(
       for (int off = 16; off > 0; off >>= 1) ej += __shfl_xor_sync(0xffffffffu, ej, off);
       denom = ej;
     } else {
-      float s = 0.f;
+      float sum = 0.f;
 #pragma unroll
       for (int i = 0; i < EPL; ++i) {
         const int e = lane + 32 * i;
-        if (e < E) s += expf(v[i] - vmax);
+        if (e < E) sum += expf(v[i] - vmax);
       }
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-      denom = s;
+      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      denom = sum;
     }
     if (lane < k) {
       topk_ids[(int64_t)t * k + lane] = my_id;
       topk_w[(int64_t)t * k + lane] = expf(my_val - vmax) / denom;
-      s_ids[tl * k + lane] = my_id;
+      atomicOr(&s_mask[my_id], 1ull << tl);
     }
+    chosen[it] = my_id;
   }
   __syncthreads();
-
-  // stable per-expert rank of the block's assignments, in flat order
-  if (warp == 0) {
-    const int na = nt * k;
-    for (int c = 0; c < na; c += 32) {
-      const int f = c + lane;
-      const bool valid = f < na;
-      const int e = valid ? s_ids[f] : -1;
-      const uint32_t peers = __match_any_sync(0xffffffffu, e);
-      const int leader = __ffs(peers) - 1;
-      const int base = valid ? s_cnt[e] : 0;
-      const int rank = base + __popc(peers & ((1u << lane) - 1u));
-      __syncwarp();
-      if (valid && lane == leader) s_cnt[e] = base + __popc(peers);
-      __syncwarp();
-      if (valid) local_rank[(int64_t)t0 * k + f] = rank;
-    }
+#pragma unroll
+  for (int it = 0; it < 2; ++it) {
+    const int tl = warp + kTopkWarps * it;
+    if (tl < nt && lane < k)
+      local_rank[(int64_t)(t0 + tl) * k + lane] =
+          __popcll(s_mask[chosen[it]] & ((1ull << tl) - 1ull));
   }
-  __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x)
-    block_hist[(int64_t)blockIdx.x * E + e] = s_cnt[e];
+    block_hist[(int64_t)blockIdx.x * E + e] = __popcll(s_mask[e]);
 }
 
 // One block of 1024 threads.  G = 1024 / E thread groups split the routing
 // blocks; hist[b][e] becomes the exclusive prefix over blocks of expert e.
 __global__ void __launch_bounds__(1024) route_scan_kernel(int32_t* __restrict__ hist, int nb,
                                                           int E, int64_t* __restrict__ counts,
-                                                          int64_t* __restrict__ offsets) {
+                                                          int64_t* __restrict__ offsets,
+                                                          int32_t* __restrict__ tile_base) {
   extern __shared__ int smem_i[];
   const int G = max(1, (int)(blockDim.x / E));
   int* s_part = smem_i;          // [G][E]
@@ -193,16 +195,47 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int32_t* __restrict__ 
     offsets[tid] = excl;
     if (tid == E - 1) offsets[E] = excl + v;
   }
+  if (tile_base == nullptr) return;
+  // exclusive prefix of the experts' 128-row tile counts (tiled scale layout)
+  __syncthreads();
+  const int tv = (v + 127) / 128;
+  int tincl = tv;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, tincl, off);
+    if (lane >= off) tincl += o;
+  }
+  if (lane == 31) s_warp[w] = tincl;
+  __syncthreads();
+  if (w == 0) {
+    int x = s_warp[lane];
+    int xi = x;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, xi, off);
+      if (lane >= off) xi += o;
+    }
+    s_warp[lane] = xi - x;
+  }
+  __syncthreads();
+  const int texcl = tincl - tv + s_warp[w];
+  if (tid < E) {
+    tile_base[tid] = texcl;
+    if (tid == E - 1) tile_base[E] = texcl + tv;
+  }
 }
 
-template <bool kQuant>
+// kTiled: xs goes to the MMA-ready tiled scale layout (tiled_scales.h)
+// instead of [M, H/32]; requires H % 128 == 0 and the experts' tile bases.
+template <bool kQuant, bool kTiled>
 __global__ void __launch_bounds__(kRouteThreads) route_permute_kernel(
     const uint16_t* __restrict__ x, int T, int H, int E, int k,
     const int32_t* __restrict__ topk_ids, const int32_t* __restrict__ block_base,
-    const int64_t* __restrict__ offsets, int32_t* __restrict__ src_to_sorted,
-    int32_t* __restrict__ sorted_to_src, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
-    uint16_t* __restrict__ xp) {
+    const int64_t* __restrict__ offsets, const int32_t* __restrict__ tile_base,
+    int32_t* __restrict__ src_to_sorted, int32_t* __restrict__ sorted_to_src,
+    uint8_t* __restrict__ xq, uint8_t* __restrict__ xs, uint16_t* __restrict__ xp) {
   __shared__ int64_t s_dest[kRouteWarps][32];
+  __shared__ int64_t s_sfrow[kRouteWarps][32];  // tiled layout: 128-row block and row
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t = blockIdx.x * kRouteWarps + warp;
   if (t >= T) return;  // warp-uniform
@@ -214,6 +247,10 @@ __global__ void __launch_bounds__(kRouteThreads) route_permute_kernel(
     src_to_sorted[f] = (int32_t)dest;
     sorted_to_src[dest] = (int32_t)f;
     s_dest[warp][lane] = dest;
+    if (kTiled) {
+      const int64_t within = dest - offsets[e];
+      s_sfrow[warp][lane] = ((int64_t)tile_base[e] + within / 128) * 128 + (within % 128);
+    }
   }
   __syncwarp();
   const uint16_t* xr = x + (int64_t)t * H;
@@ -249,7 +286,12 @@ __global__ void __launch_bounds__(kRouteThreads) route_permute_kernel(
         for (int j = 0; j < k; ++j) {
           const int64_t d = s_dest[warp][j];
           st_cs_v4(xq + d * H + c, ov);
-          if ((lane & 1) == 0) xs[d * H32 + (c >> 5)] = (uint8_t)sb;
+          if ((lane & 1) == 0) {
+            if (kTiled)
+              xs[tiled_scale_offset(s_sfrow[warp][j], c >> 5, H / 128)] = (uint8_t)sb;
+            else
+              xs[d * H32 + (c >> 5)] = (uint8_t)sb;
+          }
         }
       }
     } else if (ok) {
@@ -272,22 +314,22 @@ template <int EPL>
 static void launch_topk(int nb, size_t smem, cudaStream_t stream, const float* logits, int T,
                         int E, int k, int renorm, int32_t* ids, float* w, int32_t* rank,
                         int32_t* hist) {
-  route_topk_rank_kernel<EPL><<<nb, kRouteThreads, smem, stream>>>(logits, T, E, k, renorm, ids,
-                                                                    w, rank, hist);
+  route_topk_rank_kernel<EPL><<<nb, kTopkThreads, smem, stream>>>(logits, T, E, k, renorm, ids,
+                                                                   w, rank, hist);
 }
 
 cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, int E, int k,
                          bool renormalize, bool quant, uint8_t* xq, uint8_t* xs, uint16_t* xp,
                          int32_t* topk_ids, float* topk_w, int32_t* sorted_to_src,
                          int32_t* src_to_sorted, int64_t* counts, int64_t* offsets,
-                         int32_t* block_hist, cudaStream_t stream) {
+                         int32_t* block_hist, cudaStream_t stream, int32_t* tile_base) {
   if (T == 0) {
     cudaError_t err = cudaMemsetAsync(counts, 0, sizeof(int64_t) * E, stream);
     if (err != cudaSuccess) return err;
     return cudaMemsetAsync(offsets, 0, sizeof(int64_t) * (E + 1), stream);
   }
   const int nb = (int)ceil_div(T, kRouteTokensPerBlock);
-  const size_t smem1 = sizeof(int) * ((size_t)E + (size_t)kRouteTokensPerBlock * k);
+  const size_t smem1 = sizeof(unsigned long long) * (size_t)E;
   const int epl = (E + 31) / 32;
   const int rn = renormalize ? 1 : 0;
   // src_to_sorted holds the in-block rank between kernels 1 and 3
@@ -302,18 +344,23 @@ cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, i
 
   const int G = E >= 1024 ? 1 : 1024 / E;
   const size_t smem2 = sizeof(int) * ((size_t)G * E + E);
-  route_scan_kernel<<<1, 1024, smem2, stream>>>(block_hist, nb, E, counts, offsets);
+  route_scan_kernel<<<1, 1024, smem2, stream>>>(block_hist, nb, E, counts, offsets, tile_base);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
 
   const int nb3 = (int)ceil_div(T, kRouteWarps);
-  if (quant)
-    route_permute_kernel<true><<<nb3, kRouteThreads, 0, stream>>>(
-        x, T, H, E, k, topk_ids, block_hist, offsets, src_to_sorted, sorted_to_src, xq, xs, nullptr);
+  if (quant && tile_base)
+    route_permute_kernel<true, true><<<nb3, kRouteThreads, 0, stream>>>(
+        x, T, H, E, k, topk_ids, block_hist, offsets, tile_base, src_to_sorted, sorted_to_src, xq,
+        xs, nullptr);
+  else if (quant)
+    route_permute_kernel<true, false><<<nb3, kRouteThreads, 0, stream>>>(
+        x, T, H, E, k, topk_ids, block_hist, offsets, nullptr, src_to_sorted, sorted_to_src, xq,
+        xs, nullptr);
   else
-    route_permute_kernel<false><<<nb3, kRouteThreads, 0, stream>>>(
-        x, T, H, E, k, topk_ids, block_hist, offsets, src_to_sorted, sorted_to_src, nullptr,
-        nullptr, xp);
+    route_permute_kernel<false, false><<<nb3, kRouteThreads, 0, stream>>>(
+        x, T, H, E, k, topk_ids, block_hist, offsets, nullptr, src_to_sorted, sorted_to_src,
+        nullptr, nullptr, xp);
   return cudaGetLastError();
 }
 

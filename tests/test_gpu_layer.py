@@ -96,3 +96,64 @@ def test_layer_offline_checkpoint_235b_shape(mm):
     assert rel_frob(bits16(out), ref) <= OUT_REL_FROB
     assert finalize_bound_ok(bits16(out), y_g, r["topk_w"].cpu().numpy(),
                              r["src_to_sorted"].cpu().numpy(), shape.k) == 0.0
+
+
+def _mma_layout_numpy(s, K):
+    """Re-index [R, K/32] scales into 512-byte chunks (row block, K slice):
+    byte (r % 32) * 16 + (r // 32) * 4 + kb of chunk (row // 128, kt)."""
+    R = s.shape[0]
+    KT = K // 128
+    out = np.zeros(R * K // 32, np.uint8)
+    rows = np.arange(R)[:, None]
+    j = np.arange(K // 32)[None, :]
+    r = rows % 128
+    off = ((rows // 128) * KT + j // 4) * 512 + (r % 32) * 16 + (r // 32) * 4 + (j % 4)
+    out[off.reshape(-1)] = s.reshape(-1)
+    return out
+
+
+@pytest.mark.parametrize("E,N,K", [(1, 128, 128), (3, 256, 384), (8, 1536, 2048)])
+def test_scales_to_mma_layout(mm, E, N, K):
+    g = torch.Generator(device=DEV).manual_seed(E + N + K)
+    s = torch.randint(0, 255, (E, N, K // 32), generator=g, device=DEV, dtype=torch.int32)
+    s = s.to(torch.uint8)
+    t = mm.mx_scales_to_mma_layout(s, K)
+    torch.cuda.synchronize()
+    assert np.array_equal(u8(t).reshape(-1), _mma_layout_numpy(u8(s).reshape(E * N, -1), K))
+
+
+@pytest.mark.parametrize("cfg", ["tiny", "qwen3_30b_decode", "qwen3_30b_prefill"])
+def test_layer_entry_points_agree(mm, cfg):
+    """moe_forward_mxfp8 (canonical weight scales), moe_forward_mxfp8_mma_scales
+    and the four per-step entry points give the same bytes."""
+    shape = workloads.CONFIGS[cfg]
+    inp = workloads.make_layer(shape, DEV)
+    layer = mm.MXFP8MoELayer.from_bf16(inp["w13"], inp["w2"], shape.k)
+    del inp["w13"], inp["w2"]
+    a = mm.moe_forward_mxfp8(inp["x"], inp["logits"], layer.w13q, layer.w13s, layer.w2q,
+                             layer.w2s, shape.k)
+    b = layer(inp["x"], inp["logits"])
+    r = mm.moe_route_quant_mxfp8(inp["x"], inp["logits"], shape.k)
+    aq, as_ = mm.grouped_gemm_swiglu_quant_mxfp8(r["xq"], r["xs"], layer.w13q, layer.w13s,
+                                                 r["expert_offsets"])
+    y = mm.grouped_gemm_mxfp8(aq, as_, layer.w2q, layer.w2s, r["expert_offsets"])
+    c = mm.moe_finalize_routing(y, r["topk_w"], r["src_to_sorted"], shape.k)
+    torch.cuda.synchronize()
+    assert mm.device_status() == 0
+    assert torch.equal(a, b)
+    assert torch.equal(a, c)
+
+
+def test_layer_profile_segments(mm):
+    shape = workloads.CONFIGS["tiny"]
+    inp = workloads.make_layer(shape, DEV)
+    layer = mm.MXFP8MoELayer.from_bf16(inp["w13"], inp["w2"], shape.k)
+    mm.api.layer_profile_enable(True)
+    try:
+        layer(inp["x"], inp["logits"])
+        prof = mm.api.layer_profile_read()
+    finally:
+        mm.api.layer_profile_enable(False)
+    assert prof["weight_scale_layout"] >= 0.0
+    for key in ("route_quant", "gemm1_swiglu_quant", "gemm2", "finalize"):
+        assert prof[key] > 0.0, key
