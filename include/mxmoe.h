@@ -254,6 +254,26 @@ mxmoe_status moe_forward_mxfp8_mma_scales(const uint16_t* x, const float* logits
                                           void* stream);
 
 /*
+ * The layer on HOST buffers, with the host<->device copies overlapped with
+ * compute: the tokens are processed in n_chunks chunks (n_chunks <= 0: chunks
+ * of 4096 tokens) through three library-owned streams (copy in, compute,
+ * copy out) and two device staging slots in ws, so chunk c's layer runs while
+ * chunk c+1's inputs arrive and chunk c-1's output leaves.  Weight scales in
+ * the MMA layout (mx_scales_to_mma_layout); weights stay on the device.
+ *   x_host bf16 [T, H], logits_host fp32 [T, E], out_host bf16 [T, H]: host
+ *   memory (pinned, e.g. cudaHostAlloc, for the copies to overlap).
+ *   ws: moe_forward_mxfp8_host_workspace_size(...) bytes of device memory.
+ * The work is ordered after the caller's prior work on `stream`, and `stream`
+ * waits for the whole call (out_host is complete once `stream` is).
+ */
+size_t moe_forward_mxfp8_host_workspace_size(int T, int H, int E, int k, int I, int n_chunks);
+mxmoe_status moe_forward_mxfp8_host(const uint16_t* x_host, const float* logits_host,
+                                    const uint8_t* w13q, const uint8_t* w13s_mma,
+                                    const uint8_t* w2q, const uint8_t* w2s_mma, int T, int H,
+                                    int E, int k, int I, int renormalize, uint16_t* out_host,
+                                    int n_chunks, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Per-kernel timing of moe_forward_mxfp8 / moe_forward_mxfp8_mma_scales
  * (instrumentation, off by default; not part of the method).  While
  * enabled, each layer call records CUDA events on its stream between its
@@ -279,6 +299,15 @@ mxmoe_status mxmoe_get_device_status(int32_t* status_out, int clear);
  * Values < 1 restore the default.  Meant for tests of the timeout path.
  */
 void mxmoe_set_wait_limit_cycles(long long cycles);
+
+/*
+ * Grouped-GEMM kernel selection (not part of the method).  By default every
+ * grouped GEMM runs the 1-SM kernel.  enable != 0 sends 256-wide tiles with
+ * MMA-layout scales (the layer calls) to the 2-SM kernel (tcgen05
+ * cta_group::2 over CTA pairs) when the device can co-schedule pairs; it
+ * gives the same bytes and is kept for comparison and tests.
+ */
+void mxmoe_set_gemm_2sm(int enable);
 
 /* Library version string. */
 const char* mxmoe_version(void);

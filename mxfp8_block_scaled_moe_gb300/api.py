@@ -218,6 +218,42 @@ def moe_forward_mxfp8_mma_scales(x, logits, w13q, w13s_mma, w2q, w2s_mma, k: int
     return out
 
 
+def moe_forward_mxfp8_host_workspace_size(T: int, H: int, E: int, k: int, I: int,
+                                          n_chunks: int = 0) -> int:
+    return int(_lib.load().moe_forward_mxfp8_host_workspace_size(T, H, E, k, I, n_chunks))
+
+
+def moe_forward_mxfp8_host(x_host, logits_host, w13q, w13s_mma, w2q, w2s_mma, k: int,
+                           renormalize: bool = True, out_host=None, n_chunks: int = 0,
+                           workspace=None):
+    """The layer on host (CPU, ideally pinned) tensors, copies overlapped with compute.
+
+    Weights and their MMA-layout scales are CUDA tensors.  Returns out_host
+    (bf16 [T, H] on the host); it is complete once the current stream is.
+    """
+    w13q, w2q = _u8(w13q), _u8(w2q)
+    for t, n in ((x_host, "x_host"), (logits_host, "logits_host")):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous host tensor")
+    if x_host.dtype != torch.bfloat16 or logits_host.dtype != torch.float32:
+        raise TypeError("x_host must be bf16 and logits_host fp32")
+    for t, n in ((w13q, "w13q"), (w13s_mma, "w13s_mma"), (w2q, "w2q"), (w2s_mma, "w2s_mma")):
+        _need(t, n, torch.uint8, 3)
+    T, H = x_host.shape
+    E, N2, _ = w13q.shape
+    I = N2 // 2
+    if out_host is None:
+        out_host = torch.empty(T, H, dtype=torch.bfloat16, pin_memory=True)
+    need = moe_forward_mxfp8_host_workspace_size(T, H, E, k, I, n_chunks)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=w13q.device)
+    _lib.check("moe_forward_mxfp8_host", _lib.load().moe_forward_mxfp8_host(
+        _ptr(x_host), _ptr(logits_host), _ptr(w13q), _ptr(w13s_mma), _ptr(w2q), _ptr(w2s_mma),
+        T, H, E, k, I, int(bool(renormalize)), _ptr(out_host), int(n_chunks), _ptr(workspace),
+        workspace.numel(), _stream()))
+    return out_host
+
+
 def device_status(clear: bool = True) -> int:
     """The library's device status word (synchronizes the device)."""
     v = C.c_int32(0)
@@ -236,6 +272,11 @@ def layer_profile_read() -> dict:
     _lib.check("mxmoe_layer_profile_read", _lib.load().mxmoe_layer_profile_read(arr, 5))
     keys = ("weight_scale_layout", "route_quant", "gemm1_swiglu_quant", "gemm2", "finalize")
     return dict(zip(keys, (float(v) for v in arr)))
+
+
+def set_gemm_2sm(enable: bool = True) -> None:
+    """Send the layer's grouped GEMMs to the 2-SM kernel (default: 1-SM)."""
+    _lib.load().mxmoe_set_gemm_2sm(int(bool(enable)))
 
 
 def set_wait_limit_cycles(cycles: int) -> None:
@@ -280,6 +321,16 @@ class MXFP8MoELayer:
         if self._ws is None or self._ws.numel() < need:
             self._ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
         return self._ws
+
+    def forward_host(self, x_host, logits_host, out_host=None, n_chunks: int = 0):
+        """The layer on host tensors (copies overlapped with compute, chunked by tokens)."""
+        T = x_host.shape[0]
+        need = moe_forward_mxfp8_host_workspace_size(T, self.H, self.E, self.k, self.I, n_chunks)
+        if getattr(self, "_hws", None) is None or self._hws.numel() < need:
+            self._hws = torch.empty(max(need, 256), dtype=torch.uint8, device=self.w13q.device)
+        return moe_forward_mxfp8_host(x_host, logits_host, self.w13q, self.w13s_mma, self.w2q,
+                                      self.w2s_mma, self.k, self.renormalize, out_host=out_host,
+                                      n_chunks=n_chunks, workspace=self._hws)
 
     def __call__(self, x, logits, out=None):
         return moe_forward_mxfp8_mma_scales(x, logits, self.w13q, self.w13s_mma, self.w2q,

@@ -1,6 +1,7 @@
 // C ABI of the MXFP8 MoE library: argument validation, the device status
 // word, workspace carving and the layer orchestration (moe_forward_mxfp8).
 // The declarations and their contracts are in include/mxmoe.h.
+#include <algorithm>
 #include <atomic>
 #include <cstring>
 #include <mutex>
@@ -15,6 +16,9 @@ namespace mxmoe {
 __device__ int g_device_status = 0;
 
 static std::atomic<long long> g_wait_limit{0};
+static std::atomic<int> g_use_2sm{0};
+
+bool use_two_sm_gemm() { return g_use_2sm.load() != 0; }
 constexpr long long kDefaultWaitLimit = 1ll << 32;  // ~2 s at 2 GHz
 
 long long wait_limit_cycles() {
@@ -89,6 +93,8 @@ const char* mxmoe_status_string(mxmoe_status s) {
 const char* mxmoe_version(void) { return "mxmoe 0.1.0 (sm_103a)"; }
 
 void mxmoe_set_wait_limit_cycles(long long cycles) { g_wait_limit.store(cycles > 0 ? cycles : 0); }
+
+void mxmoe_set_gemm_2sm(int enable) { g_use_2sm.store(enable ? 1 : 0); }
 
 mxmoe_status mxmoe_get_device_status(int32_t* status_out, int clear) {
   if (!status_out) return MXMOE_ERR_NULL;
@@ -406,6 +412,128 @@ mxmoe_status moe_forward_mxfp8_mma_scales(const uint16_t* x, const float* logits
                                           void* stream) {
   return forward_impl(x, logits, w13q, w13s_mma, w2q, w2s_mma, true, T, H, E, k, I, renormalize,
                       out, ws, ws_bytes, stream);
+}
+
+// ---------------------------------------------------------------- host-buffer layer
+
+// Device staging of one chunk slot: x | logits | out | layer workspace.
+struct HostChunkLayout {
+  size_t x, logits, out, ws, ws_bytes, slot;
+};
+
+static HostChunkLayout host_chunk_layout(int Tc, int H, int E, int k, int I) {
+  HostChunkLayout L;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o += align256(bytes); return at; };
+  L.x = take((size_t)Tc * H * 2);
+  L.logits = take((size_t)Tc * E * 4);
+  L.out = take((size_t)Tc * H * 2);
+  L.ws_bytes = fwd_layout(Tc, H, E, k, I).total;
+  L.ws = take(L.ws_bytes);
+  L.slot = o;
+  return L;
+}
+
+static int host_chunk_tokens(int T, int n_chunks) {
+  if (n_chunks <= 0) n_chunks = T > 4096 ? (T + 4095) / 4096 : 1;
+  if (n_chunks > T) n_chunks = T > 0 ? T : 1;
+  return (T + n_chunks - 1) / n_chunks;
+}
+
+size_t moe_forward_mxfp8_host_workspace_size(int T, int H, int E, int k, int I, int n_chunks) {
+  if (T < 0 || H <= 0 || E <= 0 || k <= 0 || I <= 0) return 0;
+  const int Tc = host_chunk_tokens(T, n_chunks);
+  return 2 * host_chunk_layout(Tc, H, E, k, I).slot;
+}
+
+namespace {
+struct HostPipe {
+  cudaStream_t s[3] = {nullptr, nullptr, nullptr};  // h2d, compute, d2h
+  cudaEvent_t ev_in[2] = {}, ev_comp[2] = {}, ev_out[2] = {}, ev_start = {}, ev_done = {};
+  bool ok = false;
+};
+HostPipe g_pipe[kMaxDevices];
+}  // namespace
+
+static HostPipe* host_pipe() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  HostPipe& P = g_pipe[dev];
+  if (!P.ok) {
+    for (auto& st : P.s)
+      if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    cudaEvent_t* evs[] = {&P.ev_in[0], &P.ev_in[1], &P.ev_comp[0], &P.ev_comp[1],
+                          &P.ev_out[0], &P.ev_out[1], &P.ev_start, &P.ev_done};
+    for (cudaEvent_t* e : evs)
+      if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    P.ok = true;
+  }
+  return &P;
+}
+
+mxmoe_status moe_forward_mxfp8_host(const uint16_t* x_host, const float* logits_host,
+                                    const uint8_t* w13q, const uint8_t* w13s_mma,
+                                    const uint8_t* w2q, const uint8_t* w2s_mma, int T, int H,
+                                    int E, int k, int I, int renormalize, uint16_t* out_host,
+                                    int n_chunks, void* ws, size_t ws_bytes, void* stream) {
+  if (T < 0 || H <= 0 || E <= 0 || k < 1 || k > 32 || k > E || I <= 0) return MXMOE_ERR_SHAPE;
+  if (E > 256 || H % 128 != 0 || I % 128 != 0) return MXMOE_ERR_UNSUPPORTED;
+  if ((int64_t)T * k >= (1ll << 31)) return MXMOE_ERR_SHAPE;
+  if (T == 0) return MXMOE_OK;
+  if (!x_host || !logits_host || !out_host) return MXMOE_ERR_NULL;
+  MXMOE_CHECK_PTR(w13q);
+  MXMOE_CHECK_PTR(w2q);
+  MXMOE_CHECK_PTR(w13s_mma);
+  MXMOE_CHECK_PTR(w2s_mma);
+  if (!ws) return MXMOE_ERR_WORKSPACE;
+  if ((uintptr_t)ws & 255u) return MXMOE_ERR_ALIGN;
+  const int Tc = host_chunk_tokens(T, n_chunks);
+  const HostChunkLayout CL = host_chunk_layout(Tc, H, E, k, I);
+  if (ws_bytes < 2 * CL.slot) return MXMOE_ERR_WORKSPACE;
+  HostPipe* P = host_pipe();
+  if (!P) return MXMOE_ERR_CUDA;
+  cudaStream_t user = (cudaStream_t)stream;
+  auto ck = [](cudaError_t e) { return e == cudaSuccess; };
+  if (!ck(cudaEventRecord(P->ev_start, user))) return MXMOE_ERR_CUDA;
+  for (auto st : P->s)
+    if (!ck(cudaStreamWaitEvent(st, P->ev_start, 0))) return MXMOE_ERR_CUDA;
+  uint8_t* base = (uint8_t*)ws;
+  int c = 0;
+  for (int t0 = 0; t0 < T; t0 += Tc, ++c) {
+    const int tc = std::min(Tc, T - t0);
+    const int slot = c & 1;
+    uint8_t* sb = base + (size_t)slot * CL.slot;
+    uint16_t* xd = (uint16_t*)(sb + CL.x);
+    float* ld = (float*)(sb + CL.logits);
+    uint16_t* od = (uint16_t*)(sb + CL.out);
+    // h2d: the slot's inputs are free once chunk c-2's compute is done
+    if (c >= 2 && !ck(cudaStreamWaitEvent(P->s[0], P->ev_comp[slot], 0))) return MXMOE_ERR_CUDA;
+    if (!ck(cudaMemcpyAsync(xd, x_host + (size_t)t0 * H, (size_t)tc * H * 2,
+                            cudaMemcpyHostToDevice, P->s[0])) ||
+        !ck(cudaMemcpyAsync(ld, logits_host + (size_t)t0 * E, (size_t)tc * E * 4,
+                            cudaMemcpyHostToDevice, P->s[0])) ||
+        !ck(cudaEventRecord(P->ev_in[slot], P->s[0])))
+      return MXMOE_ERR_CUDA;
+    // compute: needs this chunk's inputs and the slot's output buffer back
+    if (!ck(cudaStreamWaitEvent(P->s[1], P->ev_in[slot], 0))) return MXMOE_ERR_CUDA;
+    if (c >= 2 && !ck(cudaStreamWaitEvent(P->s[1], P->ev_out[slot], 0))) return MXMOE_ERR_CUDA;
+    const mxmoe_status st =
+        forward_impl(xd, ld, w13q, w13s_mma, w2q, w2s_mma, true, tc, H, E, k, I, renormalize, od,
+                     sb + CL.ws, CL.ws_bytes, P->s[1]);
+    if (st != MXMOE_OK) return st;
+    if (!ck(cudaEventRecord(P->ev_comp[slot], P->s[1]))) return MXMOE_ERR_CUDA;
+    // d2h
+    if (!ck(cudaStreamWaitEvent(P->s[2], P->ev_comp[slot], 0)) ||
+        !ck(cudaMemcpyAsync(out_host + (size_t)t0 * H, od, (size_t)tc * H * 2,
+                            cudaMemcpyDeviceToHost, P->s[2])) ||
+        !ck(cudaEventRecord(P->ev_out[slot], P->s[2])))
+      return MXMOE_ERR_CUDA;
+  }
+  // the caller's stream continues once every copy back has been issued and done
+  if (!ck(cudaEventRecord(P->ev_done, P->s[2])) || !ck(cudaStreamWaitEvent(user, P->ev_done, 0)))
+    return MXMOE_ERR_CUDA;
+  return MXMOE_OK;
 }
 
 }  // extern "C"

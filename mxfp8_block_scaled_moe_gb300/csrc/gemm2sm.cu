@@ -1,0 +1,441 @@
+// 2-SM grouped MXFP8 GEMM (tcgen05 cta_group::2), an opt-in alternative to
+// the 1-SM kernel of gemm.cu (mxmoe_set_gemm_2sm) for 256-wide tiles; same
+// contract, scales in the tiled layout of tiled_scales.h.  Exact (it gives
+// the 1-SM kernel's bytes), but measured slower on GB300 for the MoE shapes:
+// its stage loads see ~3-4 us issue-to-landed latency against ~1.5 us for the
+// 1-SM kernel, so the 6-stage ring, not the tensor pipe, sets its pace.
+//
+// A cluster of two CTAs (on two SMs) computes a 256 x 256 tile: CTA r holds
+// m-tile 2u + r of the work unit's expert (128 token rows) and half r of the
+// 256 weight rows, in its own shared memory; one tcgen05.mma.cta_group::2
+// (M = 256, N = 256, K = 32) issued by the even CTA reads both CTAs' operands
+// and accumulates each CTA's 128 rows x 256 columns in that CTA's TMEM.  Per
+// 128-K stage each SM thus stages 32 KB (A 16 KB + half of B 16 KB) instead of
+// 48 KB (the 1-SM tile is bounded by shared-memory traffic: 48 KB written +
+// 48 KB read per stage).
+//
+// Synchronization (all waits bounded, as in the 1-SM kernel):
+//   full[s]    in the leader; count 2 (each CTA's producer arms it with its own
+//              bytes); every TMA load of both CTAs (operands and scale chunks)
+//              completes on it (cp.async.bulk.tensor .cta_group::2).
+//   empty[s]   in each CTA; the leader's tcgen05.commit is multicast to both.
+//   acc_full   in each CTA; likewise.
+//   acc_empty  in the leader; count 2 x EPI_WARPS: every epilogue warp of both
+//              CTAs arrives once it has drained its accumulator slice.
+// The tcgen05.cp of the scale factors is issued by the leader with
+// cta_group::2 and moves each CTA's staged chunks into its own TMEM (each CTA
+// stages its own A-row scales and all 256 weight rows' scales).
+#include "gemm_common.cuh"
+
+namespace mxmoe {
+namespace gemm {
+
+constexpr int STAGES2 = 6;
+
+struct Layout2 {
+  static constexpr int S = STAGES2;
+  static constexpr int A_BYTES = BM * BK;          // own 128 rows
+  static constexpr int B_BYTES = 128 * BK;         // own half of the 256 weight rows
+  static constexpr int SFA_BYTES = 512;
+  static constexpr int SFB_BYTES = 1024;           // both 128-row halves
+  static constexpr int STAGE_TX = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + S * A_BYTES;
+  static constexpr int OFF_SFA = OFF_B + S * B_BYTES;
+  static constexpr int OFF_SFB = OFF_SFA + S * SFA_BYTES;
+  static constexpr int OFF_BAR = OFF_SFB + S * SFB_BYTES;
+  // full[S], empty[S], acc_full, acc_empty, drain
+  static constexpr int NUM_BARS = 2 * S + 3;
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;   // tmem addr, abort flag
+  static constexpr int OFF_OFFS = OFF_MISC + 16;
+  static constexpr int OFF_TS = OFF_OFFS + (MAX_E + 1) * 8;
+  static constexpr int OFF_MTB = OFF_TS + (MAX_E + 1) * 4;
+  static constexpr int BYTES = OFF_MTB + (MAX_E + 1) * 4;
+  static constexpr int ALLOC = BYTES + 1024;
+};
+
+// ---------------------------------------------------------------- cta_group::2 PTX
+
+// TMA tile load into this CTA's shared memory that completes on an mbarrier
+// of either CTA of the pair (`bar` is a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int c0,
+                                                 int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cluster_bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
+                   cluster_bar),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait with cluster-scope acquire (arrivals come from both CTAs).
+__device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, long long limit,
+                                                 int* status, volatile int* abort_flag) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const long long t0 = clock64();
+  uint32_t it = 0;
+  while (!mbar_try_wait_cluster(bar, parity)) {
+    if ((++it & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (clock64() - t0 > limit) {
+        report_error(status, ERR_TIMEOUT);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+  return true;
+}
+__device__ __forceinline__ void tc2_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+__device__ __forceinline__ void tc2_mma_mxf8(uint32_t d, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+// Arrive on the barrier at `bar`'s offset in both CTAs once all prior
+// tcgen05 operations of this thread have completed.
+__device__ __forceinline__ void tc2_commit_both(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)0x3)
+      : "memory");
+}
+
+// tmSF*: the tiled scale arrays seen as [chunks * 2, 256] bytes, so one
+// 512-byte chunk is a {256, 2} TMA box at row 2 * chunk.
+template <bool kSwiglu>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmSFA,
+                   const __grid_constant__ CUtensorMap tmSFB, const Params p) {
+  using L = Layout2;
+  constexpr int STAGES = L::S;
+  constexpr int BN = 256;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~(uintptr_t)1023);
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+  int64_t* s_off = reinterpret_cast<int64_t*>(smem + L::OFF_OFFS);
+  int* s_ts = reinterpret_cast<int*>(smem + L::OFF_TS);
+  int* s_mtb = reinterpret_cast<int*>(smem + L::OFF_MTB);
+  auto bar_full = [&](int s) { return sbase + L::OFF_BAR + 8u * s; };
+  auto bar_empty = [&](int s) { return sbase + L::OFF_BAR + 8u * (STAGES + s); };
+  const uint32_t bar_acc_full = sbase + L::OFF_BAR + 8u * (2 * STAGES);
+  const uint32_t bar_acc_empty = bar_acc_full + 8;
+  const uint32_t bar_drain = bar_acc_full + 16;
+
+  const int E = p.E;
+  const int unit0 = blockIdx.x >> 1;  // cluster index
+  const int unit_step = gridDim.x >> 1;
+  // ---- set-up
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full(s), 2);       // leader: armed by both CTAs' producers
+      mbar_init(bar_empty(s), 1);      // the leader's multicast commit
+    }
+    mbar_init(bar_acc_full, 1);
+    mbar_init(bar_acc_empty, 2 * EPI_WARPS);  // leader: every epilogue warp of both CTAs
+    mbar_init(bar_drain, 1);
+    *s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    // both CTAs' warps allocate together (same columns in each TMEM)
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(s_tmem)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  if (warp == 2) build_schedule<2>(p, lane, s_off, s_ts, s_mtb);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // barriers of both CTAs initialized before any cross-CTA signal
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const int total_units = s_ts[E];
+  const int KT = p.K / BK;
+  // the leader's barriers as seen from this CTA
+  const uint32_t lead_full0 = mapa_cluster(bar_full(0), 0);
+  const uint32_t lead_acc_empty = mapa_cluster(bar_acc_empty, 0);
+
+  if (warp == 0) {
+    // ================= producer (both CTAs)
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int unit = unit0; ok && unit < total_units; unit += unit_step) {
+      int e, mt, nt;
+      decode_tile(unit, s_ts, E, p.n_tiles_n, e, mt, nt);
+      mt = 2 * mt + (int)rank;
+      const int64_t row0 = s_off[e] + (int64_t)mt * BM;
+      const int64_t brow = (int64_t)e * p.Nw;
+      const int64_t bh0 = kSwiglu ? brow + (int64_t)nt * (BN / 2) : brow + (int64_t)nt * BN;
+      const int64_t bh1 = kSwiglu ? brow + p.n_out + (int64_t)nt * (BN / 2) : bh0 + BN / 2;
+      // tiled A scales: the m-tile's block (a CTA without rows reads its expert's last block)
+      const int64_t a_blk = min(s_mtb[e] + mt, s_mtb[e + 1] - 1);
+      for (int kt = 0; kt < KT; ++kt) {
+        const bool got = wait_bar_cluster(bar_empty(stage), phase ^ 1, p.wait_limit, p.status, s_abort);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t fb = lead_full0 + 8u * stage;  // leader's full[stage]
+          mbar_arrive_expect_tx_cluster(fb, L::STAGE_TX);
+          const uint32_t sA = sbase + L::OFF_A + stage * L::A_BYTES;
+          const uint32_t sB = sbase + L::OFF_B + stage * L::B_BYTES;
+          const uint32_t sSFA = sbase + L::OFF_SFA + stage * L::SFA_BYTES;
+          const uint32_t sSFB = sbase + L::OFF_SFB + stage * L::SFB_BYTES;
+          tma_load_2d_pair(sA, &tmA, kt * BK, (int)row0, fb);
+          tma_load_2d_pair(sB, &tmB, kt * BK, (int)(rank ? bh1 : bh0), fb);
+          tma_load_2d_pair(sSFA, &tmSFA, 0, (int)(2 * (a_blk * KT + kt)), fb);
+          tma_load_2d_pair(sSFB, &tmSFB, 0, (int)(2 * ((bh0 >> 7) * KT + kt)), fb);
+          tma_load_2d_pair(sSFB + 512, &tmSFB, 0, (int)(2 * ((bh1 >> 7) * KT + kt)), fb);
+        }
+        __syncwarp();
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+      }
+    }
+    if (ok) {
+      // tail: wait until the leader's MMAs have released every stage this CTA
+      // loaded, so no commit of the pair is still on its way to this CTA
+      for (int i = 0; i < STAGES; ++i) {
+        wait_bar_cluster(bar_empty(stage), phase ^ 1, p.wait_limit, p.status, s_abort);
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+      }
+    } else {
+      // abort: loads already issued complete on the leader's barriers; give
+      // them a bounded moment to land before the CTA pair tears down
+      const long long t0 = clock64();
+      while (clock64() - t0 < 200000) __nanosleep(1000);
+    }
+  } else if (warp == 1) {
+    // ================= MMA issuer: one thread of the leader CTA
+    if (leader && lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      bool issued = false;
+      constexpr uint32_t IDESC = make_idesc(2 * BM, BN);
+      for (int unit = unit0; ok && unit < total_units; unit += unit_step) {
+        if (!wait_bar_cluster(bar_acc_empty, acc_phase ^ 1, p.wait_limit, p.status, s_abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int kt = 0; kt < KT; ++kt) {
+          if (!wait_bar_cluster(bar_full(stage), phase, p.wait_limit, p.status, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sA = sbase + L::OFF_A + stage * L::A_BYTES;
+          const uint32_t sB = sbase + L::OFF_B + stage * L::B_BYTES;
+          const uint32_t sSFA = sbase + L::OFF_SFA + stage * L::SFA_BYTES;
+          const uint32_t sSFB = sbase + L::OFF_SFB + stage * L::SFB_BYTES;
+          const uint32_t t_sfa = tmem + SF_COL0 + stage * SF_COLS_PER_STAGE;
+          const uint32_t t_sfb = t_sfa + 4;
+          tc2_cp_sf(t_sfa, make_sdesc(sSFA, 128, 128, 0));
+          tc2_cp_sf(t_sfb, make_sdesc(sSFB, 128, 128, 0));
+          tc2_cp_sf(t_sfb + 4, make_sdesc(sSFB + 512, 128, 128, 0));
+          const uint64_t adesc = make_sdesc(sA, 16, 1024, 2);
+          const uint64_t bdesc = make_sdesc(sB, 16, 1024, 2);
+#pragma unroll
+          for (int kk = 0; kk < BK / 32; ++kk) {
+            const uint32_t idesc = IDESC | ((uint32_t)kk << 29) | ((uint32_t)kk << 4);
+            tc2_mma_mxf8(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, t_sfa, t_sfb,
+                         (kt | kk) != 0 ? 1u : 0u);
+          }
+          issued = true;
+          tc2_commit_both(bar_empty(stage));
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        tc2_commit_both(bar_acc_full);
+        acc_phase ^= 1;
+      }
+      if (ok) {
+        // the last tile's releases (some from the peer CTA) land before exit
+        wait_bar_cluster(bar_acc_empty, acc_phase ^ 1, p.wait_limit, p.status, s_abort);
+      } else if (issued) {
+        tc2_commit_both(bar_drain);
+        volatile int no_abort = 0;
+        wait_bar(bar_drain, 0, 1ll << 32, nullptr, &no_abort);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ================= epilogue (both CTAs): EPI_GROUPS warps per TMEM lane quarter
+    const int q = warp & 3;
+    const int grp = (warp - 2) >> 2;
+    const int row = q * 32 + lane;
+    const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
+    uint32_t acc_phase = 0;
+    for (int unit = unit0; unit < total_units; unit += unit_step) {
+      int e, mt, nt;
+      decode_tile(unit, s_ts, E, p.n_tiles_n, e, mt, nt);
+      mt = 2 * mt + (int)rank;
+      const int64_t grow = s_off[e] + (int64_t)mt * BM + row;
+      const bool valid = grow < s_off[e + 1];
+      const bool got = wait_bar_cluster(bar_acc_full, acc_phase, p.wait_limit, p.status, s_abort);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      epilogue_tile<BN, kSwiglu, true>(
+          p, t_row, grp, row, lane, grow, valid, nt, (int64_t)(s_mtb[e] + mt) * BM + row,
+          [&] { if (lane == 0) mbar_arrive_cluster(lead_acc_empty); });
+      acc_phase ^= 1;
+    }
+  }
+
+  // ---- teardown
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // neither CTA leaves while the other may still signal it
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+// uint8 [rows, 256] view of a tiled scale array: one chunk = box {256, 2}.
+static bool make_chunk_map(CUtensorMap* m, const void* base, uint64_t chunks) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {256, 2 * chunks};
+  cuuint64_t strides[1] = {256};
+  cuuint32_t box[2] = {256, 2};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <bool kSwiglu>
+cudaError_t launch_pair_impl(const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
+                             const uint8_t* sfb, const int64_t* offsets, int64_t M, int E, int K,
+                             int Nw, int n_out, void* out, uint8_t* out_scale,
+                             cudaStream_t stream) {
+  using L = Layout2;
+  if (M == 0) return cudaSuccess;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  static int max_clusters[64];
+  static bool configured[64] = {false};
+  auto kern = gemm2sm_kernel<kSwiglu>;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = L::ALLOC;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (!configured[dev]) {
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+    if (err != cudaSuccess) return err;
+    cfg.gridDim = dim3(2 * 64, 1, 1);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    max_clusters[dev] = n;
+    configured[dev] = true;
+  }
+  if (max_clusters[dev] <= 0) return cudaErrorNotSupported;
+  const int KT = K / BK;
+  CUtensorMap tmA, tmB, tmSFA, tmSFB;
+  if (!make_map(&tmA, a, (uint64_t)K, (uint64_t)M, BK, BM)) return cudaErrorInvalidValue;
+  if (!make_map(&tmB, b, (uint64_t)K, (uint64_t)E * Nw, BK, 128)) return cudaErrorInvalidValue;
+  const uint64_t a_chunks = (uint64_t)(ceil_div(M, BM) + E) * KT;
+  const uint64_t b_chunks = (uint64_t)E * Nw / 128 * KT;
+  if (!make_chunk_map(&tmSFA, sfa, a_chunks)) return cudaErrorInvalidValue;
+  if (!make_chunk_map(&tmSFB, sfb, b_chunks)) return cudaErrorInvalidValue;
+  Params p;
+  p.sfa = sfa;
+  p.sfb = sfb;
+  p.offsets = offsets;
+  p.out = out;
+  p.out_scale = out_scale;
+  p.M = M;
+  p.E = E;
+  p.K = K;
+  p.Nw = Nw;
+  p.n_out = n_out;
+  p.n_tiles_n = kSwiglu ? n_out / 128 : n_out / 256;
+  p.status = device_status_ptr();
+  p.wait_limit = wait_limit_cycles();
+  const int64_t units_bound = (ceil_div(M, BM) / 2 + E) * (int64_t)p.n_tiles_n;
+  const int clusters = (int)std::min<int64_t>(
+      {units_bound, (int64_t)max_clusters[dev], (int64_t)num_sms() / 2});
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmSFA, tmSFB, p);
+}
+
+template <bool kSwiglu, bool kTiledSF>
+cudaError_t launch_pair(const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
+                        const uint8_t* sfb, const int64_t* offsets, int64_t M, int E, int K,
+                        int Nw, int n_out, void* out, uint8_t* out_scale, cudaStream_t stream) {
+  if (!kTiledSF) return cudaErrorNotSupported;  // scale chunks must be TMA-loadable
+  return launch_pair_impl<kSwiglu>(a, sfa, b, sfb, offsets, M, E, K, Nw, n_out, out, out_scale,
+                                   stream);
+}
+
+template cudaError_t launch_pair<true, true>(const uint8_t*, const uint8_t*, const uint8_t*,
+                                             const uint8_t*, const int64_t*, int64_t, int, int,
+                                             int, int, void*, uint8_t*, cudaStream_t);
+template cudaError_t launch_pair<false, true>(const uint8_t*, const uint8_t*, const uint8_t*,
+                                              const uint8_t*, const int64_t*, int64_t, int, int,
+                                              int, int, void*, uint8_t*, cudaStream_t);
+template cudaError_t launch_pair<true, false>(const uint8_t*, const uint8_t*, const uint8_t*,
+                                              const uint8_t*, const int64_t*, int64_t, int, int,
+                                              int, int, void*, uint8_t*, cudaStream_t);
+template cudaError_t launch_pair<false, false>(const uint8_t*, const uint8_t*, const uint8_t*,
+                                               const uint8_t*, const int64_t*, int64_t, int, int,
+                                               int, int, void*, uint8_t*, cudaStream_t);
+
+}  // namespace gemm
+}  // namespace mxmoe

@@ -157,3 +157,40 @@ def test_layer_profile_segments(mm):
     assert prof["weight_scale_layout"] >= 0.0
     for key in ("route_quant", "gemm1_swiglu_quant", "gemm2", "finalize"):
         assert prof[key] > 0.0, key
+
+
+@pytest.mark.parametrize("cfg", ["tiny", "qwen3_30b_decode", "qwen3_30b_prefill", "qwen3_235b_prefill"])
+def test_two_sm_and_one_sm_gemm_kernels_agree(mm, cfg):
+    """The 2-SM (cta_group::2) and 1-SM grouped GEMMs give the same layer bytes."""
+    shape = workloads.CONFIGS[cfg]
+    inp = workloads.make_layer(shape, DEV)
+    if shape.offline:
+        layer = mm.MXFP8MoELayer.from_quantized(inp["w13q"], inp["w13s"], inp["w2q"], inp["w2s"],
+                                                shape.k)
+    else:
+        layer = mm.MXFP8MoELayer.from_bf16(inp["w13"], inp["w2"], shape.k)
+    out1 = layer(inp["x"], inp["logits"])
+    mm.api.set_gemm_2sm(True)
+    try:
+        out2 = layer(inp["x"], inp["logits"])
+    finally:
+        mm.api.set_gemm_2sm(False)
+    torch.cuda.synchronize()
+    assert mm.device_status() == 0
+    assert torch.equal(out1, out2)
+
+
+@pytest.mark.parametrize("cfg,n_chunks", [("tiny", 3), ("qwen3_30b_decode", 0),
+                                          ("qwen3_30b_prefill", 0), ("qwen3_30b_prefill", 5)])
+def test_host_buffer_layer_matches_device_layer(mm, cfg, n_chunks):
+    """Chunked, copy-overlapped layer on host buffers == the on-device layer."""
+    shape = workloads.CONFIGS[cfg]
+    inp = workloads.make_layer(shape, DEV)
+    layer = mm.MXFP8MoELayer.from_bf16(inp["w13"], inp["w2"], shape.k)
+    ref = layer(inp["x"], inp["logits"])
+    x_h = inp["x"].cpu().pin_memory()
+    l_h = inp["logits"].cpu().pin_memory()
+    out_h = layer.forward_host(x_h, l_h, n_chunks=n_chunks)
+    torch.cuda.synchronize()
+    assert mm.device_status() == 0
+    assert torch.equal(out_h, ref.cpu())
