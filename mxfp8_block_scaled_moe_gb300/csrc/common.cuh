@@ -91,6 +91,67 @@ __device__ __forceinline__ void st_v8(void* p, const uint32_t (&v)[8]) {
                : "memory");
 }
 
+// 32-byte global load (read-only, not kept in L1) / streaming store; the
+// address must be 32-byte aligned.
+__device__ __forceinline__ void ld_nc_v8(const void* p, uint32_t (&r)[8]) {
+  asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "l"(p));
+}
+__device__ __forceinline__ void st_cs_v8(void* p, const uint32_t (&v)[8]) {
+  asm volatile("st.global.cs.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
+// Load the 32 bf16 of one MX block (64 bytes) as 16 words; 32-byte loads
+// when kV8 (64-byte aligned block), else 16-byte loads.
+template <bool kV8>
+__device__ __forceinline__ void load_block32_bf16(const uint16_t* p, uint32_t (&w)[16]) {
+  if (kV8) {
+    ld_nc_v8(p, *reinterpret_cast<uint32_t(*)[8]>(&w[0]));
+    ld_nc_v8(p + 16, *reinterpret_cast<uint32_t(*)[8]>(&w[8]));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 v = ld_nc_v4(p + 8 * i);
+      w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+    }
+  }
+}
+
+// MX-quantize one block of 32 bf16 (16 words) into 32 e4m3 bytes (8 words);
+// returns the e8m0 scale byte.
+__device__ __forceinline__ uint32_t quant_block32_bf16(const uint32_t (&w)[16], uint32_t (&o)[8]) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m = umax(m, bf16x2_absmax_bits(w[i]));
+  const uint32_t sb = e8m0_from_amax_bits(m);
+  const float inv = inv_scale_from_e8m0(sb);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t w0 = w[2 * i], w1 = w[2 * i + 1];
+    o[i] = cvt_e4m3x4(bf16_bits_to_float(w0 & 0xFFFFu) * inv, bf16_bits_to_float(w0 >> 16) * inv,
+                      bf16_bits_to_float(w1 & 0xFFFFu) * inv, bf16_bits_to_float(w1 >> 16) * inv);
+  }
+  return sb;
+}
+
+template <bool kV8>
+__device__ __forceinline__ void store_block32_e4m3(uint8_t* p, const uint32_t (&o)[8]) {
+  if (kV8) {
+    st_cs_v8(p, o);
+  } else {
+    st_cs_v4(p, make_uint4(o[0], o[1], o[2], o[3]));
+    st_cs_v4(p + 16, make_uint4(o[4], o[5], o[6], o[7]));
+  }
+}
+
+__device__ __forceinline__ bool aligned32(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 31u) == 0;
+}
+
 // Record the first device-side error in the library's status word.
 __device__ __forceinline__ void report_error(int* status, int code) {
   if (status) atomicCAS(status, 0, code);

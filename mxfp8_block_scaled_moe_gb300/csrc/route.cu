@@ -16,8 +16,9 @@
 //   2. route_scan: per-expert exclusive prefix of the block histograms (the
 //      block's base row inside each expert) and of the expert totals (offsets).
 //   3. route_permute_quant: one warp per token computes its k destination rows
-//      (offset + block base + rank), quantizes its hidden row once and writes
-//      the payload/scale to all k rows (or copies bf16 rows, two-step mode).
+//      (offset + block base + rank); each lane quantizes one 32-element block
+//      of the hidden row once and writes its 32 payload bytes and scale byte
+//      to all k rows (or copies the bf16 block, two-step mode).
 // The permutation is deterministic: rows of one expert are in flat-index
 // (token) order.
 //
@@ -227,7 +228,7 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int32_t* __restrict__ 
 
 // kTiled: xs goes to the MMA-ready tiled scale layout (tiled_scales.h)
 // instead of [M, H/32]; requires H % 128 == 0 and the experts' tile bases.
-template <bool kQuant, bool kTiled>
+template <bool kQuant, bool kTiled, bool kV8>
 __global__ void __launch_bounds__(kRouteThreads) route_permute_kernel(
     const uint16_t* __restrict__ x, int T, int H, int E, int k,
     const int32_t* __restrict__ topk_ids, const int32_t* __restrict__ block_base,
@@ -253,52 +254,37 @@ __global__ void __launch_bounds__(kRouteThreads) route_permute_kernel(
     }
   }
   __syncwarp();
+  // one lane = one 32-element block of the row: quantized once, written to
+  // the k destination rows (32 B of payload + 1 scale byte each)
   const uint16_t* xr = x + (int64_t)t * H;
   const int H32 = H / 32;
-  for (int c0 = 0; c0 < H; c0 += 512) {  // 16 elements per lane per step
-    const int c = c0 + lane * 16;
-    const bool ok = c < H;
-    uint4 a = make_uint4(0, 0, 0, 0), bb = make_uint4(0, 0, 0, 0);
-    if (ok) {
-      a = ld_nc_v4(xr + c);
-      bb = ld_nc_v4(xr + c + 8);
-    }
+  for (int j0 = 0; j0 < H32; j0 += 32) {
+    const int blk = j0 + lane;
+    if (blk >= H32) break;
+    uint32_t w[16];
+    load_block32_bf16<kV8>(xr + blk * 32, w);
     if (kQuant) {
-      uint32_t m = umax(umax(bf16x2_absmax_bits(a.x), bf16x2_absmax_bits(a.y)),
-                        umax(bf16x2_absmax_bits(a.z), bf16x2_absmax_bits(a.w)));
-      m = umax(m, umax(umax(bf16x2_absmax_bits(bb.x), bf16x2_absmax_bits(bb.y)),
-                       umax(bf16x2_absmax_bits(bb.z), bf16x2_absmax_bits(bb.w))));
-      m = umax(m, __shfl_xor_sync(0xffffffffu, m, 1));
-      const uint32_t sb = e8m0_from_amax_bits(m);
-      const float inv = inv_scale_from_e8m0(sb);
-      const uint32_t w[8] = {a.x, a.y, a.z, a.w, bb.x, bb.y, bb.z, bb.w};
-      uint32_t o[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t w0 = w[2 * i], w1 = w[2 * i + 1];
-        o[i] = cvt_e4m3x4(bf16_bits_to_float(w0 & 0xFFFFu) * inv,
-                          bf16_bits_to_float(w0 >> 16) * inv,
-                          bf16_bits_to_float(w1 & 0xFFFFu) * inv,
-                          bf16_bits_to_float(w1 >> 16) * inv);
-      }
-      if (ok) {
-        const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
-        for (int j = 0; j < k; ++j) {
-          const int64_t d = s_dest[warp][j];
-          st_cs_v4(xq + d * H + c, ov);
-          if ((lane & 1) == 0) {
-            if (kTiled)
-              xs[tiled_scale_offset(s_sfrow[warp][j], c >> 5, H / 128)] = (uint8_t)sb;
-            else
-              xs[d * H32 + (c >> 5)] = (uint8_t)sb;
-          }
-        }
-      }
-    } else if (ok) {
+      uint32_t o[8];
+      const uint32_t sb = quant_block32_bf16(w, o);
       for (int j = 0; j < k; ++j) {
         const int64_t d = s_dest[warp][j];
-        st_cs_v4(xp + d * H + c, a);
-        st_cs_v4(xp + d * H + c + 8, bb);
+        store_block32_e4m3<kV8>(xq + d * H + blk * 32, o);
+        if (kTiled)
+          xs[tiled_scale_offset(s_sfrow[warp][j], blk, H / 128)] = (uint8_t)sb;
+        else
+          xs[d * H32 + blk] = (uint8_t)sb;
+      }
+    } else {
+      for (int j = 0; j < k; ++j) {
+        uint16_t* dst = xp + s_dest[warp][j] * H + blk * 32;
+        if (kV8) {
+          st_cs_v8(dst, *reinterpret_cast<const uint32_t(*)[8]>(&w[0]));
+          st_cs_v8(dst + 16, *reinterpret_cast<const uint32_t(*)[8]>(&w[8]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            st_cs_v4(dst + 8 * i, make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]));
+        }
       }
     }
   }
@@ -349,18 +335,19 @@ cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, i
   if (err != cudaSuccess) return err;
 
   const int nb3 = (int)ceil_div(T, kRouteWarps);
-  if (quant && tile_base)
-    route_permute_kernel<true, true><<<nb3, kRouteThreads, 0, stream>>>(
-        x, T, H, E, k, topk_ids, block_hist, offsets, tile_base, src_to_sorted, sorted_to_src, xq,
-        xs, nullptr);
-  else if (quant)
-    route_permute_kernel<true, false><<<nb3, kRouteThreads, 0, stream>>>(
-        x, T, H, E, k, topk_ids, block_hist, offsets, nullptr, src_to_sorted, sorted_to_src, xq,
-        xs, nullptr);
-  else
-    route_permute_kernel<false, false><<<nb3, kRouteThreads, 0, stream>>>(
-        x, T, H, E, k, topk_ids, block_hist, offsets, nullptr, src_to_sorted, sorted_to_src,
-        nullptr, nullptr, xp);
+  const bool v8 = ((uintptr_t)x & 31u) == 0 && ((uintptr_t)(quant ? (const void*)xq : (const void*)xp) & 31u) == 0;
+#define MXMOE_PERMUTE(Q, TL, V)                                                                   \
+  route_permute_kernel<Q, TL, V><<<nb3, kRouteThreads, 0, stream>>>(                           \
+      x, T, H, E, k, topk_ids, block_hist, offsets, TL ? tile_base : nullptr, src_to_sorted,    \
+      sorted_to_src, Q ? xq : nullptr, Q ? xs : nullptr, Q ? nullptr : xp)
+  if (quant && tile_base) {
+    if (v8) MXMOE_PERMUTE(true, true, true); else MXMOE_PERMUTE(true, true, false);
+  } else if (quant) {
+    if (v8) MXMOE_PERMUTE(true, false, true); else MXMOE_PERMUTE(true, false, false);
+  } else {
+    if (v8) MXMOE_PERMUTE(false, false, true); else MXMOE_PERMUTE(false, false, false);
+  }
+#undef MXMOE_PERMUTE
   return cudaGetLastError();
 }
 

@@ -62,6 +62,27 @@ def test_mx_quantize_3d_bit_exact(mm, E, N, K):
     assert np.array_equal(u8(q), qr)
 
 
+def _offset16(t):
+    """A copy of t whose data starts 16 bytes past a 32-byte boundary."""
+    flat = torch.empty(t.numel() * t.element_size() + 48, dtype=torch.uint8, device=t.device)
+    base = (-flat.data_ptr()) % 32 + 16
+    v = flat[base:base + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+    v.copy_(t)
+    assert v.data_ptr() % 32 == 16
+    return v
+
+
+def test_mx_quantize_16_byte_aligned_input(mm):
+    """A 16-byte (not 32-byte) aligned input takes the 16-byte load path."""
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((3, 40, 256)) * np.exp2(rng.integers(-8, 8, (3, 40, 1)))
+    xb = mx.f64_to_bf16_bits(x)
+    q, s = mm.mx_quantize_3d(_offset16(to_bf16_tensor(xb, DEV)))
+    torch.cuda.synchronize()
+    qr, sr = mx.mx_quantize(mx.bf16_bits_to_f64(xb))
+    assert np.array_equal(u8(s), sr) and np.array_equal(u8(q), qr)
+
+
 @pytest.mark.parametrize("cfg", ["tiny", "qwen3_30b_decode"])
 def test_weight_quant_of_config_bit_exact(mm, cfg):
     shape = workloads.CONFIGS[cfg]
@@ -136,6 +157,27 @@ def test_route_quant_edge_shapes(mm, T, H, E, k, renorm):
     assert np.array_equal(u8(r["xq"]), xq) and np.array_equal(u8(r["xs"]), xs)
 
 
+@pytest.mark.parametrize("quant", [True, False])
+def test_route_16_byte_aligned_input(mm, quant):
+    """x 16-byte (not 32-byte) aligned: the permutation takes 16-byte accesses."""
+    g = torch.Generator(device=DEV).manual_seed(99)
+    T, H, E, k = 77, 1024, 16, 4
+    x = _offset16(torch.randn(T, H, generator=g, device=DEV).to(torch.bfloat16))
+    logits = torch.randn(T, E, generator=g, device=DEV)
+    xb = bits16(x)
+    if quant:
+        r = mm.moe_route_quant_mxfp8(x, logits, k)
+        torch.cuda.synchronize()
+        ids, _ = _check_route(r, xb, logits.cpu().numpy(), k, E, True)
+        xq, xs, *_ = moe.route_quant(mx.bf16_bits_to_f64(xb), ids, E)
+        assert np.array_equal(u8(r["xq"]), xq) and np.array_equal(u8(r["xs"]), xs)
+    else:
+        r = mm.moe_route_permute_bf16(x, logits, k)
+        torch.cuda.synchronize()
+        ref = moe.permute_rows(xb, r["sorted_to_src"].cpu().numpy(), k)
+        assert np.array_equal(bits16(r["xp"]), ref)
+
+
 def test_route_empty_batch(mm):
     x = torch.zeros(0, 256, dtype=torch.bfloat16, device=DEV)
     logits = torch.zeros(0, 8, device=DEV)
@@ -173,10 +215,17 @@ def test_route_is_deterministic(mm):
 
 # ---------------------------------------------------------------- finalize
 
-@pytest.mark.parametrize("T,H,k", [(64, 256, 2), (32, 2048, 8), (1000, 2048, 8), (5, 40, 3)])
-def test_finalize_matches_oracle(mm, T, H, k):
+# 1040 = 1024 + 16: a second column chunk holding one lane; 600 and 40 are not
+# multiples of 16 (8-column lanes); offset16 takes the 16-byte access path.
+@pytest.mark.parametrize("T,H,k,off", [(64, 256, 2, False), (32, 2048, 8, False),
+                                       (1000, 2048, 8, False), (5, 40, 3, False),
+                                       (17, 1040, 4, False), (9, 600, 5, False),
+                                       (33, 2048, 8, True), (17, 1040, 4, True)])
+def test_finalize_matches_oracle(mm, T, H, k, off):
     g = torch.Generator(device=DEV).manual_seed(T + H + k)
     y = torch.randn(T * k, H, generator=g, device=DEV).to(torch.bfloat16)
+    if off:
+        y = _offset16(y)
     w = torch.rand(T, k, generator=g, device=DEV)
     perm = torch.randperm(T * k, generator=g, device=DEV).to(torch.int32)
     out = mm.moe_finalize_routing(y, w, perm, k)
