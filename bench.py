@@ -74,10 +74,16 @@ def load_peaks():
     return dict(FALLBACK_PEAKS, source="fallback")
 
 
+GEMM_SOURCES = ("gemm.cu", "gemm_common.cuh", "tiled_scales.h", "common.cuh")
+
+
 def gemm_src_hash():
+    """Hash of the sources the 1-SM grouped GEMM kernel is compiled from; the
+    stored ncu traffic is only reported while it matches."""
     h = hashlib.sha256()
-    with open(os.path.join(ROOT, "mxfp8_block_scaled_moe_gb300", "csrc", "gemm.cu"), "rb") as f:
-        h.update(f.read())
+    for name in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "mxfp8_block_scaled_moe_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 

@@ -301,13 +301,16 @@ mxmoe_status mxmoe_get_device_status(int32_t* status_out, int clear);
 void mxmoe_set_wait_limit_cycles(long long cycles);
 
 /*
- * Grouped-GEMM kernel selection (not part of the method).  By default every
- * grouped GEMM runs the 1-SM kernel.  enable != 0 sends 256-wide tiles with
- * MMA-layout scales (the layer calls) to the 2-SM kernel (tcgen05
- * cta_group::2 over CTA pairs) when the device can co-schedule pairs; it
- * gives the same bytes and is kept for comparison and tests.
+ * Grouped-GEMM kernel selection (not part of the method; process-wide).
+ * Both kernels give the same bytes.  mode 0: every grouped GEMM runs the 1-SM
+ * kernel.  mode 1: 256-wide tiles with MMA-layout scales (the layer calls)
+ * run the 2-SM kernel (tcgen05 cta_group::2 over CTA pairs) when the device
+ * can co-schedule pairs.  mode 2 (the default): the 2-SM kernel for the
+ * bf16-output GEMM (grouped GEMM2) when its rows average at least 1024 per
+ * expert (M >= 1024 * E), the 1-SM kernel otherwise.  Other values select
+ * mode 2.
  */
-void mxmoe_set_gemm_2sm(int enable);
+void mxmoe_set_gemm_2sm(int mode);
 
 /* Library version string. */
 const char* mxmoe_version(void);

@@ -11,17 +11,19 @@
 // an opt-in 2-SM kernel in gemm2sm.cu (tcgen05 cta_group::2, M = 256 over a
 // CTA pair).
 //
-// Design of the 1-SM kernel (one persistent CTA per SM, 576 threads, warp-specialized):
+// Design of the 1-SM kernel (one persistent CTA per SM, 704 threads, warp-specialized):
 //   warp 0      producer: TMA (128B swizzle) loads of the A tile [128 x 128]
-//               and the B tile [BN x 128] e4m3, plus cp.async of the e8m0
-//               scales into the tensor-core scale-factor staging layout;
-//               all land on one mbarrier per pipeline stage.
-//   warp 1      MMA issuer (one thread): tcgen05.cp moves each stage's scale
-//               factors from shared memory into tensor memory, then four
+//               and the B tile [BN x 128] e4m3, plus the e8m0 scale chunks
+//               (bulk copies of the tiled layout, or cp.async of [rows, K/32]
+//               scales into the same staging layout); all land on one mbarrier
+//               per pipeline stage.
+//   warps 2-5   scale-factor writers, one per TMEM lane quarter: tcgen05.st
+//               moves each stage's staged scales into tensor memory.
+//   warp 1      MMA issuer (one thread): four
 //               tcgen05.mma.kind::mxf8f6f4.block_scale (M=128, N=BN, K=32,
 //               UE8M0 scales, one scale per 32 K-elements) accumulate the
 //               fp32 tile in tensor memory; tcgen05.commit frees the stage.
-//   warps 2-17  epilogue: tcgen05.ld the accumulator into registers (one
+//   warps 6-21  epilogue: tcgen05.ld the accumulator into registers (one
 //               thread per row and a quarter of the columns), release it to the
 //               MMA warp, then SwiGLU + MX requant (gmm1) or bf16 rounding
 //               (gmm2) and the stores, overlapping the next tile's mainloop.
@@ -59,8 +61,8 @@ struct Layout1 {
   static constexpr int OFF_SFA = OFF_B + S * B_BYTES;
   static constexpr int OFF_SFB = OFF_SFA + S * SFA_BYTES;
   static constexpr int OFF_BAR = OFF_SFB + S * SFB_BYTES;
-  // full[S], empty[S], acc_full, acc_empty, drain
-  static constexpr int NUM_BARS = 2 * S + 3;
+  // full[S], empty[S], acc_full, acc_empty, drain, sf_ready[S]
+  static constexpr int NUM_BARS = 3 * S + 3;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;   // tmem addr, abort flag
   static constexpr int OFF_OFFS = OFF_MISC + 16;            // int64 offsets [E+1]
   static constexpr int OFF_TS = OFF_OFFS + (MAX_E + 1) * 8; // int unit start [E+1]
@@ -73,7 +75,7 @@ struct Layout1 {
 // of tiled_scales.h and each stage's scale chunks arrive by bulk copy;
 // otherwise they are the row-major [rows, K/32] arrays, staged by cp.async.
 template <int BN, bool kSwiglu, bool kTiledSF>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS1, 1)
     gemm1sm_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, const Params p) {
   using L = Layout1<BN>;
@@ -94,6 +96,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t bar_acc_full = sbase + L::OFF_BAR + 8u * (2 * STAGES);
   const uint32_t bar_acc_empty = bar_acc_full + 8;
   const uint32_t bar_drain = bar_acc_full + 16;
+  auto bar_sf = [&](int s) { return sbase + L::OFF_BAR + 8u * (2 * STAGES + 3 + s); };
 
   const int E = p.E;
   // ---- set-up: barriers, TMEM, tile schedule
@@ -102,6 +105,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // producer expect_tx (+ 32 cp.async arrivals when scales come by cp.async)
       mbar_init(bar_full(s), kTiledSF ? 1 : 1 + 32);
       mbar_init(bar_empty(s), 1);         // tcgen05.commit
+      mbar_init(bar_sf(s), SF_WARPS);     // scale factors in TMEM
     }
     mbar_init(bar_acc_full, 1);
     mbar_init(bar_acc_empty, EPI_WARPS);  // one arrive per epilogue warp
@@ -222,21 +226,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         tc_fence_after();
         for (int kt = 0; kt < KT; ++kt) {
-          if (!wait_bar(bar_full(stage), phase, p.wait_limit, p.status, s_abort)) {
+          // operands landed, and this stage's scale factors are in TMEM
+          if (!wait_bar(bar_full(stage), phase, p.wait_limit, p.status, s_abort) ||
+              !wait_bar(bar_sf(stage), phase, p.wait_limit, p.status, s_abort)) {
             ok = false;
             break;
           }
-          if (!kTiledSF) fence_proxy_async_smem();  // cp.async-written scales -> async proxy
           tc_fence_after();
           const uint32_t sA = sbase + L::OFF_A + stage * L::A_BYTES;
           const uint32_t sB = sbase + L::OFF_B + stage * L::B_BYTES;
-          const uint32_t sSFA = sbase + L::OFF_SFA + stage * L::SFA_BYTES;
-          const uint32_t sSFB = sbase + L::OFF_SFB + stage * L::SFB_BYTES;
           const uint32_t t_sfa = tmem + SF_COL0 + stage * SF_COLS_PER_STAGE;
           const uint32_t t_sfb = t_sfa + 4;
-          tc_cp_sf(t_sfa, make_sdesc(sSFA, 128, 128, 0));
-#pragma unroll
-          for (int c = 0; c < BN / 128; ++c) tc_cp_sf(t_sfb + 4 * c, make_sdesc(sSFB + 512 * c, 128, 128, 0));
           const uint64_t adesc = make_sdesc(sA, 16, 1024, 2);
           const uint64_t bdesc = make_sdesc(sB, 16, 1024, 2);
 #pragma unroll
@@ -261,11 +261,45 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
     __syncwarp();
+  } else if (warp < EPI_WARP0) {
+    // ================= scale-factor writers, one per TMEM lane quarter
+    // (warp & 3): each stage's staged chunks (byte (r % 32) * 16 + (r / 32) *
+    // 4 + kb of 128 rows) go from shared memory into this quarter's lanes,
+    // 16 bytes (4 columns) per lane and chunk.  Every quarter holds the whole
+    // chunk, the layout the block-scaled MMA reads for M = 128.  Register
+    // stores keep these copies out of the tensor pipe, where tcgen05.cp
+    // would serialize with the MMAs.
+    const uint32_t t_q = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+      for (int kt = 0; kt < KT; ++kt) {
+        const bool got = wait_bar(bar_full(stage), phase, p.wait_limit, p.status, s_abort);
+        if (!__all_sync(0xffffffffu, got)) {  // keep the warp converged
+          ok = false;
+          break;
+        }
+        const uint8_t* sfa_s = smem + L::OFF_SFA + stage * L::SFA_BYTES;
+        const uint8_t* sfb_s = smem + L::OFF_SFB + stage * L::SFB_BYTES;
+        const uint32_t col = SF_COL0 + stage * SF_COLS_PER_STAGE;
+        tmem_st_4(t_q + col, *reinterpret_cast<const uint4*>(sfa_s + lane * 16));
+#pragma unroll
+        for (int c = 0; c < BN / 128; ++c)
+          tmem_st_4(t_q + col + 4 + 4 * c,
+                    *reinterpret_cast<const uint4*>(sfb_s + 512 * c + lane * 16));
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_sf(stage));
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+      }
+    }
   } else {
     // ================= epilogue: EPI_GROUPS warps per TMEM lane quarter
     // (warp & 3 = quarter; group g takes the g-th slice of the columns)
     const int q = warp & 3;
-    const int grp = (warp - 2) >> 2;
+    const int grp = (warp - EPI_WARP0) >> 2;
     const int row = q * 32 + lane;
     const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
     uint32_t acc_phase = 0;
@@ -337,18 +371,20 @@ static cudaError_t launch_single(const uint8_t* a, const uint8_t* sfa, const uin
   p.wait_limit = wait_limit_cycles();
   const int64_t tiles_bound = (ceil_div(M, BM) + E) * (int64_t)p.n_tiles_n;
   const int grid = (int)std::min<int64_t>(tiles_bound, num_sms());
-  kern<<<grid, THREADS, L::ALLOC, stream>>>(tmA, tmB, p);
+  kern<<<grid, THREADS1, L::ALLOC, stream>>>(tmA, tmB, p);
   return cudaGetLastError();
 }
 
-// The 1-SM kernel runs by default.  With mxmoe_set_gemm_2sm(1), 256-wide tiles
-// with MMA-layout scales go to the 2-SM kernel when the device can co-schedule
-// CTA pairs (it is exact, but measured slower on GB300 for these shapes).
+// Kernel choice (mxmoe_set_gemm_2sm): 256-wide tiles with MMA-layout scales go
+// to the 2-SM kernel when selected for this GEMM and the device can
+// co-schedule CTA pairs; both kernels give the same bytes.  By default gmm2
+// (bf16 out) takes the 2-SM kernel when experts average at least 8 m-tiles,
+// everything else the 1-SM kernel.
 template <int BN, bool kSwiglu, bool kTiledSF>
 static cudaError_t launch(const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
                           const uint8_t* sfb, const int64_t* offsets, int64_t M, int E, int K,
                           int Nw, int n_out, void* out, uint8_t* out_scale, cudaStream_t stream) {
-  if (BN == 256 && use_two_sm_gemm()) {
+  if (BN == 256 && use_two_sm_gemm(kSwiglu, M, E)) {
     const cudaError_t err = launch_pair<kSwiglu, kTiledSF>(a, sfa, b, sfb, offsets, M, E, K, Nw,
                                                            n_out, out, out_scale, stream);
     if (err != cudaErrorNotSupported) return err;

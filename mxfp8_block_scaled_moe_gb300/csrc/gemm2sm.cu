@@ -1,30 +1,35 @@
-// 2-SM grouped MXFP8 GEMM (tcgen05 cta_group::2), an opt-in alternative to
-// the 1-SM kernel of gemm.cu (mxmoe_set_gemm_2sm) for 256-wide tiles; same
-// contract, scales in the tiled layout of tiled_scales.h.  Exact (it gives
-// the 1-SM kernel's bytes), but measured slower on GB300 for the MoE shapes:
-// its stage loads see ~3-4 us issue-to-landed latency against ~1.5 us for the
-// 1-SM kernel, so the 6-stage ring, not the tensor pipe, sets its pace.
+// 2-SM grouped MXFP8 GEMM (tcgen05 cta_group::2) for 256-wide tiles with
+// scales in the tiled layout of tiled_scales.h; same contract as the 1-SM
+// kernel of gemm.cu, and bit-identical results.
 //
 // A cluster of two CTAs (on two SMs) computes a 256 x 256 tile: CTA r holds
 // m-tile 2u + r of the work unit's expert (128 token rows) and half r of the
 // 256 weight rows, in its own shared memory; one tcgen05.mma.cta_group::2
 // (M = 256, N = 256, K = 32) issued by the even CTA reads both CTAs' operands
 // and accumulates each CTA's 128 rows x 256 columns in that CTA's TMEM.  Per
-// 128-K stage each SM thus stages 32 KB (A 16 KB + half of B 16 KB) instead of
-// 48 KB (the 1-SM tile is bounded by shared-memory traffic: 48 KB written +
-// 48 KB read per stage).
+// 128-K stage each SM stages 32 KB (A 16 KB + half of B 16 KB) instead of the
+// 1-SM tile's 48 KB, so the pair pulls a third less from L2 per FLOP and six
+// stages fit where the 1-SM ring holds four.
 //
-// Synchronization (all waits bounded, as in the 1-SM kernel):
-//   full[s]    in the leader; count 2 (each CTA's producer arms it with its own
-//              bytes); every TMA load of both CTAs (operands and scale chunks)
-//              completes on it (cp.async.bulk.tensor .cta_group::2).
-//   empty[s]   in each CTA; the leader's tcgen05.commit is multicast to both.
-//   acc_full   in each CTA; likewise.
-//   acc_empty  in the leader; count 2 x EPI_WARPS: every epilogue warp of both
-//              CTAs arrives once it has drained its accumulator slice.
-// The tcgen05.cp of the scale factors is issued by the leader with
-// cta_group::2 and moves each CTA's staged chunks into its own TMEM (each CTA
-// stages its own A-row scales and all 256 weight rows' scales).
+// Roles (704 threads per CTA, as in the 1-SM kernel): warp 0 producer, warp 1
+// MMA issuer (even CTA only), warps 2-5 scale-factor writers (tcgen05.st, one
+// per TMEM lane quarter), warps 6-21 epilogue.
+//
+// Synchronization (every wait bounded, as in the 1-SM kernel):
+//   full[s]     in the leader, count 1: the leader's producer arms it with
+//               both CTAs' operand bytes; every operand TMA load of both
+//               CTAs (.cta_group::2 form) completes on it.  A peer load may
+//               land before the leader arms the phase; the pending arrival
+//               keeps the phase open until then.
+//   sf_full[s]  in each CTA, count 1: that CTA's scale chunks (bulk copies).
+//   sf_ready[s] in the leader, count 2 x SF_WARPS: the scale writers of both
+//               CTAs, once their TMEM stores of stage s are complete.
+//   empty[s]    in each CTA; the leader's tcgen05.commit is multicast to both.
+//   acc_full    in each CTA; likewise.
+//   acc_empty   in the leader, count 2 x EPI_WARPS: every epilogue warp of
+//               both CTAs, once it has drained its accumulator slice.
+// Each CTA's TMEM holds the scales of its own 128 A rows and of all 256 B
+// rows (both CTAs stage the B rows' scale chunks).
 #include "gemm_common.cuh"
 
 namespace mxmoe {
@@ -38,14 +43,13 @@ struct Layout2 {
   static constexpr int B_BYTES = 128 * BK;         // own half of the 256 weight rows
   static constexpr int SFA_BYTES = 512;
   static constexpr int SFB_BYTES = 1024;           // both 128-row halves
-  static constexpr int STAGE_TX = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + S * A_BYTES;
   static constexpr int OFF_SFA = OFF_B + S * B_BYTES;
   static constexpr int OFF_SFB = OFF_SFA + S * SFA_BYTES;
   static constexpr int OFF_BAR = OFF_SFB + S * SFB_BYTES;
-  // full[S], empty[S], acc_full, acc_empty, drain
-  static constexpr int NUM_BARS = 2 * S + 3;
+  // full[S], empty[S], sf_full[S], sf_ready[S], acc_full, acc_empty, drain
+  static constexpr int NUM_BARS = 4 * S + 3;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;   // tmem addr, abort flag
   static constexpr int OFF_OFFS = OFF_MISC + 16;
   static constexpr int OFF_TS = OFF_OFFS + (MAX_E + 1) * 8;
@@ -65,12 +69,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cluster_bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
-                   cluster_bar),
-               "r"(bytes)
-               : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -101,10 +99,6 @@ __device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, 
   }
   return true;
 }
-__device__ __forceinline__ void tc2_cp_sf(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
-               : "memory");
-}
 __device__ __forceinline__ void tc2_mma_mxf8(uint32_t d, uint64_t adesc, uint64_t bdesc,
                                              uint32_t idesc, uint32_t sfa, uint32_t sfb,
                                              uint32_t accumulate) {
@@ -126,13 +120,10 @@ __device__ __forceinline__ void tc2_commit_both(uint32_t bar) {
       : "memory");
 }
 
-// tmSF*: the tiled scale arrays seen as [chunks * 2, 256] bytes, so one
-// 512-byte chunk is a {256, 2} TMA box at row 2 * chunk.
 template <bool kSwiglu>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS1, 1)
     gemm2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmSFA,
-                   const __grid_constant__ CUtensorMap tmSFB, const Params p) {
+                   const Params p) {
   using L = Layout2;
   constexpr int STAGES = L::S;
   constexpr int BN = 256;
@@ -151,7 +142,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   int* s_mtb = reinterpret_cast<int*>(smem + L::OFF_MTB);
   auto bar_full = [&](int s) { return sbase + L::OFF_BAR + 8u * s; };
   auto bar_empty = [&](int s) { return sbase + L::OFF_BAR + 8u * (STAGES + s); };
-  const uint32_t bar_acc_full = sbase + L::OFF_BAR + 8u * (2 * STAGES);
+  auto bar_sff = [&](int s) { return sbase + L::OFF_BAR + 8u * (2 * STAGES + s); };
+  auto bar_sfr = [&](int s) { return sbase + L::OFF_BAR + 8u * (3 * STAGES + s); };
+  const uint32_t bar_acc_full = sbase + L::OFF_BAR + 8u * (4 * STAGES);
   const uint32_t bar_acc_empty = bar_acc_full + 8;
   const uint32_t bar_drain = bar_acc_full + 16;
 
@@ -161,8 +154,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   // ---- set-up
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar_full(s), 2);       // leader: armed by both CTAs' producers
-      mbar_init(bar_empty(s), 1);      // the leader's multicast commit
+      mbar_init(bar_full(s), 1);              // leader: its producer's expect_tx
+      mbar_init(bar_empty(s), 1);             // the leader's multicast commit
+      mbar_init(bar_sff(s), 1);               // this CTA's producer's expect_tx
+      mbar_init(bar_sfr(s), 2 * SF_WARPS);    // leader: scale writers of both CTAs
     }
     mbar_init(bar_acc_full, 1);
     mbar_init(bar_acc_empty, 2 * EPI_WARPS);  // leader: every epilogue warp of both CTAs
@@ -189,6 +184,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int KT = p.K / BK;
   // the leader's barriers as seen from this CTA
   const uint32_t lead_full0 = mapa_cluster(bar_full(0), 0);
+  const uint32_t lead_sfr0 = mapa_cluster(bar_sfr(0), 0);
   const uint32_t lead_acc_empty = mapa_cluster(bar_acc_empty, 0);
 
   if (warp == 0) {
@@ -207,23 +203,24 @@ __global__ void __launch_bounds__(THREADS, 1)
       // tiled A scales: the m-tile's block (a CTA without rows reads its expert's last block)
       const int64_t a_blk = min(s_mtb[e] + mt, s_mtb[e + 1] - 1);
       for (int kt = 0; kt < KT; ++kt) {
-        const bool got = wait_bar_cluster(bar_empty(stage), phase ^ 1, p.wait_limit, p.status, s_abort);
+        const bool got = wait_bar(bar_empty(stage), phase ^ 1, p.wait_limit, p.status, s_abort);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
         if (lane == 0) {
+          if (leader) mbar_arrive_expect_tx(bar_full(stage), 2 * (L::A_BYTES + L::B_BYTES));
+          mbar_arrive_expect_tx(bar_sff(stage), L::SFA_BYTES + L::SFB_BYTES);
           const uint32_t fb = lead_full0 + 8u * stage;  // leader's full[stage]
-          mbar_arrive_expect_tx_cluster(fb, L::STAGE_TX);
           const uint32_t sA = sbase + L::OFF_A + stage * L::A_BYTES;
           const uint32_t sB = sbase + L::OFF_B + stage * L::B_BYTES;
           const uint32_t sSFA = sbase + L::OFF_SFA + stage * L::SFA_BYTES;
           const uint32_t sSFB = sbase + L::OFF_SFB + stage * L::SFB_BYTES;
           tma_load_2d_pair(sA, &tmA, kt * BK, (int)row0, fb);
           tma_load_2d_pair(sB, &tmB, kt * BK, (int)(rank ? bh1 : bh0), fb);
-          tma_load_2d_pair(sSFA, &tmSFA, 0, (int)(2 * (a_blk * KT + kt)), fb);
-          tma_load_2d_pair(sSFB, &tmSFB, 0, (int)(2 * ((bh0 >> 7) * KT + kt)), fb);
-          tma_load_2d_pair(sSFB + 512, &tmSFB, 0, (int)(2 * ((bh1 >> 7) * KT + kt)), fb);
+          bulk_copy_g2s(sSFA, p.sfa + (a_blk * KT + kt) * 512, 512, bar_sff(stage));
+          bulk_copy_g2s(sSFB, p.sfb + ((bh0 >> 7) * KT + kt) * 512, 512, bar_sff(stage));
+          bulk_copy_g2s(sSFB + 512, p.sfb + ((bh1 >> 7) * KT + kt) * 512, 512, bar_sff(stage));
         }
         __syncwarp();
         if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -233,7 +230,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // tail: wait until the leader's MMAs have released every stage this CTA
       // loaded, so no commit of the pair is still on its way to this CTA
       for (int i = 0; i < STAGES; ++i) {
-        wait_bar_cluster(bar_empty(stage), phase ^ 1, p.wait_limit, p.status, s_abort);
+        wait_bar(bar_empty(stage), phase ^ 1, p.wait_limit, p.status, s_abort);
         if (++stage == STAGES) { stage = 0; phase ^= 1; }
       }
     } else {
@@ -257,20 +254,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         tc_fence_after();
         for (int kt = 0; kt < KT; ++kt) {
-          if (!wait_bar_cluster(bar_full(stage), phase, p.wait_limit, p.status, s_abort)) {
+          // both CTAs' operands landed, and both CTAs' scales are in TMEM
+          if (!wait_bar(bar_full(stage), phase, p.wait_limit, p.status, s_abort) ||
+              !wait_bar_cluster(bar_sfr(stage), phase, p.wait_limit, p.status, s_abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t sA = sbase + L::OFF_A + stage * L::A_BYTES;
           const uint32_t sB = sbase + L::OFF_B + stage * L::B_BYTES;
-          const uint32_t sSFA = sbase + L::OFF_SFA + stage * L::SFA_BYTES;
-          const uint32_t sSFB = sbase + L::OFF_SFB + stage * L::SFB_BYTES;
           const uint32_t t_sfa = tmem + SF_COL0 + stage * SF_COLS_PER_STAGE;
           const uint32_t t_sfb = t_sfa + 4;
-          tc2_cp_sf(t_sfa, make_sdesc(sSFA, 128, 128, 0));
-          tc2_cp_sf(t_sfb, make_sdesc(sSFB, 128, 128, 0));
-          tc2_cp_sf(t_sfb + 4, make_sdesc(sSFB + 512, 128, 128, 0));
           const uint64_t adesc = make_sdesc(sA, 16, 1024, 2);
           const uint64_t bdesc = make_sdesc(sB, 16, 1024, 2);
 #pragma unroll
@@ -297,10 +291,41 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
     __syncwarp();
+  } else if (warp < EPI_WARP0) {
+    // ================= scale-factor writers (both CTAs), one per TMEM lane
+    // quarter: this CTA's staged chunks (its A rows, all 256 B rows) go into
+    // its own TMEM; the leader's MMA waits for the writers of both CTAs.
+    const uint32_t t_q = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int unit = unit0; ok && unit < total_units; unit += unit_step) {
+      for (int kt = 0; kt < KT; ++kt) {
+        const bool got = wait_bar(bar_sff(stage), phase, p.wait_limit, p.status, s_abort);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* sfa_s = smem + L::OFF_SFA + stage * L::SFA_BYTES;
+        const uint8_t* sfb_s = smem + L::OFF_SFB + stage * L::SFB_BYTES;
+        const uint32_t col = SF_COL0 + stage * SF_COLS_PER_STAGE;
+        tmem_st_4(t_q + col, *reinterpret_cast<const uint4*>(sfa_s + lane * 16));
+        tmem_st_4(t_q + col + 4, *reinterpret_cast<const uint4*>(sfb_s + lane * 16));
+        tmem_st_4(t_q + col + 8, *reinterpret_cast<const uint4*>(sfb_s + 512 + lane * 16));
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) mbar_arrive(bar_sfr(stage));
+          else mbar_arrive_cluster(lead_sfr0 + 8u * stage);
+        }
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+      }
+    }
   } else {
     // ================= epilogue (both CTAs): EPI_GROUPS warps per TMEM lane quarter
     const int q = warp & 3;
-    const int grp = (warp - 2) >> 2;
+    const int grp = (warp - EPI_WARP0) >> 2;
     const int row = q * 32 + lane;
     const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
     uint32_t acc_phase = 0;
@@ -310,12 +335,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       mt = 2 * mt + (int)rank;
       const int64_t grow = s_off[e] + (int64_t)mt * BM + row;
       const bool valid = grow < s_off[e + 1];
-      const bool got = wait_bar_cluster(bar_acc_full, acc_phase, p.wait_limit, p.status, s_abort);
+      const bool got = wait_bar(bar_acc_full, acc_phase, p.wait_limit, p.status, s_abort);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
       epilogue_tile<BN, kSwiglu, true>(
           p, t_row, grp, row, lane, grow, valid, nt, (int64_t)(s_mtb[e] + mt) * BM + row,
-          [&] { if (lane == 0) mbar_arrive_cluster(lead_acc_empty); });
+          [&] {
+            if (lane == 0) {
+              if (leader) mbar_arrive(bar_acc_empty);
+              else mbar_arrive_cluster(lead_acc_empty);
+            }
+          });
       acc_phase ^= 1;
     }
   }
@@ -334,20 +364,6 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // ---------------------------------------------------------------- host side
-
-// uint8 [rows, 256] view of a tiled scale array: one chunk = box {256, 2}.
-static bool make_chunk_map(CUtensorMap* m, const void* base, uint64_t chunks) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {256, 2 * chunks};
-  cuuint64_t strides[1] = {256};
-  cuuint32_t box[2] = {256, 2};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
-                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
 
 template <bool kSwiglu>
 cudaError_t launch_pair_impl(const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
@@ -368,7 +384,7 @@ cudaError_t launch_pair_impl(const uint8_t* a, const uint8_t* sfa, const uint8_t
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.blockDim = dim3(THREADS1, 1, 1);
   cfg.dynamicSmemBytes = L::ALLOC;
   cfg.stream = stream;
   cfg.attrs = attr;
@@ -386,14 +402,9 @@ cudaError_t launch_pair_impl(const uint8_t* a, const uint8_t* sfa, const uint8_t
     configured[dev] = true;
   }
   if (max_clusters[dev] <= 0) return cudaErrorNotSupported;
-  const int KT = K / BK;
-  CUtensorMap tmA, tmB, tmSFA, tmSFB;
+  CUtensorMap tmA, tmB;
   if (!make_map(&tmA, a, (uint64_t)K, (uint64_t)M, BK, BM)) return cudaErrorInvalidValue;
   if (!make_map(&tmB, b, (uint64_t)K, (uint64_t)E * Nw, BK, 128)) return cudaErrorInvalidValue;
-  const uint64_t a_chunks = (uint64_t)(ceil_div(M, BM) + E) * KT;
-  const uint64_t b_chunks = (uint64_t)E * Nw / 128 * KT;
-  if (!make_chunk_map(&tmSFA, sfa, a_chunks)) return cudaErrorInvalidValue;
-  if (!make_chunk_map(&tmSFB, sfb, b_chunks)) return cudaErrorInvalidValue;
   Params p;
   p.sfa = sfa;
   p.sfb = sfb;
@@ -412,14 +423,14 @@ cudaError_t launch_pair_impl(const uint8_t* a, const uint8_t* sfa, const uint8_t
   const int clusters = (int)std::min<int64_t>(
       {units_bound, (int64_t)max_clusters[dev], (int64_t)num_sms() / 2});
   cfg.gridDim = dim3(2 * clusters, 1, 1);
-  return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmSFA, tmSFB, p);
+  return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
 }
 
 template <bool kSwiglu, bool kTiledSF>
 cudaError_t launch_pair(const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
                         const uint8_t* sfb, const int64_t* offsets, int64_t M, int E, int K,
                         int Nw, int n_out, void* out, uint8_t* out_scale, cudaStream_t stream) {
-  if (!kTiledSF) return cudaErrorNotSupported;  // scale chunks must be TMA-loadable
+  if (!kTiledSF) return cudaErrorNotSupported;  // scale chunks arrive by bulk copy
   return launch_pair_impl<kSwiglu>(a, sfa, b, sfb, offsets, M, E, K, Nw, n_out, out, out_scale,
                                    stream);
 }

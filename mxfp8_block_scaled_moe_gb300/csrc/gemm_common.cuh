@@ -22,7 +22,10 @@ constexpr int BM = 128;         // rows of A per CTA tile (tokens)
 constexpr int BK = 128;         // K elements (= bytes) per stage
 constexpr int EPI_WARPS = 16;   // epilogue warps (a multiple of 4)
 constexpr int EPI_GROUPS = EPI_WARPS / 4;
-constexpr int THREADS = 64 + 32 * EPI_WARPS;  // producer, MMA, epilogue
+constexpr int THREADS = 64 + 32 * EPI_WARPS;  // 2-SM kernel: producer, MMA, epilogue
+constexpr int SF_WARPS = 4;     // 1-SM kernel: one scale-factor writer per TMEM lane quarter
+constexpr int EPI_WARP0 = 2 + SF_WARPS;       // 1-SM kernel: first epilogue warp
+constexpr int THREADS1 = 32 * (EPI_WARP0 + EPI_WARPS);
 constexpr int MAX_E = 256;
 constexpr int TMEM_COLS = 512;
 constexpr int SF_COL0 = 256;    // scale factors after the accumulator
@@ -169,6 +172,15 @@ __device__ __forceinline__ void tmem_ld_32(uint32_t taddr, uint32_t (&r)[32]) {
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+// 32 TMEM lanes (this warp's quarter) x 4 columns from registers.
+__device__ __forceinline__ void tmem_st_4(uint32_t taddr, uint4 v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
 
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading
 // and stride byte offsets (>> 4), descriptor version 1 at bits 46-48, and
@@ -246,10 +258,13 @@ __device__ __forceinline__ uint32_t mapa_cluster(uint32_t saddr, uint32_t rank) 
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
-// Arrive on an mbarrier of another CTA of the cluster (cluster address).
+// Arrive on an mbarrier of another CTA of the cluster (cluster address), with
+// the default release at CTA scope: a cluster-scope release fences every prior
+// memory operation of the thread and costs on the order of a thousand cycles
+// per arrive.  The signals sent this way order tcgen05 work (TMEM stores and
+// loads, bracketed by tcgen05 thread-sync fences), not generic memory traffic.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
-               : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
 // ---------------------------------------------------------------- schedule
@@ -356,16 +371,51 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t t_row, i
     }
   } else {
     uint16_t* y = reinterpret_cast<uint16_t*>(p.out);
+    if constexpr (CH == 2) {
+      // x[s]: 32-byte sector s (16 columns) of this thread's 64-column row slice
+      uint32_t x[4][8];
 #pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      uint32_t o[16];
+      for (int c = 0; c < CH; ++c)
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        o[i] = cvt_bf16x2(__uint_as_float(v[c][2 * i]), __uint_as_float(v[c][2 * i + 1]));
-      if (valid) {
-        uint16_t* dst = y + grow * p.n_out + (int64_t)nt * BN + grp * PC + c * 32;
-        st_v8(dst, *reinterpret_cast<const uint32_t(*)[8]>(&o[0]));
-        st_v8(dst + 16, *reinterpret_cast<const uint32_t(*)[8]>(&o[8]));
+        for (int i = 0; i < 16; ++i)
+          x[2 * c + i / 8][i % 8] =
+              cvt_bf16x2(__uint_as_float(v[c][2 * i]), __uint_as_float(v[c][2 * i + 1]));
+      // 4 x 4 transpose of sectors inside each quad of lanes (two xor-shuffle
+      // rounds): afterwards lane q of a quad holds sector q of the quad's four
+      // rows, so one warp store writes 8 whole 128-byte lines instead of 32
+      // sectors of 32 different lines.
+      const int qi = lane & 3;
+      const bool odd = (qi & 1) != 0, hi = (qi & 2) != 0;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        uint32_t r = __shfl_xor_sync(0xffffffffu, odd ? x[0][w] : x[1][w], 1);
+        if (odd) x[0][w] = r; else x[1][w] = r;
+        r = __shfl_xor_sync(0xffffffffu, odd ? x[2][w] : x[3][w], 1);
+        if (odd) x[2][w] = r; else x[3][w] = r;
+        r = __shfl_xor_sync(0xffffffffu, hi ? x[0][w] : x[2][w], 2);
+        if (hi) x[0][w] = r; else x[2][w] = r;
+        r = __shfl_xor_sync(0xffffffffu, hi ? x[1][w] : x[3][w], 2);
+        if (hi) x[1][w] = r; else x[3][w] = r;
+      }
+      // the quad's rows are consecutive: row j of the quad is grow - qi + j
+      const int64_t col = (int64_t)nt * BN + grp * PC + qi * 16;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const bool ok = __shfl_sync(0xffffffffu, valid ? 1 : 0, (lane & ~3) + j) != 0;
+        if (ok) st_v8(y + (grow - qi + j) * p.n_out + col, x[j]);
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        uint32_t o[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          o[i] = cvt_bf16x2(__uint_as_float(v[c][2 * i]), __uint_as_float(v[c][2 * i + 1]));
+        if (valid) {
+          uint16_t* dst = y + grow * p.n_out + (int64_t)nt * BN + grp * PC + c * 32;
+          st_v8(dst, *reinterpret_cast<const uint32_t(*)[8]>(&o[0]));
+          st_v8(dst + 16, *reinterpret_cast<const uint32_t(*)[8]>(&o[8]));
+        }
       }
     }
   }

@@ -15,7 +15,7 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int num_sms();                       // of the current device (cached)
 int* device_status_ptr();            // library status word on the current device
 long long wait_limit_cycles();
-bool use_two_sm_gemm();              // opt-in 2-SM grouped GEMM kernel
+bool use_two_sm_gemm(bool swiglu, int64_t M, int E);  // 2-SM grouped GEMM kernel?
 
 cudaError_t launch_mx_quantize(const uint16_t* x, int64_t rows, int64_t K, uint8_t* q,
                                uint8_t* scale, cudaStream_t stream);

@@ -161,7 +161,8 @@ def test_layer_profile_segments(mm):
 
 @pytest.mark.parametrize("cfg", ["tiny", "qwen3_30b_decode", "qwen3_30b_prefill", "qwen3_235b_prefill"])
 def test_two_sm_and_one_sm_gemm_kernels_agree(mm, cfg):
-    """The 2-SM (cta_group::2) and 1-SM grouped GEMMs give the same layer bytes."""
+    """The 2-SM (cta_group::2) and 1-SM grouped GEMMs give the same layer bytes,
+    alone or mixed (the default sends gmm2 to the 2-SM kernel)."""
     shape = workloads.CONFIGS[cfg]
     inp = workloads.make_layer(shape, DEV)
     if shape.offline:
@@ -169,15 +170,16 @@ def test_two_sm_and_one_sm_gemm_kernels_agree(mm, cfg):
                                                 shape.k)
     else:
         layer = mm.MXFP8MoELayer.from_bf16(inp["w13"], inp["w2"], shape.k)
-    out1 = layer(inp["x"], inp["logits"])
-    mm.api.set_gemm_2sm(True)
+    outs = []
     try:
-        out2 = layer(inp["x"], inp["logits"])
+        for mode in (0, 1, "auto"):  # 1-SM, 2-SM, 2-SM for gmm2 only
+            mm.api.set_gemm_2sm(mode)
+            outs.append(layer(inp["x"], inp["logits"]))
     finally:
-        mm.api.set_gemm_2sm(False)
+        mm.api.set_gemm_2sm("auto")
     torch.cuda.synchronize()
     assert mm.device_status() == 0
-    assert torch.equal(out1, out2)
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
 
 
 @pytest.mark.parametrize("cfg,n_chunks", [("tiny", 3), ("qwen3_30b_decode", 0),
