@@ -38,9 +38,10 @@ L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0   # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 
-# DRAM traffic of one gmm1 launch from an ncu capture, keyed by the hash of the
-# GEMM source it was taken on (profiles/gemm1_swiglu_quant_qwen3_30b_prefill.md).
-NCU_TRAFFIC = {"0a79c3073112a1c8": 786962176}
+# dram__bytes_read.sum + dram__bytes_write.sum of one grouped GEMM1 launch on
+# the bench workload (profiles/gemm1_swiglu_quant_qwen3_30b_prefill.md), keyed
+# by the hash of the sources it was captured from
+NCU_TRAFFIC = {"12bc69eaddd33d11": 790586880}
 
 
 def parse():
