@@ -27,6 +27,7 @@ import os
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -47,7 +48,7 @@ NCU_TRAFFIC = {"12bc69eaddd33d11": 790586880}
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default=WORKLOAD)
@@ -89,7 +90,9 @@ def gemm_src_hash():
 
 
 class ClockSampler:
-    """nvidia-smi clocks/throttle sampling during the timed region."""
+    """nvidia-smi clocks/throttle sampling (every 50 ms) around the timed
+    region; `mark_start` / `mark_end` bracket the region and `summary` keeps
+    the samples that arrived inside it."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -99,34 +102,53 @@ class ClockSampler:
         self.gpu_index = gpu_index
         self.proc = None
         self.enabled = enabled
+        self.samples = []          # (arrival time, line)
+        self.t0 = self.t1 = None
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            if line.strip():
+                self.samples.append((time.time(), line))
 
     def __enter__(self):
         if self.enabled:
             try:
                 self.proc = subprocess.Popen(
                     ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
-                     "--format=csv,noheader,nounits", "-lms", "200"],
+                     "--format=csv,noheader,nounits", "-lms", "50"],
                     stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             except OSError:
                 self.proc = None
+            if self.proc is not None:
+                self.thread = threading.Thread(target=self._reader, daemon=True)
+                self.thread.start()
+                t_wait = time.time() + 3.0   # let the sampler start before the region
+                while not self.samples and time.time() < t_wait:
+                    time.sleep(0.01)
         return self
 
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
     def __exit__(self, *a):
-        self.lines = []
         if self.proc is not None:
-            time.sleep(0.25)
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+                self.proc.wait()
+            self.thread.join(timeout=5)
 
     def summary(self):
+        inside = [l for t, l in self.samples
+                  if self.t0 is not None and self.t1 is not None and self.t0 <= t <= self.t1]
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in getattr(self, "lines", []):
+        for l in inside:
             parts = [p.strip() for p in l.split(",")]
             if len(parts) < 9:
                 continue
@@ -141,7 +163,8 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "interval_ms": 50,
+                "region_s": round(self.t1 - self.t0, 3)}
 
 
 def algorithmic_bytes(T, H, E, k, I):
@@ -326,6 +349,7 @@ def main():
     mm.api.layer_profile_enable(True)   # CUDA events between the layer's kernels
     step_ms, prof = [], []
     with ClockSampler(local_rank, enabled=not args.no_clocks) as clk:
+        clk.mark_start()
         for _ in range(args.steps):
             flush.fill_(1)
             ev_a = torch.cuda.Event(enable_timing=True)
@@ -337,6 +361,7 @@ def main():
             step_ms.append(ev_a.elapsed_time(ev_b))
             prof.append(mm.api.layer_profile_read())
         torch.cuda.synchronize()
+        clk.mark_end()
     mm.api.layer_profile_enable(False)
     if world > 1:
         dist.barrier()
@@ -446,7 +471,7 @@ def main():
                     "d2h_bytes_per_step": d2h,
                     "ms_per_step": round(float(e2e_t_max.item()) / args.steps, 4)},
             "gpu_launches": 6 * args.steps,
-            "e2e_api": "moe_forward_mxfp8_host (pinned host buffers, 4096-token chunks, "
+            "e2e_api": "moe_forward_mxfp8_host (pinned host buffers, 8192-token chunks, "
                        "H2D / compute / D2H on three streams)",
             "cpu_baseline": cpu_base,
             "peaks": {"hbm_gbs": hbm, "fp8_tflops": fp8_peak, "source": peaks["source"]},

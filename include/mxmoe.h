@@ -256,7 +256,7 @@ mxmoe_status moe_forward_mxfp8_mma_scales(const uint16_t* x, const float* logits
 /*
  * The layer on HOST buffers, with the host<->device copies overlapped with
  * compute: the tokens are processed in n_chunks chunks (n_chunks <= 0: chunks
- * of 4096 tokens) through three library-owned streams (copy in, compute,
+ * of 8192 tokens) through three library-owned streams (copy in, compute,
  * copy out) and two device staging slots in ws, so chunk c's layer runs while
  * chunk c+1's inputs arrive and chunk c-1's output leaves.  Weight scales in
  * the MMA layout (mx_scales_to_mma_layout); weights stay on the device.

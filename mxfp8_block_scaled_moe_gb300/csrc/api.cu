@@ -443,8 +443,13 @@ static HostChunkLayout host_chunk_layout(int Tc, int H, int E, int k, int I) {
   return L;
 }
 
+// Default chunking: 8192-token chunks.  Every chunk re-reads all experts'
+// weights, so smaller chunks cost weight traffic while larger ones lengthen
+// the unoverlapped first copy-in and last copy-out (measured on GB300 for the
+// 16K-token Qwen3-30B-A3B layer: 2 chunks 1.27 ms, 4 chunks 1.29 ms, 8 chunks
+// 1.69 ms, 1 chunk 1.52 ms per call).
 static int host_chunk_tokens(int T, int n_chunks) {
-  if (n_chunks <= 0) n_chunks = T > 4096 ? (T + 4095) / 4096 : 1;
+  if (n_chunks <= 0) n_chunks = T > 8192 ? (T + 8191) / 8192 : 1;
   if (n_chunks > T) n_chunks = T > 0 ? T : 1;
   return (T + n_chunks - 1) / n_chunks;
 }
