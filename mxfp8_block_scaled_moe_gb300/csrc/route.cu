@@ -9,7 +9,8 @@
 //
 // Three kernels, one stream:
 //   1. route_topk_rank: one warp per token picks the top-k experts (descending
-//      logit, ties -> lower id) and their softmax weights; each 64-token block
+//      logit, ties -> lower id; k rounds of two warp reductions over
+//      order-preserving integer keys) and their softmax weights; each 64-token block
 //      marks its tokens in a per-expert 64-bit mask, from which every
 //      assignment's rank inside the block (flat order) and the block's
 //      per-expert histogram are popcounts.
@@ -33,9 +34,13 @@ namespace mxmoe {
 constexpr int kRouteThreads = 256;
 constexpr int kRouteWarps = kRouteThreads / 32;
 
-// Is (v, id) a better pick than (bv, bid)?  Larger logit, then lower id.
-__device__ __forceinline__ bool better(float v, int id, float bv, int bid) {
-  return v > bv || (v == bv && id < bid);
+// Total order of finite fp32 values as unsigned keys (-0 is ordered with +0).
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t b = __float_as_uint(v == 0.f ? 0.f : v);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
 constexpr int kTopkThreads = 1024;
@@ -66,31 +71,35 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_rank_kernel(
     const int t = t0 + tl;
     const float* row = logits + (int64_t)t * E;
     float v[EPL];
+    uint32_t key[EPL];
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
       const int e = lane + 32 * i;
-      v[i] = e < E ? row[e] : -INFINITY;
+      v[i] = e < E ? row[e] : 0.f;
+      key[i] = e < E ? order_key(v[i]) : 0u;  // 0: below every finite key
     }
+    // k rounds: the warp's largest remaining key (redux max), ties to the
+    // lowest expert id among the lanes holding it (redux min); within a lane
+    // the lowest index wins a tie (strict compare in increasing i).
     uint32_t taken = 0;
     int my_id = 0;
-    float my_val = 0.f;
+    uint32_t my_key = 0;
     for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int bid = 0x7fffffff;
+      uint32_t hk = 0u, hid = 0xFFFFFFFFu;
 #pragma unroll
       for (int i = 0; i < EPL; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u) && better(v[i], e, bv, bid)) { bv = v[i]; bid = e; }
+        const bool live = lane + 32 * i < E && !((taken >> i) & 1u);
+        if (live && (hid == 0xFFFFFFFFu || key[i] > hk)) {
+          hk = key[i];
+          hid = (uint32_t)(lane + 32 * i);
+        }
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oid = __shfl_xor_sync(0xffffffffu, bid, off);
-        if (better(ov, oid, bv, bid)) { bv = ov; bid = oid; }
-      }
-      if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
-      if (lane == j) { my_id = bid; my_val = bv; }
+      const uint32_t m = __reduce_max_sync(0xffffffffu, hk);
+      const uint32_t id = __reduce_min_sync(0xffffffffu, hk == m ? hid : 0xFFFFFFFFu);
+      if (hid == id) taken |= 1u << (id >> 5);
+      if (lane == j) { my_id = (int)id; my_key = m; }
     }
+    const float my_val = key_value(my_key);
     // softmax weights of the chosen experts
     const float vmax = __shfl_sync(0xffffffffu, my_val, 0);
     float denom;
@@ -143,9 +152,16 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int32_t* __restrict__ 
   const int per = (nb + G - 1) / G;
   const int b0 = g * per, b1 = min(nb, b0 + per);
   const bool active = g < G;
+  constexpr int R = 8;  // independent loads in flight per thread
   if (active) {
     int s = 0;
-    for (int b = b0; b < b1; ++b) s += hist[(int64_t)b * E + e];
+    for (int c = b0; c < b1; c += R) {
+      int vals[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) vals[r] = c + r < b1 ? hist[(int64_t)(c + r) * E + e] : 0;
+#pragma unroll
+      for (int r = 0; r < R; ++r) s += vals[r];
+    }
     s_part[g * E + e] = s;
   }
   __syncthreads();
@@ -161,10 +177,15 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int32_t* __restrict__ 
   __syncthreads();
   if (active) {
     int run = s_part[g * E + e];
-    for (int b = b0; b < b1; ++b) {
-      const int v = hist[(int64_t)b * E + e];
-      hist[(int64_t)b * E + e] = run;
-      run += v;
+    for (int c = b0; c < b1; c += R) {
+      int vals[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) vals[r] = c + r < b1 ? hist[(int64_t)(c + r) * E + e] : 0;
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        if (c + r < b1) hist[(int64_t)(c + r) * E + e] = run;
+        run += vals[r];
+      }
     }
   }
   // exclusive scan of the expert totals (E <= 1024), warp-shuffle based
