@@ -47,6 +47,8 @@ namespace mxmoe {
 namespace gemm {
 
 constexpr int STAGES1 = 4;
+constexpr int SEG = 8;           // k-slices per scale segment
+constexpr int SEG_COLS = 128;    // TMEM columns per segment buffer (16 per k-slice)
 
 template <int BN_>
 struct Layout1 {
@@ -54,26 +56,30 @@ struct Layout1 {
   static constexpr int S = STAGES1;
   static constexpr int A_BYTES = BM * BK;
   static constexpr int B_BYTES = BN * BK;
-  static constexpr int SFA_BYTES = 512;
-  static constexpr int SFB_BYTES = (BN / 128) * 512;
+  static constexpr int SFA_SEG = SEG * 512;               // one 512-byte chunk per k-slice
+  static constexpr int SFB_SEG = (BN / 128) * SEG * 512;  // per 128-row block of B
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + S * A_BYTES;
-  static constexpr int OFF_SFA = OFF_B + S * B_BYTES;
-  static constexpr int OFF_SFB = OFF_SFA + S * SFA_BYTES;
-  static constexpr int OFF_BAR = OFF_SFB + S * SFB_BYTES;
-  // full[S], empty[S], acc_full, acc_empty, drain, sf_ready[S]
-  static constexpr int NUM_BARS = 3 * S + 3;
+  static constexpr int OFF_SFA = OFF_B + S * B_BYTES;     // [2] segments
+  static constexpr int OFF_SFB = OFF_SFA + 2 * SFA_SEG;   // [2] segments
+  static constexpr int OFF_BAR = OFF_SFB + 2 * SFB_SEG;
+  // full[S], empty[S], acc_full, acc_empty, drain,
+  // sfs_full[2], sfs_free[2], sft_ready[2], sft_free[2]
+  static constexpr int NUM_BARS = 2 * S + 3 + 8;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;   // tmem addr, abort flag
   static constexpr int OFF_OFFS = OFF_MISC + 16;            // int64 offsets [E+1]
   static constexpr int OFF_TS = OFF_OFFS + (MAX_E + 1) * 8; // int unit start [E+1]
   static constexpr int OFF_MTB = OFF_TS + (MAX_E + 1) * 4;  // int m-tile base [E+1]
   static constexpr int BYTES = OFF_MTB + (MAX_E + 1) * 4;
   static constexpr int ALLOC = BYTES + 1024;                // 1 KB alignment slack
+  static_assert(ALLOC <= 232448, "shared memory");
+  static_assert(SF_COL0 + 2 * SEG_COLS <= TMEM_COLS, "tensor memory");
 };
 
 // kTiledSF: all scales (A, B and gmm1's output scales) use the tiled layout
-// of tiled_scales.h and each stage's scale chunks arrive by bulk copy;
-// otherwise they are the row-major [rows, K/32] arrays, staged by cp.async.
+// of tiled_scales.h (a segment's chunks are contiguous: one bulk copy per 128
+// rows); otherwise they are the row-major [rows, K/32] arrays, gathered into
+// the same staging layout by cp.async.
 template <int BN, bool kSwiglu, bool kTiledSF>
 __global__ void __launch_bounds__(THREADS1, 1)
     gemm1sm_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -96,20 +102,29 @@ __global__ void __launch_bounds__(THREADS1, 1)
   const uint32_t bar_acc_full = sbase + L::OFF_BAR + 8u * (2 * STAGES);
   const uint32_t bar_acc_empty = bar_acc_full + 8;
   const uint32_t bar_drain = bar_acc_full + 16;
-  auto bar_sf = [&](int s) { return sbase + L::OFF_BAR + 8u * (2 * STAGES + 3 + s); };
+  // scale segments: smem buffer landed / copied out, TMEM buffer written / consumed
+  auto bar_sfs_full = [&](int b) { return bar_acc_full + 24 + 8u * b; };
+  auto bar_sfs_free = [&](int b) { return bar_acc_full + 40 + 8u * b; };
+  auto bar_sft_ready = [&](int b) { return bar_acc_full + 56 + 8u * b; };
+  auto bar_sft_free = [&](int b) { return bar_acc_full + 72 + 8u * b; };
 
   const int E = p.E;
   // ---- set-up: barriers, TMEM, tile schedule
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      // producer expect_tx (+ 32 cp.async arrivals when scales come by cp.async)
-      mbar_init(bar_full(s), kTiledSF ? 1 : 1 + 32);
+      mbar_init(bar_full(s), 1);          // producer expect_tx
       mbar_init(bar_empty(s), 1);         // tcgen05.commit
-      mbar_init(bar_sf(s), SF_WARPS);     // scale factors in TMEM
     }
     mbar_init(bar_acc_full, 1);
     mbar_init(bar_acc_empty, EPI_WARPS);  // one arrive per epilogue warp
     mbar_init(bar_drain, 1);
+    for (int b = 0; b < 2; ++b) {
+      // expect_tx of the bulk copies, or the 32 producer lanes' cp.async arrivals
+      mbar_init(bar_sfs_full(b), kTiledSF ? 1 : 32);
+      mbar_init(bar_sfs_free(b), SF_WARPS);
+      mbar_init(bar_sft_ready(b), SF_WARPS);
+      mbar_init(bar_sft_free(b), 1);      // tcgen05.commit
+    }
     *s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async_smem();
@@ -129,13 +144,71 @@ __global__ void __launch_bounds__(THREADS1, 1)
   const int total_tiles = s_ts[E];
   const int KT = p.K / BK;
   const int K32 = p.K / 32;
+  const int nseg = (KT + SEG - 1) / SEG;  // scale segments per tile
 
   if (warp == 0) {
-    // ================= producer
+    // ================= producer: operand stages, and each tile segment's
+    // scales one segment ahead of the operands (segment g+1 is requested
+    // when segment g's first stage is)
     int stage = 0;
     uint32_t phase = 0;
     uint32_t armed = 0, armed_parity = 0;  // per-stage bit masks, for the abort drain
+    int g = 0;                             // global segment index of the operand loads
     bool ok = true;
+    // request the scales of segment (tile, sg) into buffer gseg & 1
+    auto load_scales = [&](int gseg, int tile, int sg) -> bool {
+      const int b = gseg & 1;
+      const uint32_t par = ((uint32_t)(gseg >> 1) & 1u) ^ 1u;
+      const bool got = wait_bar(bar_sfs_free(b), par, p.wait_limit, p.status, s_abort);
+      if (!__all_sync(0xffffffffu, got)) return false;
+      int e, mt, nt;
+      decode_tile(tile, s_ts, E, p.n_tiles_n, e, mt, nt);
+      const int64_t row0 = s_off[e] + (int64_t)mt * BM;
+      const int64_t brow = (int64_t)e * p.Nw;
+      const int64_t bh0 = kSwiglu ? brow + (int64_t)nt * (BN / 2) : brow + (int64_t)nt * BN;
+      const int64_t bh1 = brow + p.n_out + (int64_t)nt * (BN / 2);
+      const int kt0 = sg * SEG, len = min(SEG, KT - kt0);
+      const uint32_t sA = sbase + L::OFF_SFA + b * L::SFA_SEG;
+      const uint32_t sB = sbase + L::OFF_SFB + b * L::SFB_SEG;
+      if (kTiledSF) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar_sfs_full(b), (uint32_t)((1 + BN / 128) * len * 512));
+          bulk_copy_g2s(sA, p.sfa + ((int64_t)(s_mtb[e] + mt) * KT + kt0) * 512,
+                        (uint32_t)(len * 512), bar_sfs_full(b));
+#pragma unroll
+          for (int c = 0; c < BN / 128; ++c) {
+            const int64_t wrow = kSwiglu ? (c == 0 ? bh0 : bh1) : bh0 + 128 * c;
+            bulk_copy_g2s(sB + c * SEG * 512, p.sfb + ((wrow >> 7) * KT + kt0) * 512,
+                          (uint32_t)(len * 512), bar_sfs_full(b));
+          }
+        }
+      } else {
+        // 4 bytes (4 K-blocks) per row and k-slice into the staging layout
+        // byte (r % 32) * 16 + (r / 32) * 4 + kb of each 512-byte chunk
+        for (int i = 0; i < len; ++i) {
+          const int kt = kt0 + i;
+#pragma unroll
+          for (int q = 0; q < BM / 32; ++q) {
+            const int r = lane + 32 * q;
+            const int64_t grow = row0 + r;
+            const bool valid = grow < p.M;
+            const uint8_t* src = valid ? p.sfa + grow * K32 + kt * 4 : p.sfa;
+            cp_async_4(sA + i * 512 + (r & 31) * 16 + (r >> 5) * 4, src, valid ? 4u : 0u);
+          }
+#pragma unroll
+          for (int q = 0; q < BN / 32; ++q) {
+            const int r = lane + 32 * q;
+            const int64_t wrow = kSwiglu ? (r < BN / 2 ? bh0 + r : bh1 + (r - BN / 2)) : bh0 + r;
+            const int rr = r & 127;
+            cp_async_4(sB + (r >> 7) * SEG * 512 + i * 512 + (rr & 31) * 16 + (rr >> 5) * 4,
+                       p.sfb + wrow * K32 + kt * 4, 4u);
+          }
+        }
+        cp_async_mbar_arrive_noinc(bar_sfs_full(b));
+      }
+      return true;
+    };
+    if (blockIdx.x < total_tiles) ok = load_scales(0, blockIdx.x, 0);
     for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
       int e, mt, nt;
       decode_tile(tile, s_ts, E, p.n_tiles_n, e, mt, nt);
@@ -145,6 +218,16 @@ __global__ void __launch_bounds__(THREADS1, 1)
       const int64_t bh0 = kSwiglu ? brow + (int64_t)nt * (BN / 2) : brow + (int64_t)nt * BN;
       const int64_t bh1 = brow + p.n_out + (int64_t)nt * (BN / 2);
       for (int kt = 0; kt < KT; ++kt) {
+        if (kt % SEG == 0) {
+          // the next segment's scales: later in this tile, or the next tile's first
+          const int sg = kt / SEG;
+          const int ntile = sg + 1 < nseg ? tile : tile + (int)gridDim.x;
+          if (ntile < total_tiles && !load_scales(g + 1, ntile, sg + 1 < nseg ? sg + 1 : 0)) {
+            ok = false;
+            break;
+          }
+          ++g;
+        }
         const bool got = wait_bar(bar_empty(stage), phase ^ 1, p.wait_limit, p.status, s_abort);
         if (!__all_sync(0xffffffffu, got)) {  // keep the warp converged
           ok = false;
@@ -152,11 +235,8 @@ __global__ void __launch_bounds__(THREADS1, 1)
         }
         const uint32_t sA = sbase + L::OFF_A + stage * L::A_BYTES;
         const uint32_t sB = sbase + L::OFF_B + stage * L::B_BYTES;
-        const uint32_t sSFA = sbase + L::OFF_SFA + stage * L::SFA_BYTES;
-        const uint32_t sSFB = sbase + L::OFF_SFB + stage * L::SFB_BYTES;
         if (lane == 0) {
-          mbar_arrive_expect_tx(bar_full(stage), L::A_BYTES + L::B_BYTES +
-                                                     (kTiledSF ? L::SFA_BYTES + L::SFB_BYTES : 0));
+          mbar_arrive_expect_tx(bar_full(stage), L::A_BYTES + L::B_BYTES);
           tma_load_2d(sA, &tmA, kt * BK, (int)row0, bar_full(stage));
           if (kSwiglu) {
             tma_load_2d(sB, &tmB, kt * BK, (int)bh0, bar_full(stage));
@@ -164,38 +244,6 @@ __global__ void __launch_bounds__(THREADS1, 1)
           } else {
             tma_load_2d(sB, &tmB, kt * BK, (int)bh0, bar_full(stage));
           }
-          if (kTiledSF) {
-            // one 512-byte chunk per 128 rows: A's m-tile block, B's row blocks
-            bulk_copy_g2s(sSFA, p.sfa + ((int64_t)(s_mtb[e] + mt) * KT + kt) * 512, 512,
-                          bar_full(stage));
-#pragma unroll
-            for (int c = 0; c < BN / 128; ++c) {
-              const int64_t wrow = kSwiglu ? (c == 0 ? bh0 : bh1) : bh0 + 128 * c;
-              bulk_copy_g2s(sSFB + 512 * c, p.sfb + ((wrow >> 7) * KT + kt) * 512, 512,
-                            bar_full(stage));
-            }
-          }
-        }
-        if (!kTiledSF) {
-          // scale factors: 4 bytes (4 K-blocks) per row, staged as
-          // byte(r, kb) = (r % 32) * 16 + (r / 32) * 4 + kb per 128-row chunk
-#pragma unroll
-          for (int i = 0; i < BM / 32; ++i) {
-            const int r = lane + 32 * i;
-            const int64_t grow = row0 + r;
-            const bool valid = grow < p.M;
-            const uint8_t* src = valid ? p.sfa + grow * K32 + kt * 4 : p.sfa;
-            cp_async_4(sSFA + (r & 31) * 16 + (r >> 5) * 4, src, valid ? 4u : 0u);
-          }
-#pragma unroll
-          for (int i = 0; i < BN / 32; ++i) {
-            const int r = lane + 32 * i;
-            const int64_t wrow = kSwiglu ? (r < BN / 2 ? bh0 + r : bh1 + (r - BN / 2)) : bh0 + r;
-            const int rr = r & 127;
-            cp_async_4(sSFB + (r >> 7) * 512 + (rr & 31) * 16 + (rr >> 5) * 4,
-                       p.sfb + wrow * K32 + kt * 4, 4u);
-          }
-          cp_async_mbar_arrive_noinc(bar_full(stage));
         }
         armed |= 1u << stage;
         if (phase) armed_parity |= 1u << stage; else armed_parity &= ~(1u << stage);
@@ -211,11 +259,15 @@ __global__ void __launch_bounds__(THREADS1, 1)
           wait_bar(bar_full(s), (armed_parity >> s) & 1u, 1ll << 32, nullptr, &no_abort);
         }
     }
+    // every requested scale segment is consumed by the scale writers, which
+    // wait for its copies; this thread's own cp.async complete here
+    cp_async_wait_all();
   } else if (warp == 1) {
     // ================= MMA issuer (one thread)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
+      int g = 0;
       bool ok = true;
       bool issued = false;
       constexpr uint32_t IDESC = make_idesc(BM, BN);
@@ -226,16 +278,24 @@ __global__ void __launch_bounds__(THREADS1, 1)
         }
         tc_fence_after();
         for (int kt = 0; kt < KT; ++kt) {
-          // operands landed, and this stage's scale factors are in TMEM
-          if (!wait_bar(bar_full(stage), phase, p.wait_limit, p.status, s_abort) ||
-              !wait_bar(bar_sf(stage), phase, p.wait_limit, p.status, s_abort)) {
+          const int i = kt % SEG;
+          const int b = g & 1;
+          if (i == 0) {
+            // this segment's scales are in TMEM buffer b
+            if (!wait_bar(bar_sft_ready(b), (uint32_t)(g >> 1) & 1u, p.wait_limit, p.status,
+                          s_abort)) {
+              ok = false;
+              break;
+            }
+          }
+          if (!wait_bar(bar_full(stage), phase, p.wait_limit, p.status, s_abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t sA = sbase + L::OFF_A + stage * L::A_BYTES;
           const uint32_t sB = sbase + L::OFF_B + stage * L::B_BYTES;
-          const uint32_t t_sfa = tmem + SF_COL0 + stage * SF_COLS_PER_STAGE;
+          const uint32_t t_sfa = tmem + SF_COL0 + b * SEG_COLS + i * 16;
           const uint32_t t_sfb = t_sfa + 4;
           const uint64_t adesc = make_sdesc(sA, 16, 1024, 2);
           const uint64_t bdesc = make_sdesc(sB, 16, 1024, 2);
@@ -247,6 +307,10 @@ __global__ void __launch_bounds__(THREADS1, 1)
           }
           issued = true;
           tc_commit(bar_empty(stage));
+          if (i == SEG - 1 || kt == KT - 1) {
+            tc_commit(bar_sft_free(b));  // the segment's scales may be overwritten
+            ++g;
+          }
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
@@ -263,36 +327,44 @@ __global__ void __launch_bounds__(THREADS1, 1)
     __syncwarp();
   } else if (warp < EPI_WARP0) {
     // ================= scale-factor writers, one per TMEM lane quarter
-    // (warp & 3): each stage's staged chunks (byte (r % 32) * 16 + (r / 32) *
-    // 4 + kb of 128 rows) go from shared memory into this quarter's lanes,
-    // 16 bytes (4 columns) per lane and chunk.  Every quarter holds the whole
-    // chunk, the layout the block-scaled MMA reads for M = 128.  Register
-    // stores keep these copies out of the tensor pipe, where tcgen05.cp
-    // would serialize with the MMAs.
+    // (warp & 3): a segment's staged chunks (byte (r % 32) * 16 + (r / 32) *
+    // 4 + kb of 128 rows, per k-slice) go from shared memory into this
+    // quarter's lanes, 16 bytes (4 columns) per lane and chunk.  Every quarter
+    // holds the whole chunk, the layout the block-scaled MMA reads for
+    // M = 128.  Register stores keep these copies out of the tensor pipe,
+    // where tcgen05.cp would serialize with the MMAs.
     const uint32_t t_q = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    int stage = 0;
-    uint32_t phase = 0;
+    int g = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-      for (int kt = 0; kt < KT; ++kt) {
-        const bool got = wait_bar(bar_full(stage), phase, p.wait_limit, p.status, s_abort);
+      for (int sg = 0; sg < nseg; ++sg, ++g) {
+        const int b = g & 1;
+        const uint32_t par = (uint32_t)(g >> 1) & 1u;
+        // staged in shared memory, and the MMAs that last read TMEM buffer b are done
+        const bool got = wait_bar(bar_sfs_full(b), par, p.wait_limit, p.status, s_abort) &&
+                         wait_bar(bar_sft_free(b), par ^ 1u, p.wait_limit, p.status, s_abort);
         if (!__all_sync(0xffffffffu, got)) {  // keep the warp converged
           ok = false;
           break;
         }
-        const uint8_t* sfa_s = smem + L::OFF_SFA + stage * L::SFA_BYTES;
-        const uint8_t* sfb_s = smem + L::OFF_SFB + stage * L::SFB_BYTES;
-        const uint32_t col = SF_COL0 + stage * SF_COLS_PER_STAGE;
-        tmem_st_4(t_q + col, *reinterpret_cast<const uint4*>(sfa_s + lane * 16));
+        const int len = min(SEG, KT - sg * SEG);
+        const uint8_t* sfa_s = smem + L::OFF_SFA + b * L::SFA_SEG;
+        const uint8_t* sfb_s = smem + L::OFF_SFB + b * L::SFB_SEG;
+        for (int i = 0; i < len; ++i) {
+          const uint32_t col = SF_COL0 + b * SEG_COLS + i * 16;
+          tmem_st_4(t_q + col, *reinterpret_cast<const uint4*>(sfa_s + i * 512 + lane * 16));
 #pragma unroll
-        for (int c = 0; c < BN / 128; ++c)
-          tmem_st_4(t_q + col + 4 + 4 * c,
-                    *reinterpret_cast<const uint4*>(sfb_s + 512 * c + lane * 16));
+          for (int c = 0; c < BN / 128; ++c)
+            tmem_st_4(t_q + col + 4 + 4 * c, *reinterpret_cast<const uint4*>(
+                                                  sfb_s + c * SEG * 512 + i * 512 + lane * 16));
+        }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_sf(stage));
-        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        if (lane == 0) {
+          mbar_arrive(bar_sft_ready(b));
+          mbar_arrive(bar_sfs_free(b));
+        }
       }
     }
   } else {
