@@ -306,8 +306,8 @@ void mxmoe_set_wait_limit_cycles(long long cycles);
  * kernel.  mode 1: 256-wide tiles with MMA-layout scales (the layer calls)
  * run the 2-SM kernel (tcgen05 cta_group::2 over CTA pairs) when the device
  * can co-schedule pairs.  mode 2 (the default): the 2-SM kernel for the
- * bf16-output GEMM (grouped GEMM2) when its rows average at least 1024 per
- * expert (M >= 1024 * E), the 1-SM kernel otherwise.  Other values select
+ * bf16-output GEMM (grouped GEMM2) when its rows average at least 512 per
+ * expert (M >= 512 * E), the 1-SM kernel otherwise.  Other values select
  * mode 2.
  */
 void mxmoe_set_gemm_2sm(int mode);

@@ -450,7 +450,7 @@ static cudaError_t launch_single(const uint8_t* a, const uint8_t* sfa, const uin
 // Kernel choice (mxmoe_set_gemm_2sm): 256-wide tiles with MMA-layout scales go
 // to the 2-SM kernel when selected for this GEMM and the device can
 // co-schedule CTA pairs; both kernels give the same bytes.  By default gmm2
-// (bf16 out) takes the 2-SM kernel when experts average at least 8 m-tiles,
+// (bf16 out) takes the 2-SM kernel when experts average at least 4 m-tiles,
 // everything else the 1-SM kernel.
 template <int BN, bool kSwiglu, bool kTiledSF>
 static cudaError_t launch(const uint8_t* a, const uint8_t* sfa, const uint8_t* b,

@@ -36,26 +36,31 @@ namespace mxmoe {
 namespace gemm {
 
 constexpr int STAGES2 = 6;
+constexpr int SEG2 = 8;           // k-slices per scale segment
+constexpr int SEG2_COLS = 128;    // TMEM columns per segment buffer (16 per k-slice)
 
 struct Layout2 {
   static constexpr int S = STAGES2;
   static constexpr int A_BYTES = BM * BK;          // own 128 rows
   static constexpr int B_BYTES = 128 * BK;         // own half of the 256 weight rows
-  static constexpr int SFA_BYTES = 512;
-  static constexpr int SFB_BYTES = 1024;           // both 128-row halves
+  static constexpr int SFA_SEG = SEG2 * 512;       // own A rows: one chunk per k-slice
+  static constexpr int SFB_SEG = 2 * SEG2 * 512;   // both 128-row blocks of B
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + S * A_BYTES;
-  static constexpr int OFF_SFA = OFF_B + S * B_BYTES;
-  static constexpr int OFF_SFB = OFF_SFA + S * SFA_BYTES;
-  static constexpr int OFF_BAR = OFF_SFB + S * SFB_BYTES;
-  // full[S], empty[S], sf_full[S], sf_ready[S], acc_full, acc_empty, drain
-  static constexpr int NUM_BARS = 4 * S + 3;
+  static constexpr int OFF_SFA = OFF_B + S * B_BYTES;     // [2] segments
+  static constexpr int OFF_SFB = OFF_SFA + 2 * SFA_SEG;   // [2] segments
+  static constexpr int OFF_BAR = OFF_SFB + 2 * SFB_SEG;
+  // full[S], empty[S], acc_full, acc_empty, drain,
+  // sfs_full[2], sfs_free[2], sft_ready[2], sft_free[2]
+  static constexpr int NUM_BARS = 2 * S + 3 + 8;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;   // tmem addr, abort flag
   static constexpr int OFF_OFFS = OFF_MISC + 16;
   static constexpr int OFF_TS = OFF_OFFS + (MAX_E + 1) * 8;
   static constexpr int OFF_MTB = OFF_TS + (MAX_E + 1) * 4;
   static constexpr int BYTES = OFF_MTB + (MAX_E + 1) * 4;
   static constexpr int ALLOC = BYTES + 1024;
+  static_assert(ALLOC <= 232448, "shared memory");
+  static_assert(SF_COL0 + 2 * SEG2_COLS <= TMEM_COLS, "tensor memory");
 };
 
 // ---------------------------------------------------------------- cta_group::2 PTX
@@ -142,11 +147,15 @@ __global__ void __launch_bounds__(THREADS1, 1)
   int* s_mtb = reinterpret_cast<int*>(smem + L::OFF_MTB);
   auto bar_full = [&](int s) { return sbase + L::OFF_BAR + 8u * s; };
   auto bar_empty = [&](int s) { return sbase + L::OFF_BAR + 8u * (STAGES + s); };
-  auto bar_sff = [&](int s) { return sbase + L::OFF_BAR + 8u * (2 * STAGES + s); };
-  auto bar_sfr = [&](int s) { return sbase + L::OFF_BAR + 8u * (3 * STAGES + s); };
-  const uint32_t bar_acc_full = sbase + L::OFF_BAR + 8u * (4 * STAGES);
+  const uint32_t bar_acc_full = sbase + L::OFF_BAR + 8u * (2 * STAGES);
   const uint32_t bar_acc_empty = bar_acc_full + 8;
   const uint32_t bar_drain = bar_acc_full + 16;
+  // scale segments: this CTA's smem buffer landed / copied out (local), TMEM
+  // buffers of both CTAs written (leader) / consumed (multicast commit)
+  auto bar_sfs_full = [&](int b) { return bar_acc_full + 24 + 8u * b; };
+  auto bar_sfs_free = [&](int b) { return bar_acc_full + 40 + 8u * b; };
+  auto bar_sft_ready = [&](int b) { return bar_acc_full + 56 + 8u * b; };
+  auto bar_sft_free = [&](int b) { return bar_acc_full + 72 + 8u * b; };
 
   const int E = p.E;
   const int unit0 = blockIdx.x >> 1;  // cluster index
@@ -156,12 +165,16 @@ __global__ void __launch_bounds__(THREADS1, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full(s), 1);              // leader: its producer's expect_tx
       mbar_init(bar_empty(s), 1);             // the leader's multicast commit
-      mbar_init(bar_sff(s), 1);               // this CTA's producer's expect_tx
-      mbar_init(bar_sfr(s), 2 * SF_WARPS);    // leader: scale writers of both CTAs
     }
     mbar_init(bar_acc_full, 1);
     mbar_init(bar_acc_empty, 2 * EPI_WARPS);  // leader: every epilogue warp of both CTAs
     mbar_init(bar_drain, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_sfs_full(b), 1);          // this CTA's producer's expect_tx
+      mbar_init(bar_sfs_free(b), SF_WARPS);   // this CTA's scale writers
+      mbar_init(bar_sft_ready(b), 2 * SF_WARPS);  // leader: scale writers of both CTAs
+      mbar_init(bar_sft_free(b), 1);          // the leader's multicast commit
+    }
     *s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async_smem();
@@ -182,27 +195,68 @@ __global__ void __launch_bounds__(THREADS1, 1)
   const uint32_t tmem = *s_tmem;
   const int total_units = s_ts[E];
   const int KT = p.K / BK;
+  const int nseg = (KT + SEG2 - 1) / SEG2;  // scale segments per unit
   // the leader's barriers as seen from this CTA
   const uint32_t lead_full0 = mapa_cluster(bar_full(0), 0);
-  const uint32_t lead_sfr0 = mapa_cluster(bar_sfr(0), 0);
+  const uint32_t lead_sftr0 = mapa_cluster(bar_sft_ready(0), 0);
   const uint32_t lead_acc_empty = mapa_cluster(bar_acc_empty, 0);
 
+  // B row blocks of a unit: gmm1 = gate rows | up rows, gmm2 = 256 rows
+  auto unit_rows = [&](int unit, int& e, int& mt, int& nt, int64_t& bh0, int64_t& bh1) {
+    decode_tile(unit, s_ts, E, p.n_tiles_n, e, mt, nt);
+    mt = 2 * mt + (int)rank;  // this CTA's m-tile of the unit's pair
+    const int64_t brow = (int64_t)e * p.Nw;
+    bh0 = kSwiglu ? brow + (int64_t)nt * (BN / 2) : brow + (int64_t)nt * BN;
+    bh1 = kSwiglu ? brow + p.n_out + (int64_t)nt * (BN / 2) : bh0 + BN / 2;
+  };
+
   if (warp == 0) {
-    // ================= producer (both CTAs)
+    // ================= producer (both CTAs): operand stages, and each unit
+    // segment's scales (this CTA's A rows, all 256 B rows) one segment ahead
     int stage = 0;
     uint32_t phase = 0;
+    int g = 0;
     bool ok = true;
+    auto load_scales = [&](int gseg, int unit, int sg) -> bool {
+      const int b = gseg & 1;
+      const uint32_t par = ((uint32_t)(gseg >> 1) & 1u) ^ 1u;
+      const bool got = wait_bar(bar_sfs_free(b), par, p.wait_limit, p.status, s_abort);
+      if (!__all_sync(0xffffffffu, got)) return false;
+      if (lane == 0) {
+        int e, mt, nt;
+        int64_t bh0, bh1;
+        unit_rows(unit, e, mt, nt, bh0, bh1);
+        // tiled A scales: the m-tile's block (a CTA without rows reads its expert's last block)
+        const int64_t a_blk = min(s_mtb[e] + mt, s_mtb[e + 1] - 1);
+        const int kt0 = sg * SEG2, len = min(SEG2, KT - kt0);
+        const uint32_t sA = sbase + L::OFF_SFA + b * L::SFA_SEG;
+        const uint32_t sB = sbase + L::OFF_SFB + b * L::SFB_SEG;
+        mbar_arrive_expect_tx(bar_sfs_full(b), (uint32_t)(3 * len * 512));
+        bulk_copy_g2s(sA, p.sfa + (a_blk * KT + kt0) * 512, (uint32_t)(len * 512), bar_sfs_full(b));
+        bulk_copy_g2s(sB, p.sfb + ((bh0 >> 7) * KT + kt0) * 512, (uint32_t)(len * 512),
+                      bar_sfs_full(b));
+        bulk_copy_g2s(sB + SEG2 * 512, p.sfb + ((bh1 >> 7) * KT + kt0) * 512,
+                      (uint32_t)(len * 512), bar_sfs_full(b));
+      }
+      __syncwarp();
+      return true;
+    };
+    if (unit0 < total_units) ok = load_scales(0, unit0, 0);
     for (int unit = unit0; ok && unit < total_units; unit += unit_step) {
       int e, mt, nt;
-      decode_tile(unit, s_ts, E, p.n_tiles_n, e, mt, nt);
-      mt = 2 * mt + (int)rank;
+      int64_t bh0, bh1;
+      unit_rows(unit, e, mt, nt, bh0, bh1);
       const int64_t row0 = s_off[e] + (int64_t)mt * BM;
-      const int64_t brow = (int64_t)e * p.Nw;
-      const int64_t bh0 = kSwiglu ? brow + (int64_t)nt * (BN / 2) : brow + (int64_t)nt * BN;
-      const int64_t bh1 = kSwiglu ? brow + p.n_out + (int64_t)nt * (BN / 2) : bh0 + BN / 2;
-      // tiled A scales: the m-tile's block (a CTA without rows reads its expert's last block)
-      const int64_t a_blk = min(s_mtb[e] + mt, s_mtb[e + 1] - 1);
       for (int kt = 0; kt < KT; ++kt) {
+        if (kt % SEG2 == 0) {
+          const int sg = kt / SEG2;
+          const int nunit = sg + 1 < nseg ? unit : unit + unit_step;
+          if (nunit < total_units && !load_scales(g + 1, nunit, sg + 1 < nseg ? sg + 1 : 0)) {
+            ok = false;
+            break;
+          }
+          ++g;
+        }
         const bool got = wait_bar(bar_empty(stage), phase ^ 1, p.wait_limit, p.status, s_abort);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
@@ -210,17 +264,11 @@ __global__ void __launch_bounds__(THREADS1, 1)
         }
         if (lane == 0) {
           if (leader) mbar_arrive_expect_tx(bar_full(stage), 2 * (L::A_BYTES + L::B_BYTES));
-          mbar_arrive_expect_tx(bar_sff(stage), L::SFA_BYTES + L::SFB_BYTES);
           const uint32_t fb = lead_full0 + 8u * stage;  // leader's full[stage]
           const uint32_t sA = sbase + L::OFF_A + stage * L::A_BYTES;
           const uint32_t sB = sbase + L::OFF_B + stage * L::B_BYTES;
-          const uint32_t sSFA = sbase + L::OFF_SFA + stage * L::SFA_BYTES;
-          const uint32_t sSFB = sbase + L::OFF_SFB + stage * L::SFB_BYTES;
           tma_load_2d_pair(sA, &tmA, kt * BK, (int)row0, fb);
           tma_load_2d_pair(sB, &tmB, kt * BK, (int)(rank ? bh1 : bh0), fb);
-          bulk_copy_g2s(sSFA, p.sfa + (a_blk * KT + kt) * 512, 512, bar_sff(stage));
-          bulk_copy_g2s(sSFB, p.sfb + ((bh0 >> 7) * KT + kt) * 512, 512, bar_sff(stage));
-          bulk_copy_g2s(sSFB + 512, p.sfb + ((bh1 >> 7) * KT + kt) * 512, 512, bar_sff(stage));
         }
         __syncwarp();
         if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -244,6 +292,7 @@ __global__ void __launch_bounds__(THREADS1, 1)
     if (leader && lane == 0) {
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
+      int g = 0;
       bool ok = true;
       bool issued = false;
       constexpr uint32_t IDESC = make_idesc(2 * BM, BN);
@@ -254,16 +303,23 @@ __global__ void __launch_bounds__(THREADS1, 1)
         }
         tc_fence_after();
         for (int kt = 0; kt < KT; ++kt) {
-          // both CTAs' operands landed, and both CTAs' scales are in TMEM
-          if (!wait_bar(bar_full(stage), phase, p.wait_limit, p.status, s_abort) ||
-              !wait_bar_cluster(bar_sfr(stage), phase, p.wait_limit, p.status, s_abort)) {
+          const int i = kt % SEG2;
+          const int b = g & 1;
+          // both CTAs' scales of this segment are in TMEM buffer b
+          if (i == 0 && !wait_bar_cluster(bar_sft_ready(b), (uint32_t)(g >> 1) & 1u,
+                                          p.wait_limit, p.status, s_abort)) {
+            ok = false;
+            break;
+          }
+          // both CTAs' operands landed
+          if (!wait_bar(bar_full(stage), phase, p.wait_limit, p.status, s_abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t sA = sbase + L::OFF_A + stage * L::A_BYTES;
           const uint32_t sB = sbase + L::OFF_B + stage * L::B_BYTES;
-          const uint32_t t_sfa = tmem + SF_COL0 + stage * SF_COLS_PER_STAGE;
+          const uint32_t t_sfa = tmem + SF_COL0 + b * SEG2_COLS + i * 16;
           const uint32_t t_sfb = t_sfa + 4;
           const uint64_t adesc = make_sdesc(sA, 16, 1024, 2);
           const uint64_t bdesc = make_sdesc(sB, 16, 1024, 2);
@@ -275,6 +331,10 @@ __global__ void __launch_bounds__(THREADS1, 1)
           }
           issued = true;
           tc2_commit_both(bar_empty(stage));
+          if (i == SEG2 - 1 || kt == KT - 1) {
+            tc2_commit_both(bar_sft_free(b));  // the segment's scales may be overwritten
+            ++g;
+          }
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
@@ -293,33 +353,41 @@ __global__ void __launch_bounds__(THREADS1, 1)
     __syncwarp();
   } else if (warp < EPI_WARP0) {
     // ================= scale-factor writers (both CTAs), one per TMEM lane
-    // quarter: this CTA's staged chunks (its A rows, all 256 B rows) go into
-    // its own TMEM; the leader's MMA waits for the writers of both CTAs.
+    // quarter: a segment's staged chunks (this CTA's A rows, all 256 B rows)
+    // go into this CTA's TMEM (tcgen05.st, the layout of the 1-SM kernel)
+    // once the pair's MMAs are done with the buffer; the leader's MMA waits
+    // for the writers of both CTAs.
     const uint32_t t_q = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    int stage = 0;
-    uint32_t phase = 0;
+    int g = 0;
     bool ok = true;
     for (int unit = unit0; ok && unit < total_units; unit += unit_step) {
-      for (int kt = 0; kt < KT; ++kt) {
-        const bool got = wait_bar(bar_sff(stage), phase, p.wait_limit, p.status, s_abort);
+      for (int sg = 0; sg < nseg; ++sg, ++g) {
+        const int b = g & 1;
+        const uint32_t par = (uint32_t)(g >> 1) & 1u;
+        const bool got = wait_bar(bar_sfs_full(b), par, p.wait_limit, p.status, s_abort) &&
+                         wait_bar(bar_sft_free(b), par ^ 1u, p.wait_limit, p.status, s_abort);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
-        const uint8_t* sfa_s = smem + L::OFF_SFA + stage * L::SFA_BYTES;
-        const uint8_t* sfb_s = smem + L::OFF_SFB + stage * L::SFB_BYTES;
-        const uint32_t col = SF_COL0 + stage * SF_COLS_PER_STAGE;
-        tmem_st_4(t_q + col, *reinterpret_cast<const uint4*>(sfa_s + lane * 16));
-        tmem_st_4(t_q + col + 4, *reinterpret_cast<const uint4*>(sfb_s + lane * 16));
-        tmem_st_4(t_q + col + 8, *reinterpret_cast<const uint4*>(sfb_s + 512 + lane * 16));
+        const int len = min(SEG2, KT - sg * SEG2);
+        const uint8_t* sfa_s = smem + L::OFF_SFA + b * L::SFA_SEG;
+        const uint8_t* sfb_s = smem + L::OFF_SFB + b * L::SFB_SEG;
+        for (int i = 0; i < len; ++i) {
+          const uint32_t col = SF_COL0 + b * SEG2_COLS + i * 16;
+          tmem_st_4(t_q + col, *reinterpret_cast<const uint4*>(sfa_s + i * 512 + lane * 16));
+          tmem_st_4(t_q + col + 4, *reinterpret_cast<const uint4*>(sfb_s + i * 512 + lane * 16));
+          tmem_st_4(t_q + col + 8, *reinterpret_cast<const uint4*>(sfb_s + SEG2 * 512 + i * 512 +
+                                                                    lane * 16));
+        }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          if (leader) mbar_arrive(bar_sfr(stage));
-          else mbar_arrive_cluster(lead_sfr0 + 8u * stage);
+          if (leader) mbar_arrive(bar_sft_ready(b));
+          else mbar_arrive_cluster(lead_sftr0 + 8u * b);
+          mbar_arrive(bar_sfs_free(b));
         }
-        if (++stage == STAGES) { stage = 0; phase ^= 1; }
       }
     }
   } else {
