@@ -471,7 +471,7 @@ def main():
                     "d2h_bytes_per_step": d2h,
                     "ms_per_step": round(float(e2e_t_max.item()) / args.steps, 4)},
             "gpu_launches": 6 * args.steps,
-            "e2e_api": "moe_forward_mxfp8_host (pinned host buffers, 8192-token chunks, "
+            "e2e_api": "moe_forward_mxfp8_host (pinned host buffers, default chunk plan 3/16 | 5/8 | 3/16 of the tokens, "
                        "H2D / compute / D2H on three streams)",
             "cpu_baseline": cpu_base,
             "peaks": {"hbm_gbs": hbm, "fp8_tflops": fp8_peak, "source": peaks["source"]},

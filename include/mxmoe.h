@@ -255,10 +255,13 @@ mxmoe_status moe_forward_mxfp8_mma_scales(const uint16_t* x, const float* logits
 
 /*
  * The layer on HOST buffers, with the host<->device copies overlapped with
- * compute: the tokens are processed in n_chunks chunks (n_chunks <= 0: chunks
- * of 8192 tokens) through three library-owned streams (copy in, compute,
- * copy out) and two device staging slots in ws, so chunk c's layer runs while
- * chunk c+1's inputs arrive and chunk c-1's output leaves.  Weight scales in
+ * compute: the tokens are processed in chunks through three library-owned
+ * streams (copy in, compute, copy out) and two device staging slots in ws, so
+ * chunk c's layer runs while chunk c+1's inputs arrive and chunk c-1's output
+ * leaves.  n_chunks > 0: that many near-equal chunks.  n_chunks <= 0: the
+ * default plan (one chunk up to 4096 tokens; else three chunks, the first and
+ * last of 3/16 of the tokens each, which shortens the unoverlapped first
+ * copy-in and last copy-out while every chunk re-reads the weights).  Weight scales in
  * the MMA layout (mx_scales_to_mma_layout); weights stay on the device.
  *   x_host bf16 [T, H], logits_host fp32 [T, E], out_host bf16 [T, H]: host
  *   memory (pinned, e.g. cudaHostAlloc, for the copies to overlap).
@@ -272,6 +275,18 @@ mxmoe_status moe_forward_mxfp8_host(const uint16_t* x_host, const float* logits_
                                     const uint8_t* w2q, const uint8_t* w2s_mma, int T, int H,
                                     int E, int k, int I, int renormalize, uint16_t* out_host,
                                     int n_chunks, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * moe_forward_mxfp8_host with an explicit chunk plan: chunk_tokens[0..n_chunks)
+ * (host array, positive, summing to T; n_chunks <= 1024).  The workspace is
+ * moe_forward_mxfp8_host_workspace_size(max chunk, H, E, k, I, 1) bytes.
+ */
+mxmoe_status moe_forward_mxfp8_host_plan(const uint16_t* x_host, const float* logits_host,
+                                         const uint8_t* w13q, const uint8_t* w13s_mma,
+                                         const uint8_t* w2q, const uint8_t* w2s_mma, int T, int H,
+                                         int E, int k, int I, int renormalize, uint16_t* out_host,
+                                         const int32_t* chunk_tokens, int n_chunks, void* ws,
+                                         size_t ws_bytes, void* stream);
 
 /*
  * Per-kernel timing of moe_forward_mxfp8 / moe_forward_mxfp8_mma_scales

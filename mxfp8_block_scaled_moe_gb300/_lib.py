@@ -21,6 +21,7 @@ EXPORTS = (
     "moe_forward_mxfp8", "moe_route_quant_mxfp8_noalloc", "mx_scales_to_mma_layout",
     "moe_forward_mxfp8_mma_scales", "mxmoe_layer_profile_enable", "mxmoe_layer_profile_read",
     "mxmoe_set_gemm_2sm", "moe_forward_mxfp8_host", "moe_forward_mxfp8_host_workspace_size",
+    "moe_forward_mxfp8_host_plan",
 )
 
 _P = C.c_void_p
@@ -54,6 +55,8 @@ _PROTOS = {
     "moe_forward_mxfp8_host_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "moe_forward_mxfp8_host": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _I, _P,
                                     _SZ, _P]),
+    "moe_forward_mxfp8_host_plan": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P,
+                                         _I, _P, _SZ, _P]),
     "mxmoe_layer_profile_read": (_I, [C.POINTER(C.c_float), _I]),
 }
 

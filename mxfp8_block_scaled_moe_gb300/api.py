@@ -225,11 +225,13 @@ def moe_forward_mxfp8_host_workspace_size(T: int, H: int, E: int, k: int, I: int
 
 def moe_forward_mxfp8_host(x_host, logits_host, w13q, w13s_mma, w2q, w2s_mma, k: int,
                            renormalize: bool = True, out_host=None, n_chunks: int = 0,
-                           workspace=None):
+                           workspace=None, chunks=None):
     """The layer on host (CPU, ideally pinned) tensors, copies overlapped with compute.
 
     Weights and their MMA-layout scales are CUDA tensors.  Returns out_host
     (bf16 [T, H] on the host); it is complete once the current stream is.
+    `chunks` (a list of token counts summing to T) selects an explicit chunk
+    plan (moe_forward_mxfp8_host_plan); otherwise `n_chunks` (0 = default plan).
     """
     w13q, w2q = _u8(w13q), _u8(w2q)
     for t, n in ((x_host, "x_host"), (logits_host, "logits_host")):
@@ -244,13 +246,23 @@ def moe_forward_mxfp8_host(x_host, logits_host, w13q, w13s_mma, w2q, w2s_mma, k:
     I = N2 // 2
     if out_host is None:
         out_host = torch.empty(T, H, dtype=torch.bfloat16, pin_memory=True)
-    need = moe_forward_mxfp8_host_workspace_size(T, H, E, k, I, n_chunks)
+    if chunks is not None:
+        plan = (C.c_int32 * len(chunks))(*[int(c) for c in chunks])
+        need = moe_forward_mxfp8_host_workspace_size(max(chunks), H, E, k, I, 1)
+    else:
+        need = moe_forward_mxfp8_host_workspace_size(T, H, E, k, I, n_chunks)
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=w13q.device)
-    _lib.check("moe_forward_mxfp8_host", _lib.load().moe_forward_mxfp8_host(
-        _ptr(x_host), _ptr(logits_host), _ptr(w13q), _ptr(w13s_mma), _ptr(w2q), _ptr(w2s_mma),
-        T, H, E, k, I, int(bool(renormalize)), _ptr(out_host), int(n_chunks), _ptr(workspace),
-        workspace.numel(), _stream()))
+    if chunks is not None:
+        _lib.check("moe_forward_mxfp8_host_plan", _lib.load().moe_forward_mxfp8_host_plan(
+            _ptr(x_host), _ptr(logits_host), _ptr(w13q), _ptr(w13s_mma), _ptr(w2q), _ptr(w2s_mma),
+            T, H, E, k, I, int(bool(renormalize)), _ptr(out_host), C.cast(plan, C.c_void_p),
+            len(chunks), _ptr(workspace), workspace.numel(), _stream()))
+    else:
+        _lib.check("moe_forward_mxfp8_host", _lib.load().moe_forward_mxfp8_host(
+            _ptr(x_host), _ptr(logits_host), _ptr(w13q), _ptr(w13s_mma), _ptr(w2q), _ptr(w2s_mma),
+            T, H, E, k, I, int(bool(renormalize)), _ptr(out_host), int(n_chunks),
+            _ptr(workspace), workspace.numel(), _stream()))
     return out_host
 
 
@@ -326,15 +338,20 @@ class MXFP8MoELayer:
             self._ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
         return self._ws
 
-    def forward_host(self, x_host, logits_host, out_host=None, n_chunks: int = 0):
+    def forward_host(self, x_host, logits_host, out_host=None, n_chunks: int = 0, chunks=None):
         """The layer on host tensors (copies overlapped with compute, chunked by tokens)."""
         T = x_host.shape[0]
-        need = moe_forward_mxfp8_host_workspace_size(T, self.H, self.E, self.k, self.I, n_chunks)
+        if chunks is not None:
+            need = moe_forward_mxfp8_host_workspace_size(max(chunks), self.H, self.E, self.k,
+                                                         self.I, 1)
+        else:
+            need = moe_forward_mxfp8_host_workspace_size(T, self.H, self.E, self.k, self.I,
+                                                         n_chunks)
         if getattr(self, "_hws", None) is None or self._hws.numel() < need:
             self._hws = torch.empty(max(need, 256), dtype=torch.uint8, device=self.w13q.device)
         return moe_forward_mxfp8_host(x_host, logits_host, self.w13q, self.w13s_mma, self.w2q,
                                       self.w2s_mma, self.k, self.renormalize, out_host=out_host,
-                                      n_chunks=n_chunks, workspace=self._hws)
+                                      n_chunks=n_chunks, workspace=self._hws, chunks=chunks)
 
     def __call__(self, x, logits, out=None):
         return moe_forward_mxfp8_mma_scales(x, logits, self.w13q, self.w13s_mma, self.w2q,

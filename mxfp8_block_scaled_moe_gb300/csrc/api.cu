@@ -426,6 +426,8 @@ mxmoe_status moe_forward_mxfp8_mma_scales(const uint16_t* x, const float* logits
 // ---------------------------------------------------------------- host-buffer layer
 
 // Device staging of one chunk slot: x | logits | out | layer workspace.
+constexpr int kMaxHostChunks = 1024;
+
 struct HostChunkLayout {
   size_t x, logits, out, ws, ws_bytes, slot;
 };
@@ -443,20 +445,37 @@ static HostChunkLayout host_chunk_layout(int Tc, int H, int E, int k, int I) {
   return L;
 }
 
-// Default chunking: 8192-token chunks.  Every chunk re-reads all experts'
-// weights, so smaller chunks cost weight traffic while larger ones lengthen
-// the unoverlapped first copy-in and last copy-out (measured on GB300 for the
-// 16K-token Qwen3-30B-A3B layer: 2 chunks 1.27 ms, 4 chunks 1.29 ms, 8 chunks
-// 1.69 ms, 1 chunk 1.52 ms per call).
-static int host_chunk_tokens(int T, int n_chunks) {
-  if (n_chunks <= 0) n_chunks = T > 8192 ? (T + 8191) / 8192 : 1;
-  if (n_chunks > T) n_chunks = T > 0 ? T : 1;
-  return (T + n_chunks - 1) / n_chunks;
+// Chunk plans.  n_chunks > 0: that many near-equal chunks.  n_chunks <= 0:
+// the default plan, chosen from measurements on GB300 (16K-token
+// Qwen3-30B-A3B layer; host links ~0.2 TB/s each way): every chunk re-reads
+// all experts' weights, so chunks should be few and large, while the first
+// chunk's copy-in and the last chunk's copy-out are not overlapped with any
+// compute, so those two should be small.  Up to 4096 tokens: one chunk;
+// beyond: three chunks, the outer two of 3/16 of the tokens each (measured:
+// 1.17 ms per call against 1.28 ms for two equal chunks and 1.51 ms for one).
+static int host_chunk_plan(int T, int n_chunks, int* sizes) {
+  if (T <= 0) { sizes[0] = 0; return 1; }
+  if (n_chunks <= 0) {
+    if (T <= 4096) { sizes[0] = T; return 1; }
+    const int a = std::max(64, (T * 3 / 16) / 64 * 64);
+    sizes[0] = a;
+    sizes[1] = T - 2 * a;
+    sizes[2] = a;
+    return 3;
+  }
+  if (n_chunks > kMaxHostChunks) n_chunks = kMaxHostChunks;
+  if (n_chunks > T) n_chunks = T;
+  for (int i = 0; i < n_chunks; ++i)
+    sizes[i] = (int)((int64_t)T * (i + 1) / n_chunks - (int64_t)T * i / n_chunks);
+  return n_chunks;
 }
 
 size_t moe_forward_mxfp8_host_workspace_size(int T, int H, int E, int k, int I, int n_chunks) {
   if (T < 0 || H <= 0 || E <= 0 || k <= 0 || I <= 0) return 0;
-  const int Tc = host_chunk_tokens(T, n_chunks);
+  int sizes[kMaxHostChunks];
+  const int n = host_chunk_plan(T, n_chunks, sizes);
+  int Tc = 0;
+  for (int i = 0; i < n; ++i) Tc = std::max(Tc, sizes[i]);
   return 2 * host_chunk_layout(Tc, H, E, k, I).slot;
 }
 
@@ -486,11 +505,13 @@ static HostPipe* host_pipe() {
   return &P;
 }
 
-mxmoe_status moe_forward_mxfp8_host(const uint16_t* x_host, const float* logits_host,
-                                    const uint8_t* w13q, const uint8_t* w13s_mma,
-                                    const uint8_t* w2q, const uint8_t* w2s_mma, int T, int H,
-                                    int E, int k, int I, int renormalize, uint16_t* out_host,
-                                    int n_chunks, void* ws, size_t ws_bytes, void* stream) {
+// The pipeline over an explicit chunk plan (sizes[0..n), summing to T).
+static mxmoe_status host_pipeline(const uint16_t* x_host, const float* logits_host,
+                                  const uint8_t* w13q, const uint8_t* w13s_mma,
+                                  const uint8_t* w2q, const uint8_t* w2s_mma, int T, int H, int E,
+                                  int k, int I, int renormalize, uint16_t* out_host,
+                                  const int* sizes, int n, void* ws, size_t ws_bytes,
+                                  void* stream) {
   if (T < 0 || H <= 0 || E <= 0 || k < 1 || k > 32 || k > E || I <= 0) return MXMOE_ERR_SHAPE;
   if (E > 256 || H % 128 != 0 || I % 128 != 0) return MXMOE_ERR_UNSUPPORTED;
   if ((int64_t)T * k >= (1ll << 31)) return MXMOE_ERR_SHAPE;
@@ -502,7 +523,14 @@ mxmoe_status moe_forward_mxfp8_host(const uint16_t* x_host, const float* logits_
   MXMOE_CHECK_PTR(w2s_mma);
   if (!ws) return MXMOE_ERR_WORKSPACE;
   if ((uintptr_t)ws & 255u) return MXMOE_ERR_ALIGN;
-  const int Tc = host_chunk_tokens(T, n_chunks);
+  int64_t sum = 0;
+  int Tc = 0;
+  for (int i = 0; i < n; ++i) {
+    if (sizes[i] <= 0) return MXMOE_ERR_SHAPE;
+    sum += sizes[i];
+    Tc = std::max(Tc, sizes[i]);
+  }
+  if (n <= 0 || sum != T) return MXMOE_ERR_SHAPE;
   const HostChunkLayout CL = host_chunk_layout(Tc, H, E, k, I);
   if (ws_bytes < 2 * CL.slot) return MXMOE_ERR_WORKSPACE;
   HostPipe* P = host_pipe();
@@ -513,9 +541,9 @@ mxmoe_status moe_forward_mxfp8_host(const uint16_t* x_host, const float* logits_
   for (auto st : P->s)
     if (!ck(cudaStreamWaitEvent(st, P->ev_start, 0))) return MXMOE_ERR_CUDA;
   uint8_t* base = (uint8_t*)ws;
-  int c = 0;
-  for (int t0 = 0; t0 < T; t0 += Tc, ++c) {
-    const int tc = std::min(Tc, T - t0);
+  int t0 = 0;
+  for (int c = 0; c < n; t0 += sizes[c], ++c) {
+    const int tc = sizes[c];
     const int slot = c & 1;
     uint8_t* sb = base + (size_t)slot * CL.slot;
     uint16_t* xd = (uint16_t*)(sb + CL.x);
@@ -548,6 +576,31 @@ mxmoe_status moe_forward_mxfp8_host(const uint16_t* x_host, const float* logits_
   if (!ck(cudaEventRecord(P->ev_done, P->s[2])) || !ck(cudaStreamWaitEvent(user, P->ev_done, 0)))
     return MXMOE_ERR_CUDA;
   return MXMOE_OK;
+}
+
+mxmoe_status moe_forward_mxfp8_host(const uint16_t* x_host, const float* logits_host,
+                                    const uint8_t* w13q, const uint8_t* w13s_mma,
+                                    const uint8_t* w2q, const uint8_t* w2s_mma, int T, int H,
+                                    int E, int k, int I, int renormalize, uint16_t* out_host,
+                                    int n_chunks, void* ws, size_t ws_bytes, void* stream) {
+  if (T < 0) return MXMOE_ERR_SHAPE;
+  int sizes[kMaxHostChunks];
+  const int n = host_chunk_plan(T, n_chunks, sizes);
+  return host_pipeline(x_host, logits_host, w13q, w13s_mma, w2q, w2s_mma, T, H, E, k, I,
+                       renormalize, out_host, sizes, n, ws, ws_bytes, stream);
+}
+
+mxmoe_status moe_forward_mxfp8_host_plan(const uint16_t* x_host, const float* logits_host,
+                                         const uint8_t* w13q, const uint8_t* w13s_mma,
+                                         const uint8_t* w2q, const uint8_t* w2s_mma, int T, int H,
+                                         int E, int k, int I, int renormalize, uint16_t* out_host,
+                                         const int32_t* chunk_tokens, int n_chunks, void* ws,
+                                         size_t ws_bytes, void* stream) {
+  if (!chunk_tokens || n_chunks <= 0 || n_chunks > kMaxHostChunks) return MXMOE_ERR_SHAPE;
+  int sizes[kMaxHostChunks];
+  for (int i = 0; i < n_chunks; ++i) sizes[i] = chunk_tokens[i];
+  return host_pipeline(x_host, logits_host, w13q, w13s_mma, w2q, w2s_mma, T, H, E, k, I,
+                       renormalize, out_host, sizes, n_chunks, ws, ws_bytes, stream);
 }
 
 }  // extern "C"

@@ -77,6 +77,19 @@ def test_host_validation_rejects_bad_arguments(lib):
     # T == 0 is a no-op
     assert lib.moe_forward_mxfp8(nul, nul, nul, nul, nul, nul, 0, 256, 8, 2, 128, 1, nul, nul, 0,
                                  nul) == 0
+    # host-buffer layer with an explicit chunk plan: sizes must be positive
+    # and sum to T (checked before any device work)
+    big = 1 << 40
+    for plan, ok in (([30, 30], False), ([64, 0], False), ([70, -6], False), ([], False)):
+        arr = (C.c_int32 * max(1, len(plan)))(*plan)
+        st = lib.moe_forward_mxfp8_host_plan(p, p, p, p, p, p, 64, 256, 8, 2, 128, 1, p,
+                                             C.cast(arr, C.c_void_p), len(plan), p, big, nul)
+        assert st == 3, (plan, st)
+    # the default plan: one chunk up to 4096 tokens, three beyond (slot = largest chunk)
+    w1 = lib.moe_forward_mxfp8_host_workspace_size(4096, 2048, 128, 8, 768, 0)
+    assert w1 == lib.moe_forward_mxfp8_host_workspace_size(4096, 2048, 128, 8, 768, 1)
+    w3 = lib.moe_forward_mxfp8_host_workspace_size(16384, 2048, 128, 8, 768, 0)
+    assert w3 == lib.moe_forward_mxfp8_host_workspace_size(10240, 2048, 128, 8, 768, 1)
 
 
 def test_python_binding_refuses_cpu_tensors():

@@ -196,3 +196,20 @@ def test_host_buffer_layer_matches_device_layer(mm, cfg, n_chunks):
     torch.cuda.synchronize()
     assert mm.device_status() == 0
     assert torch.equal(out_h, ref.cpu())
+
+
+@pytest.mark.parametrize("cfg,chunks", [("tiny", [5, 50, 9]), ("tiny", [64]),
+                                        ("qwen3_30b_prefill", [1000, 15000, 384]),
+                                        ("qwen3_30b_prefill", [3072, 10240, 3072])])
+def test_host_buffer_layer_explicit_chunk_plan(mm, cfg, chunks):
+    """An explicit uneven chunk plan gives the on-device layer's bytes."""
+    shape = workloads.CONFIGS[cfg]
+    inp = workloads.make_layer(shape, DEV)
+    layer = mm.MXFP8MoELayer.from_bf16(inp["w13"], inp["w2"], shape.k)
+    ref = layer(inp["x"], inp["logits"])
+    x_h = inp["x"].cpu().pin_memory()
+    l_h = inp["logits"].cpu().pin_memory()
+    out_h = layer.forward_host(x_h, l_h, chunks=chunks)
+    torch.cuda.synchronize()
+    assert mm.device_status() == 0
+    assert torch.equal(out_h, ref.cpu())
