@@ -167,6 +167,45 @@ class ClockSampler:
                 "region_s": round(self.t1 - self.t0, 3)}
 
 
+def library_gemm_rates(torch, dev, n=8192, reps=10):
+    """Dense n^3 GEMM rates of the vendor library on this GPU (context for the
+    MXFP8 peak): bf16, and MXFP8 through torch._scaled_mm with e4m3 operands
+    and e8m0 block-32 scales.  Best of `reps`; None where unsupported."""
+    def best(fn):
+        fn()
+        torch.cuda.synchronize()
+        t = []
+        for _ in range(reps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            t.append(a.elapsed_time(b))
+        return 2.0 * n ** 3 / min(t) / 1e9
+    out = {"n": n}
+    try:
+        x = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+        w = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+        out["bf16_tflops"] = round(best(lambda: x @ w.t()), 1)
+        del x, w
+    except Exception:
+        out["bf16_tflops"] = None
+    try:
+        a8 = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+        b8 = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+        sc = torch.full((n * (n // 32),), 127, dtype=torch.uint8, device=dev).view(
+            torch.float8_e8m0fnu)
+        out["mxfp8_tflops"] = round(best(lambda: torch._scaled_mm(
+            a8, b8.t(), scale_a=sc, scale_b=sc, out_dtype=torch.bfloat16)), 1)
+        del a8, b8, sc
+    except Exception:
+        out["mxfp8_tflops"] = None
+    torch.cuda.empty_cache()
+    return out
+
+
 def algorithmic_bytes(T, H, E, k, I):
     M = T * k
     route = 2 * T * H + M * H + M * H // 32 + 4 * T * E + M * 4 * 4
@@ -442,6 +481,9 @@ def main():
     e2e_value = world * T * args.steps / (float(e2e_t_max.item()) / 1e3)
     h2d = x_h.numel() * 2 + l_h.numel() * 4
     d2h = o_h.numel() * 2
+    # vendor-library dense GEMM rates (context for the MXFP8 peak; after the
+    # timed work, rank 0)
+    lib_rates = library_gemm_rates(torch, dev) if rank == 0 else None
 
     cpu_base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -474,7 +516,8 @@ def main():
             "e2e_api": "moe_forward_mxfp8_host (pinned host buffers, default chunk plan 3/16 | 5/8 | 3/16 of the tokens, "
                        "H2D / compute / D2H on three streams)",
             "cpu_baseline": cpu_base,
-            "peaks": {"hbm_gbs": hbm, "fp8_tflops": fp8_peak, "source": peaks["source"]},
+            "peaks": {"hbm_gbs": hbm, "fp8_tflops": fp8_peak, "source": peaks["source"],
+                      "library_dense_gemm": lib_rates},
             "gemm_src": src_hash,
         }
         print(json.dumps(line), flush=True)
