@@ -34,7 +34,11 @@ Readings of points the pages leave open (each is one choice, stated once):
   element -> e4m3 code) is taken in the kernel's precision;
 * GEMM2's output is bf16 (round-to-nearest-even of the exact product);
 * the routing weights are applied in finalize, which accumulates exactly and
-  rounds once to bf16; no token is dropped (no capacity limit).
+  rounds once to bf16; no token is dropped (no capacity limit);
+* W4A8 (MXFP4 weights): the shared scale is floor(log2 amax) - 2 (2 = the
+  largest power-of-two exponent of e2m1, as 8 is for e4m3), elements round to
+  nearest-even and saturate at +-6, and a packed byte holds element 2i in its
+  low nibble and element 2i+1 in its high nibble.
 """
 
 from __future__ import annotations
@@ -128,13 +132,24 @@ def permute_rows(x: np.ndarray, sorted_to_src: np.ndarray, k: int) -> np.ndarray
 # 3. gmm1: grouped GEMM over w13 + SwiGLU + MXFP8 requant
 # ----------------------------------------------------------------------------
 
+def deq_weight(q, s, wfmt: str = "e4m3"):
+    """Dequantize one expert's weight matrix: MXFP8 (e4m3 codes [N, K]) or, for
+    the W4A8 path ("Quantization on Ascend", W4A8 notes), MXFP4 (packed e2m1
+    [N, K/2]); e8m0 scales [N, K/32] either way."""
+    if wfmt == "e4m3":
+        return mx.mx_dequantize(q, s)
+    if wfmt == "e2m1":
+        return mx.mxfp4_dequantize(q, s)
+    raise ValueError(f"unknown weight format {wfmt!r}")
+
+
 def silu(g: np.ndarray) -> np.ndarray:
     """silu(g) = g / (1 + e^-g) in fp64 (e^-g may overflow to inf -> -0/+0)."""
     with np.errstate(over="ignore"):
         return g / (1.0 + np.exp(-g))
 
 
-def gmm1_swiglu_quant(xq, xs, w13q, w13s, offsets, I: int, experts=None):
+def gmm1_swiglu_quant(xq, xs, w13q, w13s, offsets, I: int, experts=None, wfmt: str = "e4m3"):
     """Per expert e and its rows [off_e, off_{e+1}):
 
     h = deq(xq rows) @ deq(w13[e])^T (fp64, exact products), gate = h[:, :I],
@@ -151,7 +166,7 @@ def gmm1_swiglu_quant(xq, xs, w13q, w13s, offsets, I: int, experts=None):
         if r1 == r0:
             continue
         a_in = mx.mx_dequantize(xq[r0:r1], xs[r0:r1])
-        w = mx.mx_dequantize(w13q[e], w13s[e])
+        w = deq_weight(w13q[e], w13s[e], wfmt)
         h = a_in @ w.T
         a = silu(h[:, :I]) * h[:, I:]
         a32 = a.astype(np.float32).astype(np.float64)
@@ -159,7 +174,7 @@ def gmm1_swiglu_quant(xq, xs, w13q, w13s, offsets, I: int, experts=None):
     return aq, as_
 
 
-def gmm1_swiglu(xq, xs, w13q, w13s, offsets, I: int, experts=None):
+def gmm1_swiglu(xq, xs, w13q, w13s, offsets, I: int, experts=None, wfmt: str = "e4m3"):
     """The unquantized SwiGLU output a (fp64) of gmm1, for error reporting."""
     M = xq.shape[0]
     a_out = np.zeros((M, I))
@@ -167,7 +182,7 @@ def gmm1_swiglu(xq, xs, w13q, w13s, offsets, I: int, experts=None):
         r0, r1 = int(offsets[e]), int(offsets[e + 1])
         if r1 == r0:
             continue
-        h = mx.mx_dequantize(xq[r0:r1], xs[r0:r1]) @ mx.mx_dequantize(w13q[e], w13s[e]).T
+        h = mx.mx_dequantize(xq[r0:r1], xs[r0:r1]) @ deq_weight(w13q[e], w13s[e], wfmt).T
         a_out[r0:r1] = silu(h[:, :I]) * h[:, I:]
     return a_out
 
@@ -176,20 +191,21 @@ def gmm1_swiglu(xq, xs, w13q, w13s, offsets, I: int, experts=None):
 # 4. gmm2: grouped GEMM over w2, bf16 output
 # ----------------------------------------------------------------------------
 
-def gmm2(aq, as_, w2q, w2s, offsets, experts=None, round_bf16: bool = True):
+def gmm2(aq, as_, w2q, w2s, offsets, experts=None, round_bf16: bool = True,
+         wfmt: str = "e4m3"):
     """Per expert: y = deq(aq rows) @ deq(w2[e])^T in fp64.
 
     Returns bf16 bit patterns uint16 [M, H] (``round_bf16``) or the exact
     fp64 product.  Rows of skipped experts stay zero.
     """
     M = aq.shape[0]
-    E, H, _ = w2q.shape
+    E, H = w2q.shape[0], w2q.shape[1]
     y = np.zeros((M, H))
     for e in range(E) if experts is None else experts:
         r0, r1 = int(offsets[e]), int(offsets[e + 1])
         if r1 == r0:
             continue
-        y[r0:r1] = mx.mx_dequantize(aq[r0:r1], as_[r0:r1]) @ mx.mx_dequantize(w2q[e], w2s[e]).T
+        y[r0:r1] = mx.mx_dequantize(aq[r0:r1], as_[r0:r1]) @ deq_weight(w2q[e], w2s[e], wfmt).T
     return mx.f64_to_bf16_bits(y) if round_bf16 else y
 
 
@@ -218,8 +234,10 @@ def finalize(y_bf16_bits, topk_w, src_to_sorted, k: int, round_bf16: bool = True
 # ----------------------------------------------------------------------------
 
 def moe_forward(x_bf16_bits, logits, w13q, w13s, w2q, w2s, k: int, I: int,
-                renormalize: bool = True):
+                renormalize: bool = True, wfmt: str = "e4m3"):
     """The whole MXFP8 expert forward; returns a dict of every intermediate.
+    ``wfmt="e2m1"`` runs the W4A8 variant: MXFP4 (packed e2m1) expert weights
+    with the same MXFP8 activations, routing, requant and finalize.
 
     The routing weights fed to finalize are rounded to fp32 first: the
     kernels carry them as fp32, and the rounding of the combine input is a
@@ -229,8 +247,8 @@ def moe_forward(x_bf16_bits, logits, w13q, w13s, w2q, w2s, k: int, I: int,
     E = w13q.shape[0]
     ids, w = route_topk(logits, k, renormalize)
     xq, xs, counts, offsets, s2s, src2s = route_quant(x, ids, E)
-    aq, as_ = gmm1_swiglu_quant(xq, xs, w13q, w13s, offsets, I)
-    y = gmm2(aq, as_, w2q, w2s, offsets)
+    aq, as_ = gmm1_swiglu_quant(xq, xs, w13q, w13s, offsets, I, wfmt=wfmt)
+    y = gmm2(aq, as_, w2q, w2s, offsets, wfmt=wfmt)
     w32 = w.astype(np.float32)
     out = finalize(y, w32, src2s, k)
     return dict(topk_ids=ids, topk_w=w, xq=xq, xs=xs, counts=counts, offsets=offsets,

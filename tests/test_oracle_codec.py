@@ -226,3 +226,98 @@ def test_pair_split_padding_k4304():
     assert p[0, 67, 0] == 134 and p[0, 67, 1] == 0
     assert p.reshape(1, -1)[0, :135].tolist() == list(range(135))
     assert math.ceil(K / 64) == 68
+
+
+# ---------------------------------------------------------------- e2m1 (FP4) codec, W4A8 weights
+
+def test_e2m1_value_set():
+    """The 16 e2m1 codes decode to the FP4 value set {0, 0.5, 1, 1.5, 2, 3, 4, 6}
+    and its negatives (codes 8..15 = sign bit set)."""
+    vals = mx.e2m1_decode(np.arange(16, dtype=np.uint8))
+    assert list(vals[:8]) == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert np.array_equal(vals[8:], -vals[:8])
+    assert np.signbit(vals[8]) and not np.signbit(vals[0])
+    assert mx.E2M1_MAX == vals.max()
+
+
+def test_e2m1_values_are_exact_e4m3_values_per_torch():
+    """Every FP4 value is exactly representable in e4m3 (torch's cast is exact)."""
+    v = torch.tensor(mx.E2M1_TABLE, dtype=torch.float32)
+    back = v.to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(back, mx.E2M1_TABLE)
+
+
+def test_e2m1_encode_brute_force_nearest_even():
+    grid = mx.e2m1_decode(np.arange(8, dtype=np.uint8))
+    rng = np.random.default_rng(3)
+    mids = (grid[1:] + grid[:-1]) / 2
+    v = np.concatenate([rng.uniform(-9, 9, 20000), mids, -mids, grid, -grid,
+                        np.nextafter(mids, 0), np.nextafter(mids, 10), [6.5, 7.9, 100.0, -1e9]])
+    codes = mx.e2m1_encode(v)
+    a = np.minimum(np.abs(v), 6.0)
+    d = np.abs(a[:, None] - grid[None, :])
+    best = d.min(axis=1, keepdims=True)
+    cand = d == best
+    # ties (two candidates) go to the even code (mantissa bit 0)
+    even = cand & (np.arange(8)[None, :] % 2 == 0)
+    ref = np.where(cand.sum(1) > 1, np.argmax(even, 1), np.argmax(cand, 1))
+    assert np.array_equal(codes & 7, ref)
+    assert np.array_equal(codes >> 3, np.signbit(v).astype(np.uint8))
+    assert mx.e2m1_encode(np.array([5.0]))[0] == 6      # 5 = midpoint of 4 and 6 -> 4 (even)
+    assert mx.e2m1_encode(np.array([-0.2]))[0] == 8     # rounds to zero, sign kept
+
+
+def test_pack_fp4_nibble_order_and_roundtrip():
+    assert mx.pack_fp4(np.array([1, 2], np.uint8))[0] == 0x21   # element 0 in the low nibble
+    rng = np.random.default_rng(4)
+    c = rng.integers(0, 16, (5, 64), dtype=np.uint8)
+    assert np.array_equal(mx.unpack_fp4(mx.pack_fp4(c)), c)
+
+
+def test_mxfp4_scale_closed_form_and_range():
+    for e in range(-120, 120, 7):
+        _, s = mx.mxfp4_quantize(np.full((1, 32), 2.0 ** e))
+        assert int(s[0, 0]) - 127 == e - 2
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((64, 32)) * np.exp2(rng.integers(-20, 20, (64, 1)))
+    _, s = mx.mxfp4_quantize(x)
+    r = np.max(np.abs(x), axis=1) / np.exp2(s[:, 0].astype(np.int64) - 127)
+    assert np.all((r >= 4) & (r < 8))
+    _, s0 = mx.mxfp4_quantize(np.zeros((1, 32)))
+    assert s0[0, 0] == 0
+
+
+def test_mxfp4_dequant_error_bound_and_representable_roundtrip():
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((256, 64))
+    q, s = mx.mxfp4_quantize(x)
+    d = mx.mxfp4_dequantize(q, s)
+    sc = np.repeat(np.exp2(s.astype(np.int64) - 127), 32, axis=1)
+    a = np.abs(x) / sc
+    ulp = np.where(a < 2, 0.5, np.where(a < 4, 1.0, 2.0))
+    inside = a <= 6
+    assert np.all(np.abs(d - x)[inside] <= (ulp * sc)[inside] / 2)
+    assert np.all(np.abs(d - x)[~inside] < (2 * sc)[~inside])
+    # blocks whose values are FP4 grid points times 2^s (amax in [4, 8)) come back exactly
+    g = mx.e2m1_decode(rng.integers(0, 16, (16, 32), dtype=np.uint8))
+    g[:, 0] = 6.0
+    blk = g * np.exp2(rng.integers(-30, 30, (16, 1)))
+    q2, s2 = mx.mxfp4_quantize(blk)
+    assert np.array_equal(mx.mxfp4_dequantize(q2, s2), blk)
+
+
+def test_mxfp4_gemm_equals_mxfp8_gemm_on_reencoded_weights():
+    """W4A8 GEMM oracle == the pinned MXFP8 GEMM oracle fed the same weights
+    re-encoded as e4m3 codes under the same scales (FP4 values are exact e4m3)."""
+    from oracle import moe
+    rng = np.random.default_rng(7)
+    E, N, K, M = 3, 96, 128, 40
+    w = rng.standard_normal((E, N, K)) * 0.02
+    q4, s4 = mx.mxfp4_quantize(w)
+    q8 = mx.e4m3_encode(mx.e2m1_decode(mx.unpack_fp4(q4)))
+    assert np.array_equal(mx.mx_dequantize(q8, s4), mx.mxfp4_dequantize(q4, s4))
+    aq, as_ = mx.mx_quantize(rng.standard_normal((M, K)))
+    offs = np.array([0, 10, 10, M])
+    y4 = moe.gmm2(aq, as_, q4, s4, offs, wfmt="e2m1")
+    y8 = moe.gmm2(aq, as_, q8, s4, offs)
+    assert np.array_equal(y4, y8)

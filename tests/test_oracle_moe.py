@@ -259,3 +259,21 @@ def test_moe_forward_tiny_layer_runs_and_is_consistent():
     got = mx.bf16_bits_to_f64(r["out"])
     rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
     assert rel < 0.1, rel
+
+
+def test_w4a8_layer_equals_mxfp8_layer_on_reencoded_weights():
+    """The W4A8 layer (MXFP4 expert weights) is the MXFP8 layer fed the same
+    weight values as e4m3 codes under the same scales."""
+    rng = np.random.default_rng(11)
+    T, H, E, k, I = 24, 64, 4, 2, 32
+    x = mx.f64_to_bf16_bits(rng.standard_normal((T, H)))
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    w13 = rng.standard_normal((E, 2 * I, H)) * 0.05
+    w2 = rng.standard_normal((E, H, I)) * 0.05
+    q13, s13 = mx.mxfp4_quantize(w13)
+    q2, s2 = mx.mxfp4_quantize(w2)
+    r4 = moe.moe_forward(x, logits, q13, s13, q2, s2, k, I, wfmt="e2m1")
+    e8 = lambda q: mx.e4m3_encode(mx.e2m1_decode(mx.unpack_fp4(q)))
+    r8 = moe.moe_forward(x, logits, e8(q13), s13, e8(q2), s2, k, I)
+    for key in ("aq", "as_", "y", "out"):
+        assert np.array_equal(r4[key], r8[key]), key
