@@ -17,6 +17,9 @@
  *   moe_finalize_routing            weighted top-k combine back to token order
  *   moe_forward_mxfp8               the four above on one stream
  *   mx_quantize_3d                  load-time MX quant of [E, N, K] weights
+ *   mx_quantize_fp4_3d, moe_forward_w4a8_mma_scales
+ *                                   the W4A8 variant: MXFP4 (packed e2m1)
+ *                                   expert weights x MXFP8 activations
  *
  * Formats.  An MX block is 32 consecutive elements along the contraction
  * axis K.  Payload: one float8_e4m3fn byte per element.  Scale: one UE8M0
@@ -76,6 +79,18 @@ const char* mxmoe_status_string(mxmoe_status status);
  */
 mxmoe_status mx_quantize_3d(const uint16_t* w, int64_t E, int64_t N, int64_t K,
                             uint8_t* q, uint8_t* scale, void* stream);
+
+/*
+ * Load-time MXFP4 quantization (W4A8 weights, online path of the W4A8 notes:
+ * bf16 weights -> MXFP4 at load): per 32-element block along K, scale byte
+ * b = clamp(floor(log2 amax) - 2, -127, 127) + 127 (2 = the largest
+ * power-of-two exponent of e2m1), elements e2m1 round-to-nearest-even,
+ * saturating at +-6, packed two per byte (element 2i in the low nibble).
+ *   w bf16 [E, N, K]; q uint8 [E, N, K/2]; scale uint8 [E, N, K/32].
+ *   K % 32 == 0; w, q 16-byte aligned.
+ */
+mxmoe_status mx_quantize_fp4_3d(const uint16_t* w, int64_t E, int64_t N, int64_t K, uint8_t* q,
+                                uint8_t* scale, void* stream);
 
 /*
  * Workspace bytes moe_route_quant_mxfp8 / moe_route_permute_bf16 need for
@@ -252,6 +267,24 @@ mxmoe_status moe_forward_mxfp8_mma_scales(const uint16_t* x, const float* logits
                                           int H, int E, int k, int I, int renormalize,
                                           uint16_t* out, void* ws, size_t ws_bytes,
                                           void* stream);
+
+/*
+ * W4A8: the same layer with MXFP4 expert weights ("Quantization on Ascend",
+ * W4A8 notes: packed FP4 float4_e2m1fn_x2, two nibbles per byte, UE8M0 scale
+ * per 32-element block; activations per-token MXFP8; the path measured in
+ * sglang PR #40519).  Routing, the fused activation quant, the SwiGLU +
+ * requant epilogue and finalize are those of the MXFP8 layer; the grouped
+ * GEMMs run tcgen05 block-scaled MMAs with e4m3 activations x e2m1 weights.
+ *   w13p uint8 [E, 2I, H/2], w2p uint8 [E, H, I/2]: packed e2m1, element 2i
+ *     in the low nibble of byte i (mx_quantize_fp4_3d); 32-byte aligned.
+ *   w13s_mma, w2s_mma: their scales in the MMA layout (mx_scales_to_mma_layout).
+ * Workspace: moe_forward_mxfp8_workspace_size(T, H, E, k, I).
+ */
+mxmoe_status moe_forward_w4a8_mma_scales(const uint16_t* x, const float* logits,
+                                         const uint8_t* w13p, const uint8_t* w13s_mma,
+                                         const uint8_t* w2p, const uint8_t* w2s_mma, int T, int H,
+                                         int E, int k, int I, int renormalize, uint16_t* out,
+                                         void* ws, size_t ws_bytes, void* stream);
 
 /*
  * The layer on HOST buffers, with the host<->device copies overlapped with

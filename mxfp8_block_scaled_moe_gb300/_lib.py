@@ -21,7 +21,7 @@ EXPORTS = (
     "moe_forward_mxfp8", "moe_route_quant_mxfp8_noalloc", "mx_scales_to_mma_layout",
     "moe_forward_mxfp8_mma_scales", "mxmoe_layer_profile_enable", "mxmoe_layer_profile_read",
     "mxmoe_set_gemm_2sm", "moe_forward_mxfp8_host", "moe_forward_mxfp8_host_workspace_size",
-    "moe_forward_mxfp8_host_plan",
+    "moe_forward_mxfp8_host_plan", "mx_quantize_fp4_3d", "moe_forward_w4a8_mma_scales",
 )
 
 _P = C.c_void_p
@@ -49,6 +49,8 @@ _PROTOS = {
     "moe_forward_mxfp8": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "moe_forward_mxfp8_mma_scales": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P,
                                           _SZ, _P]),
+    "moe_forward_w4a8_mma_scales": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P,
+                                         _SZ, _P]),
     "mx_scales_to_mma_layout": (_I, [_P, _I64, _I64, _I64, _P, _P]),
     "mxmoe_layer_profile_enable": (_I, [_I]),
     "mxmoe_set_gemm_2sm": (None, [_I]),
@@ -57,6 +59,7 @@ _PROTOS = {
                                     _SZ, _P]),
     "moe_forward_mxfp8_host_plan": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P,
                                          _I, _P, _SZ, _P]),
+    "mx_quantize_fp4_3d": (_I, [_P, _I64, _I64, _I64, _P, _P, _P]),
     "mxmoe_layer_profile_read": (_I, [C.POINTER(C.c_float), _I]),
 }
 

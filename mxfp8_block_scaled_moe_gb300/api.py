@@ -58,6 +58,27 @@ def mx_quantize_3d(w: torch.Tensor):
     return q, s
 
 
+def mx_quantize_fp4_3d(w: torch.Tensor):
+    """bf16 [E, N, K] (or [N, K]) -> (packed MXFP4 uint8 [.., K/2], e8m0 scales uint8 [.., K/32]).
+
+    W4A8 weights: e2m1 elements, two per byte (element 2i in the low nibble)."""
+    _need(w, "w", torch.bfloat16)
+    shape = tuple(w.shape)
+    if w.dim() == 2:
+        E, (N, K) = 1, shape
+    elif w.dim() == 3:
+        E, N, K = shape
+    else:
+        raise ValueError("w must be 2D or 3D")
+    if K % 32:
+        raise ValueError("K must be a multiple of 32")
+    q = torch.empty(shape[:-1] + (K // 2,), dtype=torch.uint8, device=w.device)
+    s = torch.empty(shape[:-1] + (K // 32,), dtype=torch.uint8, device=w.device)
+    _lib.check("mx_quantize_fp4_3d", _lib.load().mx_quantize_fp4_3d(
+        _ptr(w), E, N, K, _ptr(q), _ptr(s), _stream()))
+    return q, s
+
+
 def _route(x, logits, k, renormalize, quant):
     _need(x, "x", torch.bfloat16, 2)
     _need(logits, "logits", torch.float32, 2)
@@ -218,6 +239,30 @@ def moe_forward_mxfp8_mma_scales(x, logits, w13q, w13s_mma, w2q, w2s_mma, k: int
     return out
 
 
+def moe_forward_w4a8_mma_scales(x, logits, w13p, w13s_mma, w2p, w2s_mma, k: int,
+                                renormalize: bool = True, out=None, workspace=None):
+    """The W4A8 layer: packed MXFP4 expert weights (mx_quantize_fp4_3d) with
+    their scales in the tensor-core layout, MXFP8 activations."""
+    _need(x, "x", torch.bfloat16, 2)
+    _need(logits, "logits", torch.float32, 2)
+    for t, n in ((w13p, "w13p"), (w13s_mma, "w13s_mma"), (w2p, "w2p"), (w2s_mma, "w2s_mma")):
+        _need(t, n, torch.uint8, 3)
+    T, H = x.shape
+    E, N2, _ = w13p.shape
+    I = N2 // 2
+    if w13p.shape[2] * 2 != H or w2p.shape[2] * 2 != I:
+        raise ValueError("w13p / w2p must be packed [E, 2I, H/2] / [E, H, I/2]")
+    ws_bytes = moe_forward_mxfp8_workspace_size(T, H, E, k, I)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=x.device)
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=x.device)
+    _lib.check("moe_forward_w4a8_mma_scales", _lib.load().moe_forward_w4a8_mma_scales(
+        _ptr(x), _ptr(logits), _ptr(w13p), _ptr(w13s_mma), _ptr(w2p), _ptr(w2s_mma), T, H, E, k, I,
+        int(bool(renormalize)), _ptr(out), _ptr(workspace), workspace.numel(), _stream()))
+    return out
+
+
 def moe_forward_mxfp8_host_workspace_size(T: int, H: int, E: int, k: int, I: int,
                                           n_chunks: int = 0) -> int:
     return int(_lib.load().moe_forward_mxfp8_host_workspace_size(T, H, E, k, I, n_chunks))
@@ -357,6 +402,47 @@ class MXFP8MoELayer:
         return moe_forward_mxfp8_mma_scales(x, logits, self.w13q, self.w13s_mma, self.w2q,
                                             self.w2s_mma, self.k, self.renormalize, out=out,
                                             workspace=self.workspace(x.shape[0], x.device))
+
+
+class W4A8MoELayer:
+    """MXFP4 (packed e2m1) expert weights with MXFP8 activations (W4A8).
+
+    ``from_bf16`` quantizes bf16 w13 [E, 2I, H] / w2 [E, H, I] to MXFP4 on the
+    device at load (the online path); ``from_quantized`` takes packed FP4
+    payloads [E, N, K/2] and e8m0 scales [E, N, K/32] as an offline checkpoint
+    ships them.  Scales are re-laid out once into the tensor-core layout.
+    """
+
+    def __init__(self, w13p, w13s, w2p, w2s, k: int, renormalize: bool = True):
+        self.w13p, self.w13s, self.w2p, self.w2s = _u8(w13p), w13s, _u8(w2p), w2s
+        self.k = k
+        self.renormalize = renormalize
+        self.E, n2, h2 = self.w13p.shape
+        self.H, self.I = 2 * h2, n2 // 2
+        self.w13s_mma = mx_scales_to_mma_layout(self.w13s, self.H)
+        self.w2s_mma = mx_scales_to_mma_layout(self.w2s, self.I)
+        self._ws = None
+
+    @classmethod
+    def from_bf16(cls, w13, w2, k: int, renormalize: bool = True):
+        w13p, w13s = mx_quantize_fp4_3d(w13)
+        w2p, w2s = mx_quantize_fp4_3d(w2)
+        return cls(w13p, w13s, w2p, w2s, k, renormalize)
+
+    @classmethod
+    def from_quantized(cls, w13p, w13s, w2p, w2s, k: int, renormalize: bool = True):
+        return cls(w13p, w13s, w2p, w2s, k, renormalize)
+
+    def workspace(self, T: int, device):
+        need = moe_forward_mxfp8_workspace_size(T, self.H, self.E, self.k, self.I)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+        return self._ws
+
+    def __call__(self, x, logits, out=None):
+        return moe_forward_w4a8_mma_scales(x, logits, self.w13p, self.w13s_mma, self.w2p,
+                                           self.w2s_mma, self.k, self.renormalize, out=out,
+                                           workspace=self.workspace(x.shape[0], x.device))
 
 
 def moe_route_quant_mxfp8_noalloc(x, logits, k: int, renormalize: bool = True) -> dict:

@@ -338,11 +338,12 @@ mxmoe_status mxmoe_layer_profile_read(float* ms, int n) {
   return MXMOE_OK;
 }
 
+// fp4_weights: w13q / w2q are packed MXFP4 (W4A8; requires mma_scales).
 static mxmoe_status forward_impl(const uint16_t* x, const float* logits, const uint8_t* w13q,
                                  const uint8_t* w13s, const uint8_t* w2q, const uint8_t* w2s,
                                  bool mma_scales, int T, int H, int E, int k, int I,
                                  int renormalize, uint16_t* out, void* ws, size_t ws_bytes,
-                                 void* stream) {
+                                 void* stream, bool fp4_weights = false) {
   if (T < 0 || H <= 0 || E <= 0 || k < 1 || k > 32 || k > E || I <= 0) return MXMOE_ERR_SHAPE;
   if (E > 256 || H % 128 != 0 || I % 128 != 0) return MXMOE_ERR_UNSUPPORTED;
   if ((int64_t)T * k >= (1ll << 31)) return MXMOE_ERR_SHAPE;
@@ -354,6 +355,8 @@ static mxmoe_status forward_impl(const uint16_t* x, const float* logits, const u
   MXMOE_CHECK_PTR(out);
   if (!w13s || !w2s) return MXMOE_ERR_NULL;
   if (mma_scales && (!aligned16(w13s) || !aligned16(w2s))) return MXMOE_ERR_ALIGN;
+  if (fp4_weights && (!mma_scales || ((uintptr_t)w13q & 31u) || ((uintptr_t)w2q & 31u)))
+    return mma_scales ? MXMOE_ERR_ALIGN : MXMOE_ERR_UNSUPPORTED;
   if (!mma_scales && (((uintptr_t)w13s & 3u) || ((uintptr_t)w2s & 3u))) return MXMOE_ERR_ALIGN;
   if (!ws) return MXMOE_ERR_WORKSPACE;
   if ((uintptr_t)ws & 255u) return MXMOE_ERR_ALIGN;
@@ -392,10 +395,11 @@ static mxmoe_status forward_impl(const uint16_t* x, const float* logits, const u
                    src2s, counts, offs, (int32_t*)(b + L.hist), s, tbase);
   if (e != cudaSuccess) return MXMOE_ERR_CUDA;
   prof.mark(2);
-  e = launch_gemm_swiglu_quant(xq, xs, w13q, w13s_t, offs, M, E, H, I, aq, as, s, true);
+  e = launch_gemm_swiglu_quant(xq, xs, w13q, w13s_t, offs, M, E, H, I, aq, as, s, true,
+                               fp4_weights);
   if (e != cudaSuccess) return MXMOE_ERR_CUDA;
   prof.mark(3);
-  e = launch_gemm_bf16(aq, as, w2q, w2s_t, offs, M, E, I, H, y, s, true);
+  e = launch_gemm_bf16(aq, as, w2q, w2s_t, offs, M, E, I, H, y, s, true, fp4_weights);
   if (e != cudaSuccess) return MXMOE_ERR_CUDA;
   prof.mark(4);
   e = launch_finalize(y, w, src2s, T, k, H, out, s);
@@ -421,6 +425,25 @@ mxmoe_status moe_forward_mxfp8_mma_scales(const uint16_t* x, const float* logits
                                           void* stream) {
   return forward_impl(x, logits, w13q, w13s_mma, w2q, w2s_mma, true, T, H, E, k, I, renormalize,
                       out, ws, ws_bytes, stream);
+}
+
+mxmoe_status moe_forward_w4a8_mma_scales(const uint16_t* x, const float* logits,
+                                         const uint8_t* w13p, const uint8_t* w13s_mma,
+                                         const uint8_t* w2p, const uint8_t* w2s_mma, int T, int H,
+                                         int E, int k, int I, int renormalize, uint16_t* out,
+                                         void* ws, size_t ws_bytes, void* stream) {
+  return forward_impl(x, logits, w13p, w13s_mma, w2p, w2s_mma, true, T, H, E, k, I, renormalize,
+                      out, ws, ws_bytes, stream, true);
+}
+
+mxmoe_status mx_quantize_fp4_3d(const uint16_t* w, int64_t E, int64_t N, int64_t K, uint8_t* q,
+                                uint8_t* scale, void* stream) {
+  if (E < 0 || N < 0 || K <= 0 || K % 32 != 0) return MXMOE_ERR_SHAPE;
+  if (E == 0 || N == 0) return MXMOE_OK;
+  MXMOE_CHECK_PTR(w);
+  MXMOE_CHECK_PTR(q);
+  if (!scale) return MXMOE_ERR_NULL;
+  return from_cuda(launch_mx_quantize_fp4(w, E * N, K, q, scale, (cudaStream_t)stream));
 }
 
 // ---------------------------------------------------------------- host-buffer layer

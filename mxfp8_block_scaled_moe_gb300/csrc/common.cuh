@@ -148,6 +148,45 @@ __device__ __forceinline__ void store_block32_e4m3(uint8_t* p, const uint32_t (&
   }
 }
 
+// ---- MXFP4 (e2m1 elements, W4A8 weights).  Same rule with the e2m1 element's
+// largest power-of-two exponent 2: b = max(ef - 2, 0), elements
+// e2m1_rn_satfinite(x * 2^(127 - b)); 2^(127 - b) stays a normal fp32 for
+// every b a bf16 input reaches (b <= 252).
+
+// Two fp32 -> one byte of two e2m1 codes (lo -> bits 0..3, hi -> bits 4..7),
+// round to nearest even, saturating to +-6.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+// MXFP4-quantize one block of 32 bf16 (16 words) into 16 packed bytes (4
+// words; element 2i in the low nibble of byte i); returns the e8m0 scale byte.
+__device__ __forceinline__ uint32_t quant_block32_bf16_fp4(const uint32_t (&w)[16],
+                                                           uint32_t (&o)[4]) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m = umax(m, bf16x2_absmax_bits(w[i]));
+  const int ef = (int)(m >> 23);
+  const uint32_t sb = (uint32_t)(ef - 2 < 0 ? 0 : ef - 2);
+  const float inv = inv_scale_from_e8m0(sb);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t wj = w[4 * i + j];
+      word |= cvt_e2m1x2(bf16_bits_to_float(wj & 0xFFFFu) * inv,
+                         bf16_bits_to_float(wj >> 16) * inv) << (8 * j);
+    }
+    o[i] = word;
+  }
+  return sb;
+}
+
 __device__ __forceinline__ bool aligned32(const void* p) {
   return (reinterpret_cast<uintptr_t>(p) & 31u) == 0;
 }

@@ -80,7 +80,7 @@ struct Layout1 {
 // of tiled_scales.h (a segment's chunks are contiguous: one bulk copy per 128
 // rows); otherwise they are the row-major [rows, K/32] arrays, gathered into
 // the same staging layout by cp.async.
-template <int BN, bool kSwiglu, bool kTiledSF>
+template <int BN, bool kSwiglu, bool kTiledSF, bool kFp4B>
 __global__ void __launch_bounds__(THREADS1, 1)
     gemm1sm_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, const Params p) {
@@ -236,7 +236,8 @@ __global__ void __launch_bounds__(THREADS1, 1)
         const uint32_t sA = sbase + L::OFF_A + stage * L::A_BYTES;
         const uint32_t sB = sbase + L::OFF_B + stage * L::B_BYTES;
         if (lane == 0) {
-          mbar_arrive_expect_tx(bar_full(stage), L::A_BYTES + L::B_BYTES);
+          // packed FP4 B counts its global (packed) bytes: half its smem footprint
+          mbar_arrive_expect_tx(bar_full(stage), L::A_BYTES + (kFp4B ? L::B_BYTES / 2 : L::B_BYTES));
           tma_load_2d(sA, &tmA, kt * BK, (int)row0, bar_full(stage));
           if (kSwiglu) {
             tma_load_2d(sB, &tmB, kt * BK, (int)bh0, bar_full(stage));
@@ -270,7 +271,7 @@ __global__ void __launch_bounds__(THREADS1, 1)
       int g = 0;
       bool ok = true;
       bool issued = false;
-      constexpr uint32_t IDESC = make_idesc(BM, BN);
+      constexpr uint32_t IDESC = make_idesc(BM, BN, kFp4B);
       for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
         if (!wait_bar(bar_acc_empty, acc_phase ^ 1, p.wait_limit, p.status, s_abort)) {
           ok = false;
@@ -404,7 +405,7 @@ __global__ void __launch_bounds__(THREADS1, 1)
 
 // ---------------------------------------------------------------- host side
 
-template <int BN, bool kSwiglu, bool kTiledSF>
+template <int BN, bool kSwiglu, bool kTiledSF, bool kFp4B>
 static cudaError_t launch_single(const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
                                  const uint8_t* sfb, const int64_t* offsets, int64_t M, int E,
                                  int K, int Nw, int n_out, void* out, uint8_t* out_scale,
@@ -415,7 +416,7 @@ static cudaError_t launch_single(const uint8_t* a, const uint8_t* sfa, const uin
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   static bool configured[64] = {false};
-  auto kern = gemm1sm_kernel<BN, kSwiglu, kTiledSF>;
+  auto kern = gemm1sm_kernel<BN, kSwiglu, kTiledSF, kFp4B>;
   if (!configured[dev]) {
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
@@ -425,7 +426,7 @@ static cudaError_t launch_single(const uint8_t* a, const uint8_t* sfa, const uin
   CUtensorMap tmA, tmB;
   const uint32_t b_box_rows = kSwiglu ? BN / 2 : BN;
   if (!make_map(&tmA, a, (uint64_t)K, (uint64_t)M, BK, BM)) return cudaErrorInvalidValue;
-  if (!make_map(&tmB, b, (uint64_t)K, (uint64_t)E * Nw, BK, b_box_rows))
+  if (!make_map(&tmB, b, (uint64_t)K, (uint64_t)E * Nw, BK, b_box_rows, kFp4B))
     return cudaErrorInvalidValue;
   Params p;
   p.sfa = sfa;
@@ -452,16 +453,16 @@ static cudaError_t launch_single(const uint8_t* a, const uint8_t* sfa, const uin
 // co-schedule CTA pairs; both kernels give the same bytes.  By default gmm2
 // (bf16 out) takes the 2-SM kernel when experts average at least 4 m-tiles,
 // everything else the 1-SM kernel.
-template <int BN, bool kSwiglu, bool kTiledSF>
+template <int BN, bool kSwiglu, bool kTiledSF, bool kFp4B>
 static cudaError_t launch(const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
                           const uint8_t* sfb, const int64_t* offsets, int64_t M, int E, int K,
                           int Nw, int n_out, void* out, uint8_t* out_scale, cudaStream_t stream) {
   if (BN == 256 && use_two_sm_gemm(kSwiglu, M, E)) {
-    const cudaError_t err = launch_pair<kSwiglu, kTiledSF>(a, sfa, b, sfb, offsets, M, E, K, Nw,
+    const cudaError_t err = launch_pair<kSwiglu, kTiledSF, kFp4B>(a, sfa, b, sfb, offsets, M, E, K, Nw,
                                                            n_out, out, out_scale, stream);
     if (err != cudaErrorNotSupported) return err;
   }
-  return launch_single<BN, kSwiglu, kTiledSF>(a, sfa, b, sfb, offsets, M, E, K, Nw, n_out, out,
+  return launch_single<BN, kSwiglu, kTiledSF, kFp4B>(a, sfa, b, sfb, offsets, M, E, K, Nw, n_out, out,
                                               out_scale, stream);
 }
 
@@ -470,29 +471,43 @@ static cudaError_t launch(const uint8_t* a, const uint8_t* sfa, const uint8_t* b
 cudaError_t launch_gemm_swiglu_quant(const uint8_t* xq, const uint8_t* xs, const uint8_t* w13q,
                                      const uint8_t* w13s, const int64_t* offsets, int64_t M,
                                      int E, int H, int I, uint8_t* aq, uint8_t* as,
-                                     cudaStream_t stream, bool tiled_scales) {
+                                     cudaStream_t stream, bool tiled_scales, bool fp4_weights) {
+  if (fp4_weights) {
+    if (!tiled_scales) return cudaErrorNotSupported;
+    return gemm::launch<256, true, true, true>(xq, xs, w13q, w13s, offsets, M, E, H, 2 * I, I, aq,
+                                               as, stream);
+  }
   if (tiled_scales)
-    return gemm::launch<256, true, true>(xq, xs, w13q, w13s, offsets, M, E, H, 2 * I, I, aq, as,
-                                         stream);
-  return gemm::launch<256, true, false>(xq, xs, w13q, w13s, offsets, M, E, H, 2 * I, I, aq, as,
-                                        stream);
+    return gemm::launch<256, true, true, false>(xq, xs, w13q, w13s, offsets, M, E, H, 2 * I, I,
+                                                aq, as, stream);
+  return gemm::launch<256, true, false, false>(xq, xs, w13q, w13s, offsets, M, E, H, 2 * I, I,
+                                               aq, as, stream);
 }
 
 cudaError_t launch_gemm_bf16(const uint8_t* aq, const uint8_t* as, const uint8_t* w2q,
                              const uint8_t* w2s, const int64_t* offsets, int64_t M, int E,
-                             int I, int H, uint16_t* y, cudaStream_t stream, bool tiled_scales) {
+                             int I, int H, uint16_t* y, cudaStream_t stream, bool tiled_scales,
+                             bool fp4_weights) {
+  if (fp4_weights) {
+    if (!tiled_scales) return cudaErrorNotSupported;
+    if (H % 256 == 0)
+      return gemm::launch<256, false, true, true>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y,
+                                                  nullptr, stream);
+    return gemm::launch<128, false, true, true>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y,
+                                                nullptr, stream);
+  }
   if (H % 256 == 0) {
     if (tiled_scales)
-      return gemm::launch<256, false, true>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y, nullptr,
-                                            stream);
-    return gemm::launch<256, false, false>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y, nullptr,
-                                           stream);
+      return gemm::launch<256, false, true, false>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y,
+                                                   nullptr, stream);
+    return gemm::launch<256, false, false, false>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y,
+                                                  nullptr, stream);
   }
   if (tiled_scales)
-    return gemm::launch<128, false, true>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y, nullptr,
-                                          stream);
-  return gemm::launch<128, false, false>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y, nullptr,
-                                         stream);
+    return gemm::launch<128, false, true, false>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y,
+                                                 nullptr, stream);
+  return gemm::launch<128, false, false, false>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y,
+                                                nullptr, stream);
 }
 
 }  // namespace mxmoe

@@ -125,7 +125,7 @@ __device__ __forceinline__ void tc2_commit_both(uint32_t bar) {
       : "memory");
 }
 
-template <bool kSwiglu>
+template <bool kSwiglu, bool kFp4B>
 __global__ void __launch_bounds__(THREADS1, 1)
     gemm2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const Params p) {
@@ -263,7 +263,10 @@ __global__ void __launch_bounds__(THREADS1, 1)
           break;
         }
         if (lane == 0) {
-          if (leader) mbar_arrive_expect_tx(bar_full(stage), 2 * (L::A_BYTES + L::B_BYTES));
+          // packed FP4 B counts its global (packed) bytes: half its smem footprint
+          if (leader)
+            mbar_arrive_expect_tx(bar_full(stage),
+                                  2 * (L::A_BYTES + (kFp4B ? L::B_BYTES / 2 : L::B_BYTES)));
           const uint32_t fb = lead_full0 + 8u * stage;  // leader's full[stage]
           const uint32_t sA = sbase + L::OFF_A + stage * L::A_BYTES;
           const uint32_t sB = sbase + L::OFF_B + stage * L::B_BYTES;
@@ -295,7 +298,7 @@ __global__ void __launch_bounds__(THREADS1, 1)
       int g = 0;
       bool ok = true;
       bool issued = false;
-      constexpr uint32_t IDESC = make_idesc(2 * BM, BN);
+      constexpr uint32_t IDESC = make_idesc(2 * BM, BN, kFp4B);
       for (int unit = unit0; ok && unit < total_units; unit += unit_step) {
         if (!wait_bar_cluster(bar_acc_empty, acc_phase ^ 1, p.wait_limit, p.status, s_abort)) {
           ok = false;
@@ -433,7 +436,7 @@ __global__ void __launch_bounds__(THREADS1, 1)
 
 // ---------------------------------------------------------------- host side
 
-template <bool kSwiglu>
+template <bool kSwiglu, bool kFp4B>
 cudaError_t launch_pair_impl(const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
                              const uint8_t* sfb, const int64_t* offsets, int64_t M, int E, int K,
                              int Nw, int n_out, void* out, uint8_t* out_scale,
@@ -445,7 +448,7 @@ cudaError_t launch_pair_impl(const uint8_t* a, const uint8_t* sfa, const uint8_t
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   static int max_clusters[64];
   static bool configured[64] = {false};
-  auto kern = gemm2sm_kernel<kSwiglu>;
+  auto kern = gemm2sm_kernel<kSwiglu, kFp4B>;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -472,7 +475,8 @@ cudaError_t launch_pair_impl(const uint8_t* a, const uint8_t* sfa, const uint8_t
   if (max_clusters[dev] <= 0) return cudaErrorNotSupported;
   CUtensorMap tmA, tmB;
   if (!make_map(&tmA, a, (uint64_t)K, (uint64_t)M, BK, BM)) return cudaErrorInvalidValue;
-  if (!make_map(&tmB, b, (uint64_t)K, (uint64_t)E * Nw, BK, 128)) return cudaErrorInvalidValue;
+  if (!make_map(&tmB, b, (uint64_t)K, (uint64_t)E * Nw, BK, 128, kFp4B))
+    return cudaErrorInvalidValue;
   Params p;
   p.sfa = sfa;
   p.sfb = sfb;
@@ -494,27 +498,26 @@ cudaError_t launch_pair_impl(const uint8_t* a, const uint8_t* sfa, const uint8_t
   return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
 }
 
-template <bool kSwiglu, bool kTiledSF>
+template <bool kSwiglu, bool kTiledSF, bool kFp4B>
 cudaError_t launch_pair(const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
                         const uint8_t* sfb, const int64_t* offsets, int64_t M, int E, int K,
                         int Nw, int n_out, void* out, uint8_t* out_scale, cudaStream_t stream) {
   if (!kTiledSF) return cudaErrorNotSupported;  // scale chunks arrive by bulk copy
-  return launch_pair_impl<kSwiglu>(a, sfa, b, sfb, offsets, M, E, K, Nw, n_out, out, out_scale,
-                                   stream);
+  return launch_pair_impl<kSwiglu, kFp4B>(a, sfa, b, sfb, offsets, M, E, K, Nw, n_out, out,
+                                          out_scale, stream);
 }
 
-template cudaError_t launch_pair<true, true>(const uint8_t*, const uint8_t*, const uint8_t*,
-                                             const uint8_t*, const int64_t*, int64_t, int, int,
-                                             int, int, void*, uint8_t*, cudaStream_t);
-template cudaError_t launch_pair<false, true>(const uint8_t*, const uint8_t*, const uint8_t*,
-                                              const uint8_t*, const int64_t*, int64_t, int, int,
-                                              int, int, void*, uint8_t*, cudaStream_t);
-template cudaError_t launch_pair<true, false>(const uint8_t*, const uint8_t*, const uint8_t*,
-                                              const uint8_t*, const int64_t*, int64_t, int, int,
-                                              int, int, void*, uint8_t*, cudaStream_t);
-template cudaError_t launch_pair<false, false>(const uint8_t*, const uint8_t*, const uint8_t*,
-                                               const uint8_t*, const int64_t*, int64_t, int, int,
+#define MXMOE_PAIR_INSTANCE(SW, TL, F4)                                                           \
+  template cudaError_t launch_pair<SW, TL, F4>(const uint8_t*, const uint8_t*, const uint8_t*,  \
+                                               const uint8_t*, const int64_t*, int64_t, int, int, \
                                                int, int, void*, uint8_t*, cudaStream_t);
+MXMOE_PAIR_INSTANCE(true, true, false)
+MXMOE_PAIR_INSTANCE(false, true, false)
+MXMOE_PAIR_INSTANCE(true, false, false)
+MXMOE_PAIR_INSTANCE(false, false, false)
+MXMOE_PAIR_INSTANCE(true, true, true)
+MXMOE_PAIR_INSTANCE(false, true, true)
+#undef MXMOE_PAIR_INSTANCE
 
 }  // namespace gemm
 }  // namespace mxmoe

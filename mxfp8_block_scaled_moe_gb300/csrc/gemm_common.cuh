@@ -195,8 +195,11 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uin
 // (format 0 at bits 7-9 / 10-12), both K-major, N >> 3 at bits 17-22, UE8M0
 // scale type (bit 23), M >> 4 at bits 24-28; the scale-factor byte selectors
 // (bits 29-30 for A, 4-5 for B) are or-ed in per K step.
-__host__ __device__ constexpr uint32_t make_idesc(int M, int N) {
-  return ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
+// B format bits 10-12: 0 = e4m3 (W8A8), 5 = e2m1 (W4A8 MXFP4 weights); A is
+// always e4m3.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool b_fp4 = false) {
+  return ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24) |
+         (b_fp4 ? 5u << 10 : 0u);
 }
 
 // Bounded mbarrier wait.  Returns false when the CTA is aborting (another
@@ -436,16 +439,20 @@ inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2D uint8 tensor [outer, inner] (inner contiguous), 128-byte swizzled box.
+// 2D tensor [outer, inner] (inner contiguous), 128-byte swizzled box.  fp4:
+// packed e2m1 (two per byte, inner counted in elements) landing in shared
+// memory as 16-element groups of 8 packed bytes in 16-byte slots, so a
+// 128-element row of the box takes 128 bytes there, as an e4m3 row does.
 inline bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
-                     uint32_t box_inner, uint32_t box_outer) {
+                     uint32_t box_inner, uint32_t box_outer, bool fp4 = false) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner};
+  cuuint64_t strides[1] = {fp4 ? inner / 2 : inner};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+  CUresult r = fn(m, fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                  const_cast<void*>(base), dims, strides, box,
                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -454,7 +461,7 @@ inline bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t 
 
 // 2-SM launch (gemm2sm.cu): returns cudaErrorNotSupported when the device
 // cannot co-schedule CTA pairs, so the caller falls back to the 1-SM kernel.
-template <bool kSwiglu, bool kTiledSF>
+template <bool kSwiglu, bool kTiledSF, bool kFp4B>
 cudaError_t launch_pair(const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
                         const uint8_t* sfb, const int64_t* offsets, int64_t M, int E, int K,
                         int Nw, int n_out, void* out, uint8_t* out_scale, cudaStream_t stream);

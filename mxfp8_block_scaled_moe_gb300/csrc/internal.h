@@ -19,6 +19,9 @@ bool use_two_sm_gemm(bool swiglu, int64_t M, int E);  // 2-SM grouped GEMM kerne
 
 cudaError_t launch_mx_quantize(const uint16_t* x, int64_t rows, int64_t K, uint8_t* q,
                                uint8_t* scale, cudaStream_t stream);
+// MXFP4 (packed e2m1, W4A8 weights): q [rows, K/2], scale [rows, K/32].
+cudaError_t launch_mx_quantize_fp4(const uint16_t* x, int64_t rows, int64_t K, uint8_t* q,
+                                   uint8_t* scale, cudaStream_t stream);
 
 // Routing + permutation.  quant == true: xq/xs outputs; false: bf16 xp output.
 cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, int E, int k,
@@ -36,14 +39,17 @@ cudaError_t launch_finalize(const uint16_t* y, const float* topk_w, const int32_
 // Grouped GEMMs.  Return cudaErrorInvalidValue when a tensor map can't be built.
 // tiled_scales: every scale array (inputs and gmm1's output scales) is in the
 // tiled layout of tiled_scales.h instead of [rows, K/32].
+// fp4_weights: w13q / w2q are packed MXFP4 (e2m1, [rows, K/2]; W4A8), which
+// requires tiled_scales.
 cudaError_t launch_gemm_swiglu_quant(const uint8_t* xq, const uint8_t* xs, const uint8_t* w13q,
                                      const uint8_t* w13s, const int64_t* offsets, int64_t M,
                                      int E, int H, int I, uint8_t* aq, uint8_t* as,
-                                     cudaStream_t stream, bool tiled_scales = false);
+                                     cudaStream_t stream, bool tiled_scales = false,
+                                     bool fp4_weights = false);
 cudaError_t launch_gemm_bf16(const uint8_t* aq, const uint8_t* as, const uint8_t* w2q,
                              const uint8_t* w2s, const int64_t* offsets, int64_t M, int E,
                              int I, int H, uint16_t* y, cudaStream_t stream,
-                             bool tiled_scales = false);
+                             bool tiled_scales = false, bool fp4_weights = false);
 
 // [rows, K/32] scales -> tiled layout (rows % 128 == 0, K % 128 == 0).
 cudaError_t launch_scales_to_tiled(const uint8_t* scale, int64_t rows, int64_t K, uint8_t* out,

@@ -48,6 +48,37 @@ cudaError_t launch_mx_quantize(const uint16_t* x, int64_t rows, int64_t K, uint8
   return cudaGetLastError();
 }
 
+// MXFP4 (W4A8 weights): one lane per block, 64 B in, 16 B + 1 scale byte out.
+template <bool kV8>
+__global__ void __launch_bounds__(256) mx_quantize_fp4_kernel(const uint16_t* __restrict__ x,
+                                                              int64_t n_blocks,
+                                                              uint8_t* __restrict__ q,
+                                                              uint8_t* __restrict__ scale) {
+  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < n_blocks;
+       b += (int64_t)gridDim.x * blockDim.x) {
+    uint32_t w[16], o[4];
+    load_block32_bf16<kV8>(x + b * 32, w);
+    const uint32_t sb = quant_block32_bf16_fp4(w, o);
+    st_cs_v4(q + b * 16, make_uint4(o[0], o[1], o[2], o[3]));
+    scale[b] = (uint8_t)sb;
+  }
+}
+
+cudaError_t launch_mx_quantize_fp4(const uint16_t* x, int64_t rows, int64_t K, uint8_t* q,
+                                   uint8_t* scale, cudaStream_t stream) {
+  const int64_t n_blocks = rows * K / 32;
+  if (n_blocks == 0) return cudaSuccess;
+  const int threads = 256;
+  int64_t blocks = ceil_div(n_blocks, threads);
+  const int64_t cap = (int64_t)num_sms() * 8;
+  if (blocks > cap) blocks = cap;
+  if (((uintptr_t)x & 31u) == 0)
+    mx_quantize_fp4_kernel<true><<<(unsigned)blocks, threads, 0, stream>>>(x, n_blocks, q, scale);
+  else
+    mx_quantize_fp4_kernel<false><<<(unsigned)blocks, threads, 0, stream>>>(x, n_blocks, q, scale);
+  return cudaGetLastError();
+}
+
 // [rows, K/32] e8m0 scales -> the tiled layout of tiled_scales.h.  One thread
 // moves one row's 4 scale bytes of one 128-element K slice (a 4-byte word:
 // K/32 is a multiple of 4, so every word is aligned).
