@@ -40,9 +40,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 FP8_OVER_BF16 = 2.0   # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one grouped GEMM1 launch on
-# the bench workload (profiles/gemm1_swiglu_quant_qwen3_30b_prefill.md), keyed
+# the bench workload (profiles/gemm1_swiglu_quant_qwen3_30b_prefill.md, the
+# DRAM-bytes capture at its end), keyed
 # by the hash of the sources it was captured from
-NCU_TRAFFIC = {"4560b5ddebeb48c3": 790313984}
+NCU_TRAFFIC = {"a9ec3d6a1d8bbad4": 786553600}
 
 
 def parse():
@@ -358,6 +359,7 @@ def main():
     if shape.offline:
         layer = mm.MXFP8MoELayer.from_quantized(inp["w13q"], inp["w13s"], inp["w2q"], inp["w2s"], k)
         wq_ms = None
+        layer4 = None
     else:
         flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
         mm.mx_quantize_3d(inp["w13"])  # warm
@@ -366,6 +368,11 @@ def main():
                        3, flush, stream)
         wq_ms = min(wq_t)
         layer = mm.MXFP8MoELayer.from_bf16(inp["w13"], inp["w2"], k)
+        # the W4A8 variant (MXFP4 weights) from the same bf16 weights, and its
+        # load-time quantizer rate
+        wq4_ms = min(time_fn(torch, lambda: (mm.mx_quantize_fp4_3d(inp["w13"]),
+                                             mm.mx_quantize_fp4_3d(inp["w2"])), 3, flush, stream))
+        layer4 = mm.W4A8MoELayer.from_bf16(inp["w13"], inp["w2"], k)
         del inp["w13"], inp["w2"]
     x, logits = inp["x"], inp["logits"]
     out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
@@ -484,6 +491,45 @@ def main():
     # vendor-library dense GEMM rates (context for the MXFP8 peak; after the
     # timed work, rank 0)
     lib_rates = library_gemm_rates(torch, dev) if rank == 0 else None
+    # the W4A8 variant (MXFP4 expert weights): the same prefill step, and a
+    # 32-token decode slice (weight-streaming bound) for both weight formats
+    w4a8 = None
+    if layer4 is not None:
+        def layer_ms(lyr, xx, ll, reps):
+            lyr(xx, ll)
+            torch.cuda.synchronize()
+            mm.api.layer_profile_enable(True)
+            ts, pr = [], []
+            for _ in range(reps):
+                flush.fill_(1)
+                a_ = torch.cuda.Event(enable_timing=True)
+                b_ = torch.cuda.Event(enable_timing=True)
+                a_.record(stream)
+                lyr(xx, ll)
+                b_.record(stream)
+                b_.synchronize()
+                ts.append(a_.elapsed_time(b_))
+                pr.append(mm.api.layer_profile_read())
+            mm.api.layer_profile_enable(False)
+            return statistics.mean(ts), statistics.mean(p_["gemm1_swiglu_quant"] for p_ in pr)
+        p_ms, p_g1 = layer_ms(layer4, x, logits, 20)
+        Td = 32
+        d4_ms, _ = layer_ms(layer4, x[:Td], logits[:Td], 50)
+        d8_ms, _ = layer_ms(layer, x[:Td], logits[:Td], 50)
+        wbytes4 = E * (2 * I * H + H * I) * (0.5 + 1 / 32)
+        wbytes8 = E * (2 * I * H + H * I) * (1 + 1 / 32)
+        w4a8 = {
+            "weights": "MXFP4: packed e2m1 + e8m0 block-32 scales; activations MXFP8",
+            "prefill": {"tokens_per_s": round(T / (p_ms / 1e3), 1), "ms_per_step": round(p_ms, 4),
+                        "gemm1_TFLOP/s": round(2.0 * T * k * 2 * I * H / (p_g1 / 1e3) / 1e12, 1)},
+            "decode_T32": {"w4a8_ms": round(d4_ms, 4), "mxfp8_ms": round(d8_ms, 4),
+                           "w4a8_weight_GB/s": round(wbytes4 / (d4_ms / 1e3) / 1e9, 1),
+                           "mxfp8_weight_GB/s": round(wbytes8 / (d8_ms / 1e3) / 1e9, 1),
+                           "note": "all experts touched: the layer streams every expert's weights"},
+            "weight_quant_load_time": {"ms": round(wq4_ms, 4),
+                                       "GB/s": round(E * 3 * I * H * (2 + 0.5 + 1 / 32) / (wq4_ms / 1e3) / 1e9, 1)},
+            "parity": "tests/test_gpu_w4a8.py (quantizer bit-exact; layer vs oracle; byte-identical to the MXFP8 layer on re-encoded weights)",
+        }
 
     cpu_base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -516,6 +562,7 @@ def main():
             "e2e_api": "moe_forward_mxfp8_host (pinned host buffers, default chunk plan 3/16 | 5/8 | 3/16 of the tokens, "
                        "H2D / compute / D2H on three streams)",
             "cpu_baseline": cpu_base,
+            "w4a8": w4a8,
             "peaks": {"hbm_gbs": hbm, "fp8_tflops": fp8_peak, "source": peaks["source"],
                       "library_dense_gemm": lib_rates},
             "gemm_src": src_hash,
