@@ -154,3 +154,41 @@ def make_layer(shape: LayerShape, device="cpu", weights=True) -> dict:
         else:
             out["w13"], out["w2"] = make_weights_bf16(shape, device)
     return out
+
+
+# ---------------------------------------------------------------------------
+# dense linear layers
+# ---------------------------------------------------------------------------
+
+@dataclass(frozen=True)
+class LinearShape:
+    name: str
+    M: int            # tokens
+    N: int            # out_features
+    K: int            # in_features (the contraction)
+    seed: int
+    w_std: float = 0.02
+
+
+# Shapes of the dense layers the pages name: Qwen3-8B (the offline W8A8
+# MXFP8 checkpoint of "Quantization on Ascend") and the Qwen3-VL vision MLP
+# (sglang PR #32266: in_features 4304 gives 135 scales, a partial last block;
+# its transpose has out_features 4304, a ragged last 128-row block).
+LINEAR_CONFIGS = {
+    "linear_tiny": LinearShape("linear_tiny", M=200, N=400, K=336, seed=20),
+    "qwen3vl_vision_fc1": LinearShape("qwen3vl_vision_fc1", M=16384, N=4304, K=1152, seed=21),
+    "qwen3vl_vision_fc2": LinearShape("qwen3vl_vision_fc2", M=16384, N=1152, K=4304, seed=22),
+    "qwen3_8b_down_prefill": LinearShape("qwen3_8b_down_prefill", M=8192, N=4096, K=12288,
+                                         seed=23),
+    "qwen3_8b_gate_up_prefill": LinearShape("qwen3_8b_gate_up_prefill", M=8192, N=24576,
+                                            K=4096, seed=24),
+    "qwen3_8b_down_decode": LinearShape("qwen3_8b_down_decode", M=32, N=4096, K=12288, seed=25),
+}
+
+
+def make_linear(shape: LinearShape, device="cpu"):
+    """(x bf16 [M, K] ~ N(0, 1), w bf16 [N, K] ~ N(0, w_std))."""
+    g = _gen(device, shape.seed * 1000 + 5)
+    x = torch.randn(shape.M, shape.K, generator=g, device=device).to(torch.bfloat16)
+    w = (torch.randn(shape.N, shape.K, generator=g, device=device) * shape.w_std)
+    return x, w.to(torch.bfloat16)

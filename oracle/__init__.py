@@ -15,6 +15,8 @@ method defines it, with no blocking, fusion or reordering:
 * ``oracle.moe`` -- top-k softmax routing, the expert permutation, the fused
   route+quant, the grouped GEMM1 + SwiGLU + requant, the grouped GEMM2, the
   finalize-routing combine and the whole layer.
+* ``oracle.linear`` -- the dense MXFP8 linear (per-token activation quant,
+  block-scaled GEMM, bf16 out), any K % 16 == 0.
 
 Sources (cited per function):
 
@@ -38,4 +40,4 @@ Sources (cited per function):
   rule; it is the plainest reading consistent with them.
 """
 
-from . import mx, moe  # noqa: F401
+from . import mx, moe, linear  # noqa: F401
