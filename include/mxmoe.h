@@ -20,6 +20,9 @@
  *   mx_quantize_fp4_3d, moe_forward_w4a8_mma_scales
  *                                   the W4A8 variant: MXFP4 (packed e2m1)
  *                                   expert weights x MXFP8 activations
+ *   mxfp8_linear, mxfp8_linear_mma_scales
+ *                                   the dense MXFP8 linear (one group of the
+ *                                   grouped GEMM), any K % 16 == 0
  *
  * Formats.  An MX block is 32 consecutive elements along the contraction
  * axis K.  Payload: one float8_e4m3fn byte per element.  Scale: one UE8M0
@@ -74,8 +77,11 @@ const char* mxmoe_status_string(mxmoe_status status);
  *
  *   w      bf16 [E, N, K] row-major (K contiguous)
  *   q      e4m3 [E, N, K]            (output)
- *   scale  e8m0 [E, N, K/32]         (output)
- * Requires K % 32 == 0, E, N >= 1.  Empty (E*N == 0) is a no-op.
+ *   scale  e8m0 [E, N, ceil(K/32)]   (output)
+ * Requires K % 16 == 0.  With K % 32 == 16 each row ends in a partial block
+ * of 16 elements whose scale is taken over the elements that exist (sglang
+ * PR #32266 summary, "Offline partial MXFP8 block-scale layout": ceil(K/32)
+ * scales per row, e.g. 135 for K = 4304).  Empty (E*N == 0) is a no-op.
  */
 mxmoe_status mx_quantize_3d(const uint16_t* w, int64_t E, int64_t N, int64_t K,
                             uint8_t* q, uint8_t* scale, void* stream);
@@ -250,11 +256,46 @@ mxmoe_status moe_forward_mxfp8(const uint16_t* x, const float* logits, const uin
  * GB300 tensor cores read each 128-row x 128-K block's 512 scale bytes as
  * one chunk, byte (r % 32) * 16 + (r / 32) * 4 + kb for row r of the block
  * and 32-element block kb, chunks ordered (row block, K slice).
- *   scale  e8m0 [E, N, K/32]   ->   out  e8m0, E*N*K/32 bytes (same size)
- * Requires N % 128 == 0, K % 128 == 0.
+ *   scale  e8m0 [E, N, ceil(K/32)]  ->  out  e8m0, E * ceil(N/128) *
+ *          ceil(K/128) * 512 bytes (the same size when N, K % 128 == 0)
+ * Requires K % 16 == 0; N % 128 == 0 when E > 1.  Slots past the data (the
+ * last K slice when K % 128 != 0, the rows of a ragged last row block when
+ * E == 1) are written as 127 (scale 1; the GEMMs read zero payload there).
  */
 mxmoe_status mx_scales_to_mma_layout(const uint8_t* scale, int64_t E, int64_t N, int64_t K,
                                      uint8_t* out, void* stream);
+
+/*
+ * Dense MXFP8 linear ("Quantization on Ascend", MXFP8 implementation notes,
+ * online path: weights quantized once at load along K, activations
+ * quantized per token at inference, then a block-scaled matmul with one
+ * e8m0 scale per 32 elements of K; that is one group of the grouped GEMM):
+ *
+ *   out[m, n] = bf16( sum_k deq(xq)[m, k] * deq(wq)[n, k] )   fp32 accumulate
+ *   xq, xs    = MX-quant(x) along K (the rule of mx_quantize_3d)
+ *
+ *   x      bf16 [M, K] row-major, 16-byte aligned
+ *   wq     e4m3 [N, K] (K contiguous: the storage of the pages' pre-transposed
+ *          [in, out] view), 16-byte aligned, from mx_quantize_3d(w, 1, N, K)
+ *          or an offline checkpoint
+ *   ws     e8m0 [N, ceil(K/32)] (mxfp8_linear) or its MMA layout from
+ *          mx_scales_to_mma_layout(ws, 1, N, K) (mxfp8_linear_mma_scales,
+ *          16-byte aligned)
+ *   out    bf16 [M, N], 32-byte aligned
+ *   workspace  mxfp8_linear_workspace_size(M, N, K) bytes, 256-byte aligned;
+ *          it holds xq, the activation scales and (mxfp8_linear only) the
+ *          re-laid weight scales.
+ * Requires K % 16 == 0 (K % 32 == 16 gives each row a partial last block of
+ * 16, PR #32266 summary, "Offline partial MXFP8 block-scale layout") and
+ * N % 16 == 0; 0 <= M < 2^31.  M == 0 is a no-op.
+ */
+size_t mxfp8_linear_workspace_size(int64_t M, int64_t N, int64_t K);
+mxmoe_status mxfp8_linear(const uint16_t* x, const uint8_t* wq, const uint8_t* ws, int64_t M,
+                          int64_t N, int64_t K, uint16_t* out, void* workspace, size_t ws_bytes,
+                          void* stream);
+mxmoe_status mxfp8_linear_mma_scales(const uint16_t* x, const uint8_t* wq, const uint8_t* ws_mma,
+                                     int64_t M, int64_t N, int64_t K, uint16_t* out,
+                                     void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * moe_forward_mxfp8 with the weight scales already in the MMA layout

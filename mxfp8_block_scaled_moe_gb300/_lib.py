@@ -22,6 +22,7 @@ EXPORTS = (
     "moe_forward_mxfp8_mma_scales", "mxmoe_layer_profile_enable", "mxmoe_layer_profile_read",
     "mxmoe_set_gemm_2sm", "moe_forward_mxfp8_host", "moe_forward_mxfp8_host_workspace_size",
     "moe_forward_mxfp8_host_plan", "mx_quantize_fp4_3d", "moe_forward_w4a8_mma_scales",
+    "mxfp8_linear_workspace_size", "mxfp8_linear", "mxfp8_linear_mma_scales",
 )
 
 _P = C.c_void_p
@@ -61,6 +62,9 @@ _PROTOS = {
                                          _I, _P, _SZ, _P]),
     "mx_quantize_fp4_3d": (_I, [_P, _I64, _I64, _I64, _P, _P, _P]),
     "mxmoe_layer_profile_read": (_I, [C.POINTER(C.c_float), _I]),
+    "mxfp8_linear_workspace_size": (_SZ, [_I64, _I64, _I64]),
+    "mxfp8_linear": (_I, [_P, _P, _P, _I64, _I64, _I64, _P, _P, _SZ, _P]),
+    "mxfp8_linear_mma_scales": (_I, [_P, _P, _P, _I64, _I64, _I64, _P, _P, _SZ, _P]),
 }
 
 _lib = None

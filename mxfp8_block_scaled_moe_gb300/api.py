@@ -41,7 +41,9 @@ def _u8(t):
 
 
 def mx_quantize_3d(w: torch.Tensor):
-    """bf16 [E, N, K] (or [N, K]) -> (e4m3 payload uint8 same shape, e8m0 scales uint8 [.., K/32])."""
+    """bf16 [E, N, K] (or [N, K]) -> (e4m3 payload uint8 same shape, e8m0 scales uint8 [.., ceil(K/32)]).
+
+    K % 16 == 0; with K % 32 == 16 each row ends in a partial block of 16."""
     _need(w, "w", torch.bfloat16)
     shape = tuple(w.shape)
     if w.dim() == 2:
@@ -51,7 +53,7 @@ def mx_quantize_3d(w: torch.Tensor):
     else:
         raise ValueError("w must be 2D or 3D")
     q = torch.empty(shape, dtype=torch.uint8, device=w.device)
-    s = torch.empty(shape[:-1] + (K // 32 if K % 32 == 0 else 0,), dtype=torch.uint8,
+    s = torch.empty(shape[:-1] + ((K + 31) // 32 if K % 16 == 0 else 0,), dtype=torch.uint8,
                     device=w.device)
     _lib.check("mx_quantize_3d", _lib.load().mx_quantize_3d(
         _ptr(w), E, N, K, _ptr(q), _ptr(s), _stream()))
@@ -203,7 +205,10 @@ def moe_forward_mxfp8(x, logits, w13q, w13s, w2q, w2s, k: int, renormalize: bool
 
 
 def mx_scales_to_mma_layout(scale, K: int):
-    """e8m0 scales [E, N, K/32] (or [N, K/32]) -> the tensor-core layout (same byte count)."""
+    """e8m0 scales [E, N, ceil(K/32)] (or [N, ceil(K/32)]) -> the tensor-core layout.
+
+    The result has shape [.., ceil(N/128)*128, ceil(K/128)*4] (the input's
+    shape when N and K are multiples of 128); it is an opaque byte array."""
     _need(scale, "scale", torch.uint8)
     if scale.dim() == 2:
         E, N = 1, scale.shape[0]
@@ -211,7 +216,8 @@ def mx_scales_to_mma_layout(scale, K: int):
         E, N = scale.shape[0], scale.shape[1]
     else:
         raise ValueError("scale must be 2D or 3D")
-    out = torch.empty_like(scale)
+    tiled = (-(-N // 128) * 128, -(-K // 128) * 4)
+    out = torch.empty(tuple(scale.shape[:-2]) + tiled, dtype=torch.uint8, device=scale.device)
     _lib.check("mx_scales_to_mma_layout", _lib.load().mx_scales_to_mma_layout(
         _ptr(scale), E, N, K, _ptr(out), _stream()))
     return out
@@ -342,6 +348,80 @@ def set_gemm_2sm(mode="auto") -> None:
 
 def set_wait_limit_cycles(cycles: int) -> None:
     _lib.load().mxmoe_set_wait_limit_cycles(int(cycles))
+
+
+def mxfp8_linear_workspace_size(M: int, N: int, K: int) -> int:
+    return int(_lib.load().mxfp8_linear_workspace_size(M, N, K))
+
+
+def _linear(fn, x, wq, ws, out, workspace):
+    wq = _u8(wq)
+    _need(x, "x", torch.bfloat16)
+    _need(wq, "wq", torch.uint8, 2)
+    _need(ws, "ws", torch.uint8, 2)
+    K = x.shape[-1]
+    N = wq.shape[0]
+    if wq.shape[1] != K:
+        raise ValueError(f"wq is {tuple(wq.shape)}, x has K = {K}")
+    M = x.numel() // K if K else 0
+    need = mxfp8_linear_workspace_size(M, N, K)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+    if out is None:
+        out = torch.empty(tuple(x.shape[:-1]) + (N,), dtype=torch.bfloat16, device=x.device)
+    _need(out, "out", torch.bfloat16)
+    _lib.check(fn, getattr(_lib.load(), fn)(
+        _ptr(x), _ptr(wq), _ptr(ws), M, N, K, _ptr(out), _ptr(workspace), workspace.numel(),
+        _stream()))
+    return out
+
+
+def mxfp8_linear(x, wq, ws, out=None, workspace=None):
+    """Dense MXFP8 linear: bf16 x [.., K] -> bf16 [.., N], x MX-quantized per
+    token on the device; wq e4m3 [N, K] and ws e8m0 [N, ceil(K/32)] from
+    mx_quantize_3d (or an offline checkpoint)."""
+    return _linear("mxfp8_linear", x, wq, ws, out, workspace)
+
+
+def mxfp8_linear_mma_scales(x, wq, ws_mma, out=None, workspace=None):
+    """mxfp8_linear with the weight scales already in the tensor-core layout."""
+    return _linear("mxfp8_linear_mma_scales", x, wq, ws_mma, out, workspace)
+
+
+class MXFP8Linear:
+    """A dense MXFP8 linear layer: e4m3 weights [N, K] with e8m0 block scales.
+
+    ``from_bf16`` quantizes a bf16 weight [N, K] (out_features, in_features)
+    on the device at load (the online path); ``from_quantized`` takes an
+    offline checkpoint's payload and [N, ceil(K/32)] scales.  The scales are
+    re-laid out once into the tensor-core layout; calls quantize the
+    activations per token and run the block-scaled GEMM.
+    """
+
+    def __init__(self, wq, ws):
+        self.wq, self.ws = _u8(wq), ws
+        self.N, self.K = self.wq.shape
+        self.ws_mma = mx_scales_to_mma_layout(self.ws, self.K)
+        self._ws = None
+
+    @classmethod
+    def from_bf16(cls, w):
+        return cls(*mx_quantize_3d(w))
+
+    @classmethod
+    def from_quantized(cls, wq, ws):
+        return cls(wq, ws)
+
+    def workspace(self, M: int, device):
+        need = mxfp8_linear_workspace_size(M, self.N, self.K)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+        return self._ws
+
+    def __call__(self, x, out=None):
+        M = x.numel() // self.K
+        return mxfp8_linear_mma_scales(x, self.wq, self.ws_mma, out=out,
+                                       workspace=self.workspace(M, x.device))
 
 
 class MXFP8MoELayer:

@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(THREADS1, 1)
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
   const int total_tiles = s_ts[E];
-  const int KT = p.K / BK;
+  const int KT = (p.K + BK - 1) / BK;  // a partial last K slice is zero-filled by TMA
   const int K32 = p.K / 32;
   const int nseg = (KT + SEG - 1) / SEG;  // scale segments per tile
 
@@ -439,7 +439,7 @@ static cudaError_t launch_single(const uint8_t* a, const uint8_t* sfa, const uin
   p.K = K;
   p.Nw = Nw;
   p.n_out = n_out;
-  p.n_tiles_n = kSwiglu ? n_out / (BN / 2) : n_out / BN;
+  p.n_tiles_n = kSwiglu ? n_out / (BN / 2) : (int)ceil_div(n_out, BN);  // ragged last n-tile: E == 1
   p.status = device_status_ptr();
   p.wait_limit = wait_limit_cycles();
   const int64_t tiles_bound = (ceil_div(M, BM) + E) * (int64_t)p.n_tiles_n;
@@ -490,13 +490,15 @@ cudaError_t launch_gemm_bf16(const uint8_t* aq, const uint8_t* as, const uint8_t
                              bool fp4_weights) {
   if (fp4_weights) {
     if (!tiled_scales) return cudaErrorNotSupported;
-    if (H % 256 == 0)
+    if (ceil_div(H, 128) % 2 == 0)
       return gemm::launch<256, false, true, true>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y,
                                                   nullptr, stream);
     return gemm::launch<128, false, true, true>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y,
                                                 nullptr, stream);
   }
-  if (H % 256 == 0) {
+  // 256-wide tiles when the 128-row weight blocks pair up (a ragged last
+  // block, H % 128 != 0, only with E == 1 and MMA-layout scales)
+  if (ceil_div(H, 128) % 2 == 0) {
     if (tiled_scales)
       return gemm::launch<256, false, true, false>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y,
                                                    nullptr, stream);

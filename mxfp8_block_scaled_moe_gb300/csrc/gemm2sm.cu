@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(THREADS1, 1)
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
   const int total_units = s_ts[E];
-  const int KT = p.K / BK;
+  const int KT = (p.K + BK - 1) / BK;  // a partial last K slice is zero-filled by TMA
   const int nseg = (KT + SEG2 - 1) / SEG2;  // scale segments per unit
   // the leader's barriers as seen from this CTA
   const uint32_t lead_full0 = mapa_cluster(bar_full(0), 0);
@@ -488,7 +488,7 @@ cudaError_t launch_pair_impl(const uint8_t* a, const uint8_t* sfa, const uint8_t
   p.K = K;
   p.Nw = Nw;
   p.n_out = n_out;
-  p.n_tiles_n = kSwiglu ? n_out / 128 : n_out / 256;
+  p.n_tiles_n = kSwiglu ? n_out / 128 : (int)ceil_div(n_out, 256);
   p.status = device_status_ptr();
   p.wait_limit = wait_limit_cycles();
   const int64_t units_bound = (ceil_div(M, BM) / 2 + E) * (int64_t)p.n_tiles_n;

@@ -401,11 +401,13 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t t_row, i
         if (hi) x[1][w] = r; else x[3][w] = r;
       }
       // the quad's rows are consecutive: row j of the quad is grow - qi + j
+      // (a ragged last n-tile, n_out % 16 == 0, masks whole sectors)
       const int64_t col = (int64_t)nt * BN + grp * PC + qi * 16;
+      const bool col_ok = col < p.n_out;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const bool ok = __shfl_sync(0xffffffffu, valid ? 1 : 0, (lane & ~3) + j) != 0;
-        if (ok) st_v8(y + (grow - qi + j) * p.n_out + col, x[j]);
+        if (ok && col_ok) st_v8(y + (grow - qi + j) * p.n_out + col, x[j]);
       }
     } else {
 #pragma unroll
@@ -414,10 +416,11 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t t_row, i
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           o[i] = cvt_bf16x2(__uint_as_float(v[c][2 * i]), __uint_as_float(v[c][2 * i + 1]));
+        const int64_t col = (int64_t)nt * BN + grp * PC + c * 32;
         if (valid) {
-          uint16_t* dst = y + grow * p.n_out + (int64_t)nt * BN + grp * PC + c * 32;
-          st_v8(dst, *reinterpret_cast<const uint32_t(*)[8]>(&o[0]));
-          st_v8(dst + 16, *reinterpret_cast<const uint32_t(*)[8]>(&o[8]));
+          uint16_t* dst = y + grow * p.n_out + col;
+          if (col < p.n_out) st_v8(dst, *reinterpret_cast<const uint32_t(*)[8]>(&o[0]));
+          if (col + 16 < p.n_out) st_v8(dst + 16, *reinterpret_cast<const uint32_t(*)[8]>(&o[8]));
         }
       }
     }

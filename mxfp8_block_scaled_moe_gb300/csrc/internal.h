@@ -19,6 +19,10 @@ bool use_two_sm_gemm(bool swiglu, int64_t M, int E);  // 2-SM grouped GEMM kerne
 
 cudaError_t launch_mx_quantize(const uint16_t* x, int64_t rows, int64_t K, uint8_t* q,
                                uint8_t* scale, cudaStream_t stream);
+// Any K % 16 == 0 (ceil(K/32) scales, a partial last block of 16), scales
+// written in the tiled layout (KT = ceil(K/128)); offsets (nullable) <- {0, rows}.
+cudaError_t launch_mx_quantize_tiled(const uint16_t* x, int64_t rows, int64_t K, uint8_t* q,
+                                     uint8_t* scale_tiled, int64_t* offsets, cudaStream_t stream);
 // MXFP4 (packed e2m1, W4A8 weights): q [rows, K/2], scale [rows, K/32].
 cudaError_t launch_mx_quantize_fp4(const uint16_t* x, int64_t rows, int64_t K, uint8_t* q,
                                    uint8_t* scale, cudaStream_t stream);
@@ -51,7 +55,8 @@ cudaError_t launch_gemm_bf16(const uint8_t* aq, const uint8_t* as, const uint8_t
                              int I, int H, uint16_t* y, cudaStream_t stream,
                              bool tiled_scales = false, bool fp4_weights = false);
 
-// [rows, K/32] scales -> tiled layout (rows % 128 == 0, K % 128 == 0).
+// [rows, ceil(K/32)] scales -> tiled layout with KT = ceil(K/128); rows and
+// slots past the data (a ragged row block or K slice) are written as 127.
 cudaError_t launch_scales_to_tiled(const uint8_t* scale, int64_t rows, int64_t K, uint8_t* out,
                                    cudaStream_t stream);
 
