@@ -55,6 +55,7 @@ def parse():
     ap.add_argument("--config", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-linear", action="store_true")
     return ap.parse_args()
 
 
@@ -204,6 +205,77 @@ def library_gemm_rates(torch, dev, n=8192, reps=10):
     except Exception:
         out["mxfp8_tflops"] = None
     torch.cuda.empty_cache()
+    return out
+
+
+LINEAR_BENCH = ("qwen3vl_vision_fc2", "qwen3vl_vision_fc1", "qwen3_8b_down_prefill",
+                "qwen3_8b_gate_up_prefill", "qwen3_8b_down_decode")
+
+
+def dense_linear_bench(torch, mm, workloads, dev, flush, stream, fp8_peak, hbm):
+    """The dense MXFP8 linear on the pages' dense shapes: per call (L2
+    flushed), the activation quant and the GEMM from the library's event
+    profiler, GEMM TFLOP/s against the MXFP8 peak (weight GB/s against HBM
+    for the 32-token decode), and the vendor library's MXFP8 GEMM on the same
+    shape with unit scales (GEMM only; None where it rejects the shape)."""
+    out = {}
+    for name in LINEAR_BENCH:
+        shape = workloads.LINEAR_CONFIGS[name]
+        M, N, K = shape.M, shape.N, shape.K
+        x, w = workloads.make_linear(shape, dev)
+        lin = mm.MXFP8Linear.from_bf16(w)
+        del w
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        for _ in range(3):
+            lin(x, out=y)
+        torch.cuda.synchronize()
+        reps = 50 if M <= 128 else 20
+        mm.api.layer_profile_enable(True)
+        tot, q, g = [], [], []
+        for _ in range(reps):
+            flush.fill_(1)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            lin(x, out=y)
+            b.record(stream)
+            b.synchronize()
+            tot.append(a.elapsed_time(b))
+            pr = mm.api.linear_profile_read()
+            q.append(pr["act_quant"])
+            g.append(pr["gemm"])
+        mm.api.layer_profile_enable(False)
+        t_ms, q_ms, g_ms = (statistics.mean(v) for v in (tot, q, g))
+        flops = 2.0 * M * N * K
+        wbytes = N * K * (1 + 1 / 32)
+        ent = {"M": M, "N": N, "K": K, "scales_per_row": -(-K // 32),
+               "ms": round(t_ms, 4), "act_quant_ms": round(q_ms, 4), "gemm_ms": round(g_ms, 4),
+               "gemm_TFLOP/s": round(flops / (g_ms / 1e3) / 1e12, 1),
+               "gemm_frac_fp8_peak": round(flops / (g_ms / 1e3) / 1e12 / fp8_peak, 3),
+               "call_TFLOP/s": round(flops / (t_ms / 1e3) / 1e12, 1)}
+        if M <= 128:
+            ent["gemm_weight_GB/s"] = round(wbytes / (g_ms / 1e3) / 1e9, 1)
+            ent["gemm_frac_hbm"] = round(wbytes / (g_ms / 1e3) / 1e9 / hbm, 3)
+        ent["vendor_mxfp8_gemm_ms"] = None
+        if K % 32 == 0:
+            try:
+                a8 = torch.randn(M, K, device=dev).to(torch.float8_e4m3fn)
+                b8 = torch.randn(N, K, device=dev).to(torch.float8_e4m3fn)
+                sa = torch.full((M * K // 32,), 127, dtype=torch.uint8, device=dev).view(
+                    torch.float8_e8m0fnu)
+                sb = torch.full((N * K // 32,), 127, dtype=torch.uint8, device=dev).view(
+                    torch.float8_e8m0fnu)
+                fn = lambda: torch._scaled_mm(a8, b8.t(), scale_a=sa, scale_b=sb,  # noqa: E731
+                                              out_dtype=torch.bfloat16)
+                fn()
+                vt = time_fn(torch, fn, reps, flush, torch.cuda.current_stream())
+                ent["vendor_mxfp8_gemm_ms"] = round(statistics.mean(vt), 4)
+                del a8, b8, sa, sb
+            except Exception:
+                pass
+        out[name] = ent
+        del x, y, lin
+        torch.cuda.empty_cache()
     return out
 
 
@@ -531,6 +603,13 @@ def main():
             "parity": "tests/test_gpu_w4a8.py (quantizer bit-exact; layer vs oracle; byte-identical to the MXFP8 layer on re-encoded weights)",
         }
 
+    # the dense MXFP8 linear (partial K blocks, ragged N) on the pages' dense shapes
+    dense = None
+    if rank == 0 and not args.no_linear:
+        dense = dense_linear_bench(torch, mm, workloads, dev, flush, stream, fp8_peak, hbm)
+        dense["parity"] = ("tests/test_gpu_linear.py (row quant bit-exact incl. the partial block; "
+                           "exact structured GEMM; sampled outputs of every shape vs oracle)")
+
     cpu_base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from oracle import mx as omx  # noqa: F401
@@ -563,6 +642,7 @@ def main():
                        "H2D / compute / D2H on three streams)",
             "cpu_baseline": cpu_base,
             "w4a8": w4a8,
+            "dense_linear": dense,
             "peaks": {"hbm_gbs": hbm, "fp8_tflops": fp8_peak, "source": peaks["source"],
                       "library_dense_gemm": lib_rates},
             "gemm_src": src_hash,

@@ -363,13 +363,15 @@ mxmoe_status moe_forward_mxfp8_host_plan(const uint16_t* x_host, const float* lo
                                          size_t ws_bytes, void* stream);
 
 /*
- * Per-kernel timing of moe_forward_mxfp8 / moe_forward_mxfp8_mma_scales
+ * Per-kernel timing of moe_forward_mxfp8 / moe_forward_mxfp8_mma_scales / mxfp8_linear*
  * (instrumentation, off by default; not part of the method).  While
  * enabled, each layer call records CUDA events on its stream between its
  * kernels; mxmoe_layer_profile_read then returns, for the last such call on
  * the current device, n <= 5 segment times in milliseconds:
  *   [0] weight-scale re-layout (0 for the _mma_scales entry point),
  *   [1] route + fused quant, [2] gmm1, [3] gmm2, [4] finalize.
+ * A dense-linear call (mxfp8_linear*) records [0] weight-scale re-layout,
+ * [1] activation quant, [2] GEMM, and 0 for [3], [4].
  * The read synchronizes on the call's last event.  Not thread-safe.
  */
 mxmoe_status mxmoe_layer_profile_enable(int enable);

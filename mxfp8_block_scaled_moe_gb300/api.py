@@ -337,6 +337,13 @@ def layer_profile_read() -> dict:
     return dict(zip(keys, (float(v) for v in arr)))
 
 
+def linear_profile_read() -> dict:
+    """Per-kernel milliseconds of the last profiled dense-linear call (synchronizes)."""
+    arr = (C.c_float * 3)()
+    _lib.check("mxmoe_layer_profile_read", _lib.load().mxmoe_layer_profile_read(arr, 3))
+    return dict(zip(("weight_scale_layout", "act_quant", "gemm"), (float(v) for v in arr)))
+
+
 def set_gemm_2sm(mode="auto") -> None:
     """Grouped-GEMM kernel choice: False/0 = 1-SM kernel, True/1 = 2-SM kernel
     (cta_group::2) for the layer's 256-wide tiles, "auto"/2 (the default) =

@@ -288,79 +288,6 @@ mxmoe_status mx_scales_to_mma_layout(const uint8_t* scale, int64_t E, int64_t N,
   return from_cuda(launch_scales_to_tiled(scale, E * N, K, out, (cudaStream_t)stream));
 }
 
-// Dense linear workspace, each part 256-byte aligned:
-// xq [M, K] | xs tiled (ceil(M/128) + 1 row blocks) | offsets [2] | w scales
-// tiled (ceil(N/128) row blocks; the row-major-scale entry point only).
-struct LinearLayout {
-  size_t xq, xs, offs, ws, total;
-};
-
-static LinearLayout linear_layout(int64_t M, int64_t N, int64_t K, bool w_scales) {
-  LinearLayout L;
-  const size_t slice_bytes = (size_t)((K + 127) / 128) * 512;  // one row block, one K slice each
-  size_t o = 0;
-  auto take = [&](size_t bytes) { size_t at = o; o += align256(bytes); return at; };
-  L.xq = take((size_t)M * K);
-  L.xs = take(((size_t)(M + 127) / 128 + 1) * slice_bytes);
-  L.offs = take(2 * sizeof(int64_t));
-  L.ws = w_scales ? take((size_t)(N + 127) / 128 * slice_bytes) : 0;
-  L.total = o;
-  return L;
-}
-
-static bool linear_shape_ok(int64_t M, int64_t N, int64_t K) {
-  return M >= 0 && M < (1ll << 31) && N > 0 && N < (1ll << 31) && K > 0 && K < (1ll << 31) &&
-         N % 16 == 0 && K % 16 == 0;
-}
-
-size_t mxfp8_linear_workspace_size(int64_t M, int64_t N, int64_t K) {
-  if (!linear_shape_ok(M, N, K)) return 0;
-  return linear_layout(M, N, K, true).total;
-}
-
-static mxmoe_status linear_impl(const uint16_t* x, const uint8_t* wq, const uint8_t* ws,
-                                bool ws_tiled, int64_t M, int64_t N, int64_t K, uint16_t* out,
-                                void* workspace, size_t ws_bytes, void* stream) {
-  if (!linear_shape_ok(M, N, K)) return MXMOE_ERR_SHAPE;
-  if (M == 0) return MXMOE_OK;
-  MXMOE_CHECK_PTR(x);
-  MXMOE_CHECK_PTR(wq);
-  MXMOE_CHECK_PTR(out);
-  if ((uintptr_t)out & 31u) return MXMOE_ERR_ALIGN;  // 32-byte sector stores
-  if (!ws) return MXMOE_ERR_NULL;
-  if (ws_tiled && !aligned16(ws)) return MXMOE_ERR_ALIGN;  // bulk copies
-  const LinearLayout L = linear_layout(M, N, K, !ws_tiled);
-  if (!workspace || ws_bytes < L.total) return MXMOE_ERR_WORKSPACE;
-  if ((uintptr_t)workspace & 255u) return MXMOE_ERR_ALIGN;
-  cudaStream_t st = (cudaStream_t)stream;
-  uint8_t* base = (uint8_t*)workspace;
-  uint8_t* xq = base + L.xq;
-  uint8_t* xs = base + L.xs;
-  int64_t* offs = (int64_t*)(base + L.offs);
-  const uint8_t* wst = ws;
-  cudaError_t err;
-  if (!ws_tiled) {
-    err = launch_scales_to_tiled(ws, N, K, base + L.ws, st);
-    if (err != cudaSuccess) return MXMOE_ERR_CUDA;
-    wst = base + L.ws;
-  }
-  err = launch_mx_quantize_tiled(x, M, K, xq, xs, offs, st);
-  if (err != cudaSuccess) return MXMOE_ERR_CUDA;
-  return from_cuda(launch_gemm_bf16(xq, xs, wq, wst, offs, M, 1, (int)K, (int)N, out, st, true));
-}
-
-mxmoe_status mxfp8_linear(const uint16_t* x, const uint8_t* wq, const uint8_t* ws, int64_t M,
-                          int64_t N, int64_t K, uint16_t* out, void* workspace, size_t ws_bytes,
-                          void* stream) {
-  return linear_impl(x, wq, ws, false, M, N, K, out, workspace, ws_bytes, stream);
-}
-
-mxmoe_status mxfp8_linear_mma_scales(const uint16_t* x, const uint8_t* wq, const uint8_t* ws_mma,
-                                     int64_t M, int64_t N, int64_t K, uint16_t* out,
-                                     void* workspace, size_t ws_bytes, void* stream) {
-  return linear_impl(x, wq, ws_mma, true, M, N, K, out, workspace, ws_bytes, stream);
-}
-
 // Opt-in per-kernel timing of the layer call: events recorded on the call's
 // stream between its kernels (one set per device, reused by every call).
 namespace {
@@ -517,6 +444,87 @@ mxmoe_status mx_quantize_fp4_3d(const uint16_t* w, int64_t E, int64_t N, int64_t
   MXMOE_CHECK_PTR(q);
   if (!scale) return MXMOE_ERR_NULL;
   return from_cuda(launch_mx_quantize_fp4(w, E * N, K, q, scale, (cudaStream_t)stream));
+}
+
+// Dense linear workspace, each part 256-byte aligned:
+// xq [M, K] | xs tiled (ceil(M/128) + 1 row blocks) | offsets [2] | w scales
+// tiled (ceil(N/128) row blocks; the row-major-scale entry point only).
+struct LinearLayout {
+  size_t xq, xs, offs, ws, total;
+};
+
+static LinearLayout linear_layout(int64_t M, int64_t N, int64_t K, bool w_scales) {
+  LinearLayout L;
+  const size_t slice_bytes = (size_t)((K + 127) / 128) * 512;  // one row block, one K slice each
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o += align256(bytes); return at; };
+  L.xq = take((size_t)M * K);
+  L.xs = take(((size_t)(M + 127) / 128 + 1) * slice_bytes);
+  L.offs = take(2 * sizeof(int64_t));
+  L.ws = w_scales ? take((size_t)(N + 127) / 128 * slice_bytes) : 0;
+  L.total = o;
+  return L;
+}
+
+static bool linear_shape_ok(int64_t M, int64_t N, int64_t K) {
+  return M >= 0 && M < (1ll << 31) && N > 0 && N < (1ll << 31) && K > 0 && K < (1ll << 31) &&
+         N % 16 == 0 && K % 16 == 0;
+}
+
+size_t mxfp8_linear_workspace_size(int64_t M, int64_t N, int64_t K) {
+  if (!linear_shape_ok(M, N, K)) return 0;
+  return linear_layout(M, N, K, true).total;
+}
+
+static mxmoe_status linear_impl(const uint16_t* x, const uint8_t* wq, const uint8_t* ws,
+                                bool ws_tiled, int64_t M, int64_t N, int64_t K, uint16_t* out,
+                                void* workspace, size_t ws_bytes, void* stream) {
+  if (!linear_shape_ok(M, N, K)) return MXMOE_ERR_SHAPE;
+  if (M == 0) return MXMOE_OK;
+  MXMOE_CHECK_PTR(x);
+  MXMOE_CHECK_PTR(wq);
+  MXMOE_CHECK_PTR(out);
+  if ((uintptr_t)out & 31u) return MXMOE_ERR_ALIGN;  // 32-byte sector stores
+  if (!ws) return MXMOE_ERR_NULL;
+  if (ws_tiled && !aligned16(ws)) return MXMOE_ERR_ALIGN;  // bulk copies
+  const LinearLayout L = linear_layout(M, N, K, !ws_tiled);
+  if (!workspace || ws_bytes < L.total) return MXMOE_ERR_WORKSPACE;
+  if ((uintptr_t)workspace & 255u) return MXMOE_ERR_ALIGN;
+  cudaStream_t st = (cudaStream_t)stream;
+  uint8_t* base = (uint8_t*)workspace;
+  uint8_t* xq = base + L.xq;
+  uint8_t* xs = base + L.xs;
+  int64_t* offs = (int64_t*)(base + L.offs);
+  const uint8_t* wst = ws;
+  cudaError_t err;
+  LayerProfiler prof(st);
+  prof.mark(0);
+  if (!ws_tiled) {
+    err = launch_scales_to_tiled(ws, N, K, base + L.ws, st);
+    if (err != cudaSuccess) return MXMOE_ERR_CUDA;
+    wst = base + L.ws;
+  }
+  prof.mark(1);
+  err = launch_mx_quantize_tiled(x, M, K, xq, xs, offs, st);
+  if (err != cudaSuccess) return MXMOE_ERR_CUDA;
+  prof.mark(2);
+  err = launch_gemm_bf16(xq, xs, wq, wst, offs, M, 1, (int)K, (int)N, out, st, true);
+  if (err != cudaSuccess) return MXMOE_ERR_CUDA;
+  for (int i = 3; i < kProfEvents; ++i) prof.mark(i);
+  prof.done();
+  return MXMOE_OK;
+}
+
+mxmoe_status mxfp8_linear(const uint16_t* x, const uint8_t* wq, const uint8_t* ws, int64_t M,
+                          int64_t N, int64_t K, uint16_t* out, void* workspace, size_t ws_bytes,
+                          void* stream) {
+  return linear_impl(x, wq, ws, false, M, N, K, out, workspace, ws_bytes, stream);
+}
+
+mxmoe_status mxfp8_linear_mma_scales(const uint16_t* x, const uint8_t* wq, const uint8_t* ws_mma,
+                                     int64_t M, int64_t N, int64_t K, uint16_t* out,
+                                     void* workspace, size_t ws_bytes, void* stream) {
+  return linear_impl(x, wq, ws_mma, true, M, N, K, out, workspace, ws_bytes, stream);
 }
 
 // ---------------------------------------------------------------- host-buffer layer

@@ -1,10 +1,13 @@
 """Small, self-contained launch sequence of one kernel for ncu captures.
 
     python -m mxfp8_block_scaled_moe_gb300.profile_case --kernel gemm1 --iters 3
+    python -m mxfp8_block_scaled_moe_gb300.profile_case --kernel linear \
+        --config qwen3_8b_down_prefill --iters 3
 
 Builds one layer's inputs (default: the 16K-token Qwen3-30B-A3B-shaped
 prefill), runs the routing step once, then launches the chosen kernel
-``--iters`` times.  It holds about 1-2 GB on the device, more than the L2, so
+``--iters`` times.  ``--kernel linear`` takes a dense-linear shape instead and
+runs the whole linear call (activation quant + GEMM) ``--iters`` times.  It holds about 1-2 GB on the device, more than the L2, so
 DRAM counters are meaningful, and it launches only a few kernels before the
 captured ones.
 """
@@ -23,11 +26,23 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--config", default="qwen3_30b_prefill")
     ap.add_argument("--kernel", default="gemm1",
-                    choices=["gemm1", "gemm2", "route", "finalize", "wquant", "layer"])
+                    choices=["gemm1", "gemm2", "route", "finalize", "wquant", "layer", "linear"])
     ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--gemm-2sm", default="auto", choices=["0", "1", "auto"])
     args = ap.parse_args()
-    shape = workloads.CONFIGS[args.config]
     dev = torch.device("cuda", 0)
+    mm.set_gemm_2sm(args.gemm_2sm)
+    if args.kernel == "linear":
+        lshape = workloads.LINEAR_CONFIGS[args.config]
+        x, w = workloads.make_linear(lshape, dev)
+        lin = mm.MXFP8Linear.from_bf16(w)
+        for _ in range(args.iters):
+            lin(x)
+        torch.cuda.synchronize()
+        if mm.device_status() != 0:
+            raise SystemExit("device status error")
+        return
+    shape = workloads.CONFIGS[args.config]
     inp = workloads.make_layer(shape, dev)
     if shape.offline:
         layer = mm.MXFP8MoELayer.from_quantized(inp["w13q"], inp["w13s"], inp["w2q"], inp["w2s"],
