@@ -38,7 +38,12 @@ Readings of points the pages leave open (each is one choice, stated once):
 * W4A8 (MXFP4 weights): the shared scale is floor(log2 amax) - 2 (2 = the
   largest power-of-two exponent of e2m1, as 8 is for e4m3), elements round to
   nearest-even and saturate at +-6, and a packed byte holds element 2i in its
-  low nibble and element 2i+1 in its high nibble.
+  low nibble and element 2i+1 in its high nibble;
+* W4A4 ("Quantization on Ascend", W4A4 MoE notes: each expert input is
+  quantized to MXFP4 right before the grouped matmul): the routed hidden
+  states and the SwiGLU output (the inputs of gmm1 and gmm2) are MXFP4 with
+  the rule above, the SwiGLU output rounded to fp32 first as in the MXFP8
+  requant.
 """
 
 from __future__ import annotations
@@ -108,17 +113,28 @@ def permute(topk_ids: np.ndarray, E: int):
     return counts, offsets, sorted_to_src, src_to_sorted
 
 
-def route_quant(x: np.ndarray, topk_ids: np.ndarray, E: int):
+def act_quant(x: np.ndarray, afmt: str = "e4m3"):
+    """MX-quantize activations along the last axis: MXFP8 (e4m3 codes) or,
+    for W4A4, MXFP4 (packed e2m1, [..., K/2])."""
+    if afmt == "e4m3":
+        return mx.mx_quantize(x)
+    if afmt == "e2m1":
+        return mx.mxfp4_quantize(x)
+    raise ValueError(f"unknown activation format {afmt!r}")
+
+
+def route_quant(x: np.ndarray, topk_ids: np.ndarray, E: int, afmt: str = "e4m3"):
     """init_routing with quant_mode=3: permuted rows, MX-quantized along H.
 
     ``x`` float64 [T, H] (exact values of the bf16 hidden states).  Each token
     row is quantized (its blocks depend only on the row) and the result is
-    placed in its k expanded rows.  Returns (xq uint8 [M, H], xs uint8
-    [M, ceil(H/32)], counts, offsets, sorted_to_src, src_to_sorted).
+    placed in its k expanded rows.  Returns (xq uint8 [M, H] (packed [M, H/2]
+    for ``afmt="e2m1"``), xs uint8 [M, ceil(H/32)], counts, offsets,
+    sorted_to_src, src_to_sorted).
     """
     k = topk_ids.shape[1]
     counts, offsets, s2s, src2s = permute(topk_ids, E)
-    q_tok, s_tok = mx.mx_quantize(x)
+    q_tok, s_tok = act_quant(x, afmt)
     tok = s2s.astype(np.int64) // k
     return q_tok[tok], s_tok[tok], counts, offsets, s2s, src2s
 
@@ -133,9 +149,10 @@ def permute_rows(x: np.ndarray, sorted_to_src: np.ndarray, k: int) -> np.ndarray
 # ----------------------------------------------------------------------------
 
 def deq_weight(q, s, wfmt: str = "e4m3"):
-    """Dequantize one expert's weight matrix: MXFP8 (e4m3 codes [N, K]) or, for
-    the W4A8 path ("Quantization on Ascend", W4A8 notes), MXFP4 (packed e2m1
-    [N, K/2]); e8m0 scales [N, K/32] either way."""
+    """Dequantize an MX matrix (one expert's weights, or activation rows):
+    MXFP8 (e4m3 codes [N, K]) or, for the W4A8 / W4A4 paths ("Quantization on
+    Ascend", W4A8 and W4A4 notes), MXFP4 (packed e2m1 [N, K/2]); e8m0 scales
+    [N, K/32] either way."""
     if wfmt == "e4m3":
         return mx.mx_dequantize(q, s)
     if wfmt == "e2m1":
@@ -149,32 +166,36 @@ def silu(g: np.ndarray) -> np.ndarray:
         return g / (1.0 + np.exp(-g))
 
 
-def gmm1_swiglu_quant(xq, xs, w13q, w13s, offsets, I: int, experts=None, wfmt: str = "e4m3"):
+def gmm1_swiglu_quant(xq, xs, w13q, w13s, offsets, I: int, experts=None, wfmt: str = "e4m3",
+                      afmt: str = "e4m3"):
     """Per expert e and its rows [off_e, off_{e+1}):
 
     h = deq(xq rows) @ deq(w13[e])^T (fp64, exact products), gate = h[:, :I],
     up = h[:, I:], a = silu(gate) * up, rounded to fp32, then MX-quantized
-    along I.  Returns (aq uint8 [M, I], as uint8 [M, I/32]); rows of experts
-    not listed in ``experts`` (default: all) stay zero.
+    along I (in ``afmt``: the activations' format is also gmm2's input
+    format).  Returns (aq uint8 [M, I] (packed [M, I/2] for e2m1), as uint8
+    [M, I/32]); rows of experts not listed in ``experts`` (default: all)
+    stay zero.
     """
-    M, H = xq.shape
+    M = xq.shape[0]
     E = w13q.shape[0]
-    aq = np.zeros((M, I), np.uint8)
+    aq = np.zeros((M, I // 2 if afmt == "e2m1" else I), np.uint8)
     as_ = np.zeros((M, mx.n_scales(I)), np.uint8)
     for e in range(E) if experts is None else experts:
         r0, r1 = int(offsets[e]), int(offsets[e + 1])
         if r1 == r0:
             continue
-        a_in = mx.mx_dequantize(xq[r0:r1], xs[r0:r1])
+        a_in = deq_weight(xq[r0:r1], xs[r0:r1], afmt)
         w = deq_weight(w13q[e], w13s[e], wfmt)
         h = a_in @ w.T
         a = silu(h[:, :I]) * h[:, I:]
         a32 = a.astype(np.float32).astype(np.float64)
-        aq[r0:r1], as_[r0:r1] = mx.mx_quantize(a32)
+        aq[r0:r1], as_[r0:r1] = act_quant(a32, afmt)
     return aq, as_
 
 
-def gmm1_swiglu(xq, xs, w13q, w13s, offsets, I: int, experts=None, wfmt: str = "e4m3"):
+def gmm1_swiglu(xq, xs, w13q, w13s, offsets, I: int, experts=None, wfmt: str = "e4m3",
+                afmt: str = "e4m3"):
     """The unquantized SwiGLU output a (fp64) of gmm1, for error reporting."""
     M = xq.shape[0]
     a_out = np.zeros((M, I))
@@ -182,7 +203,7 @@ def gmm1_swiglu(xq, xs, w13q, w13s, offsets, I: int, experts=None, wfmt: str = "
         r0, r1 = int(offsets[e]), int(offsets[e + 1])
         if r1 == r0:
             continue
-        h = mx.mx_dequantize(xq[r0:r1], xs[r0:r1]) @ deq_weight(w13q[e], w13s[e], wfmt).T
+        h = deq_weight(xq[r0:r1], xs[r0:r1], afmt) @ deq_weight(w13q[e], w13s[e], wfmt).T
         a_out[r0:r1] = silu(h[:, :I]) * h[:, I:]
     return a_out
 
@@ -192,7 +213,7 @@ def gmm1_swiglu(xq, xs, w13q, w13s, offsets, I: int, experts=None, wfmt: str = "
 # ----------------------------------------------------------------------------
 
 def gmm2(aq, as_, w2q, w2s, offsets, experts=None, round_bf16: bool = True,
-         wfmt: str = "e4m3"):
+         wfmt: str = "e4m3", afmt: str = "e4m3"):
     """Per expert: y = deq(aq rows) @ deq(w2[e])^T in fp64.
 
     Returns bf16 bit patterns uint16 [M, H] (``round_bf16``) or the exact
@@ -205,7 +226,7 @@ def gmm2(aq, as_, w2q, w2s, offsets, experts=None, round_bf16: bool = True,
         r0, r1 = int(offsets[e]), int(offsets[e + 1])
         if r1 == r0:
             continue
-        y[r0:r1] = mx.mx_dequantize(aq[r0:r1], as_[r0:r1]) @ deq_weight(w2q[e], w2s[e], wfmt).T
+        y[r0:r1] = deq_weight(aq[r0:r1], as_[r0:r1], afmt) @ deq_weight(w2q[e], w2s[e], wfmt).T
     return mx.f64_to_bf16_bits(y) if round_bf16 else y
 
 
@@ -234,10 +255,11 @@ def finalize(y_bf16_bits, topk_w, src_to_sorted, k: int, round_bf16: bool = True
 # ----------------------------------------------------------------------------
 
 def moe_forward(x_bf16_bits, logits, w13q, w13s, w2q, w2s, k: int, I: int,
-                renormalize: bool = True, wfmt: str = "e4m3"):
+                renormalize: bool = True, wfmt: str = "e4m3", afmt: str = "e4m3"):
     """The whole MXFP8 expert forward; returns a dict of every intermediate.
     ``wfmt="e2m1"`` runs the W4A8 variant: MXFP4 (packed e2m1) expert weights
-    with the same MXFP8 activations, routing, requant and finalize.
+    with the same MXFP8 activations, routing, requant and finalize; adding
+    ``afmt="e2m1"`` runs W4A4 (both grouped GEMMs' inputs MXFP4).
 
     The routing weights fed to finalize are rounded to fp32 first: the
     kernels carry them as fp32, and the rounding of the combine input is a
@@ -246,9 +268,9 @@ def moe_forward(x_bf16_bits, logits, w13q, w13s, w2q, w2s, k: int, I: int,
     x = mx.bf16_bits_to_f64(x_bf16_bits)
     E = w13q.shape[0]
     ids, w = route_topk(logits, k, renormalize)
-    xq, xs, counts, offsets, s2s, src2s = route_quant(x, ids, E)
-    aq, as_ = gmm1_swiglu_quant(xq, xs, w13q, w13s, offsets, I, wfmt=wfmt)
-    y = gmm2(aq, as_, w2q, w2s, offsets, wfmt=wfmt)
+    xq, xs, counts, offsets, s2s, src2s = route_quant(x, ids, E, afmt)
+    aq, as_ = gmm1_swiglu_quant(xq, xs, w13q, w13s, offsets, I, wfmt=wfmt, afmt=afmt)
+    y = gmm2(aq, as_, w2q, w2s, offsets, wfmt=wfmt, afmt=afmt)
     w32 = w.astype(np.float32)
     out = finalize(y, w32, src2s, k)
     return dict(topk_ids=ids, topk_w=w, xq=xq, xs=xs, counts=counts, offsets=offsets,

@@ -12,7 +12,9 @@ Each check ties ``oracle.linear`` to something other than itself:
   the amax, elements by exhaustive nearest-value search over the e4m3 grid
   built from its bit fields (ties to the even code), exact rational sums;
 * the pages' K = 4304 example: 135 scales per row, 68 pairs after padding;
-* with one group the linear equals the grouped GEMM2 of the MoE oracle.
+* with one group the linear equals the grouped GEMM2 of the MoE oracle;
+* W4A4: MXFP4-lossless inputs give the exact matmul, and the W4A4 linear is
+  the (pinned) MXFP8 linear fed the same values as e4m3 codes.
 """
 
 from fractions import Fraction
@@ -147,3 +149,38 @@ def test_linear_equals_one_group_gmm2():
     xq, xs = linear.quantize_activations(xb)
     ref = moe.gmm2(xq, xs, wq[None], ws[None], np.array([0, M]))
     assert np.array_equal(linear.mxfp8_linear(xb, wq, ws), ref)
+
+
+def _lossless_fp4_rows(rng, rows, K):
+    """Rows that MXFP4-quantize exactly: per block one element +-4 * 2^s (it
+    fixes the scale at 2^s) and e2m1 grid values * 2^s elsewhere."""
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    x = grid[rng.integers(0, 8, (rows, K))] * np.where(rng.random((rows, K)) < 0.5, -1, 1)
+    nb = K // 32
+    s = rng.integers(-3, 4, (rows, nb))
+    pos = rng.integers(0, 32, (rows, nb))
+    for j in range(nb):
+        x[np.arange(rows), 32 * j + pos[:, j]] = 4.0 * np.where(rng.random(rows) < 0.5, -1, 1)
+    return x * np.exp2(np.repeat(s, 32, axis=1))
+
+
+@pytest.mark.parametrize("M,N,K", [(5, 3, 64), (2, 7, 32), (4, 4, 160)])
+def test_w4a4_lossless_inputs_give_the_exact_matmul(M, N, K):
+    rng = np.random.default_rng(M * 31 + N + K)
+    x = _lossless_fp4_rows(rng, M, K)
+    w = _lossless_fp4_rows(rng, N, K) / 8.0
+    wp, ws = mx.mxfp4_quantize(w)
+    assert np.array_equal(mx.mxfp4_dequantize(wp, ws), w)
+    got = linear.mxfp4_linear(_bf16_bits(x), wp, ws, round_bf16=False)
+    assert np.array_equal(got, x @ w.T)
+
+
+def test_w4a4_linear_equals_mxfp8_linear_on_reencoded_values():
+    rng = np.random.default_rng(9)
+    M, N, K = 9, 12, 96
+    xb = _bf16_bits(torch.randn(M, K, dtype=torch.float64).to(torch.bfloat16).double().numpy())
+    wp, ws = mx.mxfp4_quantize(rng.normal(0, 0.02, (N, K)))
+    xp, xs = linear.quantize_activations(xb, "e2m1")
+    assert xp.shape == (M, K // 2)
+    e8 = lambda q: mx.e4m3_encode(mx.e2m1_decode(mx.unpack_fp4(q)))
+    assert np.array_equal(linear.mxfp4_linear(xb, wp, ws), linear.linear(e8(xp), xs, e8(wp), ws))

@@ -277,3 +277,32 @@ def test_w4a8_layer_equals_mxfp8_layer_on_reencoded_weights():
     r8 = moe.moe_forward(x, logits, e8(q13), s13, e8(q2), s2, k, I)
     for key in ("aq", "as_", "y", "out"):
         assert np.array_equal(r4[key], r8[key]), key
+
+
+def test_w4a4_layer_reduces_to_the_mxfp8_steps_on_reencoded_values():
+    """The W4A4 layer (MXFP4 weights and expert inputs) is, step by step, the
+    MXFP8 one fed the same values as e4m3 codes under the same scales: the
+    routed inputs are the MXFP4 quant of the token rows, gmm1's pre-quant
+    SwiGLU output equals the MXFP8 gmm1's on re-encoded operands, its
+    requant is the MXFP4 quant of that output rounded to fp32, and gmm2
+    equals the MXFP8 gmm2 on re-encoded operands."""
+    rng = np.random.default_rng(12)
+    T, H, E, k, I = 24, 64, 4, 2, 32
+    xb = mx.f64_to_bf16_bits(rng.standard_normal((T, H)))
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    q13, s13 = mx.mxfp4_quantize(rng.standard_normal((E, 2 * I, H)) * 0.05)
+    q2, s2 = mx.mxfp4_quantize(rng.standard_normal((E, H, I)) * 0.05)
+    r4 = moe.moe_forward(xb, logits, q13, s13, q2, s2, k, I, wfmt="e2m1", afmt="e2m1")
+    e8 = lambda q: mx.e4m3_encode(mx.e2m1_decode(mx.unpack_fp4(q)))
+    tok = r4["sorted_to_src"].astype(np.int64) // k
+    xq_tok, xs_tok = mx.mxfp4_quantize(mx.bf16_bits_to_f64(xb))
+    assert np.array_equal(r4["xq"], xq_tok[tok]) and np.array_equal(r4["xs"], xs_tok[tok])
+    assert r4["xq"].shape == (T * k, H // 2) and r4["aq"].shape == (T * k, I // 2)
+    offs = r4["offsets"]
+    a8 = moe.gmm1_swiglu(e8(r4["xq"]), r4["xs"], e8(q13), s13, offs, I)
+    a4 = moe.gmm1_swiglu(r4["xq"], r4["xs"], q13, s13, offs, I, wfmt="e2m1", afmt="e2m1")
+    assert np.array_equal(a4, a8)
+    aq, as_ = mx.mxfp4_quantize(a8.astype(np.float32).astype(np.float64))
+    assert np.array_equal(r4["aq"], aq) and np.array_equal(r4["as_"], as_)
+    y8 = moe.gmm2(e8(r4["aq"]), r4["as_"], e8(q2), s2, offs)
+    assert np.array_equal(r4["y"], y8)
