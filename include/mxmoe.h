@@ -20,9 +20,13 @@
  *   mx_quantize_fp4_3d, moe_forward_w4a8_mma_scales
  *                                   the W4A8 variant: MXFP4 (packed e2m1)
  *                                   expert weights x MXFP8 activations
+ *   moe_forward_w4a4_mma_scales     the W4A4 variant: MXFP4 weights and MXFP4
+ *                                   expert inputs
  *   mxfp8_linear, mxfp8_linear_mma_scales
  *                                   the dense MXFP8 linear (one group of the
  *                                   grouped GEMM), any K % 16 == 0
+ *   mxfp4_linear, mxfp4_linear_mma_scales
+ *                                   the W4A4 dense linear
  *
  * Formats.  An MX block is 32 consecutive elements along the contraction
  * axis K.  Payload: one float8_e4m3fn byte per element.  Scale: one UE8M0
@@ -298,6 +302,26 @@ mxmoe_status mxfp8_linear_mma_scales(const uint16_t* x, const uint8_t* wq, const
                                      void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * W4A4 dense linear ("Quantization on Ascend", W4A4 notes, offline
+ * single-level path: both matmul inputs packed float4_e2m1fn_x2 with one
+ * UE8M0 scale per 32 elements of K, group sizes [1, 1, 32]): the activations
+ * are MXFP4-quantized per token (the rule of mx_quantize_fp4_3d), then
+ *   out[m, n] = bf16( sum_k deq(xp)[m, k] * deq(wp)[n, k] )   fp32 accumulate
+ *   wp     packed e2m1 [N, K/2] from mx_quantize_fp4_3d(w, 1, N, K), 32-byte
+ *          aligned; ws e8m0 [N, K/32] (mxfp4_linear) or its MMA layout
+ *          (mxfp4_linear_mma_scales, 16-byte aligned)
+ *   x, out, workspace as mxfp8_linear (mxfp8_linear_workspace_size bytes).
+ * Requires K % 128 == 0 (the unpacking TMA of packed e2m1 rows needs a row
+ * length that is a multiple of 128 elements) and N % 16 == 0.
+ */
+mxmoe_status mxfp4_linear(const uint16_t* x, const uint8_t* wp, const uint8_t* ws, int64_t M,
+                          int64_t N, int64_t K, uint16_t* out, void* workspace, size_t ws_bytes,
+                          void* stream);
+mxmoe_status mxfp4_linear_mma_scales(const uint16_t* x, const uint8_t* wp, const uint8_t* ws_mma,
+                                     int64_t M, int64_t N, int64_t K, uint16_t* out,
+                                     void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * moe_forward_mxfp8 with the weight scales already in the MMA layout
  * (mx_scales_to_mma_layout, done once at load); saves re-laying them out on
  * every call.  All other arguments and results as moe_forward_mxfp8.
@@ -322,6 +346,24 @@ mxmoe_status moe_forward_mxfp8_mma_scales(const uint16_t* x, const float* logits
  * Workspace: moe_forward_mxfp8_workspace_size(T, H, E, k, I).
  */
 mxmoe_status moe_forward_w4a8_mma_scales(const uint16_t* x, const float* logits,
+                                         const uint8_t* w13p, const uint8_t* w13s_mma,
+                                         const uint8_t* w2p, const uint8_t* w2s_mma, int T, int H,
+                                         int E, int k, int I, int renormalize, uint16_t* out,
+                                         void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * W4A4: MXFP4 expert weights and MXFP4 expert inputs ("Quantization on
+ * Ascend", W4A4 MoE notes: packed MXFP4 w13 / w2 with UE8M0 block-32 scales;
+ * each expert input is quantized to MXFP4 right before the grouped matmul).
+ * The routing step quantizes the permuted hidden states to MXFP4 (scale byte
+ * clamp(floor(log2 amax) - 2, -127, 127) + 127, e2m1 round-to-nearest-even
+ * saturating at +-6, element 2i in the low nibble of byte i); gmm1's epilogue
+ * requantizes the SwiGLU output (rounded to fp32) to MXFP4 by the same rule;
+ * both grouped GEMMs run e2m1 x e2m1 block-scaled tcgen05 MMAs
+ * (kind::mxf8f6f4).  Arguments, weights and workspace as
+ * moe_forward_w4a8_mma_scales.
+ */
+mxmoe_status moe_forward_w4a4_mma_scales(const uint16_t* x, const float* logits,
                                          const uint8_t* w13p, const uint8_t* w13s_mma,
                                          const uint8_t* w2p, const uint8_t* w2s_mma, int T, int H,
                                          int E, int k, int I, int renormalize, uint16_t* out,

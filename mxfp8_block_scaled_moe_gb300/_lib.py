@@ -23,6 +23,7 @@ EXPORTS = (
     "mxmoe_set_gemm_2sm", "moe_forward_mxfp8_host", "moe_forward_mxfp8_host_workspace_size",
     "moe_forward_mxfp8_host_plan", "mx_quantize_fp4_3d", "moe_forward_w4a8_mma_scales",
     "mxfp8_linear_workspace_size", "mxfp8_linear", "mxfp8_linear_mma_scales",
+    "moe_forward_w4a4_mma_scales", "mxfp4_linear", "mxfp4_linear_mma_scales",
 )
 
 _P = C.c_void_p
@@ -65,6 +66,10 @@ _PROTOS = {
     "mxfp8_linear_workspace_size": (_SZ, [_I64, _I64, _I64]),
     "mxfp8_linear": (_I, [_P, _P, _P, _I64, _I64, _I64, _P, _P, _SZ, _P]),
     "mxfp8_linear_mma_scales": (_I, [_P, _P, _P, _I64, _I64, _I64, _P, _P, _SZ, _P]),
+    "moe_forward_w4a4_mma_scales": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P,
+                                         _SZ, _P]),
+    "mxfp4_linear": (_I, [_P, _P, _P, _I64, _I64, _I64, _P, _P, _SZ, _P]),
+    "mxfp4_linear_mma_scales": (_I, [_P, _P, _P, _I64, _I64, _I64, _P, _P, _SZ, _P]),
 }
 
 _lib = None

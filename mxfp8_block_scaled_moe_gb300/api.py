@@ -249,6 +249,20 @@ def moe_forward_w4a8_mma_scales(x, logits, w13p, w13s_mma, w2p, w2s_mma, k: int,
                                 renormalize: bool = True, out=None, workspace=None):
     """The W4A8 layer: packed MXFP4 expert weights (mx_quantize_fp4_3d) with
     their scales in the tensor-core layout, MXFP8 activations."""
+    return _fp4_layer("moe_forward_w4a8_mma_scales", x, logits, w13p, w13s_mma, w2p, w2s_mma, k,
+                      renormalize, out, workspace)
+
+
+def moe_forward_w4a4_mma_scales(x, logits, w13p, w13s_mma, w2p, w2s_mma, k: int,
+                                renormalize: bool = True, out=None, workspace=None):
+    """The W4A4 layer: packed MXFP4 expert weights, and each grouped GEMM's
+    input quantized to MXFP4 on the device (the routed hidden states, and
+    the SwiGLU output)."""
+    return _fp4_layer("moe_forward_w4a4_mma_scales", x, logits, w13p, w13s_mma, w2p, w2s_mma, k,
+                      renormalize, out, workspace)
+
+
+def _fp4_layer(fn, x, logits, w13p, w13s_mma, w2p, w2s_mma, k, renormalize, out, workspace):
     _need(x, "x", torch.bfloat16, 2)
     _need(logits, "logits", torch.float32, 2)
     for t, n in ((w13p, "w13p"), (w13s_mma, "w13s_mma"), (w2p, "w2p"), (w2s_mma, "w2s_mma")):
@@ -263,7 +277,7 @@ def moe_forward_w4a8_mma_scales(x, logits, w13p, w13s_mma, w2p, w2s_mma, k: int,
         workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=x.device)
     if out is None:
         out = torch.empty(T, H, dtype=torch.bfloat16, device=x.device)
-    _lib.check("moe_forward_w4a8_mma_scales", _lib.load().moe_forward_w4a8_mma_scales(
+    _lib.check(fn, getattr(_lib.load(), fn)(
         _ptr(x), _ptr(logits), _ptr(w13p), _ptr(w13s_mma), _ptr(w2p), _ptr(w2s_mma), T, H, E, k, I,
         int(bool(renormalize)), _ptr(out), _ptr(workspace), workspace.numel(), _stream()))
     return out
@@ -361,14 +375,14 @@ def mxfp8_linear_workspace_size(M: int, N: int, K: int) -> int:
     return int(_lib.load().mxfp8_linear_workspace_size(M, N, K))
 
 
-def _linear(fn, x, wq, ws, out, workspace):
+def _linear(fn, x, wq, ws, out, workspace, packed=False):
     wq = _u8(wq)
     _need(x, "x", torch.bfloat16)
     _need(wq, "wq", torch.uint8, 2)
     _need(ws, "ws", torch.uint8, 2)
     K = x.shape[-1]
     N = wq.shape[0]
-    if wq.shape[1] != K:
+    if wq.shape[1] * (2 if packed else 1) != K:
         raise ValueError(f"wq is {tuple(wq.shape)}, x has K = {K}")
     M = x.numel() // K if K else 0
     need = mxfp8_linear_workspace_size(M, N, K)
@@ -393,6 +407,49 @@ def mxfp8_linear(x, wq, ws, out=None, workspace=None):
 def mxfp8_linear_mma_scales(x, wq, ws_mma, out=None, workspace=None):
     """mxfp8_linear with the weight scales already in the tensor-core layout."""
     return _linear("mxfp8_linear_mma_scales", x, wq, ws_mma, out, workspace)
+
+
+def mxfp4_linear(x, wp, ws, out=None, workspace=None):
+    """W4A4 dense linear: bf16 x [.., K] -> bf16 [.., N], x MXFP4-quantized per
+    token on the device; wp packed MXFP4 [N, K/2] and ws e8m0 [N, K/32] from
+    mx_quantize_fp4_3d (or an offline checkpoint).  K % 128 == 0."""
+    return _linear("mxfp4_linear", x, wp, ws, out, workspace, packed=True)
+
+
+def mxfp4_linear_mma_scales(x, wp, ws_mma, out=None, workspace=None):
+    """mxfp4_linear with the weight scales already in the tensor-core layout."""
+    return _linear("mxfp4_linear_mma_scales", x, wp, ws_mma, out, workspace, packed=True)
+
+
+class MXFP4Linear:
+    """A W4A4 dense linear layer: packed MXFP4 weights [N, K/2] with e8m0 block
+    scales; activations quantized to MXFP4 per token at each call."""
+
+    def __init__(self, wp, ws):
+        self.wp, self.ws = _u8(wp), ws
+        self.N, k2 = self.wp.shape
+        self.K = 2 * k2
+        self.ws_mma = mx_scales_to_mma_layout(self.ws, self.K)
+        self._ws = None
+
+    @classmethod
+    def from_bf16(cls, w):
+        return cls(*mx_quantize_fp4_3d(w))
+
+    @classmethod
+    def from_quantized(cls, wp, ws):
+        return cls(wp, ws)
+
+    def workspace(self, M: int, device):
+        need = mxfp8_linear_workspace_size(M, self.N, self.K)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+        return self._ws
+
+    def __call__(self, x, out=None):
+        M = x.numel() // self.K
+        return mxfp4_linear_mma_scales(x, self.wp, self.ws_mma, out=out,
+                                       workspace=self.workspace(M, x.device))
 
 
 class MXFP8Linear:
@@ -489,6 +546,46 @@ class MXFP8MoELayer:
         return moe_forward_mxfp8_mma_scales(x, logits, self.w13q, self.w13s_mma, self.w2q,
                                             self.w2s_mma, self.k, self.renormalize, out=out,
                                             workspace=self.workspace(x.shape[0], x.device))
+
+
+class W4A4MoELayer:
+    """MXFP4 (packed e2m1) expert weights with MXFP4 expert inputs (W4A4).
+
+    The routed hidden states and the SwiGLU output are quantized to MXFP4 on
+    the device right before the grouped GEMM that reads them.  Weights as for
+    ``W4A8MoELayer``.
+    """
+
+    def __init__(self, w13p, w13s, w2p, w2s, k: int, renormalize: bool = True):
+        self.w13p, self.w13s, self.w2p, self.w2s = _u8(w13p), w13s, _u8(w2p), w2s
+        self.k = k
+        self.renormalize = renormalize
+        self.E, n2, h2 = self.w13p.shape
+        self.H, self.I = 2 * h2, n2 // 2
+        self.w13s_mma = mx_scales_to_mma_layout(self.w13s, self.H)
+        self.w2s_mma = mx_scales_to_mma_layout(self.w2s, self.I)
+        self._ws = None
+
+    @classmethod
+    def from_bf16(cls, w13, w2, k: int, renormalize: bool = True):
+        w13p, w13s = mx_quantize_fp4_3d(w13)
+        w2p, w2s = mx_quantize_fp4_3d(w2)
+        return cls(w13p, w13s, w2p, w2s, k, renormalize)
+
+    @classmethod
+    def from_quantized(cls, w13p, w13s, w2p, w2s, k: int, renormalize: bool = True):
+        return cls(w13p, w13s, w2p, w2s, k, renormalize)
+
+    def workspace(self, T: int, device):
+        need = moe_forward_mxfp8_workspace_size(T, self.H, self.E, self.k, self.I)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+        return self._ws
+
+    def __call__(self, x, logits, out=None):
+        return moe_forward_w4a4_mma_scales(x, logits, self.w13p, self.w13s_mma, self.w2p,
+                                           self.w2s_mma, self.k, self.renormalize, out=out,
+                                           workspace=self.workspace(x.shape[0], x.device))
 
 
 class W4A8MoELayer:

@@ -338,12 +338,14 @@ mxmoe_status mxmoe_layer_profile_read(float* ms, int n) {
   return MXMOE_OK;
 }
 
-// fp4_weights: w13q / w2q are packed MXFP4 (W4A8; requires mma_scales).
+// fmt: 0 = W8A8; 1 = W4A8 (w13q / w2q packed MXFP4); 2 = W4A4 (the expert
+// inputs of both grouped GEMMs are MXFP4 as well).  1 and 2 require mma_scales.
 static mxmoe_status forward_impl(const uint16_t* x, const float* logits, const uint8_t* w13q,
                                  const uint8_t* w13s, const uint8_t* w2q, const uint8_t* w2s,
                                  bool mma_scales, int T, int H, int E, int k, int I,
                                  int renormalize, uint16_t* out, void* ws, size_t ws_bytes,
-                                 void* stream, bool fp4_weights = false) {
+                                 void* stream, int fmt = 0) {
+  const bool fp4_weights = fmt != 0;
   if (T < 0 || H <= 0 || E <= 0 || k < 1 || k > 32 || k > E || I <= 0) return MXMOE_ERR_SHAPE;
   if (E > 256 || H % 128 != 0 || I % 128 != 0) return MXMOE_ERR_UNSUPPORTED;
   if ((int64_t)T * k >= (1ll << 31)) return MXMOE_ERR_SHAPE;
@@ -391,15 +393,14 @@ static mxmoe_status forward_impl(const uint16_t* x, const float* logits, const u
     w2s_t = b + L.w2s;
   }
   prof.mark(1);
-  e = launch_route(x, logits, T, H, E, k, renormalize != 0, true, xq, xs, nullptr, ids, w, s2s,
-                   src2s, counts, offs, (int32_t*)(b + L.hist), s, tbase);
+  e = launch_route(x, logits, T, H, E, k, renormalize != 0, fmt == 2 ? 2 : 1, xq, xs, nullptr, ids,
+                   w, s2s, src2s, counts, offs, (int32_t*)(b + L.hist), s, tbase);
   if (e != cudaSuccess) return MXMOE_ERR_CUDA;
   prof.mark(2);
-  e = launch_gemm_swiglu_quant(xq, xs, w13q, w13s_t, offs, M, E, H, I, aq, as, s, true,
-                               fp4_weights);
+  e = launch_gemm_swiglu_quant(xq, xs, w13q, w13s_t, offs, M, E, H, I, aq, as, s, true, fmt);
   if (e != cudaSuccess) return MXMOE_ERR_CUDA;
   prof.mark(3);
-  e = launch_gemm_bf16(aq, as, w2q, w2s_t, offs, M, E, I, H, y, s, true, fp4_weights);
+  e = launch_gemm_bf16(aq, as, w2q, w2s_t, offs, M, E, I, H, y, s, true, fmt);
   if (e != cudaSuccess) return MXMOE_ERR_CUDA;
   prof.mark(4);
   e = launch_finalize(y, w, src2s, T, k, H, out, s);
@@ -433,7 +434,16 @@ mxmoe_status moe_forward_w4a8_mma_scales(const uint16_t* x, const float* logits,
                                          int E, int k, int I, int renormalize, uint16_t* out,
                                          void* ws, size_t ws_bytes, void* stream) {
   return forward_impl(x, logits, w13p, w13s_mma, w2p, w2s_mma, true, T, H, E, k, I, renormalize,
-                      out, ws, ws_bytes, stream, true);
+                      out, ws, ws_bytes, stream, 1);
+}
+
+mxmoe_status moe_forward_w4a4_mma_scales(const uint16_t* x, const float* logits,
+                                         const uint8_t* w13p, const uint8_t* w13s_mma,
+                                         const uint8_t* w2p, const uint8_t* w2s_mma, int T, int H,
+                                         int E, int k, int I, int renormalize, uint16_t* out,
+                                         void* ws, size_t ws_bytes, void* stream) {
+  return forward_impl(x, logits, w13p, w13s_mma, w2p, w2s_mma, true, T, H, E, k, I, renormalize,
+                      out, ws, ws_bytes, stream, 2);
 }
 
 mxmoe_status mx_quantize_fp4_3d(const uint16_t* w, int64_t E, int64_t N, int64_t K, uint8_t* q,
@@ -476,13 +486,17 @@ size_t mxfp8_linear_workspace_size(int64_t M, int64_t N, int64_t K) {
   return linear_layout(M, N, K, true).total;
 }
 
+// fp4: W4A4 (packed MXFP4 weights [N, K/2], 32-byte aligned; activations
+// quantized to MXFP4).  K % 128 == 0: the unpacking tensor maps of packed
+// e2m1 operands need a row length that is a multiple of 128 elements.
 static mxmoe_status linear_impl(const uint16_t* x, const uint8_t* wq, const uint8_t* ws,
                                 bool ws_tiled, int64_t M, int64_t N, int64_t K, uint16_t* out,
-                                void* workspace, size_t ws_bytes, void* stream) {
-  if (!linear_shape_ok(M, N, K)) return MXMOE_ERR_SHAPE;
+                                void* workspace, size_t ws_bytes, void* stream, bool fp4 = false) {
+  if (!linear_shape_ok(M, N, K) || (fp4 && K % 128 != 0)) return MXMOE_ERR_SHAPE;
   if (M == 0) return MXMOE_OK;
   MXMOE_CHECK_PTR(x);
   MXMOE_CHECK_PTR(wq);
+  if (fp4 && ((uintptr_t)wq & 31u)) return MXMOE_ERR_ALIGN;
   MXMOE_CHECK_PTR(out);
   if ((uintptr_t)out & 31u) return MXMOE_ERR_ALIGN;  // 32-byte sector stores
   if (!ws) return MXMOE_ERR_NULL;
@@ -505,10 +519,10 @@ static mxmoe_status linear_impl(const uint16_t* x, const uint8_t* wq, const uint
     wst = base + L.ws;
   }
   prof.mark(1);
-  err = launch_mx_quantize_tiled(x, M, K, xq, xs, offs, st);
+  err = launch_mx_quantize_tiled(x, M, K, xq, xs, offs, st, fp4);
   if (err != cudaSuccess) return MXMOE_ERR_CUDA;
   prof.mark(2);
-  err = launch_gemm_bf16(xq, xs, wq, wst, offs, M, 1, (int)K, (int)N, out, st, true);
+  err = launch_gemm_bf16(xq, xs, wq, wst, offs, M, 1, (int)K, (int)N, out, st, true, fp4 ? 2 : 0);
   if (err != cudaSuccess) return MXMOE_ERR_CUDA;
   for (int i = 3; i < kProfEvents; ++i) prof.mark(i);
   prof.done();
@@ -525,6 +539,18 @@ mxmoe_status mxfp8_linear_mma_scales(const uint16_t* x, const uint8_t* wq, const
                                      int64_t M, int64_t N, int64_t K, uint16_t* out,
                                      void* workspace, size_t ws_bytes, void* stream) {
   return linear_impl(x, wq, ws_mma, true, M, N, K, out, workspace, ws_bytes, stream);
+}
+
+mxmoe_status mxfp4_linear(const uint16_t* x, const uint8_t* wp, const uint8_t* ws, int64_t M,
+                          int64_t N, int64_t K, uint16_t* out, void* workspace, size_t ws_bytes,
+                          void* stream) {
+  return linear_impl(x, wp, ws, false, M, N, K, out, workspace, ws_bytes, stream, true);
+}
+
+mxmoe_status mxfp4_linear_mma_scales(const uint16_t* x, const uint8_t* wp, const uint8_t* ws_mma,
+                                     int64_t M, int64_t N, int64_t K, uint16_t* out,
+                                     void* workspace, size_t ws_bytes, void* stream) {
+  return linear_impl(x, wp, ws_mma, true, M, N, K, out, workspace, ws_bytes, stream, true);
 }
 
 // ---------------------------------------------------------------- host-buffer layer

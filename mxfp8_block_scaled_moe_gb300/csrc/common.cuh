@@ -153,6 +153,12 @@ __device__ __forceinline__ void store_block32_e4m3(uint8_t* p, const uint32_t (&
 // e2m1_rn_satfinite(x * 2^(127 - b)); 2^(127 - b) stays a normal fp32 for
 // every b a bf16 input reaches (b <= 252).
 
+// MXFP4 scale byte from the bit pattern of |amax| as fp32 (sign cleared).
+__device__ __forceinline__ uint32_t e8m0_fp4_from_amax_bits(uint32_t amax_bits) {
+  const int ef = (int)(amax_bits >> 23);
+  return (uint32_t)(ef - 2 < 0 ? 0 : ef - 2);
+}
+
 // Two fp32 -> one byte of two e2m1 codes (lo -> bits 0..3, hi -> bits 4..7),
 // round to nearest even, saturating to +-6.
 __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
@@ -170,8 +176,7 @@ __device__ __forceinline__ uint32_t quant_block32_bf16_fp4(const uint32_t (&w)[1
   uint32_t m = 0;
 #pragma unroll
   for (int i = 0; i < 16; ++i) m = umax(m, bf16x2_absmax_bits(w[i]));
-  const int ef = (int)(m >> 23);
-  const uint32_t sb = (uint32_t)(ef - 2 < 0 ? 0 : ef - 2);
+  const uint32_t sb = e8m0_fp4_from_amax_bits(m);
   const float inv = inv_scale_from_e8m0(sb);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {

@@ -80,12 +80,13 @@ struct Layout1 {
 // of tiled_scales.h (a segment's chunks are contiguous: one bulk copy per 128
 // rows); otherwise they are the row-major [rows, K/32] arrays, gathered into
 // the same staging layout by cp.async.
-template <int BN, bool kSwiglu, bool kTiledSF, bool kFp4B>
+template <int BN, bool kSwiglu, bool kTiledSF, int kFmt>
 __global__ void __launch_bounds__(THREADS1, 1)
     gemm1sm_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, const Params p) {
   using L = Layout1<BN>;
   constexpr int STAGES = L::S;
+  constexpr bool kFp4B = kFmt != FMT_W8A8, kFp4A = kFmt == FMT_W4A4;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
@@ -237,7 +238,8 @@ __global__ void __launch_bounds__(THREADS1, 1)
         const uint32_t sB = sbase + L::OFF_B + stage * L::B_BYTES;
         if (lane == 0) {
           // packed FP4 B counts its global (packed) bytes: half its smem footprint
-          mbar_arrive_expect_tx(bar_full(stage), L::A_BYTES + (kFp4B ? L::B_BYTES / 2 : L::B_BYTES));
+          mbar_arrive_expect_tx(bar_full(stage), (kFp4A ? L::A_BYTES / 2 : L::A_BYTES) +
+                                                     (kFp4B ? L::B_BYTES / 2 : L::B_BYTES));
           tma_load_2d(sA, &tmA, kt * BK, (int)row0, bar_full(stage));
           if (kSwiglu) {
             tma_load_2d(sB, &tmB, kt * BK, (int)bh0, bar_full(stage));
@@ -271,7 +273,7 @@ __global__ void __launch_bounds__(THREADS1, 1)
       int g = 0;
       bool ok = true;
       bool issued = false;
-      constexpr uint32_t IDESC = make_idesc(BM, BN, kFp4B);
+      constexpr uint32_t IDESC = make_idesc(BM, BN, kFp4B, kFp4A);
       for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
         if (!wait_bar(bar_acc_empty, acc_phase ^ 1, p.wait_limit, p.status, s_abort)) {
           ok = false;
@@ -384,7 +386,7 @@ __global__ void __launch_bounds__(THREADS1, 1)
       const bool got = wait_bar(bar_acc_full, acc_phase, p.wait_limit, p.status, s_abort);
       if (!__all_sync(0xffffffffu, got)) break;  // keep the warp converged
       tc_fence_after();
-      epilogue_tile<BN, kSwiglu, kTiledSF>(
+      epilogue_tile<BN, kSwiglu, kTiledSF, kFp4A>(
           p, t_row, grp, row, lane, grow, valid, nt, (int64_t)(s_mtb[e] + mt) * BM + row,
           [&] { if (lane == 0) mbar_arrive(bar_acc_empty); });
       acc_phase ^= 1;
@@ -405,7 +407,7 @@ __global__ void __launch_bounds__(THREADS1, 1)
 
 // ---------------------------------------------------------------- host side
 
-template <int BN, bool kSwiglu, bool kTiledSF, bool kFp4B>
+template <int BN, bool kSwiglu, bool kTiledSF, int kFmt>
 static cudaError_t launch_single(const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
                                  const uint8_t* sfb, const int64_t* offsets, int64_t M, int E,
                                  int K, int Nw, int n_out, void* out, uint8_t* out_scale,
@@ -416,7 +418,7 @@ static cudaError_t launch_single(const uint8_t* a, const uint8_t* sfa, const uin
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   static bool configured[64] = {false};
-  auto kern = gemm1sm_kernel<BN, kSwiglu, kTiledSF, kFp4B>;
+  auto kern = gemm1sm_kernel<BN, kSwiglu, kTiledSF, kFmt>;
   if (!configured[dev]) {
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
@@ -425,8 +427,9 @@ static cudaError_t launch_single(const uint8_t* a, const uint8_t* sfa, const uin
   }
   CUtensorMap tmA, tmB;
   const uint32_t b_box_rows = kSwiglu ? BN / 2 : BN;
-  if (!make_map(&tmA, a, (uint64_t)K, (uint64_t)M, BK, BM)) return cudaErrorInvalidValue;
-  if (!make_map(&tmB, b, (uint64_t)K, (uint64_t)E * Nw, BK, b_box_rows, kFp4B))
+  if (!make_map(&tmA, a, (uint64_t)K, (uint64_t)M, BK, BM, kFmt == FMT_W4A4))
+    return cudaErrorInvalidValue;
+  if (!make_map(&tmB, b, (uint64_t)K, (uint64_t)E * Nw, BK, b_box_rows, kFmt != FMT_W8A8))
     return cudaErrorInvalidValue;
   Params p;
   p.sfa = sfa;
@@ -453,16 +456,16 @@ static cudaError_t launch_single(const uint8_t* a, const uint8_t* sfa, const uin
 // co-schedule CTA pairs; both kernels give the same bytes.  By default gmm2
 // (bf16 out) takes the 2-SM kernel when experts average at least 4 m-tiles,
 // everything else the 1-SM kernel.
-template <int BN, bool kSwiglu, bool kTiledSF, bool kFp4B>
+template <int BN, bool kSwiglu, bool kTiledSF, int kFmt>
 static cudaError_t launch(const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
                           const uint8_t* sfb, const int64_t* offsets, int64_t M, int E, int K,
                           int Nw, int n_out, void* out, uint8_t* out_scale, cudaStream_t stream) {
   if (BN == 256 && use_two_sm_gemm(kSwiglu, M, E)) {
-    const cudaError_t err = launch_pair<kSwiglu, kTiledSF, kFp4B>(a, sfa, b, sfb, offsets, M, E, K, Nw,
+    const cudaError_t err = launch_pair<kSwiglu, kTiledSF, kFmt>(a, sfa, b, sfb, offsets, M, E, K, Nw,
                                                            n_out, out, out_scale, stream);
     if (err != cudaErrorNotSupported) return err;
   }
-  return launch_single<BN, kSwiglu, kTiledSF, kFp4B>(a, sfa, b, sfb, offsets, M, E, K, Nw, n_out, out,
+  return launch_single<BN, kSwiglu, kTiledSF, kFmt>(a, sfa, b, sfb, offsets, M, E, K, Nw, n_out, out,
                                               out_scale, stream);
 }
 
@@ -471,45 +474,54 @@ static cudaError_t launch(const uint8_t* a, const uint8_t* sfa, const uint8_t* b
 cudaError_t launch_gemm_swiglu_quant(const uint8_t* xq, const uint8_t* xs, const uint8_t* w13q,
                                      const uint8_t* w13s, const int64_t* offsets, int64_t M,
                                      int E, int H, int I, uint8_t* aq, uint8_t* as,
-                                     cudaStream_t stream, bool tiled_scales, bool fp4_weights) {
-  if (fp4_weights) {
+                                     cudaStream_t stream, bool tiled_scales, int fmt) {
+  if (fmt == gemm::FMT_W4A8 || fmt == gemm::FMT_W4A4) {
     if (!tiled_scales) return cudaErrorNotSupported;
-    return gemm::launch<256, true, true, true>(xq, xs, w13q, w13s, offsets, M, E, H, 2 * I, I, aq,
-                                               as, stream);
+    if (fmt == gemm::FMT_W4A8)
+      return gemm::launch<256, true, true, gemm::FMT_W4A8>(xq, xs, w13q, w13s, offsets, M, E, H, 2 * I,
+                                                     I, aq, as, stream);
+    return gemm::launch<256, true, true, gemm::FMT_W4A4>(xq, xs, w13q, w13s, offsets, M, E, H, 2 * I, I,
+                                                   aq, as, stream);
   }
+  if (fmt != gemm::FMT_W8A8) return cudaErrorNotSupported;
   if (tiled_scales)
-    return gemm::launch<256, true, true, false>(xq, xs, w13q, w13s, offsets, M, E, H, 2 * I, I,
-                                                aq, as, stream);
-  return gemm::launch<256, true, false, false>(xq, xs, w13q, w13s, offsets, M, E, H, 2 * I, I,
-                                               aq, as, stream);
+    return gemm::launch<256, true, true, gemm::FMT_W8A8>(xq, xs, w13q, w13s, offsets, M, E, H, 2 * I,
+                                                   I, aq, as, stream);
+  return gemm::launch<256, true, false, gemm::FMT_W8A8>(xq, xs, w13q, w13s, offsets, M, E, H, 2 * I,
+                                                  I, aq, as, stream);
+}
+
+// 256-wide tiles when the 128-row weight blocks pair up (a ragged last block,
+// H % 128 != 0, only with E == 1 and MMA-layout scales), 128-wide otherwise.
+template <int kFmt>
+static cudaError_t launch_bf16_fmt(const uint8_t* aq, const uint8_t* as, const uint8_t* w2q,
+                                   const uint8_t* w2s, const int64_t* offsets, int64_t M, int E,
+                                   int I, int H, uint16_t* y, cudaStream_t stream) {
+  if (ceil_div(H, 128) % 2 == 0)
+    return gemm::launch<256, false, true, kFmt>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y,
+                                                nullptr, stream);
+  return gemm::launch<128, false, true, kFmt>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y,
+                                              nullptr, stream);
 }
 
 cudaError_t launch_gemm_bf16(const uint8_t* aq, const uint8_t* as, const uint8_t* w2q,
                              const uint8_t* w2s, const int64_t* offsets, int64_t M, int E,
                              int I, int H, uint16_t* y, cudaStream_t stream, bool tiled_scales,
-                             bool fp4_weights) {
-  if (fp4_weights) {
+                             int fmt) {
+  if (fmt == gemm::FMT_W4A8 || fmt == gemm::FMT_W4A4) {
     if (!tiled_scales) return cudaErrorNotSupported;
-    if (ceil_div(H, 128) % 2 == 0)
-      return gemm::launch<256, false, true, true>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y,
-                                                  nullptr, stream);
-    return gemm::launch<128, false, true, true>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y,
-                                                nullptr, stream);
+    return fmt == gemm::FMT_W4A8
+               ? launch_bf16_fmt<gemm::FMT_W4A8>(aq, as, w2q, w2s, offsets, M, E, I, H, y, stream)
+               : launch_bf16_fmt<gemm::FMT_W4A4>(aq, as, w2q, w2s, offsets, M, E, I, H, y, stream);
   }
-  // 256-wide tiles when the 128-row weight blocks pair up (a ragged last
-  // block, H % 128 != 0, only with E == 1 and MMA-layout scales)
-  if (ceil_div(H, 128) % 2 == 0) {
-    if (tiled_scales)
-      return gemm::launch<256, false, true, false>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y,
-                                                   nullptr, stream);
-    return gemm::launch<256, false, false, false>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y,
-                                                  nullptr, stream);
-  }
+  if (fmt != gemm::FMT_W8A8) return cudaErrorNotSupported;
   if (tiled_scales)
-    return gemm::launch<128, false, true, false>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y,
-                                                 nullptr, stream);
-  return gemm::launch<128, false, false, false>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y,
-                                                nullptr, stream);
+    return launch_bf16_fmt<gemm::FMT_W8A8>(aq, as, w2q, w2s, offsets, M, E, I, H, y, stream);
+  if (ceil_div(H, 128) % 2 == 0)
+    return gemm::launch<256, false, false, gemm::FMT_W8A8>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y,
+                                                     nullptr, stream);
+  return gemm::launch<128, false, false, gemm::FMT_W8A8>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y,
+                                                   nullptr, stream);
 }
 
 }  // namespace mxmoe

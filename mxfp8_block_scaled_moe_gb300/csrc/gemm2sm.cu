@@ -125,13 +125,14 @@ __device__ __forceinline__ void tc2_commit_both(uint32_t bar) {
       : "memory");
 }
 
-template <bool kSwiglu, bool kFp4B>
+template <bool kSwiglu, int kFmt>
 __global__ void __launch_bounds__(THREADS1, 1)
     gemm2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const Params p) {
   using L = Layout2;
   constexpr int STAGES = L::S;
   constexpr int BN = 256;
+  constexpr bool kFp4B = kFmt != FMT_W8A8, kFp4A = kFmt == FMT_W4A4;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
@@ -266,7 +267,8 @@ __global__ void __launch_bounds__(THREADS1, 1)
           // packed FP4 B counts its global (packed) bytes: half its smem footprint
           if (leader)
             mbar_arrive_expect_tx(bar_full(stage),
-                                  2 * (L::A_BYTES + (kFp4B ? L::B_BYTES / 2 : L::B_BYTES)));
+                                  2 * ((kFp4A ? L::A_BYTES / 2 : L::A_BYTES) +
+                                       (kFp4B ? L::B_BYTES / 2 : L::B_BYTES)));
           const uint32_t fb = lead_full0 + 8u * stage;  // leader's full[stage]
           const uint32_t sA = sbase + L::OFF_A + stage * L::A_BYTES;
           const uint32_t sB = sbase + L::OFF_B + stage * L::B_BYTES;
@@ -298,7 +300,7 @@ __global__ void __launch_bounds__(THREADS1, 1)
       int g = 0;
       bool ok = true;
       bool issued = false;
-      constexpr uint32_t IDESC = make_idesc(2 * BM, BN, kFp4B);
+      constexpr uint32_t IDESC = make_idesc(2 * BM, BN, kFp4B, kFp4A);
       for (int unit = unit0; ok && unit < total_units; unit += unit_step) {
         if (!wait_bar_cluster(bar_acc_empty, acc_phase ^ 1, p.wait_limit, p.status, s_abort)) {
           ok = false;
@@ -409,7 +411,7 @@ __global__ void __launch_bounds__(THREADS1, 1)
       const bool got = wait_bar(bar_acc_full, acc_phase, p.wait_limit, p.status, s_abort);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
-      epilogue_tile<BN, kSwiglu, true>(
+      epilogue_tile<BN, kSwiglu, true, kFp4A>(
           p, t_row, grp, row, lane, grow, valid, nt, (int64_t)(s_mtb[e] + mt) * BM + row,
           [&] {
             if (lane == 0) {
@@ -436,7 +438,7 @@ __global__ void __launch_bounds__(THREADS1, 1)
 
 // ---------------------------------------------------------------- host side
 
-template <bool kSwiglu, bool kFp4B>
+template <bool kSwiglu, int kFmt>
 cudaError_t launch_pair_impl(const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
                              const uint8_t* sfb, const int64_t* offsets, int64_t M, int E, int K,
                              int Nw, int n_out, void* out, uint8_t* out_scale,
@@ -448,7 +450,7 @@ cudaError_t launch_pair_impl(const uint8_t* a, const uint8_t* sfa, const uint8_t
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   static int max_clusters[64];
   static bool configured[64] = {false};
-  auto kern = gemm2sm_kernel<kSwiglu, kFp4B>;
+  auto kern = gemm2sm_kernel<kSwiglu, kFmt>;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -474,8 +476,9 @@ cudaError_t launch_pair_impl(const uint8_t* a, const uint8_t* sfa, const uint8_t
   }
   if (max_clusters[dev] <= 0) return cudaErrorNotSupported;
   CUtensorMap tmA, tmB;
-  if (!make_map(&tmA, a, (uint64_t)K, (uint64_t)M, BK, BM)) return cudaErrorInvalidValue;
-  if (!make_map(&tmB, b, (uint64_t)K, (uint64_t)E * Nw, BK, 128, kFp4B))
+  if (!make_map(&tmA, a, (uint64_t)K, (uint64_t)M, BK, BM, kFmt == FMT_W4A4))
+    return cudaErrorInvalidValue;
+  if (!make_map(&tmB, b, (uint64_t)K, (uint64_t)E * Nw, BK, 128, kFmt != FMT_W8A8))
     return cudaErrorInvalidValue;
   Params p;
   p.sfa = sfa;
@@ -498,12 +501,12 @@ cudaError_t launch_pair_impl(const uint8_t* a, const uint8_t* sfa, const uint8_t
   return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
 }
 
-template <bool kSwiglu, bool kTiledSF, bool kFp4B>
+template <bool kSwiglu, bool kTiledSF, int kFmt>
 cudaError_t launch_pair(const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
                         const uint8_t* sfb, const int64_t* offsets, int64_t M, int E, int K,
                         int Nw, int n_out, void* out, uint8_t* out_scale, cudaStream_t stream) {
   if (!kTiledSF) return cudaErrorNotSupported;  // scale chunks arrive by bulk copy
-  return launch_pair_impl<kSwiglu, kFp4B>(a, sfa, b, sfb, offsets, M, E, K, Nw, n_out, out,
+  return launch_pair_impl<kSwiglu, kFmt>(a, sfa, b, sfb, offsets, M, E, K, Nw, n_out, out,
                                           out_scale, stream);
 }
 
@@ -511,12 +514,14 @@ cudaError_t launch_pair(const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
   template cudaError_t launch_pair<SW, TL, F4>(const uint8_t*, const uint8_t*, const uint8_t*,  \
                                                const uint8_t*, const int64_t*, int64_t, int, int, \
                                                int, int, void*, uint8_t*, cudaStream_t);
-MXMOE_PAIR_INSTANCE(true, true, false)
-MXMOE_PAIR_INSTANCE(false, true, false)
-MXMOE_PAIR_INSTANCE(true, false, false)
-MXMOE_PAIR_INSTANCE(false, false, false)
-MXMOE_PAIR_INSTANCE(true, true, true)
-MXMOE_PAIR_INSTANCE(false, true, true)
+MXMOE_PAIR_INSTANCE(true, true, FMT_W8A8)
+MXMOE_PAIR_INSTANCE(false, true, FMT_W8A8)
+MXMOE_PAIR_INSTANCE(true, false, FMT_W8A8)
+MXMOE_PAIR_INSTANCE(false, false, FMT_W8A8)
+MXMOE_PAIR_INSTANCE(true, true, FMT_W4A8)
+MXMOE_PAIR_INSTANCE(false, true, FMT_W4A8)
+MXMOE_PAIR_INSTANCE(true, true, FMT_W4A4)
+MXMOE_PAIR_INSTANCE(false, true, FMT_W4A4)
 #undef MXMOE_PAIR_INSTANCE
 
 }  // namespace gemm

@@ -195,12 +195,18 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uin
 // (format 0 at bits 7-9 / 10-12), both K-major, N >> 3 at bits 17-22, UE8M0
 // scale type (bit 23), M >> 4 at bits 24-28; the scale-factor byte selectors
 // (bits 29-30 for A, 4-5 for B) are or-ed in per K step.
-// B format bits 10-12: 0 = e4m3 (W8A8), 5 = e2m1 (W4A8 MXFP4 weights); A is
-// always e4m3.
-__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool b_fp4 = false) {
+// Formats: 0 = e4m3, 5 = e2m1.  B is e2m1 for MXFP4 weights (W4A8, W4A4), A
+// for MXFP4 activations (W4A4).
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool b_fp4 = false,
+                                                  bool a_fp4 = false) {
   return ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24) |
-         (b_fp4 ? 5u << 10 : 0u);
+         (b_fp4 ? 5u << 10 : 0u) | (a_fp4 ? 5u << 7 : 0u);
 }
+
+// Operand formats of a GEMM instantiation: W8A8 (e4m3 x e4m3), W4A8 (e4m3
+// activations x e2m1 weights), W4A4 (e2m1 x e2m1; gmm1 then requantizes its
+// output to MXFP4 as well).
+enum : int { FMT_W8A8 = 0, FMT_W4A8 = 1, FMT_W4A4 = 2 };
 
 // Bounded mbarrier wait.  Returns false when the CTA is aborting (another
 // role timed out) or this wait ran out of time (then it starts the abort).
@@ -321,7 +327,7 @@ __device__ __forceinline__ void build_schedule(const Params& p, int lane, int64_
 // overwritten), then SwiGLU + MX requant (gmm1) or bf16 rounding (gmm2) and
 // the stores.  BN = accumulator columns, grp = column slice of this warp.
 // `release` is called by every thread; it arrives once per warp.
-template <int BN, bool kSwiglu, bool kTiledSF, typename Release>
+template <int BN, bool kSwiglu, bool kTiledSF, bool kFp4Out, typename Release>
 __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t t_row, int grp, int row,
                                               int lane, int64_t grow, bool valid, int nt,
                                               int64_t tiled_row, Release release) {
@@ -356,16 +362,31 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t t_row, i
         a[i] = swiglu(__uint_as_float(v[c][i]), __uint_as_float(v[CH / 2 + c][i]));
         m = umax(m, __float_as_uint(a[i]) & 0x7FFFFFFFu);
       }
-      const uint32_t sb = e8m0_from_amax_bits(m);
+      const uint32_t sb = kFp4Out ? e8m0_fp4_from_amax_bits(m) : e8m0_from_amax_bits(m);
       const float inv = inv_scale_from_e8m0(sb);
       uint32_t o[8];
+      if (kFp4Out) {
+        // MXFP4: 16 packed bytes, element 2i in the low nibble of byte i
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        o[i] = cvt_e4m3x4(a[4 * i] * inv, a[4 * i + 1] * inv, a[4 * i + 2] * inv,
-                          a[4 * i + 3] * inv);
+        for (int i = 0; i < 4; ++i) {
+          uint32_t word = 0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            word |= cvt_e2m1x2(a[8 * i + 2 * j] * inv, a[8 * i + 2 * j + 1] * inv) << (8 * j);
+          o[i] = word;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          o[i] = cvt_e4m3x4(a[4 * i] * inv, a[4 * i + 1] * inv, a[4 * i + 2] * inv,
+                            a[4 * i + 3] * inv);
+      }
       if (valid) {
         const int64_t col = (int64_t)nt * (BN / 2) + grp * GC + c * 32;
-        st_v8(aq + grow * p.n_out + col, o);
+        if (kFp4Out)
+          st_v4(aq + grow * (p.n_out / 2) + col / 2, make_uint4(o[0], o[1], o[2], o[3]));
+        else
+          st_v8(aq + grow * p.n_out + col, o);
         if (kTiledSF)
           p.out_scale[tiled_scale_offset(tiled_row, (int)(col >> 5), p.n_out / 128)] = (uint8_t)sb;
         else
@@ -464,7 +485,7 @@ inline bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t 
 
 // 2-SM launch (gemm2sm.cu): returns cudaErrorNotSupported when the device
 // cannot co-schedule CTA pairs, so the caller falls back to the 1-SM kernel.
-template <bool kSwiglu, bool kTiledSF, bool kFp4B>
+template <bool kSwiglu, bool kTiledSF, int kFmt>
 cudaError_t launch_pair(const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
                         const uint8_t* sfb, const int64_t* offsets, int64_t M, int E, int K,
                         int Nw, int n_out, void* out, uint8_t* out_scale, cudaStream_t stream);

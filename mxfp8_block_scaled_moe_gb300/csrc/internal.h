@@ -21,15 +21,18 @@ cudaError_t launch_mx_quantize(const uint16_t* x, int64_t rows, int64_t K, uint8
                                uint8_t* scale, cudaStream_t stream);
 // Any K % 16 == 0 (ceil(K/32) scales, a partial last block of 16), scales
 // written in the tiled layout (KT = ceil(K/128)); offsets (nullable) <- {0, rows}.
+// fp4: MXFP4 rows, q [rows, K/2] packed e2m1, K % 32 == 0.
 cudaError_t launch_mx_quantize_tiled(const uint16_t* x, int64_t rows, int64_t K, uint8_t* q,
-                                     uint8_t* scale_tiled, int64_t* offsets, cudaStream_t stream);
+                                     uint8_t* scale_tiled, int64_t* offsets, cudaStream_t stream,
+                                     bool fp4 = false);
 // MXFP4 (packed e2m1, W4A8 weights): q [rows, K/2], scale [rows, K/32].
 cudaError_t launch_mx_quantize_fp4(const uint16_t* x, int64_t rows, int64_t K, uint8_t* q,
                                    uint8_t* scale, cudaStream_t stream);
 
-// Routing + permutation.  quant == true: xq/xs outputs; false: bf16 xp output.
+// Routing + permutation.  quant 1: MXFP8 xq [M, H] / xs outputs; 2: MXFP4 xq
+// [M, H/2] / xs (tiled scales only); 0: bf16 xp output.
 cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, int E, int k,
-                         bool renormalize, bool quant, uint8_t* xq, uint8_t* xs, uint16_t* xp,
+                         bool renormalize, int quant, uint8_t* xq, uint8_t* xs, uint16_t* xp,
                          int32_t* topk_ids, float* topk_w, int32_t* sorted_to_src,
                          int32_t* src_to_sorted, int64_t* counts, int64_t* offsets,
                          int32_t* block_hist, cudaStream_t stream,
@@ -43,17 +46,18 @@ cudaError_t launch_finalize(const uint16_t* y, const float* topk_w, const int32_
 // Grouped GEMMs.  Return cudaErrorInvalidValue when a tensor map can't be built.
 // tiled_scales: every scale array (inputs and gmm1's output scales) is in the
 // tiled layout of tiled_scales.h instead of [rows, K/32].
-// fp4_weights: w13q / w2q are packed MXFP4 (e2m1, [rows, K/2]; W4A8), which
-// requires tiled_scales.
+// fmt: 0 = W8A8; 1 = W4A8 (w13q / w2q packed MXFP4, e2m1 [rows, K/2]); 2 =
+// W4A4 (the activations packed MXFP4 too, and gmm1's output aq [M, I/2]); 1
+// and 2 require tiled_scales.
 cudaError_t launch_gemm_swiglu_quant(const uint8_t* xq, const uint8_t* xs, const uint8_t* w13q,
                                      const uint8_t* w13s, const int64_t* offsets, int64_t M,
                                      int E, int H, int I, uint8_t* aq, uint8_t* as,
                                      cudaStream_t stream, bool tiled_scales = false,
-                                     bool fp4_weights = false);
+                                     int fmt = 0);
 cudaError_t launch_gemm_bf16(const uint8_t* aq, const uint8_t* as, const uint8_t* w2q,
                              const uint8_t* w2s, const int64_t* offsets, int64_t M, int E,
                              int I, int H, uint16_t* y, cudaStream_t stream,
-                             bool tiled_scales = false, bool fp4_weights = false);
+                             bool tiled_scales = false, int fmt = 0);
 
 // [rows, ceil(K/32)] scales -> tiled layout with KT = ceil(K/128); rows and
 // slots past the data (a ragged row block or K slice) are written as 127.

@@ -42,7 +42,9 @@ __global__ void __launch_bounds__(256) mx_quantize_kernel(const uint16_t* __rest
 // slices; the slots of the last slice past nbr get 127 (scale 1 over an
 // all-zero payload, so they add exactly 0 in the GEMM).  `offsets` (optional)
 // receives the one-group offsets {0, rows} the grouped GEMM reads.
-template <bool kV8, bool kTiled>
+// kFp4: MXFP4 rows (W4A4 activations; K % 32 == 0): q is [rows, K/2] packed
+// e2m1, 16 bytes per block.
+template <bool kV8, bool kTiled, bool kFp4 = false>
 __global__ void __launch_bounds__(256) mx_quantize_rows_kernel(const uint16_t* __restrict__ x,
                                                                int64_t rows, int64_t K,
                                                                uint8_t* __restrict__ q,
@@ -62,7 +64,12 @@ __global__ void __launch_bounds__(256) mx_quantize_rows_kernel(const uint16_t* _
     const uint16_t* xb = x + r * K + 32 * j;
     uint8_t* qb = q + r * K + 32 * j;
     uint32_t sb;
-    if (j != nbr - 1 || (K & 31) == 0) {
+    if (kFp4) {
+      uint32_t w[16], o[4];
+      load_block32_bf16<kV8>(xb, w);
+      sb = quant_block32_bf16_fp4(w, o);
+      st_cs_v4(q + (r * K + 32 * j) / 2, make_uint4(o[0], o[1], o[2], o[3]));
+    } else if (j != nbr - 1 || (K & 31) == 0) {
       uint32_t w[16], o[8];
       load_block32_bf16<kV8>(xb, w);
       sb = quant_block32_bf16(w, o);
@@ -97,7 +104,7 @@ __global__ void __launch_bounds__(256) mx_quantize_rows_kernel(const uint16_t* _
   }
 }
 
-template <bool kTiled>
+template <bool kTiled, bool kFp4 = false>
 static cudaError_t launch_rows(const uint16_t* x, int64_t rows, int64_t K, uint8_t* q,
                                uint8_t* scale, cudaStream_t stream, int64_t* offsets = nullptr) {
   const int64_t n = rows * ((K + 31) / 32);
@@ -106,16 +113,21 @@ static cudaError_t launch_rows(const uint16_t* x, int64_t rows, int64_t K, uint8
   const int64_t cap = (int64_t)num_sms() * 8;
   if (blocks > cap) blocks = cap;
   if (((uintptr_t)x & 31u) == 0)
-    mx_quantize_rows_kernel<true, kTiled>
+    mx_quantize_rows_kernel<true, kTiled, kFp4>
         <<<(unsigned)blocks, 256, 0, stream>>>(x, rows, K, q, scale, offsets);
   else
-    mx_quantize_rows_kernel<false, kTiled>
+    mx_quantize_rows_kernel<false, kTiled, kFp4>
         <<<(unsigned)blocks, 256, 0, stream>>>(x, rows, K, q, scale, offsets);
   return cudaGetLastError();
 }
 
 cudaError_t launch_mx_quantize_tiled(const uint16_t* x, int64_t rows, int64_t K, uint8_t* q,
-                                     uint8_t* scale_tiled, int64_t* offsets, cudaStream_t stream) {
+                                     uint8_t* scale_tiled, int64_t* offsets, cudaStream_t stream,
+                                     bool fp4) {
+  if (fp4) {
+    if (K % 32 != 0) return cudaErrorInvalidValue;
+    return launch_rows<true, true>(x, rows, K, q, scale_tiled, stream, offsets);
+  }
   return launch_rows<true>(x, rows, K, q, scale_tiled, stream, offsets);
 }
 

@@ -247,9 +247,11 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int32_t* __restrict__ 
   }
 }
 
-// kTiled: xs goes to the MMA-ready tiled scale layout (tiled_scales.h)
-// instead of [M, H/32]; requires H % 128 == 0 and the experts' tile bases.
-template <bool kQuant, bool kTiled, bool kV8>
+// kQ: 0 = bf16 rows to xp; 1 = MXFP8 (xq [M, H] e4m3); 2 = MXFP4 (xq [M, H/2]
+// packed e2m1, the W4A4 path).  kTiled: xs goes to the MMA-ready tiled scale
+// layout (tiled_scales.h) instead of [M, H/32]; requires H % 128 == 0 and the
+// experts' tile bases.
+template <int kQ, bool kTiled, bool kV8>
 __global__ void __launch_bounds__(kRouteThreads) route_permute_kernel(
     const uint16_t* __restrict__ x, int T, int H, int E, int k,
     const int32_t* __restrict__ topk_ids, const int32_t* __restrict__ block_base,
@@ -284,7 +286,18 @@ __global__ void __launch_bounds__(kRouteThreads) route_permute_kernel(
     if (blk >= H32) break;
     uint32_t w[16];
     load_block32_bf16<kV8>(xr + blk * 32, w);
-    if (kQuant) {
+    if (kQ == 2) {
+      uint32_t o[4];
+      const uint32_t sb = quant_block32_bf16_fp4(w, o);
+      for (int j = 0; j < k; ++j) {
+        const int64_t d = s_dest[warp][j];
+        st_cs_v4(xq + d * (H / 2) + blk * 16, make_uint4(o[0], o[1], o[2], o[3]));
+        if (kTiled)
+          xs[tiled_scale_offset(s_sfrow[warp][j], blk, H / 128)] = (uint8_t)sb;
+        else
+          xs[d * H32 + blk] = (uint8_t)sb;
+      }
+    } else if (kQ == 1) {
       uint32_t o[8];
       const uint32_t sb = quant_block32_bf16(w, o);
       for (int j = 0; j < k; ++j) {
@@ -326,10 +339,11 @@ static void launch_topk(int nb, size_t smem, cudaStream_t stream, const float* l
 }
 
 cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, int E, int k,
-                         bool renormalize, bool quant, uint8_t* xq, uint8_t* xs, uint16_t* xp,
+                         bool renormalize, int quant, uint8_t* xq, uint8_t* xs, uint16_t* xp,
                          int32_t* topk_ids, float* topk_w, int32_t* sorted_to_src,
                          int32_t* src_to_sorted, int64_t* counts, int64_t* offsets,
                          int32_t* block_hist, cudaStream_t stream, int32_t* tile_base) {
+  if (quant == 2 && !tile_base) return cudaErrorNotSupported;  // MXFP4 rows: tiled scales only
   if (T == 0) {
     cudaError_t err = cudaMemsetAsync(counts, 0, sizeof(int64_t) * E, stream);
     if (err != cudaSuccess) return err;
@@ -361,12 +375,14 @@ cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, i
   route_permute_kernel<Q, TL, V><<<nb3, kRouteThreads, 0, stream>>>(                           \
       x, T, H, E, k, topk_ids, block_hist, offsets, TL ? tile_base : nullptr, src_to_sorted,    \
       sorted_to_src, Q ? xq : nullptr, Q ? xs : nullptr, Q ? nullptr : xp)
-  if (quant && tile_base) {
-    if (v8) MXMOE_PERMUTE(true, true, true); else MXMOE_PERMUTE(true, true, false);
+  if (quant == 2) {
+    if (v8) MXMOE_PERMUTE(2, true, true); else MXMOE_PERMUTE(2, true, false);
+  } else if (quant && tile_base) {
+    if (v8) MXMOE_PERMUTE(1, true, true); else MXMOE_PERMUTE(1, true, false);
   } else if (quant) {
-    if (v8) MXMOE_PERMUTE(true, false, true); else MXMOE_PERMUTE(true, false, false);
+    if (v8) MXMOE_PERMUTE(1, false, true); else MXMOE_PERMUTE(1, false, false);
   } else {
-    if (v8) MXMOE_PERMUTE(false, false, true); else MXMOE_PERMUTE(false, false, false);
+    if (v8) MXMOE_PERMUTE(0, false, true); else MXMOE_PERMUTE(0, false, false);
   }
 #undef MXMOE_PERMUTE
   return cudaGetLastError();
