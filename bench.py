@@ -43,7 +43,7 @@ FP8_OVER_BF16 = 2.0   # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 # the bench workload (profiles/gemm1_swiglu_quant_qwen3_30b_prefill.md, the
 # DRAM-bytes capture at its end), keyed
 # by the hash of the sources it was captured from
-NCU_TRAFFIC = {"a9ec3d6a1d8bbad4": 786553600}
+NCU_TRAFFIC = {"a9ec3d6a1d8bbad4": 786553600, "64d58b0d55536f8c": 786384128}
 
 
 def parse():
@@ -212,7 +212,7 @@ LINEAR_BENCH = ("qwen3vl_vision_fc2", "qwen3vl_vision_fc1", "qwen3_8b_down_prefi
                 "qwen3_8b_gate_up_prefill", "qwen3_8b_down_decode")
 
 
-def dense_linear_bench(torch, mm, workloads, dev, flush, stream, fp8_peak, hbm):
+def dense_linear_bench(torch, mm, workloads, dev, flush, stream, fp8_peak, hbm, fp4=False):
     """The dense MXFP8 linear on the pages' dense shapes: per call (L2
     flushed), the activation quant and the GEMM from the library's event
     profiler, GEMM TFLOP/s against the MXFP8 peak (weight GB/s against HBM
@@ -222,8 +222,10 @@ def dense_linear_bench(torch, mm, workloads, dev, flush, stream, fp8_peak, hbm):
     for name in LINEAR_BENCH:
         shape = workloads.LINEAR_CONFIGS[name]
         M, N, K = shape.M, shape.N, shape.K
+        if fp4 and K % 128:
+            continue
         x, w = workloads.make_linear(shape, dev)
-        lin = mm.MXFP8Linear.from_bf16(w)
+        lin = (mm.MXFP4Linear if fp4 else mm.MXFP8Linear).from_bf16(w)
         del w
         y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
         for _ in range(3):
@@ -247,7 +249,7 @@ def dense_linear_bench(torch, mm, workloads, dev, flush, stream, fp8_peak, hbm):
         mm.api.layer_profile_enable(False)
         t_ms, q_ms, g_ms = (statistics.mean(v) for v in (tot, q, g))
         flops = 2.0 * M * N * K
-        wbytes = N * K * (1 + 1 / 32)
+        wbytes = N * K * ((0.5 if fp4 else 1) + 1 / 32)
         ent = {"M": M, "N": N, "K": K, "scales_per_row": -(-K // 32),
                "ms": round(t_ms, 4), "act_quant_ms": round(q_ms, 4), "gemm_ms": round(g_ms, 4),
                "gemm_TFLOP/s": round(flops / (g_ms / 1e3) / 1e12, 1),
@@ -257,7 +259,7 @@ def dense_linear_bench(torch, mm, workloads, dev, flush, stream, fp8_peak, hbm):
             ent["gemm_weight_GB/s"] = round(wbytes / (g_ms / 1e3) / 1e9, 1)
             ent["gemm_frac_hbm"] = round(wbytes / (g_ms / 1e3) / 1e9 / hbm, 3)
         ent["vendor_mxfp8_gemm_ms"] = None
-        if K % 32 == 0:
+        if K % 32 == 0 and not fp4:
             try:
                 a8 = torch.randn(M, K, device=dev).to(torch.float8_e4m3fn)
                 b8 = torch.randn(N, K, device=dev).to(torch.float8_e4m3fn)
@@ -431,7 +433,7 @@ def main():
     if shape.offline:
         layer = mm.MXFP8MoELayer.from_quantized(inp["w13q"], inp["w13s"], inp["w2q"], inp["w2s"], k)
         wq_ms = None
-        layer4 = None
+        layer4 = layer44 = None
     else:
         flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
         mm.mx_quantize_3d(inp["w13"])  # warm
@@ -445,6 +447,9 @@ def main():
         wq4_ms = min(time_fn(torch, lambda: (mm.mx_quantize_fp4_3d(inp["w13"]),
                                              mm.mx_quantize_fp4_3d(inp["w2"])), 3, flush, stream))
         layer4 = mm.W4A8MoELayer.from_bf16(inp["w13"], inp["w2"], k)
+        # W4A4: the same MXFP4 weights, MXFP4 expert inputs
+        layer44 = mm.W4A4MoELayer.from_quantized(layer4.w13p, layer4.w13s, layer4.w2p, layer4.w2s,
+                                                 k)
         del inp["w13"], inp["w2"]
     x, logits = inp["x"], inp["logits"]
     out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
@@ -602,6 +607,21 @@ def main():
                                        "GB/s": round(E * 3 * I * H * (2 + 0.5 + 1 / 32) / (wq4_ms / 1e3) / 1e9, 1)},
             "parity": "tests/test_gpu_w4a8.py (quantizer bit-exact; layer vs oracle; byte-identical to the MXFP8 layer on re-encoded weights)",
         }
+    w4a4 = None
+    if layer44 is not None:
+        p_ms, p_g1 = layer_ms(layer44, x, logits, 20)
+        d44_ms, _ = layer_ms(layer44, x[:32], logits[:32], 50)
+        w4a4 = {
+            "weights": "MXFP4 (packed e2m1 + e8m0 block-32 scales); both grouped GEMMs' inputs "
+                       "MXFP4-quantized on the device; e2m1 x e2m1 MMAs of kind::mxf8f6f4",
+            "prefill": {"tokens_per_s": round(T / (p_ms / 1e3), 1), "ms_per_step": round(p_ms, 4),
+                        "gemm1_TFLOP/s": round(2.0 * T * k * 2 * I * H / (p_g1 / 1e3) / 1e12, 1)},
+            "decode_T32": {"ms": round(d44_ms, 4)},
+            "dense_linear": (dense_linear_bench(torch, mm, workloads, dev, flush, stream, fp8_peak,
+                                                hbm, fp4=True) if not args.no_linear else None),
+            "parity": "tests/test_gpu_w4a4.py (exact W4A4 GEMM pins; layer vs oracle; sampled "
+                      "prefill tokens vs oracle)",
+        }
 
     # the dense MXFP8 linear (partial K blocks, ragged N) on the pages' dense shapes
     dense = None
@@ -643,6 +663,7 @@ def main():
             "cpu_baseline": cpu_base,
             "w4a8": w4a8,
             "dense_linear": dense,
+            "w4a4": w4a4,
             "peaks": {"hbm_gbs": hbm, "fp8_tflops": fp8_peak, "source": peaks["source"],
                       "library_dense_gemm": lib_rates},
             "gemm_src": src_hash,
