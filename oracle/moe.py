@@ -54,6 +54,27 @@ from . import mx
 
 
 # ----------------------------------------------------------------------------
+# 0. router gate (upstream of the routing)
+# ----------------------------------------------------------------------------
+
+def router_logits(x_bf16_bits, gate_bf16_bits) -> np.ndarray:
+    """The router gate, a plain linear layer without bias: logits[t, e] =
+    sum_h x[t, h] * gate[e, h], exact (fp64) on the bf16 values.
+    ("Quantization on Ascend", MoE MXFP8 notes: the gate is a
+    ReplicatedLinear, bf16 on the online path.)"""
+    return mx.bf16_bits_to_f64(x_bf16_bits) @ mx.bf16_bits_to_f64(gate_bf16_bits).T
+
+
+def dequantize_gate(q, s) -> np.ndarray:
+    """An offline MXFP8 router gate dequantized to bf16 bits: each element's
+    decoded e4m3 value times its block's 2^(scale - 127), rounded once to
+    bf16 (exact when the value is in bf16's range).  The pages: the offline
+    gate must be dequantized with its block scale (PR #32266 router-gate
+    note)."""
+    return mx.f64_to_bf16_bits(mx.mx_dequantize(q, s))
+
+
+# ----------------------------------------------------------------------------
 # 1. routing
 # ----------------------------------------------------------------------------
 

@@ -306,3 +306,29 @@ def test_w4a4_layer_reduces_to_the_mxfp8_steps_on_reencoded_values():
     assert np.array_equal(r4["aq"], aq) and np.array_equal(r4["as_"], as_)
     y8 = moe.gmm2(e8(r4["aq"]), r4["as_"], e8(q2), s2, offs)
     assert np.array_equal(r4["y"], y8)
+
+
+def test_router_logits_integer_brute_force():
+    """Integer-valued bf16 inputs: the gate GEMM is an integer dot product."""
+    rng = np.random.default_rng(21)
+    T, H, E = 3, 40, 5
+    xi = rng.integers(-9, 10, (T, H))
+    gi = rng.integers(-5, 6, (E, H))
+    got = moe.router_logits(mx.f64_to_bf16_bits(xi.astype(np.float64)),
+                            mx.f64_to_bf16_bits(gi.astype(np.float64)))
+    for t in range(T):
+        for e in range(E):
+            assert got[t, e] == sum(int(xi[t, h]) * int(gi[e, h]) for h in range(H))
+
+
+def test_dequantize_gate_matches_torch_casts():
+    """e4m3 decode (torch float8_e4m3fn) times 2^(s-127), cast to bf16 by torch."""
+    rng = np.random.default_rng(22)
+    E, H = 6, 96
+    codes = rng.integers(0, 256, (E, H)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x3C          # NaN codes are outside the contract
+    s = rng.integers(100, 140, (E, H // 32)).astype(np.uint8)
+    dec = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64)
+    val = dec * torch.from_numpy(np.exp2(np.repeat(s.astype(np.float64) - 127, 32, axis=1)))
+    ref = val.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(moe.dequantize_gate(codes, s), ref)
