@@ -27,6 +27,10 @@
  *                                   grouped GEMM), any K % 16 == 0
  *   mxfp4_linear, mxfp4_linear_mma_scales
  *                                   the W4A4 dense linear
+ *   moe_router_gate_topk            the router gate GEMM fused with softmax top-k
+ *   moe_forward_mxfp8_gated_mma_scales
+ *                                   the layer from hidden states + router gate
+ *   mx_dequantize_bf16_2d           load-time dequant of an MXFP8 router gate
  *
  * Formats.  An MX block is 32 consecutive elements along the contraction
  * axis K.  Payload: one float8_e4m3fn byte per element.  Scale: one UE8M0
@@ -268,6 +272,48 @@ mxmoe_status moe_forward_mxfp8(const uint16_t* x, const float* logits, const uin
  */
 mxmoe_status mx_scales_to_mma_layout(const uint8_t* scale, int64_t E, int64_t N, int64_t K,
                                      uint8_t* out, void* stream);
+
+/*
+ * Router gate GEMM fused with softmax top-k (the step upstream of the
+ * routing; "Quantization on Ascend", MoE MXFP8 notes: the router gate is a
+ * ReplicatedLinear kept in bf16 on the online path and dequantized on the
+ * offline path, see mx_dequantize_bf16_2d):
+ *   logits[t, e] = sum_h x[t, h] * gate[e, h]      tensor cores, fp32 accumulate
+ *   topk_ids[t, :], topk_w[t, :] = top-k softmax of logits[t, :], the rule of
+ *   moe_route_quant_mxfp8 (ties to the lower id, descending; renormalize
+ *   divides by the k weights' sum); on the same fp32 logits both give the same
+ *   bytes.
+ *   x bf16 [T, H], gate bf16 [E, H] (16-byte aligned); logits_out fp32 [T, E]
+ *   (NULL: not written); topk_ids int32 [T, k], topk_w fp32 [T, k].
+ * Requires H % 64 == 0, 1 <= E <= 256, 1 <= k <= min(16, E).
+ */
+mxmoe_status moe_router_gate_topk(const uint16_t* x, const uint16_t* gate, int T, int H, int E,
+                                  int k, int renormalize, float* logits_out, int32_t* topk_ids,
+                                  float* topk_w, void* stream);
+
+/*
+ * The MXFP8 layer from the hidden states and the bf16 router gate: the gate
+ * GEMM and softmax top-k run fused (moe_router_gate_topk's kernel, which also
+ * leaves the routing step's ranks and histograms), then the layer as
+ * moe_forward_mxfp8_mma_scales.  Arguments as that call with `gate` bf16
+ * [E, H] in place of the logits, plus moe_router_gate_topk's limits on E, k.
+ */
+mxmoe_status moe_forward_mxfp8_gated_mma_scales(const uint16_t* x, const uint16_t* gate,
+                                                const uint8_t* w13q, const uint8_t* w13s_mma,
+                                                const uint8_t* w2q, const uint8_t* w2s_mma, int T,
+                                                int H, int E, int k, int I, int renormalize,
+                                                uint16_t* out, void* ws, size_t ws_bytes,
+                                                void* stream);
+
+/*
+ * Load-time dequant of an MXFP8 tensor to bf16 (the offline router gate: a
+ * quantized gate used without its block scale scrambles the routing, PR
+ * #32266 router-gate note): out[r, j] = bf16(dec(q[r, j]) * 2^(s[r, j/32] -
+ * 127)), exact for every value in bf16's range.
+ *   q e4m3 [rows, K], scale e8m0 [rows, K/32], out bf16 [rows, K]; K % 32 == 0.
+ */
+mxmoe_status mx_dequantize_bf16_2d(const uint8_t* q, const uint8_t* scale, int64_t rows,
+                                   int64_t K, uint16_t* out, void* stream);
 
 /*
  * Dense MXFP8 linear ("Quantization on Ascend", MXFP8 implementation notes,

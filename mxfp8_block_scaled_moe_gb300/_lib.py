@@ -24,6 +24,7 @@ EXPORTS = (
     "moe_forward_mxfp8_host_plan", "mx_quantize_fp4_3d", "moe_forward_w4a8_mma_scales",
     "mxfp8_linear_workspace_size", "mxfp8_linear", "mxfp8_linear_mma_scales",
     "moe_forward_w4a4_mma_scales", "mxfp4_linear", "mxfp4_linear_mma_scales",
+    "moe_router_gate_topk", "mx_dequantize_bf16_2d", "moe_forward_mxfp8_gated_mma_scales",
 )
 
 _P = C.c_void_p
@@ -70,6 +71,10 @@ _PROTOS = {
                                          _SZ, _P]),
     "mxfp4_linear": (_I, [_P, _P, _P, _I64, _I64, _I64, _P, _P, _SZ, _P]),
     "mxfp4_linear_mma_scales": (_I, [_P, _P, _P, _I64, _I64, _I64, _P, _P, _SZ, _P]),
+    "moe_router_gate_topk": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
+    "mx_dequantize_bf16_2d": (_I, [_P, _P, _I64, _I64, _P, _P]),
+    "moe_forward_mxfp8_gated_mma_scales": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                                _P, _P, _SZ, _P]),
 }
 
 _lib = None

@@ -371,6 +371,67 @@ def set_wait_limit_cycles(cycles: int) -> None:
     _lib.load().mxmoe_set_wait_limit_cycles(int(cycles))
 
 
+def moe_router_gate_topk(x, gate, k: int, renormalize: bool = True, logits=False) -> dict:
+    """The router gate GEMM fused with softmax top-k: bf16 x [T, H] and bf16
+    gate [E, H] -> topk_ids int32 [T, k], topk_w fp32 [T, k] (and the fp32
+    logits [T, E] when ``logits``)."""
+    _need(x, "x", torch.bfloat16, 2)
+    _need(gate, "gate", torch.bfloat16, 2)
+    T, H = x.shape
+    E = gate.shape[0]
+    if gate.shape[1] != H:
+        raise ValueError(f"gate is {tuple(gate.shape)}, x has H = {H}")
+    dev = x.device
+    ids = torch.empty(T, k, dtype=torch.int32, device=dev)
+    w = torch.empty(T, k, dtype=torch.float32, device=dev)
+    lg = torch.empty(T, E, dtype=torch.float32, device=dev) if logits else None
+    _lib.check("moe_router_gate_topk", _lib.load().moe_router_gate_topk(
+        _ptr(x), _ptr(gate), T, H, E, k, int(bool(renormalize)), _ptr(lg), _ptr(ids), _ptr(w),
+        _stream()))
+    out = dict(topk_ids=ids, topk_w=w)
+    if logits:
+        out["logits"] = lg
+    return out
+
+
+def mx_dequantize_bf16_2d(q, scale):
+    """e4m3 [N, K] (uint8 codes) + e8m0 [N, K/32] -> bf16 [N, K] (the offline
+    MXFP8 router gate, dequantized once at load)."""
+    q = _u8(q)
+    _need(q, "q", torch.uint8, 2)
+    _need(scale, "scale", torch.uint8, 2)
+    N, K = q.shape
+    out = torch.empty(N, K, dtype=torch.bfloat16, device=q.device)
+    _lib.check("mx_dequantize_bf16_2d", _lib.load().mx_dequantize_bf16_2d(
+        _ptr(q), _ptr(scale), N, K, _ptr(out), _stream()))
+    return out
+
+
+def moe_forward_mxfp8_gated_mma_scales(x, gate, w13q, w13s_mma, w2q, w2s_mma, k: int,
+                                       renormalize: bool = True, out=None, workspace=None):
+    """The MXFP8 layer from the hidden states and the bf16 router gate [E, H]:
+    the gate GEMM and softmax top-k run fused in the routing step."""
+    w13q, w2q = _u8(w13q), _u8(w2q)
+    _need(x, "x", torch.bfloat16, 2)
+    _need(gate, "gate", torch.bfloat16, 2)
+    for t, n in ((w13q, "w13q"), (w13s_mma, "w13s_mma"), (w2q, "w2q"), (w2s_mma, "w2s_mma")):
+        _need(t, n, torch.uint8, 3)
+    T, H = x.shape
+    E, N2, _ = w13q.shape
+    I = N2 // 2
+    ws_bytes = moe_forward_mxfp8_workspace_size(T, H, E, k, I)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=x.device)
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=x.device)
+    _lib.check("moe_forward_mxfp8_gated_mma_scales",
+               _lib.load().moe_forward_mxfp8_gated_mma_scales(
+                   _ptr(x), _ptr(gate), _ptr(w13q), _ptr(w13s_mma), _ptr(w2q), _ptr(w2s_mma), T,
+                   H, E, k, I, int(bool(renormalize)), _ptr(out), _ptr(workspace),
+                   workspace.numel(), _stream()))
+    return out
+
+
 def mxfp8_linear_workspace_size(M: int, N: int, K: int) -> int:
     return int(_lib.load().mxfp8_linear_workspace_size(M, N, K))
 
@@ -546,6 +607,14 @@ class MXFP8MoELayer:
         return moe_forward_mxfp8_mma_scales(x, logits, self.w13q, self.w13s_mma, self.w2q,
                                             self.w2s_mma, self.k, self.renormalize, out=out,
                                             workspace=self.workspace(x.shape[0], x.device))
+
+    def forward_gated(self, x, gate, out=None):
+        """The layer from the hidden states and the bf16 router gate [E, H] (the
+        gate GEMM and top-k fused into the routing step)."""
+        return moe_forward_mxfp8_gated_mma_scales(x, gate, self.w13q, self.w13s_mma, self.w2q,
+                                                  self.w2s_mma, self.k, self.renormalize,
+                                                  out=out,
+                                                  workspace=self.workspace(x.shape[0], x.device))
 
 
 class W4A4MoELayer:

@@ -20,7 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libmxmoe.so")
 
-SOURCES = ["api.cu", "quant.cu", "route.cu", "finalize.cu", "gemm.cu", "gemm2sm.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "quant.cu", "route.cu", "finalize.cu", "gemm.cu", "gemm2sm.cu", "noalloc.cu",
+           "router.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
               "-I" + INCLUDE, "-I" + CSRC]

@@ -344,14 +344,15 @@ static mxmoe_status forward_impl(const uint16_t* x, const float* logits, const u
                                  const uint8_t* w13s, const uint8_t* w2q, const uint8_t* w2s,
                                  bool mma_scales, int T, int H, int E, int k, int I,
                                  int renormalize, uint16_t* out, void* ws, size_t ws_bytes,
-                                 void* stream, int fmt = 0) {
+                                 void* stream, int fmt = 0, const uint16_t* gate = nullptr) {
   const bool fp4_weights = fmt != 0;
   if (T < 0 || H <= 0 || E <= 0 || k < 1 || k > 32 || k > E || I <= 0) return MXMOE_ERR_SHAPE;
   if (E > 256 || H % 128 != 0 || I % 128 != 0) return MXMOE_ERR_UNSUPPORTED;
+  if (gate && k > 16) return MXMOE_ERR_UNSUPPORTED;
   if ((int64_t)T * k >= (1ll << 31)) return MXMOE_ERR_SHAPE;
   if (T == 0) return MXMOE_OK;
   MXMOE_CHECK_PTR(x);
-  MXMOE_CHECK_PTR(logits);
+  if (gate) MXMOE_CHECK_PTR(gate); else MXMOE_CHECK_PTR(logits);
   MXMOE_CHECK_PTR(w13q);
   MXMOE_CHECK_PTR(w2q);
   MXMOE_CHECK_PTR(out);
@@ -393,8 +394,14 @@ static mxmoe_status forward_impl(const uint16_t* x, const float* logits, const u
     w2s_t = b + L.w2s;
   }
   prof.mark(1);
+  if (gate) {
+    // the fused router leaves ids, weights, in-block ranks and histograms
+    e = launch_router_gate_topk(x, gate, T, H, E, k, renormalize != 0, nullptr, ids, w, src2s,
+                                (int32_t*)(b + L.hist), s);
+    if (e != cudaSuccess) return MXMOE_ERR_CUDA;
+  }
   e = launch_route(x, logits, T, H, E, k, renormalize != 0, fmt == 2 ? 2 : 1, xq, xs, nullptr, ids,
-                   w, s2s, src2s, counts, offs, (int32_t*)(b + L.hist), s, tbase);
+                   w, s2s, src2s, counts, offs, (int32_t*)(b + L.hist), s, tbase, gate != nullptr);
   if (e != cudaSuccess) return MXMOE_ERR_CUDA;
   prof.mark(2);
   e = launch_gemm_swiglu_quant(xq, xs, w13q, w13s_t, offs, M, E, H, I, aq, as, s, true, fmt);
@@ -444,6 +451,42 @@ mxmoe_status moe_forward_w4a4_mma_scales(const uint16_t* x, const float* logits,
                                          void* ws, size_t ws_bytes, void* stream) {
   return forward_impl(x, logits, w13p, w13s_mma, w2p, w2s_mma, true, T, H, E, k, I, renormalize,
                       out, ws, ws_bytes, stream, 2);
+}
+
+mxmoe_status moe_forward_mxfp8_gated_mma_scales(const uint16_t* x, const uint16_t* gate,
+                                                const uint8_t* w13q, const uint8_t* w13s_mma,
+                                                const uint8_t* w2q, const uint8_t* w2s_mma, int T,
+                                                int H, int E, int k, int I, int renormalize,
+                                                uint16_t* out, void* ws, size_t ws_bytes,
+                                                void* stream) {
+  return forward_impl(x, nullptr, w13q, w13s_mma, w2q, w2s_mma, true, T, H, E, k, I, renormalize,
+                      out, ws, ws_bytes, stream, 0, gate);
+}
+
+mxmoe_status moe_router_gate_topk(const uint16_t* x, const uint16_t* gate, int T, int H, int E,
+                                  int k, int renormalize, float* logits_out, int32_t* topk_ids,
+                                  float* topk_w, void* stream) {
+  if (T < 0 || H <= 0 || E <= 0 || k < 1 || k > E) return MXMOE_ERR_SHAPE;
+  if (H % 64 != 0 || E > 256 || k > 16) return MXMOE_ERR_UNSUPPORTED;
+  if (T == 0) return MXMOE_OK;
+  MXMOE_CHECK_PTR(x);
+  MXMOE_CHECK_PTR(gate);
+  MXMOE_CHECK_PTR(topk_ids);
+  MXMOE_CHECK_PTR(topk_w);
+  if (logits_out && !aligned16(logits_out)) return MXMOE_ERR_ALIGN;
+  return from_cuda(launch_router_gate_topk(x, gate, T, H, E, k, renormalize != 0, logits_out,
+                                           topk_ids, topk_w, nullptr, nullptr,
+                                           (cudaStream_t)stream));
+}
+
+mxmoe_status mx_dequantize_bf16_2d(const uint8_t* q, const uint8_t* scale, int64_t rows,
+                                   int64_t K, uint16_t* out, void* stream) {
+  if (rows < 0 || K <= 0 || K % 32 != 0) return MXMOE_ERR_SHAPE;
+  if (rows == 0) return MXMOE_OK;
+  MXMOE_CHECK_PTR(q);
+  MXMOE_CHECK_PTR(out);
+  if (!scale) return MXMOE_ERR_NULL;
+  return from_cuda(launch_mx_dequantize_bf16(q, scale, rows, K, out, (cudaStream_t)stream));
 }
 
 mxmoe_status mx_quantize_fp4_3d(const uint16_t* w, int64_t E, int64_t N, int64_t K, uint8_t* q,

@@ -192,6 +192,15 @@ __device__ __forceinline__ uint32_t quant_block32_bf16_fp4(const uint32_t (&w)[1
   return sb;
 }
 
+// Total order of finite fp32 values as unsigned keys (top-k selection) (-0 is ordered with +0).
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t b = __float_as_uint(v == 0.f ? 0.f : v);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
 __device__ __forceinline__ bool aligned32(const void* p) {
   return (reinterpret_cast<uintptr_t>(p) & 31u) == 0;
 }

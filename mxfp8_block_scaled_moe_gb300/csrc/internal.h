@@ -36,7 +36,22 @@ cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, i
                          int32_t* topk_ids, float* topk_w, int32_t* sorted_to_src,
                          int32_t* src_to_sorted, int64_t* counts, int64_t* offsets,
                          int32_t* block_hist, cudaStream_t stream,
-                         int32_t* tile_base = nullptr);
+                         int32_t* tile_base = nullptr, bool topk_done = false);
+
+// Router gate GEMM (bf16 x [T, H] . bf16 gate [E, H]^T, fp32 accumulate on the
+// tensor cores) fused with softmax top-k.  logits (nullable) receives the fp32
+// logits.  local_rank / block_hist (both nullable) receive the routing step's
+// in-block ranks and per-block expert histograms (the state launch_route's
+// first kernel leaves), so launch_route can continue with topk_done.
+// Requires H % 64 == 0, 1 <= E <= 256, 1 <= k <= min(16, E).
+cudaError_t launch_router_gate_topk(const uint16_t* x, const uint16_t* gate, int T, int H, int E,
+                                    int k, bool renormalize, float* logits, int32_t* topk_ids,
+                                    float* topk_w, int32_t* local_rank, int32_t* block_hist,
+                                    cudaStream_t stream);
+// e4m3 [rows, K] + e8m0 [rows, K/32] -> bf16 [rows, K] (value dec(q) * 2^(s - 127)
+// rounded to bf16, exact for every value in bf16's range); K % 32 == 0.
+cudaError_t launch_mx_dequantize_bf16(const uint8_t* q, const uint8_t* s, int64_t rows, int64_t K,
+                                      uint16_t* out, cudaStream_t stream);
 
 size_t route_workspace_bytes(int T, int E);
 

@@ -34,14 +34,6 @@ namespace mxmoe {
 constexpr int kRouteThreads = 256;
 constexpr int kRouteWarps = kRouteThreads / 32;
 
-// Total order of finite fp32 values as unsigned keys (-0 is ordered with +0).
-__device__ __forceinline__ uint32_t order_key(float v) {
-  const uint32_t b = __float_as_uint(v == 0.f ? 0.f : v);
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-__device__ __forceinline__ float key_value(uint32_t key) {
-  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
-}
 
 constexpr int kTopkThreads = 1024;
 constexpr int kTopkWarps = kTopkThreads / 32;
@@ -342,7 +334,8 @@ cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, i
                          bool renormalize, int quant, uint8_t* xq, uint8_t* xs, uint16_t* xp,
                          int32_t* topk_ids, float* topk_w, int32_t* sorted_to_src,
                          int32_t* src_to_sorted, int64_t* counts, int64_t* offsets,
-                         int32_t* block_hist, cudaStream_t stream, int32_t* tile_base) {
+                         int32_t* block_hist, cudaStream_t stream, int32_t* tile_base,
+                         bool topk_done) {
   if (quant == 2 && !tile_base) return cudaErrorNotSupported;  // MXFP4 rows: tiled scales only
   if (T == 0) {
     cudaError_t err = cudaMemsetAsync(counts, 0, sizeof(int64_t) * E, stream);
@@ -353,8 +346,11 @@ cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, i
   const size_t smem1 = sizeof(unsigned long long) * (size_t)E;
   const int epl = (E + 31) / 32;
   const int rn = renormalize ? 1 : 0;
-  // src_to_sorted holds the in-block rank between kernels 1 and 3
-  if (epl <= 1)       launch_topk<1>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist);
+  // src_to_sorted holds the in-block rank between kernels 1 and 3.  topk_done:
+  // the fused router (router.cu) already wrote ids, weights, ranks and
+  // histograms.
+  if (topk_done) {
+  } else if (epl <= 1)       launch_topk<1>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist);
   else if (epl <= 2)  launch_topk<2>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist);
   else if (epl <= 4)  launch_topk<4>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist);
   else if (epl <= 8)  launch_topk<8>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist);

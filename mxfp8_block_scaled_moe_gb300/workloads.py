@@ -105,9 +105,22 @@ def make_logits(shape: LayerShape, x: torch.Tensor, device="cpu") -> torch.Tenso
         u = u.clamp_(1e-300, 1.0 - 1e-16)
         gumbel = -torch.log(-torch.log(u))
         return (logp[None, :] + gumbel).to(torch.float32)
-    gate = (torch.randn(shape.H, shape.E, generator=g, device=device, dtype=torch.float32)
-            * shape.gate_std).to(torch.bfloat16)
+    gate = _draw_gate(shape, g, device)
     return x.float() @ gate.float()
+
+
+def _draw_gate(shape: LayerShape, g, device):
+    return (torch.randn(shape.H, shape.E, generator=g, device=device, dtype=torch.float32)
+            * shape.gate_std).to(torch.bfloat16)
+
+
+def make_gate(shape: LayerShape, device="cpu") -> torch.Tensor:
+    """The router gate bf16 [E, H] (out_features, in_features) whose product
+    with the hidden states gives ``make_logits`` (the same seeded draw)."""
+    if shape.zipf_s > 0:
+        raise ValueError("the skewed-load shape draws its logits directly (no gate)")
+    g = _gen(device, shape.seed * 1000 + 2)
+    return _draw_gate(shape, g, device).t().contiguous()
 
 
 def make_weights_bf16(shape: LayerShape, device="cpu"):
