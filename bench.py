@@ -623,6 +623,34 @@ def main():
                       "prefill tokens vs oracle)",
         }
 
+    # the router gate GEMM fused with softmax top-k (the step upstream of the
+    # routing), and the layer run from hidden states + gate
+    router = None
+    if rank == 0 and not shape.offline and shape.zipf_s == 0:
+        gate = workloads.make_gate(shape, dev)
+        mm.moe_router_gate_topk(x, gate, k)
+        torch.cuda.synchronize()
+        r_t = time_fn(torch, lambda: mm.moe_router_gate_topk(x, gate, k), 50, flush, stream)
+        r_ms = statistics.mean(r_t)
+        v_t = time_fn(torch, lambda: torch.matmul(x, gate.t()).float(), 50, flush, stream)
+        g_t = time_fn(torch, lambda: layer.forward_gated(x, gate, out=out), 20, flush, stream)
+        r_bytes = T * H * 2 + E * H * 2 + T * k * 8
+        router = {
+            "ms": round(r_ms, 4), "GB/s": round(r_bytes / (r_ms / 1e3) / 1e9, 1),
+            "frac_hbm": round(r_bytes / (r_ms / 1e3) / 1e9 / hbm, 3),
+            "TFLOP/s": round(2.0 * T * E * H / (r_ms / 1e3) / 1e12, 1),
+            "algorithmic_bytes": r_bytes,
+            "vendor_bf16_gate_gemm_ms": round(statistics.mean(v_t), 4),
+            "gated_layer_ms": round(statistics.mean(g_t), 4),
+            "gated_layer_tokens_per_s": round(T / (statistics.mean(g_t) / 1e3), 1),
+            "note": "gate GEMM + top-k + weights + in-block ranks in one kernel; the vendor "
+                    "figure is the logits GEMM alone (torch.matmul, bf16 -> fp32)",
+            "parity": "tests/test_gpu_router.py (exact integer logits with ties; top-k equal to "
+                      "the oracle on the device logits and byte-identical to the logits-input "
+                      "routing; gated layer byte-identical)",
+        }
+        del gate
+
     # the dense MXFP8 linear (partial K blocks, ragged N) on the pages' dense shapes
     dense = None
     if rank == 0 and not args.no_linear:
@@ -662,6 +690,7 @@ def main():
                        "H2D / compute / D2H on three streams)",
             "cpu_baseline": cpu_base,
             "w4a8": w4a8,
+            "router": router,
             "dense_linear": dense,
             "w4a4": w4a4,
             "peaks": {"hbm_gbs": hbm, "fp8_tflops": fp8_peak, "source": peaks["source"],

@@ -285,7 +285,7 @@ mxmoe_status mx_scales_to_mma_layout(const uint8_t* scale, int64_t E, int64_t N,
  *   bytes.
  *   x bf16 [T, H], gate bf16 [E, H] (16-byte aligned); logits_out fp32 [T, E]
  *   (NULL: not written); topk_ids int32 [T, k], topk_w fp32 [T, k].
- * Requires H % 64 == 0, 1 <= E <= 256, 1 <= k <= min(16, E).
+ * Requires H % 64 == 0, 1 <= E <= 256, 1 <= k <= min(32, E).
  */
 mxmoe_status moe_router_gate_topk(const uint16_t* x, const uint16_t* gate, int T, int H, int E,
                                   int k, int renormalize, float* logits_out, int32_t* topk_ids,
@@ -296,7 +296,7 @@ mxmoe_status moe_router_gate_topk(const uint16_t* x, const uint16_t* gate, int T
  * GEMM and softmax top-k run fused (moe_router_gate_topk's kernel, which also
  * leaves the routing step's ranks and histograms), then the layer as
  * moe_forward_mxfp8_mma_scales.  Arguments as that call with `gate` bf16
- * [E, H] in place of the logits, plus moe_router_gate_topk's limits on E, k.
+ * [E, H] in place of the logits.
  */
 mxmoe_status moe_forward_mxfp8_gated_mma_scales(const uint16_t* x, const uint16_t* gate,
                                                 const uint8_t* w13q, const uint8_t* w13s_mma,

@@ -348,7 +348,6 @@ static mxmoe_status forward_impl(const uint16_t* x, const float* logits, const u
   const bool fp4_weights = fmt != 0;
   if (T < 0 || H <= 0 || E <= 0 || k < 1 || k > 32 || k > E || I <= 0) return MXMOE_ERR_SHAPE;
   if (E > 256 || H % 128 != 0 || I % 128 != 0) return MXMOE_ERR_UNSUPPORTED;
-  if (gate && k > 16) return MXMOE_ERR_UNSUPPORTED;
   if ((int64_t)T * k >= (1ll << 31)) return MXMOE_ERR_SHAPE;
   if (T == 0) return MXMOE_OK;
   MXMOE_CHECK_PTR(x);
@@ -467,7 +466,7 @@ mxmoe_status moe_router_gate_topk(const uint16_t* x, const uint16_t* gate, int T
                                   int k, int renormalize, float* logits_out, int32_t* topk_ids,
                                   float* topk_w, void* stream) {
   if (T < 0 || H <= 0 || E <= 0 || k < 1 || k > E) return MXMOE_ERR_SHAPE;
-  if (H % 64 != 0 || E > 256 || k > 16) return MXMOE_ERR_UNSUPPORTED;
+  if (H % 64 != 0 || E > 256 || k > 32) return MXMOE_ERR_UNSUPPORTED;
   if (T == 0) return MXMOE_OK;
   MXMOE_CHECK_PTR(x);
   MXMOE_CHECK_PTR(gate);

@@ -43,7 +43,7 @@ cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, i
 // logits.  local_rank / block_hist (both nullable) receive the routing step's
 // in-block ranks and per-block expert histograms (the state launch_route's
 // first kernel leaves), so launch_route can continue with topk_done.
-// Requires H % 64 == 0, 1 <= E <= 256, 1 <= k <= min(16, E).
+// Requires H % 64 == 0, 1 <= E <= 256, 1 <= k <= min(32, E).
 cudaError_t launch_router_gate_topk(const uint16_t* x, const uint16_t* gate, int T, int H, int E,
                                     int k, bool renormalize, float* logits, int32_t* topk_ids,
                                     float* topk_w, int32_t* local_rank, int32_t* block_hist,

@@ -26,6 +26,7 @@
 // Roofline (kernel 3 dominates): x read once (2 B/elem) + k copies of the
 // payload (1 B) and scales (1/32 B) written; ids/weights/indices are small.
 #include "common.cuh"
+#include "topk.cuh"
 #include "internal.h"
 #include "tiled_scales.h"
 
@@ -55,68 +56,38 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_rank_kernel(
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_mask[e] = 0ull;
   __syncthreads();
 
-  int chosen[2] = {0, 0};
+  // the warp's two tokens go through the top-k together (one at a time for
+  // wide rows, where two would not fit in the registers of 1024 threads)
+  const float* rows[2];
 #pragma unroll
   for (int it = 0; it < 2; ++it) {
     const int tl = warp + kTopkWarps * it;
-    if (tl >= nt) break;  // warp-uniform
-    const int t = t0 + tl;
-    const float* row = logits + (int64_t)t * E;
-    float v[EPL];
-    uint32_t key[EPL];
+    rows[it] = tl < nt ? logits + (int64_t)(t0 + tl) * E : nullptr;
+  }
+  int chosen[2];
+  float vals[2], ws[2];
+  if constexpr (EPL <= 4) {
+    warp_topk_softmax<EPL, 2>(rows, E, k, renormalize != 0, lane, chosen, vals, ws);
+  } else {
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      const int e = lane + 32 * i;
-      v[i] = e < E ? row[e] : 0.f;
-      key[i] = e < E ? order_key(v[i]) : 0u;  // 0: below every finite key
+    for (int it = 0; it < 2; ++it) {
+      const float* r1[1] = {rows[it]};
+      int c1[1];
+      float v1[1], w1[1];
+      warp_topk_softmax<EPL, 1>(r1, E, k, renormalize != 0, lane, c1, v1, w1);
+      chosen[it] = c1[0];
+      ws[it] = w1[0];
     }
-    // k rounds: the warp's largest remaining key (redux max), ties to the
-    // lowest expert id among the lanes holding it (redux min); within a lane
-    // the lowest index wins a tie (strict compare in increasing i).
-    uint32_t taken = 0;
-    int my_id = 0;
-    uint32_t my_key = 0;
-    for (int j = 0; j < k; ++j) {
-      uint32_t hk = 0u, hid = 0xFFFFFFFFu;
+  }
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) {
-        const bool live = lane + 32 * i < E && !((taken >> i) & 1u);
-        if (live && (hid == 0xFFFFFFFFu || key[i] > hk)) {
-          hk = key[i];
-          hid = (uint32_t)(lane + 32 * i);
-        }
-      }
-      const uint32_t m = __reduce_max_sync(0xffffffffu, hk);
-      const uint32_t id = __reduce_min_sync(0xffffffffu, hk == m ? hid : 0xFFFFFFFFu);
-      if (hid == id) taken |= 1u << (id >> 5);
-      if (lane == j) { my_id = (int)id; my_key = m; }
+  for (int it = 0; it < 2; ++it) {
+    const int tl = warp + kTopkWarps * it;
+    if (tl < nt && lane < k) {
+      const int64_t f = (int64_t)(t0 + tl) * k + lane;
+      topk_ids[f] = chosen[it];
+      topk_w[f] = ws[it];
+      atomicOr(&s_mask[chosen[it]], 1ull << tl);
     }
-    const float my_val = key_value(my_key);
-    // softmax weights of the chosen experts
-    const float vmax = __shfl_sync(0xffffffffu, my_val, 0);
-    float denom;
-    if (renormalize) {
-      float ej = lane < k ? expf(my_val - vmax) : 0.f;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) ej += __shfl_xor_sync(0xffffffffu, ej, off);
-      denom = ej;
-    } else {
-      float sum = 0.f;
-#pragma unroll
-      for (int i = 0; i < EPL; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E) sum += expf(v[i] - vmax);
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-      denom = sum;
-    }
-    if (lane < k) {
-      topk_ids[(int64_t)t * k + lane] = my_id;
-      topk_w[(int64_t)t * k + lane] = expf(my_val - vmax) / denom;
-      atomicOr(&s_mask[my_id], 1ull << tl);
-    }
-    chosen[it] = my_id;
   }
   __syncthreads();
 #pragma unroll

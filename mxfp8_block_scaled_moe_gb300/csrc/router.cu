@@ -10,16 +10,18 @@
 // One CTA per 128 tokens: warp 0 streams x and gate tiles (64 bf16 of K per
 // stage, 128-byte swizzle) by TMA, warp 1 issues tcgen05.mma kind::f16 (M=128
 // tokens, N = E rounded up to 16 experts, the gate rows past E zero-filled by
-// the TMA, K=16) into a TMEM accumulator, warps 2-5 (one per TMEM
-// lane quarter, one token per thread) read the token's E logits, keep the k
-// largest in registers, and write ids, weights and, when asked, the logits.
-// The same threads then build the routing step's per-64-token expert masks in
-// shared memory and write the in-block ranks and per-block histograms, so the
-// permutation continues from here (route.cu, scan and permute kernels).
+// the TMA, K=16) into a TMEM accumulator, warps 2-17 (four per TMEM
+// lane quarter) move the accumulator into shared memory, then take the tokens
+// warp by warp with the routing kernel's top-k (topk.cuh) and write ids,
+// weights and, when asked, the logits.  The same warps then build the routing
+// step's per-64-token expert masks in shared memory and write the in-block
+// ranks and per-block histograms, so the permutation continues from here
+// (route.cu, scan and permute kernels).
 //
 // Roofline: HBM-bound on x (2 B per element, read once); the gate (E x H
 // bf16) stays in L2 and is re-read by every CTA.
 #include "gemm_common.cuh"
+#include "topk.cuh"
 
 namespace mxmoe {
 namespace router {
@@ -36,11 +38,15 @@ using gemm::wait_bar;
 constexpr int TOK = 128;            // tokens per CTA (the MMA's M)
 constexpr int KS = 64;              // bf16 elements of K per stage (one 128-byte row)
 constexpr int STAGES = 4;
-constexpr int THREADS = 192;        // producer, MMA, 4 epilogue warps
+constexpr int EPI = 16;             // epilogue warps (four per TMEM lane quarter)
+constexpr int THREADS = 64 + 32 * EPI;  // producer, MMA, epilogue
 constexpr int A_BYTES = TOK * 128;  // 16 KB
 constexpr int MAX_E = 256;
 constexpr int STAGE_MAX = A_BYTES + MAX_E * 128;
 constexpr int OFF_BAR = STAGES * STAGE_MAX;
+// epilogue scratch over the stages: fp32 logits [TOK][E | 1], chosen ids [TOK][32]
+constexpr int OFF_IDS = TOK * (MAX_E + 1) * 4;
+static_assert(OFF_IDS + TOK * 32 * 4 <= OFF_BAR, "epilogue scratch fits in the stages");
 constexpr int OFF_MASK = OFF_BAR + 128;                  // uint64 [2][MAX_E]
 constexpr int OFF_TMEM = OFF_MASK + 2 * MAX_E * 8;
 constexpr int ALLOC = OFF_TMEM + 16 + 1024;              // + alignment slack
@@ -73,7 +79,7 @@ __device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t adesc, uint64_t bd
       : "memory");
 }
 
-template <int MAXK>
+template <int EPL>
 __global__ void __launch_bounds__(THREADS, 1)
     router_gate_topk_kernel(const __grid_constant__ CUtensorMap tmX,
                             const __grid_constant__ CUtensorMap tmG, const Params p) {
@@ -172,124 +178,76 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     __syncwarp();
   } else {
-    // ================= epilogue: one token per thread
-    const int q = warp & 3;
-    const int r = q * 32 + lane;  // TMEM lane = token row of the tile
-    const int t = t0 + r;
-    const bool valid = t < p.T;
+    // ================= epilogue warps: the accumulator goes to shared memory
+    // (over the stages, idle once every MMA is done), then each warp takes
+    // tokens ew, ew + EPI, ... with the routing kernel's warp top-k (one warp
+    // per token is latency-bound: the token count per warp sets the time)
+    const int q = warp & 3;        // TMEM lane quarter
+    const int r = q * 32 + lane;   // token row this thread moves out of TMEM
+    const int ew = warp - 2;       // 0..EPI-1
+    const int cg = ew >> 2;        // column group: 32-column chunks cg, cg + EPI/4, ...
     const bool got = wait_bar(bar_acc, 0, p.wait_limit, p.status, s_abort);
     const bool ok = __all_sync(0xffffffffu, got) && !*s_abort;
     tc_fence_after();
-    const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
-    const int k = p.k;
-    uint32_t keys[MAXK];
-    int ids[MAXK];
-#pragma unroll
-    for (int j = 0; j < MAXK; ++j) { keys[j] = 0u; ids[j] = 0; }
-    uint32_t thr = 0u;  // keys[k - 1], the smallest key kept
+    const int LD = E | 1;  // odd row stride: the row-per-lane writes hit 32 banks
+    float* s_log = reinterpret_cast<float*>(smem);                  // [TOK][LD]
+    int* s_ids = reinterpret_cast<int*>(smem + OFF_IDS);            // [TOK][32]
     if (ok) {
-      for (int c = 0; c < E; c += 32) {
+      const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
+      for (int c = 32 * cg; c < E; c += 32 * (EPI / 4)) {
         uint32_t v[32];
         gemm::tmem_ld_32(t_row + c, v);
         gemm::tmem_ld_wait();
-        // columns at and past E (the last chunk when E % 32 != 0) are not experts
-        if (valid && p.logits) {
-          float* row = p.logits + (int64_t)t * E + c;
-          if ((E & 3) == 0) {
-            float4* dst = reinterpret_cast<float4*>(row);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              if (c + 4 * i < E)
-                dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                     __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-          } else {
+        for (int i = 0; i < 32; ++i)  // columns at and past E are not experts
+          if (c + i < E) s_log[r * LD + c + i] = __uint_as_float(v[i]);
+      }
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * EPI) : "memory");
+    const int k = p.k;
+    if (ok) {
+      // NT tokens per call: tl = ew + EPI * (g * NT + n)
+      constexpr int NT = EPL <= 4 ? TOK / EPI / 2 : TOK / EPI / 4;  // registers
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (c + i < E) row[i] = __uint_as_float(v[i]);
-          }
+      for (int g = 0; g < TOK / EPI / NT; ++g) {
+        const float* rows[NT];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          const int tl = ew + EPI * (g * NT + n);
+          rows[n] = t0 + tl < p.T ? s_log + tl * LD : nullptr;
+          if (rows[n] && p.logits)
+            for (int e = lane; e < E; e += 32) p.logits[(int64_t)(t0 + tl) * E + e] = rows[n][e];
         }
-        // keep the k largest keys, descending; an equal key never displaces an
-        // earlier (lower) expert id
+        int ids[NT];
+        float vals[NT], ws[NT];
+        warp_topk_softmax<EPL, NT>(rows, E, k, p.renormalize != 0, lane, ids, vals, ws);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const uint32_t key = order_key(__uint_as_float(v[i]));
-          if (c + i < E && key > thr) {
-            bool placed = false;
-#pragma unroll
-            for (int j = MAXK - 1; j >= 0; --j) {
-              if (j < k && !placed) {
-                if (j > 0 && keys[j - 1] < key) {
-                  keys[j] = keys[j - 1];
-                  ids[j] = ids[j - 1];
-                } else {
-                  keys[j] = key;
-                  ids[j] = c + i;
-                  placed = true;
-                }
-              }
+        for (int n = 0; n < NT; ++n) {
+          const int tl = ew + EPI * (g * NT + n);
+          if (rows[n] && lane < k) {
+            const int64_t f = (int64_t)(t0 + tl) * k + lane;
+            p.topk_ids[f] = ids[n];
+            p.topk_w[f] = ws[n];
+            if (p.local_rank) {
+              atomicOr(&s_mask[(tl >> 6) * MAX_E + ids[n]], 1ull << (tl & 63));
+              s_ids[tl * 32 + lane] = ids[n];
             }
-#pragma unroll
-            for (int j = 0; j < MAXK; ++j)
-              if (j == k - 1) thr = keys[j];
-          }
-        }
-      }
-      // softmax weights of the chosen experts.  The sums are taken in the
-      // order of the logits-input routing kernel (route.cu: per-lane partial
-      // sums over e = lane + 32 i, then an xor butterfly over the lanes), so
-      // both paths give the same weights bit for bit on the same logits.
-      const float vmax = key_value(keys[0]);
-      float denom;
-      if (p.renormalize) {
-        float s[MAXK];
-#pragma unroll
-        for (int j = 0; j < MAXK; ++j) s[j] = j < k ? expf(key_value(keys[j]) - vmax) : 0.f;
-#pragma unroll
-        for (int off = MAXK / 2; off > 0; off >>= 1)
-#pragma unroll
-          for (int j = 0; j < off; ++j) s[j] = s[j] + s[j + off];
-        denom = s[0];
-      } else {
-        float s[32];
-#pragma unroll
-        for (int l = 0; l < 32; ++l) s[l] = 0.f;
-        for (int c = 0; c < E; c += 32) {
-          uint32_t v[32];
-          gemm::tmem_ld_32(t_row + c, v);
-          gemm::tmem_ld_wait();
-#pragma unroll
-          for (int l = 0; l < 32; ++l)
-            if (c + l < E) s[l] += expf(__uint_as_float(v[l]) - vmax);
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-          for (int l = 0; l < off; ++l) s[l] = s[l] + s[l + off];
-        denom = s[0];
-      }
-      if (valid) {
-#pragma unroll
-        for (int j = 0; j < MAXK; ++j) {
-          if (j < k) {
-            p.topk_ids[(int64_t)t * k + j] = ids[j];
-            p.topk_w[(int64_t)t * k + j] = expf(key_value(keys[j]) - vmax) / denom;
-            if (p.local_rank) atomicOr(&s_mask[(r >> 6) * MAX_E + ids[j]], 1ull << (r & 63));
           }
         }
       }
     }
     // ranks inside each 64-token routing block and its expert histogram
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * EPI) : "memory");
     if (ok && p.local_rank) {
-      if (valid) {
-        const unsigned long long below = (1ull << (r & 63)) - 1ull;
-#pragma unroll
-        for (int j = 0; j < MAXK; ++j)
-          if (j < k)
-            p.local_rank[(int64_t)t * k + j] =
-                __popcll(s_mask[(r >> 6) * MAX_E + ids[j]] & below);
+      for (int tl = ew; tl < TOK; tl += EPI) {
+        const int t = t0 + tl;
+        if (t >= p.T) break;
+        if (lane < k)
+          p.local_rank[(int64_t)t * k + lane] =
+              __popcll(s_mask[(tl >> 6) * MAX_E + s_ids[tl * 32 + lane]] &
+                       ((1ull << (tl & 63)) - 1ull));
       }
-      for (int i = threadIdx.x - 64; i < 2 * E; i += 128) {
+      for (int i = threadIdx.x - 64; i < 2 * E; i += 32 * EPI) {
         const int half = i / E, e = i - half * E;
         const int b = 2 * blockIdx.x + half;
         if (b < p.n_blocks) p.block_hist[(int64_t)b * E + e] = __popcll(s_mask[half * MAX_E + e]);
@@ -325,27 +283,31 @@ static bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint
 
 }  // namespace router
 
+template <int EPL>
+static cudaError_t launch_router_epl(const CUtensorMap& tmX, const CUtensorMap& tmG,
+                                     const router::Params& p, int grid, cudaStream_t stream) {
+  using namespace router;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  static bool configured[64] = {};
+  if (!configured[dev]) {
+    const cudaError_t err = cudaFuncSetAttribute(router_gate_topk_kernel<EPL>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, ALLOC);
+    if (err != cudaSuccess) return err;
+    configured[dev] = true;
+  }
+  router_gate_topk_kernel<EPL><<<grid, THREADS, ALLOC, stream>>>(tmX, tmG, p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_router_gate_topk(const uint16_t* x, const uint16_t* gate, int T, int H, int E,
                                     int k, bool renormalize, float* logits, int32_t* topk_ids,
                                     float* topk_w, int32_t* local_rank, int32_t* block_hist,
                                     cudaStream_t stream) {
   using namespace router;
   if (T == 0) return cudaSuccess;
-  if (H % KS != 0 || E < 1 || E > MAX_E || k < 1 || k > 16 || k > E) return cudaErrorInvalidValue;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  static bool configured[2][64] = {};
-  const int which = k <= 8 ? 0 : 1;
-  if (!configured[which][dev]) {
-    const cudaError_t err =
-        which == 0 ? cudaFuncSetAttribute(router_gate_topk_kernel<8>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, ALLOC)
-                   : cudaFuncSetAttribute(router_gate_topk_kernel<16>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, ALLOC);
-    if (err != cudaSuccess) return err;
-    configured[which][dev] = true;
-  }
+  if (H % KS != 0 || E < 1 || E > MAX_E || k < 1 || k > 32 || k > E) return cudaErrorInvalidValue;
   CUtensorMap tmX, tmG;
   if (!make_map_bf16(&tmX, x, (uint64_t)H, (uint64_t)T, TOK)) return cudaErrorInvalidValue;
   // the box covers the MMA's N rows; rows past E read the zero fill
@@ -366,11 +328,11 @@ cudaError_t launch_router_gate_topk(const uint16_t* x, const uint16_t* gate, int
   p.status = device_status_ptr();
   p.wait_limit = wait_limit_cycles();
   const int grid = (int)ceil_div(T, TOK);
-  if (which == 0)
-    router_gate_topk_kernel<8><<<grid, THREADS, ALLOC, stream>>>(tmX, tmG, p);
-  else
-    router_gate_topk_kernel<16><<<grid, THREADS, ALLOC, stream>>>(tmX, tmG, p);
-  return cudaGetLastError();
+  const int epl = (E + 31) / 32;
+  if (epl <= 1) return launch_router_epl<1>(tmX, tmG, p, grid, stream);
+  if (epl <= 2) return launch_router_epl<2>(tmX, tmG, p, grid, stream);
+  if (epl <= 4) return launch_router_epl<4>(tmX, tmG, p, grid, stream);
+  return launch_router_epl<8>(tmX, tmG, p, grid, stream);
 }
 
 // ---------------------------------------------------------------- dequant

@@ -26,7 +26,8 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--config", default="qwen3_30b_prefill")
     ap.add_argument("--kernel", default="gemm1",
-                    choices=["gemm1", "gemm2", "route", "finalize", "wquant", "layer", "linear"])
+                    choices=["gemm1", "gemm2", "route", "finalize", "wquant", "layer", "linear",
+                             "router"])
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--gemm-2sm", default="auto", choices=["0", "1", "auto"])
     args = ap.parse_args()
@@ -43,6 +44,15 @@ def main():
             raise SystemExit("device status error")
         return
     shape = workloads.CONFIGS[args.config]
+    if args.kernel == "router":
+        x = workloads.make_hidden(shape, dev)
+        gate = workloads.make_gate(shape, dev)
+        for _ in range(args.iters):
+            mm.moe_router_gate_topk(x, gate, shape.k)
+        torch.cuda.synchronize()
+        if mm.device_status() != 0:
+            raise SystemExit("device status error")
+        return
     inp = workloads.make_layer(shape, dev)
     if shape.offline:
         layer = mm.MXFP8MoELayer.from_quantized(inp["w13q"], inp["w13s"], inp["w2q"], inp["w2s"],

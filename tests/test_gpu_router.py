@@ -54,7 +54,7 @@ def _check_topk_against(mm, x, gate, k, renorm, r, logits):
 
 @pytest.mark.parametrize("T,H,E,k", [(1, 64, 16, 1), (200, 256, 128, 8), (1000, 2048, 128, 8),
                                      (333, 512, 256, 16), (64, 128, 48, 5), (77, 192, 8, 2),
-                                     (130, 64, 6, 6)])
+                                     (130, 64, 6, 6), (257, 128, 64, 32)])
 @pytest.mark.parametrize("renorm", [True, False])
 def test_router_exact_integer_inputs(mm, T, H, E, k, renorm):
     rng = np.random.default_rng(T + H + E + k)
@@ -138,7 +138,7 @@ def test_offline_gate_layer(mm):
 def test_router_argument_errors(mm):
     from mxfp8_block_scaled_moe_gb300._lib import MXMoEError
     x = torch.zeros(8, 128, dtype=torch.bfloat16, device=DEV)
-    for E, k, H in ((128, 17, 128), (272, 2, 128), (128, 2, 96)):
+    for E, k, H in ((128, 33, 128), (272, 2, 128), (128, 2, 96)):
         g = torch.zeros(E, H, dtype=torch.bfloat16, device=DEV)
         with pytest.raises(MXMoEError) as ei:
             mm.moe_router_gate_topk(x[:, :H].contiguous(), g, k)
