@@ -43,7 +43,8 @@ FP8_OVER_BF16 = 2.0   # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 # the bench workload (profiles/gemm1_swiglu_quant_qwen3_30b_prefill.md, the
 # DRAM-bytes capture at its end), keyed
 # by the hash of the sources it was captured from
-NCU_TRAFFIC = {"a9ec3d6a1d8bbad4": 786553600, "64d58b0d55536f8c": 786384128}
+NCU_TRAFFIC = {"a9ec3d6a1d8bbad4": 786553600, "64d58b0d55536f8c": 786384128,
+               "f21fe81032a4b103": 786399488}
 
 
 def parse():

@@ -500,9 +500,11 @@ mxmoe_status mx_quantize_fp4_3d(const uint16_t* w, int64_t E, int64_t N, int64_t
 
 // Dense linear workspace, each part 256-byte aligned:
 // xq [M, K] | xs tiled (ceil(M/128) + 1 row blocks) | offsets [2] | w scales
-// tiled (ceil(N/128) row blocks; the row-major-scale entry point only).
+// tiled (ceil(N/128) row blocks; the row-major-scale entry point only) |
+// split-K partial sums fp32 [ksplit][M][N] (small M only).
 struct LinearLayout {
-  size_t xq, xs, offs, ws, total;
+  size_t xq, xs, offs, ws, partial, total;
+  int ksplit;
 };
 
 static LinearLayout linear_layout(int64_t M, int64_t N, int64_t K, bool w_scales) {
@@ -514,6 +516,8 @@ static LinearLayout linear_layout(int64_t M, int64_t N, int64_t K, bool w_scales
   L.xs = take(((size_t)(M + 127) / 128 + 1) * slice_bytes);
   L.offs = take(2 * sizeof(int64_t));
   L.ws = w_scales ? take((size_t)(N + 127) / 128 * slice_bytes) : 0;
+  L.ksplit = M > 0 ? gemm_bf16_ksplit(M, (int)N, (int)K) : 1;
+  L.partial = L.ksplit > 1 ? take((size_t)L.ksplit * M * N * sizeof(float)) : 0;
   L.total = o;
   return L;
 }
@@ -564,7 +568,8 @@ static mxmoe_status linear_impl(const uint16_t* x, const uint8_t* wq, const uint
   err = launch_mx_quantize_tiled(x, M, K, xq, xs, offs, st, fp4);
   if (err != cudaSuccess) return MXMOE_ERR_CUDA;
   prof.mark(2);
-  err = launch_gemm_bf16(xq, xs, wq, wst, offs, M, 1, (int)K, (int)N, out, st, true, fp4 ? 2 : 0);
+  err = launch_gemm_bf16(xq, xs, wq, wst, offs, M, 1, (int)K, (int)N, out, st, true, fp4 ? 2 : 0,
+                         L.ksplit, L.ksplit > 1 ? (float*)(base + L.partial) : nullptr);
   if (err != cudaSuccess) return MXMOE_ERR_CUDA;
   for (int i = 3; i < kProfEvents; ++i) prof.mark(i);
   prof.done();

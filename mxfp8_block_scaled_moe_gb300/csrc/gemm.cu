@@ -80,7 +80,9 @@ struct Layout1 {
 // of tiled_scales.h (a segment's chunks are contiguous: one bulk copy per 128
 // rows); otherwise they are the row-major [rows, K/32] arrays, gathered into
 // the same staging layout by cp.async.
-template <int BN, bool kSwiglu, bool kTiledSF, int kFmt>
+// kSplit: split-K tiles (Params::ksplit); the other instantiations fold the
+// split arithmetic away.
+template <int BN, bool kSwiglu, bool kTiledSF, int kFmt, bool kSplit>
 __global__ void __launch_bounds__(THREADS1, 1)
     gemm1sm_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, const Params p) {
@@ -142,10 +144,19 @@ __global__ void __launch_bounds__(THREADS1, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
-  const int total_tiles = s_ts[E];
   const int KT = (p.K + BK - 1) / BK;  // a partial last K slice is zero-filled by TMA
   const int K32 = p.K / 32;
-  const int nseg = (KT + SEG - 1) / SEG;  // scale segments per tile
+  const int KSPL = kSplit ? p.ksplit : 1;
+  const int kper = (KT + KSPL - 1) / KSPL;  // K slices per split (every split non-empty)
+  const int total_tiles = s_ts[E] * KSPL;
+  // tile -> (expert, m tile, n tile, split) and the split's K slices [k0, k1)
+  auto tile_at = [&](int tile, int& e, int& mt, int& nt, int& ks, int& k0, int& k1) {
+    const int base = tile / KSPL;
+    ks = tile - base * KSPL;
+    decode_tile(base, s_ts, E, p.n_tiles_n, e, mt, nt);
+    k0 = ks * kper;
+    k1 = min(KT, k0 + kper);
+  };
 
   if (warp == 0) {
     // ================= producer: operand stages, and each tile segment's
@@ -162,13 +173,13 @@ __global__ void __launch_bounds__(THREADS1, 1)
       const uint32_t par = ((uint32_t)(gseg >> 1) & 1u) ^ 1u;
       const bool got = wait_bar(bar_sfs_free(b), par, p.wait_limit, p.status, s_abort);
       if (!__all_sync(0xffffffffu, got)) return false;
-      int e, mt, nt;
-      decode_tile(tile, s_ts, E, p.n_tiles_n, e, mt, nt);
+      int e, mt, nt, ks, k0, k1;
+      tile_at(tile, e, mt, nt, ks, k0, k1);
       const int64_t row0 = s_off[e] + (int64_t)mt * BM;
       const int64_t brow = (int64_t)e * p.Nw;
       const int64_t bh0 = kSwiglu ? brow + (int64_t)nt * (BN / 2) : brow + (int64_t)nt * BN;
       const int64_t bh1 = brow + p.n_out + (int64_t)nt * (BN / 2);
-      const int kt0 = sg * SEG, len = min(SEG, KT - kt0);
+      const int kt0 = k0 + sg * SEG, len = min(SEG, k1 - kt0);
       const uint32_t sA = sbase + L::OFF_SFA + b * L::SFA_SEG;
       const uint32_t sB = sbase + L::OFF_SFB + b * L::SFB_SEG;
       if (kTiledSF) {
@@ -211,17 +222,18 @@ __global__ void __launch_bounds__(THREADS1, 1)
     };
     if (blockIdx.x < total_tiles) ok = load_scales(0, blockIdx.x, 0);
     for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-      int e, mt, nt;
-      decode_tile(tile, s_ts, E, p.n_tiles_n, e, mt, nt);
+      int e, mt, nt, ks, k0, k1;
+      tile_at(tile, e, mt, nt, ks, k0, k1);
+      const int nseg = (k1 - k0 + SEG - 1) / SEG;  // scale segments of this tile
       const int64_t row0 = s_off[e] + (int64_t)mt * BM;
       const int64_t brow = (int64_t)e * p.Nw;
       // B tile halves: gmm1 = gate rows | up rows; gmm2 = one BN-row box
       const int64_t bh0 = kSwiglu ? brow + (int64_t)nt * (BN / 2) : brow + (int64_t)nt * BN;
       const int64_t bh1 = brow + p.n_out + (int64_t)nt * (BN / 2);
-      for (int kt = 0; kt < KT; ++kt) {
-        if (kt % SEG == 0) {
+      for (int kt = k0; kt < k1; ++kt) {
+        if ((kt - k0) % SEG == 0) {
           // the next segment's scales: later in this tile, or the next tile's first
-          const int sg = kt / SEG;
+          const int sg = (kt - k0) / SEG;
           const int ntile = sg + 1 < nseg ? tile : tile + (int)gridDim.x;
           if (ntile < total_tiles && !load_scales(g + 1, ntile, sg + 1 < nseg ? sg + 1 : 0)) {
             ok = false;
@@ -275,13 +287,15 @@ __global__ void __launch_bounds__(THREADS1, 1)
       bool issued = false;
       constexpr uint32_t IDESC = make_idesc(BM, BN, kFp4B, kFp4A);
       for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        int e, mt, nt, ks, k0, k1;
+        tile_at(tile, e, mt, nt, ks, k0, k1);
         if (!wait_bar(bar_acc_empty, acc_phase ^ 1, p.wait_limit, p.status, s_abort)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        for (int kt = 0; kt < KT; ++kt) {
-          const int i = kt % SEG;
+        for (int kt = k0; kt < k1; ++kt) {
+          const int i = (kt - k0) % SEG;
           const int b = g & 1;
           if (i == 0) {
             // this segment's scales are in TMEM buffer b
@@ -306,11 +320,11 @@ __global__ void __launch_bounds__(THREADS1, 1)
           for (int kk = 0; kk < BK / 32; ++kk) {
             const uint32_t idesc = IDESC | ((uint32_t)kk << 29) | ((uint32_t)kk << 4);
             tc_mma_mxf8(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, t_sfa, t_sfb,
-                        (kt | kk) != 0 ? 1u : 0u);
+                        ((kt - k0) | kk) != 0 ? 1u : 0u);
           }
           issued = true;
           tc_commit(bar_empty(stage));
-          if (i == SEG - 1 || kt == KT - 1) {
+          if (i == SEG - 1 || kt == k1 - 1) {
             tc_commit(bar_sft_free(b));  // the segment's scales may be overwritten
             ++g;
           }
@@ -340,6 +354,9 @@ __global__ void __launch_bounds__(THREADS1, 1)
     int g = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+      int e, mt, nt, ks, k0, k1;
+      tile_at(tile, e, mt, nt, ks, k0, k1);
+      const int nseg = (k1 - k0 + SEG - 1) / SEG;
       for (int sg = 0; sg < nseg; ++sg, ++g) {
         const int b = g & 1;
         const uint32_t par = (uint32_t)(g >> 1) & 1u;
@@ -350,7 +367,7 @@ __global__ void __launch_bounds__(THREADS1, 1)
           ok = false;
           break;
         }
-        const int len = min(SEG, KT - sg * SEG);
+        const int len = min(SEG, k1 - (k0 + sg * SEG));
         const uint8_t* sfa_s = smem + L::OFF_SFA + b * L::SFA_SEG;
         const uint8_t* sfb_s = smem + L::OFF_SFB + b * L::SFB_SEG;
         for (int i = 0; i < len; ++i) {
@@ -379,16 +396,16 @@ __global__ void __launch_bounds__(THREADS1, 1)
     const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-      int e, mt, nt;
-      decode_tile(tile, s_ts, E, p.n_tiles_n, e, mt, nt);
+      int e, mt, nt, ks, k0, k1;
+      tile_at(tile, e, mt, nt, ks, k0, k1);
       const int64_t grow = s_off[e] + (int64_t)mt * BM + row;
       const bool valid = grow < s_off[e + 1];
       const bool got = wait_bar(bar_acc_full, acc_phase, p.wait_limit, p.status, s_abort);
       if (!__all_sync(0xffffffffu, got)) break;  // keep the warp converged
       tc_fence_after();
-      epilogue_tile<BN, kSwiglu, kTiledSF, kFp4A>(
+      epilogue_tile<BN, kSwiglu, kTiledSF, kFp4A, kSplit>(
           p, t_row, grp, row, lane, grow, valid, nt, (int64_t)(s_mtb[e] + mt) * BM + row,
-          [&] { if (lane == 0) mbar_arrive(bar_acc_empty); });
+          [&] { if (lane == 0) mbar_arrive(bar_acc_empty); }, ks);
       acc_phase ^= 1;
     }
   }
@@ -407,18 +424,18 @@ __global__ void __launch_bounds__(THREADS1, 1)
 
 // ---------------------------------------------------------------- host side
 
-template <int BN, bool kSwiglu, bool kTiledSF, int kFmt>
+template <int BN, bool kSwiglu, bool kTiledSF, int kFmt, bool kSplit = false>
 static cudaError_t launch_single(const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
                                  const uint8_t* sfb, const int64_t* offsets, int64_t M, int E,
                                  int K, int Nw, int n_out, void* out, uint8_t* out_scale,
-                                 cudaStream_t stream) {
+                                 cudaStream_t stream, int ksplit = 1, float* partial = nullptr) {
   using L = Layout1<BN>;
   if (M == 0) return cudaSuccess;
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   static bool configured[64] = {false};
-  auto kern = gemm1sm_kernel<BN, kSwiglu, kTiledSF, kFmt>;
+  auto kern = gemm1sm_kernel<BN, kSwiglu, kTiledSF, kFmt, kSplit>;
   if (!configured[dev]) {
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
@@ -445,7 +462,9 @@ static cudaError_t launch_single(const uint8_t* a, const uint8_t* sfa, const uin
   p.n_tiles_n = kSwiglu ? n_out / (BN / 2) : (int)ceil_div(n_out, BN);  // ragged last n-tile: E == 1
   p.status = device_status_ptr();
   p.wait_limit = wait_limit_cycles();
-  const int64_t tiles_bound = (ceil_div(M, BM) + E) * (int64_t)p.n_tiles_n;
+  p.ksplit = kSplit ? ksplit : 1;
+  p.partial = kSplit ? partial : nullptr;
+  const int64_t tiles_bound = (ceil_div(M, BM) + E) * (int64_t)p.n_tiles_n * ksplit;
   const int grid = (int)std::min<int64_t>(tiles_bound, num_sms());
   kern<<<grid, THREADS1, L::ALLOC, stream>>>(tmA, tmB, p);
   return cudaGetLastError();
@@ -459,7 +478,17 @@ static cudaError_t launch_single(const uint8_t* a, const uint8_t* sfa, const uin
 template <int BN, bool kSwiglu, bool kTiledSF, int kFmt>
 static cudaError_t launch(const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
                           const uint8_t* sfb, const int64_t* offsets, int64_t M, int E, int K,
-                          int Nw, int n_out, void* out, uint8_t* out_scale, cudaStream_t stream) {
+                          int Nw, int n_out, void* out, uint8_t* out_scale, cudaStream_t stream,
+                          int ksplit = 1, float* partial = nullptr) {
+  if (ksplit > 1) {
+    if constexpr (kSwiglu) {
+      return cudaErrorNotSupported;
+    } else {
+      return launch_single<BN, false, kTiledSF, kFmt, true>(a, sfa, b, sfb, offsets, M, E, K, Nw,
+                                                            n_out, out, out_scale, stream, ksplit,
+                                                            partial);
+    }
+  }
   if (BN == 256 && use_two_sm_gemm(kSwiglu, M, E)) {
     const cudaError_t err = launch_pair<kSwiglu, kTiledSF, kFmt>(a, sfa, b, sfb, offsets, M, E, K, Nw,
                                                            n_out, out, out_scale, stream);
@@ -491,32 +520,78 @@ cudaError_t launch_gemm_swiglu_quant(const uint8_t* xq, const uint8_t* xs, const
                                                   I, aq, as, stream);
 }
 
+// Split-K sums: out[m, n] = bf16(sum over s in order of partial[s][m][n]);
+// one thread per 8 columns (N % 8 == 0, 16-byte aligned rows).
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ partial,
+                                                            int S, int64_t M, int N,
+                                                            uint16_t* __restrict__ out) {
+  const int64_t n8 = M * N / 8;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int s = 0; s < S; ++s) {
+      const float4* src = reinterpret_cast<const float4*>(partial + (int64_t)s * M * N + i * 8);
+      const float4 u = src[0], w = src[1];
+      a[0] += u.x; a[1] += u.y; a[2] += u.z; a[3] += u.w;
+      a[4] += w.x; a[5] += w.y; a[6] += w.z; a[7] += w.w;
+    }
+    st_v4(out + i * 8, make_uint4(cvt_bf16x2(a[0], a[1]), cvt_bf16x2(a[2], a[3]),
+                                  cvt_bf16x2(a[4], a[5]), cvt_bf16x2(a[6], a[7])));
+  }
+}
+
 // 256-wide tiles when the 128-row weight blocks pair up (a ragged last block,
 // H % 128 != 0, only with E == 1 and MMA-layout scales), 128-wide otherwise.
 template <int kFmt>
 static cudaError_t launch_bf16_fmt(const uint8_t* aq, const uint8_t* as, const uint8_t* w2q,
                                    const uint8_t* w2s, const int64_t* offsets, int64_t M, int E,
-                                   int I, int H, uint16_t* y, cudaStream_t stream) {
+                                   int I, int H, uint16_t* y, cudaStream_t stream, int ksplit,
+                                   float* partial) {
+  cudaError_t err;
   if (ceil_div(H, 128) % 2 == 0)
-    return gemm::launch<256, false, true, kFmt>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y,
-                                                nullptr, stream);
-  return gemm::launch<128, false, true, kFmt>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y,
-                                              nullptr, stream);
+    err = gemm::launch<256, false, true, kFmt>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y,
+                                               nullptr, stream, ksplit, partial);
+  else
+    err = gemm::launch<128, false, true, kFmt>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y,
+                                               nullptr, stream, ksplit, partial);
+  if (err != cudaSuccess || ksplit <= 1 || M == 0) return err;
+  const int64_t n8 = M * H / 8;
+  int64_t blocks = ceil_div(n8, 256);
+  const int64_t cap = (int64_t)num_sms() * 8;
+  if (blocks > cap) blocks = cap;
+  splitk_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(partial, ksplit, M, H, y);
+  return cudaGetLastError();
+}
+
+int gemm_bf16_ksplit(int64_t M, int N, int K) {
+  const int64_t n_tiles = ceil_div(N, ceil_div(N, 128) % 2 == 0 ? 256 : 128);
+  const int64_t tiles = ceil_div(M, gemm::BM) * n_tiles;
+  const int KT = (int)ceil_div(K, 128);
+  const int sms = num_sms();
+  if (tiles * 2 > sms) return 1;  // enough tiles to fill the GPU
+  int S = (int)std::min<int64_t>({(int64_t)sms / tiles, (int64_t)KT / 4, 32});
+  if (S <= 1) return 1;
+  const int kper = (int)ceil_div(KT, S);
+  return (int)ceil_div(KT, kper);  // every split non-empty
 }
 
 cudaError_t launch_gemm_bf16(const uint8_t* aq, const uint8_t* as, const uint8_t* w2q,
                              const uint8_t* w2s, const int64_t* offsets, int64_t M, int E,
                              int I, int H, uint16_t* y, cudaStream_t stream, bool tiled_scales,
-                             int fmt) {
+                             int fmt, int ksplit, float* partial) {
+  if (ksplit > 1 && (E != 1 || !tiled_scales || !partial)) return cudaErrorNotSupported;
   if (fmt == gemm::FMT_W4A8 || fmt == gemm::FMT_W4A4) {
     if (!tiled_scales) return cudaErrorNotSupported;
     return fmt == gemm::FMT_W4A8
-               ? launch_bf16_fmt<gemm::FMT_W4A8>(aq, as, w2q, w2s, offsets, M, E, I, H, y, stream)
-               : launch_bf16_fmt<gemm::FMT_W4A4>(aq, as, w2q, w2s, offsets, M, E, I, H, y, stream);
+               ? launch_bf16_fmt<gemm::FMT_W4A8>(aq, as, w2q, w2s, offsets, M, E, I, H, y, stream,
+                                                 ksplit, partial)
+               : launch_bf16_fmt<gemm::FMT_W4A4>(aq, as, w2q, w2s, offsets, M, E, I, H, y, stream,
+                                                 ksplit, partial);
   }
   if (fmt != gemm::FMT_W8A8) return cudaErrorNotSupported;
   if (tiled_scales)
-    return launch_bf16_fmt<gemm::FMT_W8A8>(aq, as, w2q, w2s, offsets, M, E, I, H, y, stream);
+    return launch_bf16_fmt<gemm::FMT_W8A8>(aq, as, w2q, w2s, offsets, M, E, I, H, y, stream,
+                                           ksplit, partial);
   if (ceil_div(H, 128) % 2 == 0)
     return gemm::launch<256, false, false, gemm::FMT_W8A8>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y,
                                                      nullptr, stream);

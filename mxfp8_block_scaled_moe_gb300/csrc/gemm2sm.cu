@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(THREADS1, 1)
       const bool got = wait_bar(bar_acc_full, acc_phase, p.wait_limit, p.status, s_abort);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
-      epilogue_tile<BN, kSwiglu, true, kFp4A>(
+      epilogue_tile<BN, kSwiglu, true, kFp4A, false>(
           p, t_row, grp, row, lane, grow, valid, nt, (int64_t)(s_mtb[e] + mt) * BM + row,
           [&] {
             if (lane == 0) {
@@ -492,6 +492,8 @@ cudaError_t launch_pair_impl(const uint8_t* a, const uint8_t* sfa, const uint8_t
   p.Nw = Nw;
   p.n_out = n_out;
   p.n_tiles_n = kSwiglu ? n_out / 128 : (int)ceil_div(n_out, 256);
+  p.ksplit = 1;
+  p.partial = nullptr;
   p.status = device_status_ptr();
   p.wait_limit = wait_limit_cycles();
   const int64_t units_bound = (ceil_div(M, BM) / 2 + E) * (int64_t)p.n_tiles_n;

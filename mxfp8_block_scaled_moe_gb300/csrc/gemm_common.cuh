@@ -42,6 +42,11 @@ struct Params {
   int E, K, Nw, n_out, n_tiles_n;
   int* status;
   long long wait_limit;
+  // split-K (1-SM kernel, bf16-out GEMM with one group): tile = base * ksplit
+  // + ks covers K slices [ks * kper, min(KT, (ks + 1) * kper)) and writes its
+  // fp32 partial sums to partial [ksplit][M][n_out]; ksplit = 1 otherwise
+  int ksplit;
+  float* partial;
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -327,10 +332,10 @@ __device__ __forceinline__ void build_schedule(const Params& p, int lane, int64_
 // overwritten), then SwiGLU + MX requant (gmm1) or bf16 rounding (gmm2) and
 // the stores.  BN = accumulator columns, grp = column slice of this warp.
 // `release` is called by every thread; it arrives once per warp.
-template <int BN, bool kSwiglu, bool kTiledSF, bool kFp4Out, typename Release>
+template <int BN, bool kSwiglu, bool kTiledSF, bool kFp4Out, bool kPartial, typename Release>
 __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t t_row, int grp, int row,
                                               int lane, int64_t grow, bool valid, int nt,
-                                              int64_t tiled_row, Release release) {
+                                              int64_t tiled_row, Release release, int ks = 0) {
   constexpr int GC = BN / 2 / EPI_GROUPS;
   constexpr int PC = BN / EPI_GROUPS;
   constexpr int CH = kSwiglu ? 2 * (GC / 32) : PC / 32;  // 32-column chunks
@@ -392,6 +397,22 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t t_row, i
         else
           p.out_scale[grow * (p.n_out / 32) + (col >> 5)] = (uint8_t)sb;
       }
+    }
+  } else if (kPartial) {
+    // split-K: this K range's fp32 partial sums (the ranges are added in a
+    // fixed order and rounded to bf16 by splitk_reduce_kernel)
+    if (valid) {
+      float* dst = p.partial + ((int64_t)ks * p.M + grow) * p.n_out;
+#pragma unroll
+      for (int c = 0; c < CH; ++c)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int64_t col = (int64_t)nt * BN + grp * PC + c * 32 + 4 * i;
+          if (col < p.n_out)
+            *reinterpret_cast<float4*>(dst + col) =
+                make_float4(__uint_as_float(v[c][4 * i]), __uint_as_float(v[c][4 * i + 1]),
+                            __uint_as_float(v[c][4 * i + 2]), __uint_as_float(v[c][4 * i + 3]));
+        }
     }
   } else {
     uint16_t* y = reinterpret_cast<uint16_t*>(p.out);

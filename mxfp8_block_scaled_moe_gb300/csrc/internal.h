@@ -69,10 +69,17 @@ cudaError_t launch_gemm_swiglu_quant(const uint8_t* xq, const uint8_t* xs, const
                                      int E, int H, int I, uint8_t* aq, uint8_t* as,
                                      cudaStream_t stream, bool tiled_scales = false,
                                      int fmt = 0);
+// ksplit > 1 (E == 1, tiled scales): split-K over ksplit K ranges whose fp32
+// partial sums go to partial [ksplit][M][H], then one reduce kernel rounds
+// their in-order sum to bf16.
 cudaError_t launch_gemm_bf16(const uint8_t* aq, const uint8_t* as, const uint8_t* w2q,
                              const uint8_t* w2s, const int64_t* offsets, int64_t M, int E,
                              int I, int H, uint16_t* y, cudaStream_t stream,
-                             bool tiled_scales = false, int fmt = 0);
+                             bool tiled_scales = false, int fmt = 0, int ksplit = 1,
+                             float* partial = nullptr);
+// Split count the dense linear uses for an [M, K] x [N, K]^T product on the
+// current device (1 when the tiles alone fill the GPU).
+int gemm_bf16_ksplit(int64_t M, int N, int K);
 
 // [rows, ceil(K/32)] scales -> tiled layout with KT = ceil(K/128); rows and
 // slots past the data (a ragged row block or K slice) are written as 127.
