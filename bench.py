@@ -47,6 +47,21 @@ NCU_TRAFFIC = {"a9ec3d6a1d8bbad4": 786553600, "64d58b0d55536f8c": 786384128,
                "f21fe81032a4b103": 786399488}
 
 
+def max_over_ranks(torch, dist, ms, world, device):
+    """The slowest rank's time (MAX all-reduce over the job; the local time
+    when world == 1)."""
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, tokens_per_rank, steps, max_ms):
+    """Whole-job tokens/s: every replica processes its tokens in every step;
+    the job takes as long as its slowest rank."""
+    return world * tokens_per_rank * steps / (max_ms / 1e3)
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -489,12 +504,8 @@ def main():
     mm.api.layer_profile_enable(False)
     if world > 1:
         dist.barrier()
-    total_ms = sum(step_ms)
-    t_max = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
-    total_ms = float(t_max.item())
-    value = world * T * args.steps / (total_ms / 1e3)
+    total_ms = max_over_ranks(torch, dist, sum(step_ms), world, dev)
+    value = whole_job_rate(world, T, args.steps, total_ms)
 
     # ---- per-kernel times inside the timed steps (library events on the stream)
     def kmean(key):
@@ -559,11 +570,8 @@ def main():
     if not torch.equal(o_h, out.cpu()):
         raise RuntimeError("host-buffer layer output differs from the device layer")
     e2e_t = time_fn(torch, e2e_step, args.steps, flush, stream)
-    e2e_ms = sum(e2e_t)
-    e2e_t_max = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(e2e_t_max, op=dist.ReduceOp.MAX)
-    e2e_value = world * T * args.steps / (float(e2e_t_max.item()) / 1e3)
+    e2e_max_ms = max_over_ranks(torch, dist, sum(e2e_t), world, dev)
+    e2e_value = whole_job_rate(world, T, args.steps, e2e_max_ms)
     h2d = x_h.numel() * 2 + l_h.numel() * 4
     d2h = o_h.numel() * 2
     # vendor-library dense GEMM rates (context for the MXFP8 peak; after the
@@ -685,7 +693,7 @@ def main():
             "clocks": clk.summary(),
             "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,
-                    "ms_per_step": round(float(e2e_t_max.item()) / args.steps, 4)},
+                    "ms_per_step": round(e2e_max_ms / args.steps, 4)},
             "gpu_launches": 6 * args.steps,
             "e2e_api": "moe_forward_mxfp8_host (pinned host buffers, default chunk plan 3/16 | 5/8 | 3/16 of the tokens, "
                        "H2D / compute / D2H on three streams)",
