@@ -332,9 +332,12 @@ mxmoe_status mx_dequantize_bf16_2d(const uint8_t* q, const uint8_t* scale, int64
  *          mx_scales_to_mma_layout(ws, 1, N, K) (mxfp8_linear_mma_scales,
  *          16-byte aligned)
  *   out    bf16 [M, N], 32-byte aligned
- *   workspace  mxfp8_linear_workspace_size(M, N, K) bytes, 256-byte aligned;
- *          it holds xq, the activation scales and (mxfp8_linear only) the
- *          re-laid weight scales.
+ *   workspace  mxfp8_linear_workspace_size(M, N, K) bytes, 256-byte aligned,
+ *          sized for the current device; it holds xq, the activation scales,
+ *          (mxfp8_linear only) the re-laid weight scales and, when M is too
+ *          small to fill the GPU with tiles, the split-K partial sums (each
+ *          tile's K slices split over idle SMs, fp32 partials added in a fixed
+ *          order and rounded once to bf16).
  * Requires K % 16 == 0 (K % 32 == 16 gives each row a partial last block of
  * 16, PR #32266 summary, "Offline partial MXFP8 block-scale layout") and
  * N % 16 == 0; 0 <= M < 2^31.  M == 0 is a no-op.

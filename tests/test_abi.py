@@ -97,3 +97,33 @@ def test_python_binding_refuses_cpu_tensors():
     import mxfp8_block_scaled_moe_gb300 as mm
     with pytest.raises(ValueError, match="CUDA"):
         mm.mx_quantize_3d(torch.zeros(2, 64, dtype=torch.bfloat16))
+
+
+def test_host_validation_of_the_linear_router_and_fp4_entry_points(lib):
+    p = C.c_void_p(4096)
+    nul = C.c_void_p(0)
+    # dense linear: K % 16 != 0 / N % 16 != 0 -> shape; M == 0 is a no-op
+    assert lib.mxfp8_linear(p, p, p, 8, 64, 40, p, p, 1 << 30, nul) == 3
+    assert lib.mxfp8_linear(p, p, p, 8, 40, 64, p, p, 1 << 30, nul) == 3
+    assert lib.mxfp8_linear(nul, nul, nul, 0, 64, 64, nul, nul, 0, nul) == 0
+    # output not 32-byte aligned, workspace too small
+    assert lib.mxfp8_linear(p, p, p, 8, 64, 64, C.c_void_p(4096 + 16), p, 1 << 30, nul) == 2
+    assert lib.mxfp8_linear(p, p, p, 8, 64, 64, p, p, 16, nul) == 5
+    assert lib.mxfp8_linear_workspace_size(8, 64, 40) == 0
+    assert lib.mxfp8_linear_workspace_size(128, 4096, 4304) >= 128 * 4304
+    # W4A4 linear: K % 128 != 0 -> shape; packed weights must be 32-byte aligned
+    assert lib.mxfp4_linear(p, p, p, 8, 64, 192, p, p, 1 << 30, nul) == 3
+    assert lib.mxfp4_linear(p, C.c_void_p(4096 + 16), p, 8, 64, 256, p, p, 1 << 30, nul) == 2
+    # router: H % 64, E > 256, k > 32 -> unsupported; k > E -> shape
+    assert lib.moe_router_gate_topk(p, p, 8, 96, 128, 8, 1, nul, p, p, nul) == 4
+    assert lib.moe_router_gate_topk(p, p, 8, 128, 300, 8, 1, nul, p, p, nul) == 4
+    assert lib.moe_router_gate_topk(p, p, 8, 128, 128, 33, 1, nul, p, p, nul) == 4
+    assert lib.moe_router_gate_topk(p, p, 8, 128, 4, 8, 1, nul, p, p, nul) == 3
+    assert lib.moe_router_gate_topk(nul, nul, 0, 128, 16, 2, 1, nul, nul, nul, nul) == 0
+    # gate dequant: K % 32 != 0
+    assert lib.mx_dequantize_bf16_2d(p, p, 4, 48, p, nul) == 3
+    # W4A4 and gated layers share the layer's checks (k > E -> shape)
+    assert lib.moe_forward_w4a4_mma_scales(p, p, p, p, p, p, 64, 256, 8, 9, 128, 1, p, p,
+                                           1 << 30, nul) == 3
+    assert lib.moe_forward_mxfp8_gated_mma_scales(p, p, p, p, p, p, 64, 256, 8, 9, 128, 1, p, p,
+                                                  1 << 30, nul) == 3
