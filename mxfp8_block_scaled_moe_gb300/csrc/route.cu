@@ -36,15 +36,18 @@ constexpr int kRouteThreads = 256;
 constexpr int kRouteWarps = kRouteThreads / 32;
 
 
-constexpr int kTopkThreads = 1024;
-constexpr int kTopkWarps = kTopkThreads / 32;
-static_assert(kRouteTokensPerBlock == 2 * kTopkWarps, "two tokens per warp");
+// TPW tokens per warp (kRouteTokensPerBlock / TPW warps per block): four for
+// narrow rows, whose warp reductions interleave; two for wide rows, where
+// more would not fit in the registers.
+template <int EPL>
+constexpr int topk_tokens_per_warp() { return EPL <= 4 ? 4 : 2; }
 
-template <int EPL>  // logits per lane: E <= 32 * EPL
-__global__ void __launch_bounds__(kTopkThreads) route_topk_rank_kernel(
+template <int EPL, int TPW = topk_tokens_per_warp<EPL>()>  // logits per lane: E <= 32 * EPL
+__global__ void __launch_bounds__(32 * (kRouteTokensPerBlock / TPW)) route_topk_rank_kernel(
     const float* __restrict__ logits, int T, int E, int k, int renormalize,
     int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
     int32_t* __restrict__ local_rank, int32_t* __restrict__ block_hist) {
+  constexpr int WARPS = kRouteTokensPerBlock / TPW;
   // s_mask[e] bit tl: token tl of this block chose expert e.  A token's k
   // experts are distinct, so its rank among the block's rows of expert e in
   // flat (token) order is the number of earlier tokens with that bit set.
@@ -56,32 +59,31 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_rank_kernel(
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_mask[e] = 0ull;
   __syncthreads();
 
-  // the warp's two tokens go through the top-k together (one at a time for
-  // wide rows, where two would not fit in the registers of 1024 threads)
-  const float* rows[2];
+  // the warp's tokens warp, warp + WARPS, ... go through the top-k NT at a
+  // time (all together for narrow rows)
+  constexpr int NT = EPL <= 4 ? TPW : 1;
+  int chosen[TPW];
+  float ws[TPW];
 #pragma unroll
-  for (int it = 0; it < 2; ++it) {
-    const int tl = warp + kTopkWarps * it;
-    rows[it] = tl < nt ? logits + (int64_t)(t0 + tl) * E : nullptr;
-  }
-  int chosen[2];
-  float vals[2], ws[2];
-  if constexpr (EPL <= 4) {
-    warp_topk_softmax<EPL, 2>(rows, E, k, renormalize != 0, lane, chosen, vals, ws);
-  } else {
+  for (int g = 0; g < TPW / NT; ++g) {
+    const float* rows[NT];
 #pragma unroll
-    for (int it = 0; it < 2; ++it) {
-      const float* r1[1] = {rows[it]};
-      int c1[1];
-      float v1[1], w1[1];
-      warp_topk_softmax<EPL, 1>(r1, E, k, renormalize != 0, lane, c1, v1, w1);
-      chosen[it] = c1[0];
-      ws[it] = w1[0];
+    for (int n = 0; n < NT; ++n) {
+      const int tl = warp + WARPS * (g * NT + n);
+      rows[n] = tl < nt ? logits + (int64_t)(t0 + tl) * E : nullptr;
+    }
+    int c[NT];
+    float v[NT], w[NT];
+    warp_topk_softmax<EPL, NT>(rows, E, k, renormalize != 0, lane, c, v, w);
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      chosen[g * NT + n] = c[n];
+      ws[g * NT + n] = w[n];
     }
   }
 #pragma unroll
-  for (int it = 0; it < 2; ++it) {
-    const int tl = warp + kTopkWarps * it;
+  for (int it = 0; it < TPW; ++it) {
+    const int tl = warp + WARPS * it;
     if (tl < nt && lane < k) {
       const int64_t f = (int64_t)(t0 + tl) * k + lane;
       topk_ids[f] = chosen[it];
@@ -91,8 +93,8 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_rank_kernel(
   }
   __syncthreads();
 #pragma unroll
-  for (int it = 0; it < 2; ++it) {
-    const int tl = warp + kTopkWarps * it;
+  for (int it = 0; it < TPW; ++it) {
+    const int tl = warp + WARPS * it;
     if (tl < nt && lane < k)
       local_rank[(int64_t)(t0 + tl) * k + lane] =
           __popcll(s_mask[chosen[it]] & ((1ull << tl) - 1ull));
@@ -116,7 +118,19 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int32_t* __restrict__ 
   const int b0 = g * per, b1 = min(nb, b0 + per);
   const bool active = g < G;
   constexpr int R = 8;  // independent loads in flight per thread
-  if (active) {
+  // up to RR blocks per thread: one round of loads, kept in registers for the
+  // second pass (the common case: nb <= RR * G)
+  constexpr int RR = 32;
+  const bool one_round = b1 - b0 <= RR;
+  int keep[RR];
+  if (active && one_round) {
+    int s = 0;
+#pragma unroll
+    for (int r = 0; r < RR; ++r) keep[r] = b0 + r < b1 ? hist[(int64_t)(b0 + r) * E + e] : 0;
+#pragma unroll
+    for (int r = 0; r < RR; ++r) s += keep[r];
+    s_part[g * E + e] = s;
+  } else if (active) {
     int s = 0;
     for (int c = b0; c < b1; c += R) {
       int vals[R];
@@ -138,7 +152,14 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int32_t* __restrict__ 
     s_tot[threadIdx.x] = run;
   }
   __syncthreads();
-  if (active) {
+  if (active && one_round) {
+    int run = s_part[g * E + e];
+#pragma unroll
+    for (int r = 0; r < RR; ++r) {
+      if (b0 + r < b1) hist[(int64_t)(b0 + r) * E + e] = run;
+      run += keep[r];
+    }
+  } else if (active) {
     int run = s_part[g * E + e];
     for (int c = b0; c < b1; c += R) {
       int vals[R];
@@ -297,7 +318,8 @@ template <int EPL>
 static void launch_topk(int nb, size_t smem, cudaStream_t stream, const float* logits, int T,
                         int E, int k, int renorm, int32_t* ids, float* w, int32_t* rank,
                         int32_t* hist) {
-  route_topk_rank_kernel<EPL><<<nb, kTopkThreads, smem, stream>>>(logits, T, E, k, renorm, ids,
+  constexpr int threads = 32 * (kRouteTokensPerBlock / topk_tokens_per_warp<EPL>());
+  route_topk_rank_kernel<EPL><<<nb, threads, smem, stream>>>(logits, T, E, k, renorm, ids,
                                                                    w, rank, hist);
 }
 
