@@ -108,7 +108,7 @@ def gemm_src_hash():
 
 
 class ClockSampler:
-    """nvidia-smi clocks/throttle sampling (every 50 ms) around the timed
+    """nvidia-smi clocks/throttle sampling (every 20 ms) around the timed
     region; `mark_start` / `mark_end` bracket the region and `summary` keeps
     the samples that arrived inside it."""
 
@@ -133,7 +133,7 @@ class ClockSampler:
             try:
                 self.proc = subprocess.Popen(
                     ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
-                     "--format=csv,noheader,nounits", "-lms", "50"],
+                     "--format=csv,noheader,nounits", "-lms", "20"],
                     stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             except OSError:
                 self.proc = None
@@ -181,7 +181,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm), "interval_ms": 50,
+                "samples": len(sm), "interval_ms": 20,
                 "region_s": round(self.t1 - self.t0, 3)}
 
 
