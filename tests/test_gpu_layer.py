@@ -40,6 +40,29 @@ def test_layer_matches_oracle(mm, cfg):
     assert rel_frob(bits16(out), ref["out"]) <= OUT_REL_FROB
 
 
+@pytest.mark.parametrize("mode", [0, 1])
+def test_layer_at_the_expert_limit(mm, mode):
+    """E = 256 (the layer's maximum) with top-8 over a ragged batch: many
+    experts hold 0-3 rows, the tile schedule spans every lane's 8 experts."""
+    T, H, E, k, I = 300, 256, 256, 8, 128
+    g = torch.Generator(device=DEV).manual_seed(256)
+    x = torch.randn(T, H, generator=g, device=DEV).to(torch.bfloat16)
+    logits = torch.randn(T, E, generator=g, device=DEV)
+    w13 = (torch.randn(E, 2 * I, H, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    w2 = (torch.randn(E, H, I, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    layer = mm.MXFP8MoELayer.from_bf16(w13, w2, k)
+    mm.set_gemm_2sm(mode)
+    try:
+        out = layer(x, logits)
+        torch.cuda.synchronize()
+    finally:
+        mm.set_gemm_2sm("auto")
+    assert mm.device_status() == 0
+    ref = moe.moe_forward(bits16(x), logits.cpu().numpy(), u8(layer.w13q), u8(layer.w13s),
+                          u8(layer.w2q), u8(layer.w2s), k, I)
+    assert rel_frob(bits16(out), ref["out"]) <= OUT_REL_FROB
+
+
 def test_layer_prefill_stagewise(mm):
     """16K-token prefill: route parity in full, GEMM parity on sampled experts
     (in test_gpu_gemm), finalize parity in full from the device's own y."""

@@ -142,7 +142,9 @@ def test_route_quant_skewed_load(mm, T):
 
 @pytest.mark.parametrize("T,H,E,k,renorm", [(1, 32, 1, 1, True), (65, 96, 5, 3, False),
                                              (130, 512, 40, 8, True), (7, 2048, 128, 8, False),
-                                             (300, 64, 256, 32, True), (64, 256, 8, 8, True)])
+                                             (300, 64, 256, 32, True), (64, 256, 8, 8, True),
+                                             (200, 64, 600, 32, True), (130, 96, 1000, 4, False),
+                                             (70, 64, 1024, 8, True)])
 def test_route_quant_edge_shapes(mm, T, H, E, k, renorm):
     g = torch.Generator(device=DEV).manual_seed(T * 7 + E)
     x = torch.randn(T, H, generator=g, device=DEV).to(torch.bfloat16)
