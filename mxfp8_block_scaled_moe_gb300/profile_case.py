@@ -7,7 +7,8 @@
 Builds one layer's inputs (default: the 16K-token Qwen3-30B-A3B-shaped
 prefill), runs the routing step once, then launches the chosen kernel
 ``--iters`` times.  ``--kernel linear`` takes a dense-linear shape instead and
-runs the whole linear call (activation quant + GEMM) ``--iters`` times.  It holds about 1-2 GB on the device, more than the L2, so
+runs the whole linear call (activation quant + GEMM) ``--iters`` times;
+``--kernel layer --fmt w4a8|w4a4`` runs the MXFP4-weight layers.  It holds about 1-2 GB on the device, more than the L2, so
 DRAM counters are meaningful, and it launches only a few kernels before the
 captured ones.
 """
@@ -30,6 +31,8 @@ def main():
                              "router"])
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--gemm-2sm", default="auto", choices=["0", "1", "auto"])
+    ap.add_argument("--fmt", default="w8a8", choices=["w8a8", "w4a8", "w4a4"],
+                    help="weight/activation formats of --kernel layer")
     args = ap.parse_args()
     dev = torch.device("cuda", 0)
     mm.set_gemm_2sm(args.gemm_2sm)
@@ -63,7 +66,11 @@ def main():
                 mm.mx_quantize_3d(inp["w13"])
             torch.cuda.synchronize()
             return
-        layer = mm.MXFP8MoELayer.from_bf16(inp["w13"], inp["w2"], shape.k)
+        cls = {"w8a8": mm.MXFP8MoELayer, "w4a8": mm.W4A8MoELayer,
+               "w4a4": mm.W4A4MoELayer}[args.fmt]
+        if args.fmt != "w8a8" and args.kernel != "layer":
+            raise SystemExit("--fmt applies to --kernel layer only")
+        layer = cls.from_bf16(inp["w13"], inp["w2"], shape.k)
         del inp["w13"], inp["w2"]
     x, logits = inp["x"], inp["logits"]
     r = mm.moe_route_quant_mxfp8(x, logits, shape.k)
