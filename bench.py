@@ -38,13 +38,14 @@ WORKLOAD = "qwen3_30b_prefill"
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0   # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+FP4_OVER_BF16 = 6.0   # nominal dense ratio (13.5 / 2.25 PFLOP/s): e2m1 x e2m1 MMAs
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one grouped GEMM1 launch on
 # the bench workload (profiles/gemm1_swiglu_quant_qwen3_30b_prefill.md, the
 # DRAM-bytes capture at its end), keyed
 # by the hash of the sources it was captured from
 NCU_TRAFFIC = {"a9ec3d6a1d8bbad4": 786553600, "64d58b0d55536f8c": 786384128,
-               "f21fe81032a4b103": 786399488}
+               "f21fe81032a4b103": 786399488, "afe529db44d76b76": 787179008}
 
 
 def max_over_ranks(torch, dist, ms, world, device):
@@ -228,12 +229,13 @@ LINEAR_BENCH = ("qwen3vl_vision_fc2", "qwen3vl_vision_fc1", "qwen3_8b_down_prefi
                 "qwen3_8b_gate_up_prefill", "qwen3_8b_down_decode")
 
 
-def dense_linear_bench(torch, mm, workloads, dev, flush, stream, fp8_peak, hbm, fp4=False):
-    """The dense MXFP8 linear on the pages' dense shapes: per call (L2
-    flushed), the activation quant and the GEMM from the library's event
-    profiler, GEMM TFLOP/s against the MXFP8 peak (weight GB/s against HBM
-    for the 32-token decode), and the vendor library's MXFP8 GEMM on the same
-    shape with unit scales (GEMM only; None where it rejects the shape)."""
+def dense_linear_bench(torch, mm, workloads, dev, flush, stream, peak, hbm, fp4=False):
+    """The dense MXFP8 (or, fp4, W4A4) linear on the pages' dense shapes: per
+    call (L2 flushed), the activation quant and the GEMM from the library's
+    event profiler, GEMM TFLOP/s against the MXFP8 (MXFP4) peak `peak` (weight
+    GB/s against HBM for the 32-token decode), and the vendor library's MXFP8
+    GEMM on the same shape with unit scales (GEMM only; None where it rejects
+    the shape)."""
     out = {}
     for name in LINEAR_BENCH:
         shape = workloads.LINEAR_CONFIGS[name]
@@ -269,7 +271,8 @@ def dense_linear_bench(torch, mm, workloads, dev, flush, stream, fp8_peak, hbm, 
         ent = {"M": M, "N": N, "K": K, "scales_per_row": -(-K // 32),
                "ms": round(t_ms, 4), "act_quant_ms": round(q_ms, 4), "gemm_ms": round(g_ms, 4),
                "gemm_TFLOP/s": round(flops / (g_ms / 1e3) / 1e12, 1),
-               "gemm_frac_fp8_peak": round(flops / (g_ms / 1e3) / 1e12 / fp8_peak, 3),
+               ("gemm_frac_fp4_peak" if fp4 else "gemm_frac_fp8_peak"):
+                   round(flops / (g_ms / 1e3) / 1e12 / peak, 3),
                "call_TFLOP/s": round(flops / (t_ms / 1e3) / 1e12, 1)}
         if M <= 128:
             ent["gemm_weight_GB/s"] = round(wbytes / (g_ms / 1e3) / 1e9, 1)
@@ -622,12 +625,20 @@ def main():
         d44_ms, _ = layer_ms(layer44, x[:32], logits[:32], 50)
         w4a4 = {
             "weights": "MXFP4 (packed e2m1 + e8m0 block-32 scales); both grouped GEMMs' inputs "
-                       "MXFP4-quantized on the device; e2m1 x e2m1 MMAs of kind::mxf8f6f4",
+                       "MXFP4-quantized on the device; e2m1 x e2m1 MMAs of kind::mxf4 on packed "
+                       "operands",
             "prefill": {"tokens_per_s": round(T / (p_ms / 1e3), 1), "ms_per_step": round(p_ms, 4),
-                        "gemm1_TFLOP/s": round(2.0 * T * k * 2 * I * H / (p_g1 / 1e3) / 1e12, 1)},
+                        "gemm1_TFLOP/s": round(2.0 * T * k * 2 * I * H / (p_g1 / 1e3) / 1e12, 1),
+                        "gemm1_frac_fp4_peak": round(2.0 * T * k * 2 * I * H / (p_g1 / 1e3) / 1e12
+                                                     / (fp8_peak / FP8_OVER_BF16 * FP4_OVER_BF16),
+                                                     3)},
             "decode_T32": {"ms": round(d44_ms, 4)},
-            "dense_linear": (dense_linear_bench(torch, mm, workloads, dev, flush, stream, fp8_peak,
-                                                hbm, fp4=True) if not args.no_linear else None),
+            "dense_linear": (dense_linear_bench(torch, mm, workloads, dev, flush, stream,
+                                                fp8_peak / FP8_OVER_BF16 * FP4_OVER_BF16, hbm,
+                                                fp4=True) if not args.no_linear else None),
+            "fp4_peak": {"TFLOP/s": round(fp8_peak / FP8_OVER_BF16 * FP4_OVER_BF16, 1),
+                         "source": f"{peaks['source']}: bf16 dense burst x {FP4_OVER_BF16} "
+                                   "(nominal fp4/bf16 ratio)"},
             "parity": "tests/test_gpu_w4a4.py (exact W4A4 GEMM pins; layer vs oracle; sampled "
                       "prefill tokens vs oracle)",
         }

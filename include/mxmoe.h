@@ -360,8 +360,8 @@ mxmoe_status mxfp8_linear_mma_scales(const uint16_t* x, const uint8_t* wq, const
  *          aligned; ws e8m0 [N, K/32] (mxfp4_linear) or its MMA layout
  *          (mxfp4_linear_mma_scales, 16-byte aligned)
  *   x, out, workspace as mxfp8_linear (mxfp8_linear_workspace_size bytes).
- * Requires K % 128 == 0 (the unpacking TMA of packed e2m1 rows needs a row
- * length that is a multiple of 128 elements) and N % 16 == 0.
+ * Requires K % 128 == 0 (each 256-element k-slice of the packed e2m1 x e2m1
+ * GEMM holds one or two whole 128-element scale chunks) and N % 16 == 0.
  */
 mxmoe_status mxfp4_linear(const uint16_t* x, const uint8_t* wp, const uint8_t* ws, int64_t M,
                           int64_t N, int64_t K, uint16_t* out, void* workspace, size_t ws_bytes,
@@ -408,8 +408,8 @@ mxmoe_status moe_forward_w4a8_mma_scales(const uint16_t* x, const float* logits,
  * clamp(floor(log2 amax) - 2, -127, 127) + 127, e2m1 round-to-nearest-even
  * saturating at +-6, element 2i in the low nibble of byte i); gmm1's epilogue
  * requantizes the SwiGLU output (rounded to fp32) to MXFP4 by the same rule;
- * both grouped GEMMs run e2m1 x e2m1 block-scaled tcgen05 MMAs
- * (kind::mxf8f6f4).  Arguments, weights and workspace as
+ * both grouped GEMMs run e2m1 x e2m1 block-scaled tcgen05 MMAs on packed
+ * operands (kind::mxf4, K = 64 per instruction).  Arguments, weights and workspace as
  * moe_forward_w4a8_mma_scales.
  */
 mxmoe_status moe_forward_w4a4_mma_scales(const uint16_t* x, const float* logits,

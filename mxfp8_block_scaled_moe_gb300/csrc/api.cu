@@ -533,8 +533,8 @@ size_t mxfp8_linear_workspace_size(int64_t M, int64_t N, int64_t K) {
 }
 
 // fp4: W4A4 (packed MXFP4 weights [N, K/2], 32-byte aligned; activations
-// quantized to MXFP4).  K % 128 == 0: the unpacking tensor maps of packed
-// e2m1 operands need a row length that is a multiple of 128 elements.
+// quantized to MXFP4), K % 128 == 0: every k-slice of the packed GEMM holds
+// one or two whole 128-element scale chunks.
 static mxmoe_status linear_impl(const uint16_t* x, const uint8_t* wq, const uint8_t* ws,
                                 bool ws_tiled, int64_t M, int64_t N, int64_t K, uint16_t* out,
                                 void* workspace, size_t ws_bytes, void* stream, bool fp4 = false) {
@@ -568,8 +568,11 @@ static mxmoe_status linear_impl(const uint16_t* x, const uint8_t* wq, const uint
   err = launch_mx_quantize_tiled(x, M, K, xq, xs, offs, st, fp4);
   if (err != cudaSuccess) return MXMOE_ERR_CUDA;
   prof.mark(2);
+  // the workspace holds L.ksplit partial planes, at least the W4A4 count
+  const int ksplit = fp4 ? gemm_bf16_ksplit(M, (int)N, (int)K, true) : L.ksplit;
+  if (ksplit > L.ksplit) return MXMOE_ERR_WORKSPACE;
   err = launch_gemm_bf16(xq, xs, wq, wst, offs, M, 1, (int)K, (int)N, out, st, true, fp4 ? 2 : 0,
-                         L.ksplit, L.ksplit > 1 ? (float*)(base + L.partial) : nullptr);
+                         ksplit, ksplit > 1 ? (float*)(base + L.partial) : nullptr);
   if (err != cudaSuccess) return MXMOE_ERR_CUDA;
   for (int i = 3; i < kProfEvents; ++i) prof.mark(i);
   prof.done();

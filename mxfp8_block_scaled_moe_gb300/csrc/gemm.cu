@@ -23,6 +23,9 @@
 //               tcgen05.mma.kind::mxf8f6f4.block_scale (M=128, N=BN, K=32,
 //               UE8M0 scales, one scale per 32 K-elements) accumulate the
 //               fp32 tile in tensor memory; tcgen05.commit frees the stage.
+//               W4A4 takes kind::mxf4 on packed e2m1 operands instead: a
+//               128-byte stage then holds 256 K elements, four K=64 MMAs
+//               with two scales per row each (scale_vec::2X).
 //   warps 6-21  epilogue: tcgen05.ld the accumulator into registers (one
 //               thread per row and a quarter of the columns), release it to the
 //               MMA warp, then SwiGLU + MX requant (gmm1) or bf16 rounding
@@ -89,6 +92,15 @@ __global__ void __launch_bounds__(THREADS1, 1)
   using L = Layout1<BN>;
   constexpr int STAGES = L::S;
   constexpr bool kFp4B = kFmt != FMT_W8A8, kFp4A = kFmt == FMT_W4A4;
+  // W4A4: kind::mxf4 on packed operands, so a 128-byte k-slice holds 256
+  // K elements (two 128-element scale chunks) and takes four K = 64 MMAs
+  constexpr bool kPacked = kFmt == FMT_W4A4;
+  constexpr int CH = kPacked ? 2 : 1;          // scale chunks per k-slice
+  constexpr int SEGK = SEG / CH;               // k-slices per scale segment
+  constexpr int SLICE_COLS = SF_COLS_PER_STAGE * CH;  // TMEM scale columns per k-slice
+  constexpr int MPC = (BK / 32) / CH;          // MMAs per scale chunk
+  static_assert(!kPacked || kTiledSF, "packed operands take tiled scales");
+  static_assert(SEGK * SLICE_COLS == SEG_COLS, "segment columns");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
@@ -144,7 +156,9 @@ __global__ void __launch_bounds__(THREADS1, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
-  const int KT = (p.K + BK - 1) / BK;  // a partial last K slice is zero-filled by TMA
+  // k-slices; a partial last slice is zero-filled by TMA
+  const int KT = (p.K + BK * CH - 1) / (BK * CH);
+  const int KTC = (p.K + BK - 1) / BK;  // 128-element scale chunks per row block
   const int K32 = p.K / 32;
   const int KSPL = kSplit ? p.ksplit : 1;
   const int kper = (KT + KSPL - 1) / KSPL;  // K slices per split (every split non-empty)
@@ -179,19 +193,21 @@ __global__ void __launch_bounds__(THREADS1, 1)
       const int64_t brow = (int64_t)e * p.Nw;
       const int64_t bh0 = kSwiglu ? brow + (int64_t)nt * (BN / 2) : brow + (int64_t)nt * BN;
       const int64_t bh1 = brow + p.n_out + (int64_t)nt * (BN / 2);
-      const int kt0 = k0 + sg * SEG, len = min(SEG, k1 - kt0);
+      const int kt0 = k0 + sg * SEGK, len = min(SEGK, k1 - kt0);
+      // the segment's scale chunks (a packed last k-slice may hold only one)
+      const int c0 = kt0 * CH, nch = min(len * CH, KTC - c0);
       const uint32_t sA = sbase + L::OFF_SFA + b * L::SFA_SEG;
       const uint32_t sB = sbase + L::OFF_SFB + b * L::SFB_SEG;
       if (kTiledSF) {
         if (lane == 0) {
-          mbar_arrive_expect_tx(bar_sfs_full(b), (uint32_t)((1 + BN / 128) * len * 512));
-          bulk_copy_g2s(sA, p.sfa + ((int64_t)(s_mtb[e] + mt) * KT + kt0) * 512,
-                        (uint32_t)(len * 512), bar_sfs_full(b));
+          mbar_arrive_expect_tx(bar_sfs_full(b), (uint32_t)((1 + BN / 128) * nch * 512));
+          bulk_copy_g2s(sA, p.sfa + ((int64_t)(s_mtb[e] + mt) * KTC + c0) * 512,
+                        (uint32_t)(nch * 512), bar_sfs_full(b));
 #pragma unroll
           for (int c = 0; c < BN / 128; ++c) {
             const int64_t wrow = kSwiglu ? (c == 0 ? bh0 : bh1) : bh0 + 128 * c;
-            bulk_copy_g2s(sB + c * SEG * 512, p.sfb + ((wrow >> 7) * KT + kt0) * 512,
-                          (uint32_t)(len * 512), bar_sfs_full(b));
+            bulk_copy_g2s(sB + c * SEG * 512, p.sfb + ((wrow >> 7) * KTC + c0) * 512,
+                          (uint32_t)(nch * 512), bar_sfs_full(b));
           }
         }
       } else {
@@ -224,16 +240,16 @@ __global__ void __launch_bounds__(THREADS1, 1)
     for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
       int e, mt, nt, ks, k0, k1;
       tile_at(tile, e, mt, nt, ks, k0, k1);
-      const int nseg = (k1 - k0 + SEG - 1) / SEG;  // scale segments of this tile
+      const int nseg = (k1 - k0 + SEGK - 1) / SEGK;  // scale segments of this tile
       const int64_t row0 = s_off[e] + (int64_t)mt * BM;
       const int64_t brow = (int64_t)e * p.Nw;
       // B tile halves: gmm1 = gate rows | up rows; gmm2 = one BN-row box
       const int64_t bh0 = kSwiglu ? brow + (int64_t)nt * (BN / 2) : brow + (int64_t)nt * BN;
       const int64_t bh1 = brow + p.n_out + (int64_t)nt * (BN / 2);
       for (int kt = k0; kt < k1; ++kt) {
-        if ((kt - k0) % SEG == 0) {
+        if ((kt - k0) % SEGK == 0) {
           // the next segment's scales: later in this tile, or the next tile's first
-          const int sg = (kt - k0) / SEG;
+          const int sg = (kt - k0) / SEGK;
           const int ntile = sg + 1 < nseg ? tile : tile + (int)gridDim.x;
           if (ntile < total_tiles && !load_scales(g + 1, ntile, sg + 1 < nseg ? sg + 1 : 0)) {
             ok = false;
@@ -249,9 +265,10 @@ __global__ void __launch_bounds__(THREADS1, 1)
         const uint32_t sA = sbase + L::OFF_A + stage * L::A_BYTES;
         const uint32_t sB = sbase + L::OFF_B + stage * L::B_BYTES;
         if (lane == 0) {
-          // packed FP4 B counts its global (packed) bytes: half its smem footprint
-          mbar_arrive_expect_tx(bar_full(stage), (kFp4A ? L::A_BYTES / 2 : L::A_BYTES) +
-                                                     (kFp4B ? L::B_BYTES / 2 : L::B_BYTES));
+          // W4A8's unpacked FP4 B counts its global (packed) bytes: half its
+          // smem footprint; packed W4A4 operands land byte for byte
+          mbar_arrive_expect_tx(bar_full(stage),
+                                L::A_BYTES + (kFp4B && !kPacked ? L::B_BYTES / 2 : L::B_BYTES));
           tma_load_2d(sA, &tmA, kt * BK, (int)row0, bar_full(stage));
           if (kSwiglu) {
             tma_load_2d(sB, &tmB, kt * BK, (int)bh0, bar_full(stage));
@@ -285,7 +302,8 @@ __global__ void __launch_bounds__(THREADS1, 1)
       int g = 0;
       bool ok = true;
       bool issued = false;
-      constexpr uint32_t IDESC = make_idesc(BM, BN, kFp4B, kFp4A);
+      constexpr uint32_t IDESC =
+          kPacked ? make_idesc_mxf4(BM, BN) : make_idesc(BM, BN, kFp4B);
       for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
         int e, mt, nt, ks, k0, k1;
         tile_at(tile, e, mt, nt, ks, k0, k1);
@@ -295,7 +313,7 @@ __global__ void __launch_bounds__(THREADS1, 1)
         }
         tc_fence_after();
         for (int kt = k0; kt < k1; ++kt) {
-          const int i = (kt - k0) % SEG;
+          const int i = (kt - k0) % SEGK;
           const int b = g & 1;
           if (i == 0) {
             // this segment's scales are in TMEM buffer b
@@ -312,19 +330,29 @@ __global__ void __launch_bounds__(THREADS1, 1)
           tc_fence_after();
           const uint32_t sA = sbase + L::OFF_A + stage * L::A_BYTES;
           const uint32_t sB = sbase + L::OFF_B + stage * L::B_BYTES;
-          const uint32_t t_sfa = tmem + SF_COL0 + b * SEG_COLS + i * 16;
-          const uint32_t t_sfb = t_sfa + 4;
+          // k-slice i's scale columns: A chunk j at 4j, B chunk j (BN / 32
+          // columns, 128-row blocks side by side) at 4 CH + (BN / 32) j
+          const uint32_t t_sf = tmem + SF_COL0 + b * SEG_COLS + i * SLICE_COLS;
           const uint64_t adesc = make_sdesc(sA, 16, 1024, 2);
           const uint64_t bdesc = make_sdesc(sB, 16, 1024, 2);
 #pragma unroll
           for (int kk = 0; kk < BK / 32; ++kk) {
-            const uint32_t idesc = IDESC | ((uint32_t)kk << 29) | ((uint32_t)kk << 4);
-            tc_mma_mxf8(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, t_sfa, t_sfb,
-                        ((kt - k0) | kk) != 0 ? 1u : 0u);
+            // 32 bytes of each row per MMA; a packed K tail of 128 elements
+            // takes the first two only (the slice's second chunk has no scales)
+            if (kPacked && (kt * (BK / 32) + kk) * 64 >= p.K) break;
+            const int j = kk / MPC;
+            const uint32_t sfid = (uint32_t)((kk % MPC) * CH);
+            const uint32_t idesc = IDESC | (sfid << 29) | (sfid << 4);
+            const uint32_t t_sfa = t_sf + 4 * j, t_sfb = t_sf + 4 * CH + (BN / 32) * j;
+            const uint32_t acc = ((kt - k0) | kk) != 0 ? 1u : 0u;
+            if constexpr (kPacked)
+              tc_mma_mxf4(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, t_sfa, t_sfb, acc);
+            else
+              tc_mma_mxf8(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, t_sfa, t_sfb, acc);
           }
           issued = true;
           tc_commit(bar_empty(stage));
-          if (i == SEG - 1 || kt == k1 - 1) {
+          if (i == SEGK - 1 || kt == k1 - 1) {
             tc_commit(bar_sft_free(b));  // the segment's scales may be overwritten
             ++g;
           }
@@ -356,7 +384,7 @@ __global__ void __launch_bounds__(THREADS1, 1)
     for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
       int e, mt, nt, ks, k0, k1;
       tile_at(tile, e, mt, nt, ks, k0, k1);
-      const int nseg = (k1 - k0 + SEG - 1) / SEG;
+      const int nseg = (k1 - k0 + SEGK - 1) / SEGK;
       for (int sg = 0; sg < nseg; ++sg, ++g) {
         const int b = g & 1;
         const uint32_t par = (uint32_t)(g >> 1) & 1u;
@@ -367,16 +395,23 @@ __global__ void __launch_bounds__(THREADS1, 1)
           ok = false;
           break;
         }
-        const int len = min(SEG, k1 - (k0 + sg * SEG));
+        const int len = min(SEGK, k1 - (k0 + sg * SEGK));
         const uint8_t* sfa_s = smem + L::OFF_SFA + b * L::SFA_SEG;
         const uint8_t* sfb_s = smem + L::OFF_SFB + b * L::SFB_SEG;
+        // (a chunk past K is never copied in; its columns are never read)
         for (int i = 0; i < len; ++i) {
-          const uint32_t col = SF_COL0 + b * SEG_COLS + i * 16;
-          tmem_st_4(t_q + col, *reinterpret_cast<const uint4*>(sfa_s + i * 512 + lane * 16));
+          const uint32_t col = SF_COL0 + b * SEG_COLS + i * SLICE_COLS;
 #pragma unroll
-          for (int c = 0; c < BN / 128; ++c)
-            tmem_st_4(t_q + col + 4 + 4 * c, *reinterpret_cast<const uint4*>(
-                                                  sfb_s + c * SEG * 512 + i * 512 + lane * 16));
+          for (int j = 0; j < CH; ++j) {
+            const int ch = i * CH + j;
+            tmem_st_4(t_q + col + 4 * j,
+                      *reinterpret_cast<const uint4*>(sfa_s + ch * 512 + lane * 16));
+#pragma unroll
+            for (int c = 0; c < BN / 128; ++c)
+              tmem_st_4(t_q + col + 4 * CH + (BN / 32) * j + 4 * c,
+                        *reinterpret_cast<const uint4*>(sfb_s + c * SEG * 512 + ch * 512 +
+                                                        lane * 16));
+          }
         }
         tmem_st_wait();
         tc_fence_before();
@@ -444,9 +479,11 @@ static cudaError_t launch_single(const uint8_t* a, const uint8_t* sfa, const uin
   }
   CUtensorMap tmA, tmB;
   const uint32_t b_box_rows = kSwiglu ? BN / 2 : BN;
-  if (!make_map(&tmA, a, (uint64_t)K, (uint64_t)M, BK, BM, kFmt == FMT_W4A4))
+  // W4A4: packed bytes as they are (K / 2 per row); W4A8: B unpacked
+  const uint64_t inner = kFmt == FMT_W4A4 ? (uint64_t)K / 2 : (uint64_t)K;
+  if (!make_map(&tmA, a, inner, (uint64_t)M, BK, BM))
     return cudaErrorInvalidValue;
-  if (!make_map(&tmB, b, (uint64_t)K, (uint64_t)E * Nw, BK, b_box_rows, kFmt != FMT_W8A8))
+  if (!make_map(&tmB, b, inner, (uint64_t)E * Nw, BK, b_box_rows, kFmt == FMT_W4A8))
     return cudaErrorInvalidValue;
   Params p;
   p.sfa = sfa;
@@ -563,10 +600,10 @@ static cudaError_t launch_bf16_fmt(const uint8_t* aq, const uint8_t* as, const u
   return cudaGetLastError();
 }
 
-int gemm_bf16_ksplit(int64_t M, int N, int K) {
+int gemm_bf16_ksplit(int64_t M, int N, int K, bool packed_fp4) {
   const int64_t n_tiles = ceil_div(N, ceil_div(N, 128) % 2 == 0 ? 256 : 128);
   const int64_t tiles = ceil_div(M, gemm::BM) * n_tiles;
-  const int KT = (int)ceil_div(K, 128);
+  const int KT = (int)ceil_div(K, packed_fp4 ? 256 : 128);  // the kernel's k-slices
   const int sms = num_sms();
   if (tiles * 2 > sms) return 1;  // enough tiles to fill the GPU
   int S = (int)std::min<int64_t>({(int64_t)sms / tiles, (int64_t)KT / 4, 32});

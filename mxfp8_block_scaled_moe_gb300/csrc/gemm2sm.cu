@@ -104,6 +104,17 @@ __device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, 
   }
   return true;
 }
+__device__ __forceinline__ void tc2_mma_mxf4(uint32_t d, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X"
+      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+      : "memory");
+}
 __device__ __forceinline__ void tc2_mma_mxf8(uint32_t d, uint64_t adesc, uint64_t bdesc,
                                              uint32_t idesc, uint32_t sfa, uint32_t sfb,
                                              uint32_t accumulate) {
@@ -133,6 +144,14 @@ __global__ void __launch_bounds__(THREADS1, 1)
   constexpr int STAGES = L::S;
   constexpr int BN = 256;
   constexpr bool kFp4B = kFmt != FMT_W8A8, kFp4A = kFmt == FMT_W4A4;
+  // W4A4: kind::mxf4 on packed operands (as in the 1-SM kernel): 256 K
+  // elements and two scale chunks per k-slice, four K = 64 MMAs
+  constexpr bool kPacked = kFmt == FMT_W4A4;
+  constexpr int CH = kPacked ? 2 : 1;
+  constexpr int SEGK = SEG2 / CH;
+  constexpr int SLICE_COLS = SF_COLS_PER_STAGE * CH;
+  constexpr int MPC = (BK / 32) / CH;
+  static_assert(SEGK * SLICE_COLS == SEG2_COLS, "segment columns");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
@@ -195,8 +214,10 @@ __global__ void __launch_bounds__(THREADS1, 1)
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
   const int total_units = s_ts[E];
-  const int KT = (p.K + BK - 1) / BK;  // a partial last K slice is zero-filled by TMA
-  const int nseg = (KT + SEG2 - 1) / SEG2;  // scale segments per unit
+  // k-slices; a partial last slice is zero-filled by TMA
+  const int KT = (p.K + BK * CH - 1) / (BK * CH);
+  const int KTC = (p.K + BK - 1) / BK;  // 128-element scale chunks per row block
+  const int nseg = (KT + SEGK - 1) / SEGK;  // scale segments per unit
   // the leader's barriers as seen from this CTA
   const uint32_t lead_full0 = mapa_cluster(bar_full(0), 0);
   const uint32_t lead_sftr0 = mapa_cluster(bar_sft_ready(0), 0);
@@ -229,15 +250,18 @@ __global__ void __launch_bounds__(THREADS1, 1)
         unit_rows(unit, e, mt, nt, bh0, bh1);
         // tiled A scales: the m-tile's block (a CTA without rows reads its expert's last block)
         const int64_t a_blk = min(s_mtb[e] + mt, s_mtb[e + 1] - 1);
-        const int kt0 = sg * SEG2, len = min(SEG2, KT - kt0);
+        const int kt0 = sg * SEGK, len = min(SEGK, KT - kt0);
+        // the segment's scale chunks (a packed last k-slice may hold only one)
+        const int c0 = kt0 * CH, nch = min(len * CH, KTC - c0);
         const uint32_t sA = sbase + L::OFF_SFA + b * L::SFA_SEG;
         const uint32_t sB = sbase + L::OFF_SFB + b * L::SFB_SEG;
-        mbar_arrive_expect_tx(bar_sfs_full(b), (uint32_t)(3 * len * 512));
-        bulk_copy_g2s(sA, p.sfa + (a_blk * KT + kt0) * 512, (uint32_t)(len * 512), bar_sfs_full(b));
-        bulk_copy_g2s(sB, p.sfb + ((bh0 >> 7) * KT + kt0) * 512, (uint32_t)(len * 512),
+        mbar_arrive_expect_tx(bar_sfs_full(b), (uint32_t)(3 * nch * 512));
+        bulk_copy_g2s(sA, p.sfa + (a_blk * KTC + c0) * 512, (uint32_t)(nch * 512),
                       bar_sfs_full(b));
-        bulk_copy_g2s(sB + SEG2 * 512, p.sfb + ((bh1 >> 7) * KT + kt0) * 512,
-                      (uint32_t)(len * 512), bar_sfs_full(b));
+        bulk_copy_g2s(sB, p.sfb + ((bh0 >> 7) * KTC + c0) * 512, (uint32_t)(nch * 512),
+                      bar_sfs_full(b));
+        bulk_copy_g2s(sB + SEG2 * 512, p.sfb + ((bh1 >> 7) * KTC + c0) * 512,
+                      (uint32_t)(nch * 512), bar_sfs_full(b));
       }
       __syncwarp();
       return true;
@@ -249,8 +273,8 @@ __global__ void __launch_bounds__(THREADS1, 1)
       unit_rows(unit, e, mt, nt, bh0, bh1);
       const int64_t row0 = s_off[e] + (int64_t)mt * BM;
       for (int kt = 0; kt < KT; ++kt) {
-        if (kt % SEG2 == 0) {
-          const int sg = kt / SEG2;
+        if (kt % SEGK == 0) {
+          const int sg = kt / SEGK;
           const int nunit = sg + 1 < nseg ? unit : unit + unit_step;
           if (nunit < total_units && !load_scales(g + 1, nunit, sg + 1 < nseg ? sg + 1 : 0)) {
             ok = false;
@@ -264,11 +288,12 @@ __global__ void __launch_bounds__(THREADS1, 1)
           break;
         }
         if (lane == 0) {
-          // packed FP4 B counts its global (packed) bytes: half its smem footprint
+          // W4A8's unpacked FP4 B counts its global (packed) bytes: half its
+          // smem footprint; packed W4A4 operands land byte for byte
           if (leader)
             mbar_arrive_expect_tx(bar_full(stage),
-                                  2 * ((kFp4A ? L::A_BYTES / 2 : L::A_BYTES) +
-                                       (kFp4B ? L::B_BYTES / 2 : L::B_BYTES)));
+                                  2 * (L::A_BYTES +
+                                       (kFp4B && !kPacked ? L::B_BYTES / 2 : L::B_BYTES)));
           const uint32_t fb = lead_full0 + 8u * stage;  // leader's full[stage]
           const uint32_t sA = sbase + L::OFF_A + stage * L::A_BYTES;
           const uint32_t sB = sbase + L::OFF_B + stage * L::B_BYTES;
@@ -300,7 +325,8 @@ __global__ void __launch_bounds__(THREADS1, 1)
       int g = 0;
       bool ok = true;
       bool issued = false;
-      constexpr uint32_t IDESC = make_idesc(2 * BM, BN, kFp4B, kFp4A);
+      constexpr uint32_t IDESC =
+          kPacked ? make_idesc_mxf4(2 * BM, BN) : make_idesc(2 * BM, BN, kFp4B);
       for (int unit = unit0; ok && unit < total_units; unit += unit_step) {
         if (!wait_bar_cluster(bar_acc_empty, acc_phase ^ 1, p.wait_limit, p.status, s_abort)) {
           ok = false;
@@ -308,7 +334,7 @@ __global__ void __launch_bounds__(THREADS1, 1)
         }
         tc_fence_after();
         for (int kt = 0; kt < KT; ++kt) {
-          const int i = kt % SEG2;
+          const int i = kt % SEGK;
           const int b = g & 1;
           // both CTAs' scales of this segment are in TMEM buffer b
           if (i == 0 && !wait_bar_cluster(bar_sft_ready(b), (uint32_t)(g >> 1) & 1u,
@@ -324,19 +350,27 @@ __global__ void __launch_bounds__(THREADS1, 1)
           tc_fence_after();
           const uint32_t sA = sbase + L::OFF_A + stage * L::A_BYTES;
           const uint32_t sB = sbase + L::OFF_B + stage * L::B_BYTES;
-          const uint32_t t_sfa = tmem + SF_COL0 + b * SEG2_COLS + i * 16;
-          const uint32_t t_sfb = t_sfa + 4;
+          // scale columns of k-slice i as in the 1-SM kernel (B chunk j:
+          // 8 columns, both 128-row blocks)
+          const uint32_t t_sf = tmem + SF_COL0 + b * SEG2_COLS + i * SLICE_COLS;
           const uint64_t adesc = make_sdesc(sA, 16, 1024, 2);
           const uint64_t bdesc = make_sdesc(sB, 16, 1024, 2);
 #pragma unroll
           for (int kk = 0; kk < BK / 32; ++kk) {
-            const uint32_t idesc = IDESC | ((uint32_t)kk << 29) | ((uint32_t)kk << 4);
-            tc2_mma_mxf8(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, t_sfa, t_sfb,
-                         (kt | kk) != 0 ? 1u : 0u);
+            if (kPacked && (kt * (BK / 32) + kk) * 64 >= p.K) break;  // packed K tail
+            const int j = kk / MPC;
+            const uint32_t sfid = (uint32_t)((kk % MPC) * CH);
+            const uint32_t idesc = IDESC | (sfid << 29) | (sfid << 4);
+            const uint32_t t_sfa = t_sf + 4 * j, t_sfb = t_sf + 4 * CH + 8 * j;
+            const uint32_t acc = (kt | kk) != 0 ? 1u : 0u;
+            if constexpr (kPacked)
+              tc2_mma_mxf4(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, t_sfa, t_sfb, acc);
+            else
+              tc2_mma_mxf8(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, t_sfa, t_sfb, acc);
           }
           issued = true;
           tc2_commit_both(bar_empty(stage));
-          if (i == SEG2 - 1 || kt == KT - 1) {
+          if (i == SEGK - 1 || kt == KT - 1) {
             tc2_commit_both(bar_sft_free(b));  // the segment's scales may be overwritten
             ++g;
           }
@@ -375,15 +409,22 @@ __global__ void __launch_bounds__(THREADS1, 1)
           ok = false;
           break;
         }
-        const int len = min(SEG2, KT - sg * SEG2);
+        const int len = min(SEGK, KT - sg * SEGK);
         const uint8_t* sfa_s = smem + L::OFF_SFA + b * L::SFA_SEG;
         const uint8_t* sfb_s = smem + L::OFF_SFB + b * L::SFB_SEG;
+        // (a chunk past K is never copied in; its columns are never read)
         for (int i = 0; i < len; ++i) {
-          const uint32_t col = SF_COL0 + b * SEG2_COLS + i * 16;
-          tmem_st_4(t_q + col, *reinterpret_cast<const uint4*>(sfa_s + i * 512 + lane * 16));
-          tmem_st_4(t_q + col + 4, *reinterpret_cast<const uint4*>(sfb_s + i * 512 + lane * 16));
-          tmem_st_4(t_q + col + 8, *reinterpret_cast<const uint4*>(sfb_s + SEG2 * 512 + i * 512 +
-                                                                    lane * 16));
+          const uint32_t col = SF_COL0 + b * SEG2_COLS + i * SLICE_COLS;
+#pragma unroll
+          for (int j = 0; j < CH; ++j) {
+            const int ch = i * CH + j;
+            tmem_st_4(t_q + col + 4 * j,
+                      *reinterpret_cast<const uint4*>(sfa_s + ch * 512 + lane * 16));
+            tmem_st_4(t_q + col + 4 * CH + 8 * j,
+                      *reinterpret_cast<const uint4*>(sfb_s + ch * 512 + lane * 16));
+            tmem_st_4(t_q + col + 4 * CH + 8 * j + 4,
+                      *reinterpret_cast<const uint4*>(sfb_s + SEG2 * 512 + ch * 512 + lane * 16));
+          }
         }
         tmem_st_wait();
         tc_fence_before();
@@ -476,9 +517,10 @@ cudaError_t launch_pair_impl(const uint8_t* a, const uint8_t* sfa, const uint8_t
   }
   if (max_clusters[dev] <= 0) return cudaErrorNotSupported;
   CUtensorMap tmA, tmB;
-  if (!make_map(&tmA, a, (uint64_t)K, (uint64_t)M, BK, BM, kFmt == FMT_W4A4))
+  const uint64_t inner = kFmt == FMT_W4A4 ? (uint64_t)K / 2 : (uint64_t)K;  // packed W4A4 bytes
+  if (!make_map(&tmA, a, inner, (uint64_t)M, BK, BM))
     return cudaErrorInvalidValue;
-  if (!make_map(&tmB, b, (uint64_t)K, (uint64_t)E * Nw, BK, 128, kFmt != FMT_W8A8))
+  if (!make_map(&tmB, b, inner, (uint64_t)E * Nw, BK, 128, kFmt == FMT_W4A8))
     return cudaErrorInvalidValue;
   Params p;
   p.sfa = sfa;

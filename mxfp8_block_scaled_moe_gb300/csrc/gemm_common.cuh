@@ -161,6 +161,20 @@ __device__ __forceinline__ void tc_mma_mxf8(uint32_t d, uint64_t adesc, uint64_t
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
       : "memory");
 }
+// kind::mxf4: packed e2m1 x e2m1 operands (two elements per byte in shared
+// memory), K = 64 per instruction, two UE8M0 scales per row (scale_vec::2X:
+// bytes id and id + 1 of the row's scale word, id = 0 or 2).
+__device__ __forceinline__ void tc_mma_mxf4(uint32_t d, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X"
+      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+      : "memory");
+}
 __device__ __forceinline__ void tmem_ld_32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -196,21 +210,28 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uin
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)swizzle << 61);
 }
 
-// Instruction descriptor of kind::mxf8f6f4 with block scaling: A and B e4m3
-// (format 0 at bits 7-9 / 10-12), both K-major, N >> 3 at bits 17-22, UE8M0
-// scale type (bit 23), M >> 4 at bits 24-28; the scale-factor byte selectors
-// (bits 29-30 for A, 4-5 for B) are or-ed in per K step.
-// Formats: 0 = e4m3, 5 = e2m1.  B is e2m1 for MXFP4 weights (W4A8, W4A4), A
-// for MXFP4 activations (W4A4).
-__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool b_fp4 = false,
-                                                  bool a_fp4 = false) {
+// Instruction descriptor of kind::mxf8f6f4 with block scaling: A e4m3
+// (format 0 at bits 7-9), B e4m3 or, for the MXFP4 weights of W4A8, e2m1
+// (format 5 at bits 10-12), both K-major, N >> 3 at bits 17-22, UE8M0 scale
+// type (bit 23), M >> 4 at bits 24-28; the scale-factor byte selectors (bits
+// 29-30 for A, 4-5 for B) are or-ed in per K step.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool b_fp4 = false) {
   return ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24) |
-         (b_fp4 ? 5u << 10 : 0u) | (a_fp4 ? 5u << 7 : 0u);
+         (b_fp4 ? 5u << 10 : 0u);
+}
+
+// Instruction descriptor of kind::mxf4 (both operands packed e2m1, format 1
+// at bits 7-9 / 10-12), K-major, same N / M / UE8M0 fields as above; with
+// scale_vec::2X the byte selectors are 0 or 2.
+__host__ __device__ constexpr uint32_t make_idesc_mxf4(int M, int N) {
+  return ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24) | (1u << 10) |
+         (1u << 7);
 }
 
 // Operand formats of a GEMM instantiation: W8A8 (e4m3 x e4m3), W4A8 (e4m3
-// activations x e2m1 weights), W4A4 (e2m1 x e2m1; gmm1 then requantizes its
-// output to MXFP4 as well).
+// activations x e2m1 weights; kind::mxf8f6f4, the weights unpacked to one
+// element per byte by the tensor map), W4A4 (e2m1 x e2m1, kind::mxf4 on
+// packed operands; gmm1 then requantizes its output to MXFP4 as well).
 enum : int { FMT_W8A8 = 0, FMT_W4A8 = 1, FMT_W4A4 = 2 };
 
 // Bounded mbarrier wait.  Returns false when the CTA is aborting (another
@@ -484,10 +505,12 @@ inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2D tensor [outer, inner] (inner contiguous), 128-byte swizzled box.  fp4:
-// packed e2m1 (two per byte, inner counted in elements) landing in shared
-// memory as 16-element groups of 8 packed bytes in 16-byte slots, so a
-// 128-element row of the box takes 128 bytes there, as an e4m3 row does.
+// 2D tensor [outer, inner] (inner contiguous), 128-byte swizzled box.  fp4
+// (W4A8's weights, read by kind::mxf8f6f4): packed e2m1 (two per byte, inner
+// counted in elements) landing in shared memory as 16-element groups of 8
+// packed bytes in 16-byte slots, so a 128-element row of the box takes 128
+// bytes there, as an e4m3 row does.  W4A4's packed operands (kind::mxf4) are
+// plain bytes: inner = K / 2.
 inline bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                      uint32_t box_inner, uint32_t box_outer, bool fp4 = false) {
   auto fn = encode_fn();

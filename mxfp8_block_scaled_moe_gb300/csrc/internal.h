@@ -78,8 +78,10 @@ cudaError_t launch_gemm_bf16(const uint8_t* aq, const uint8_t* as, const uint8_t
                              bool tiled_scales = false, int fmt = 0, int ksplit = 1,
                              float* partial = nullptr);
 // Split count the dense linear uses for an [M, K] x [N, K]^T product on the
-// current device (1 when the tiles alone fill the GPU).
-int gemm_bf16_ksplit(int64_t M, int N, int K);
+// current device (1 when the tiles alone fill the GPU).  packed_fp4: the W4A4
+// kernel, whose k-slices hold 256 K elements instead of 128 (never more splits
+// than the MXFP8 count for the same shape).
+int gemm_bf16_ksplit(int64_t M, int N, int K, bool packed_fp4 = false);
 
 // [rows, ceil(K/32)] scales -> tiled layout with KT = ceil(K/128); rows and
 // slots past the data (a ragged row block or K slice) are written as 127.

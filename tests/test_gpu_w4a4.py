@@ -62,7 +62,8 @@ def _fp4_weights(rng, N, K):
     return mx.pack_fp4(codes), s
 
 
-# packed e2m1 operands need K % 128 == 0 (the unpacking TMA's row rule)
+# the W4A4 linear takes K % 128 == 0; K % 256 == 128 leaves a packed k-slice
+# with one scale chunk (two of its four K = 64 MMAs)
 EXACT_SHAPES = [
     (200, 400, 384),     # N = 3 row blocks + 16 (128-wide tiles, ragged)
     (1, 16, 128),        # one row, one sector, one K slice
