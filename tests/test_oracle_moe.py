@@ -332,3 +332,23 @@ def test_dequantize_gate_matches_torch_casts():
     val = dec * torch.from_numpy(np.exp2(np.repeat(s.astype(np.float64) - 127, 32, axis=1)))
     ref = val.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(moe.dequantize_gate(codes, s), ref)
+
+
+def test_act_quant_and_deq_weight_dispatch_known_values():
+    """The format dispatchers against hand-worked codes (OCP MX): a block of
+    ones takes scale 2^(0 - 8) in MXFP8 (byte 119, e4m3 256 = 0x78) and
+    2^(0 - 2) in MXFP4 (byte 125, e2m1 4 = code 6, two per byte); e4m3 0x38 is
+    1.0, e2m1 codes 1 / 2 are 0.5 / 1.0 with the low nibble first."""
+    ones = np.ones((2, 32))
+    q, s = moe.act_quant(ones, "e4m3")
+    assert q.dtype == np.uint8 and np.all(q == 0x78) and np.all(s == 119)
+    q, s = moe.act_quant(ones, "e2m1")
+    assert q.shape == (2, 16) and np.all(q == 0x66) and np.all(s == 125)
+    w = moe.deq_weight(np.full((1, 32), 0x38, np.uint8), np.array([[128]], np.uint8), "e4m3")
+    assert np.array_equal(w, np.full((1, 32), 2.0))
+    w = moe.deq_weight(np.full((1, 16), 0x21, np.uint8), np.array([[126]], np.uint8), "e2m1")
+    assert np.array_equal(w, np.tile([0.25, 0.5], 16)[None, :])
+    with pytest.raises(ValueError):
+        moe.act_quant(ones, "e5m2")
+    with pytest.raises(ValueError):
+        moe.deq_weight(q, s, "int4")
