@@ -174,6 +174,44 @@ def test_golden_blocks(case):
     assert gq[0].tolist() == q.tolist(), name
 
 
+GOLDEN_FP4 = os.path.join(os.path.dirname(__file__), "golden", "mxfp4_blocks.txt")
+
+
+def _num(v):
+    v = v.strip()
+    return float.fromhex(v) if "p" in v.lower() else float(v)
+
+
+def _golden_fp4():
+    cases = []
+    with open(GOLDEN_FP4) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            name, K, xs, sc, packed = [p.strip() for p in line.split("|")]
+            K = int(K)
+            x = np.zeros(K)
+            vals = [_num(v) for v in xs.split(",")]
+            x[:len(vals)] = vals
+            q = np.zeros(K // 2, np.uint8)
+            pl = [int(c, 16) for c in packed.split(",")]
+            q[:len(pl)] = pl
+            cases.append((name, x, np.array([int(v) for v in sc.split(",")], np.uint8), q))
+    return cases
+
+
+@pytest.mark.parametrize("case", _golden_fp4(), ids=lambda c: c[0])
+def test_golden_mxfp4_blocks(case):
+    """Hand-worked MXFP4 blocks: scale rule, ties to even, saturation, the
+    e8m0 clamps and the nibble order of the packed bytes."""
+    name, x, scales, q = case
+    assert np.array_equal(mx.bf16_bits_to_f64(mx.f64_to_bf16_bits(x)), x), name  # bf16 inputs
+    gq, gs = mx.mxfp4_quantize(x[None, :])
+    assert gs[0].tolist() == scales.tolist(), name
+    assert gq[0].tolist() == q.tolist(), name
+
+
 # ---------------------------------------------------------------- dequant error
 
 def test_dequant_error_bound():
