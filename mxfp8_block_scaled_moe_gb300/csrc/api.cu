@@ -550,6 +550,9 @@ static mxmoe_status linear_impl(const uint16_t* x, const uint8_t* wq, const uint
   const LinearLayout L = linear_layout(M, N, K, !ws_tiled);
   if (!workspace || ws_bytes < L.total) return MXMOE_ERR_WORKSPACE;
   if ((uintptr_t)workspace & 255u) return MXMOE_ERR_ALIGN;
+  // the workspace holds L.ksplit partial planes, at least the W4A4 count
+  const int ksplit = fp4 ? gemm_bf16_ksplit(M, (int)N, (int)K, true) : L.ksplit;
+  if (ksplit > L.ksplit) return MXMOE_ERR_WORKSPACE;
   cudaStream_t st = (cudaStream_t)stream;
   uint8_t* base = (uint8_t*)workspace;
   uint8_t* xq = base + L.xq;
@@ -568,9 +571,6 @@ static mxmoe_status linear_impl(const uint16_t* x, const uint8_t* wq, const uint
   err = launch_mx_quantize_tiled(x, M, K, xq, xs, offs, st, fp4);
   if (err != cudaSuccess) return MXMOE_ERR_CUDA;
   prof.mark(2);
-  // the workspace holds L.ksplit partial planes, at least the W4A4 count
-  const int ksplit = fp4 ? gemm_bf16_ksplit(M, (int)N, (int)K, true) : L.ksplit;
-  if (ksplit > L.ksplit) return MXMOE_ERR_WORKSPACE;
   err = launch_gemm_bf16(xq, xs, wq, wst, offs, M, 1, (int)K, (int)N, out, st, true, fp4 ? 2 : 0,
                          ksplit, ksplit > 1 ? (float*)(base + L.partial) : nullptr);
   if (err != cudaSuccess) return MXMOE_ERR_CUDA;
