@@ -352,3 +352,51 @@ def test_act_quant_and_deq_weight_dispatch_known_values():
         moe.act_quant(ones, "e5m2")
     with pytest.raises(ValueError):
         moe.deq_weight(q, s, "int4")
+
+
+def _tiny_layer_q():
+    shape = workloads.CONFIGS["tiny"]
+    inp = workloads.make_layer(shape, "cpu")
+    xb = inp["x"].view(torch.int16).numpy().view(np.uint16)
+    w13q, w13s = mx.mx_quantize(mx.bf16_bits_to_f64(inp["w13"].view(torch.int16).numpy().view(np.uint16)))
+    w2q, w2s = mx.mx_quantize(mx.bf16_bits_to_f64(inp["w2"].view(torch.int16).numpy().view(np.uint16)))
+    return shape, xb, inp["logits"].numpy().astype(np.float64), w13q, w13s, w2q, w2s
+
+
+def test_layer_invariant_under_expert_relabeling():
+    """Renaming the experts (logit columns and weight slabs permuted together)
+    leaves every token's output bit-identical: a wrong expert index or offset
+    anywhere in the chain breaks it."""
+    shape, xb, logits, w13q, w13s, w2q, w2s = _tiny_layer_q()
+    E = w13q.shape[0]
+    perm = np.random.default_rng(11).permutation(E)   # new id of expert e = perm[e]
+    inv = np.argsort(perm)
+    ref = moe.moe_forward(xb, logits, w13q, w13s, w2q, w2s, shape.k, shape.I)
+    got = moe.moe_forward(xb, logits[:, inv], w13q[inv], w13s[inv], w2q[inv], w2s[inv],
+                          shape.k, shape.I)
+    assert np.array_equal(got["topk_ids"], perm[ref["topk_ids"]])
+    # the softmax sums run over the experts in id order: fp64 rounding only
+    np.testing.assert_allclose(got["topk_w"], ref["topk_w"], rtol=1e-13, atol=0)
+    assert np.array_equal(got["counts"], ref["counts"][inv])
+    for key in ("xq", "xs", "aq", "as_", "y"):   # expanded rows keep their order
+        src = np.argsort(ref["sorted_to_src"])    # source slot -> sorted row (reference)
+        rows_got = got[key][np.argsort(got["sorted_to_src"])]
+        assert np.array_equal(rows_got, ref[key][src]), key
+    # tokens whose fp32 combine weights agree have bit-identical outputs
+    same = np.all(got["topk_w"].astype(np.float32) == ref["topk_w"].astype(np.float32), axis=1)
+    assert same.mean() > 0.9
+    assert np.array_equal(got["out"][same], ref["out"][same])
+
+
+def test_layer_equivariant_under_token_permutation():
+    """Tokens are independent: permuting them permutes the routing exactly and
+    the outputs up to the summation order inside the library matmul."""
+    shape, xb, logits, w13q, w13s, w2q, w2s = _tiny_layer_q()
+    p = np.random.default_rng(12).permutation(shape.T)
+    ref = moe.moe_forward(xb, logits, w13q, w13s, w2q, w2s, shape.k, shape.I)
+    got = moe.moe_forward(xb[p], logits[p], w13q, w13s, w2q, w2s, shape.k, shape.I)
+    assert np.array_equal(got["topk_ids"], ref["topk_ids"][p])
+    assert np.array_equal(got["topk_w"], ref["topk_w"][p])
+    a = mx.bf16_bits_to_f64(got["out"])
+    b = mx.bf16_bits_to_f64(ref["out"][p])
+    assert np.linalg.norm(a - b) <= 1e-3 * np.linalg.norm(b)
