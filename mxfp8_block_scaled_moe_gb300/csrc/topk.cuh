@@ -12,6 +12,23 @@
 
 namespace mxmoe {
 
+// Exact rounding error of h = fl(a + b) (Knuth's two-sum; no ordering
+// condition on |a|, |b|), written with explicit round-to-nearest adds so the
+// compiler cannot reassociate them.
+__device__ __forceinline__ float two_sum_err(float a, float b, float h) {
+  const float bb = __fsub_rn(h, a);
+  return __fadd_rn(__fsub_rn(a, __fsub_rn(h, bb)), __fsub_rn(b, bb));
+}
+
+// e^(v - m) with the difference carried exactly: hi = fl(v - m), lo its
+// rounding error, e^(hi + lo) = e^hi + e^hi * lo to first order in lo.
+__device__ __forceinline__ float exp_of_difference(float v, float m) {
+  const float hi = __fsub_rn(v, m);
+  const float lo = two_sum_err(v, -m, hi);
+  const float e = expf(hi);
+  return __fmaf_rn(e, lo, e);
+}
+
 // NT tokens per call, each with the same arithmetic as a call for that token
 // alone (the tokens only share the warp's instruction stream, so the latency
 // of one token's warp reductions hides behind the others').  rows[n] points
@@ -59,29 +76,43 @@ __device__ __forceinline__ void warp_topk_softmax(const float* const (&rows)[NT]
       if (lane == j) { ids[n] = (int)id; my_key[n] = m; }
     }
   }
-  // softmax weights of the chosen experts
+  // softmax weights of the chosen experts.  Every exponent argument
+  // a = v - vmax is carried exactly as an fp32 pair (hi + lo, Knuth's
+  // two-sum), e^a = e^hi (1 + lo) to first order, and the denominator is a
+  // compensated sum (each addition's exact rounding error kept in a second
+  // fp32 word), so the weights carry only the fp32 exp error and the final
+  // roundings: a few 1e-7 relative to the exact softmax.  xor butterflies
+  // leave the same bits on every lane (fp32 addition and the two-sum error
+  // are both symmetric in their operands).
 #pragma unroll
   for (int n = 0; n < NT; ++n) {
     vals[n] = key_value(my_key[n]);
     const float vmax = __shfl_sync(0xffffffffu, vals[n], 0);
-    float denom;
+    float s_hi = 0.f, s_lo = 0.f;
     if (renormalize) {
-      float ej = lane < k ? expf(vals[n] - vmax) : 0.f;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) ej += __shfl_xor_sync(0xffffffffu, ej, off);
-      denom = ej;
+      if (lane < k) s_hi = exp_of_difference(vals[n], vmax);
     } else {
-      float sum = 0.f;
 #pragma unroll
       for (int i = 0; i < EPL; ++i) {
         const int e = lane + 32 * i;
-        if (e < E) sum += expf(v[n][i] - vmax);
+        if (e < E) {
+          const float t = exp_of_difference(v[n][i], vmax);
+          const float h = __fadd_rn(s_hi, t);
+          s_lo = __fadd_rn(s_lo, two_sum_err(s_hi, t, h));
+          s_hi = h;
+        }
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-      denom = sum;
     }
-    ws[n] = expf(vals[n] - vmax) / denom;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float oh = __shfl_xor_sync(0xffffffffu, s_hi, off);
+      const float ol = __shfl_xor_sync(0xffffffffu, s_lo, off);
+      const float h = __fadd_rn(s_hi, oh);
+      s_lo = __fadd_rn(__fadd_rn(s_lo, ol), two_sum_err(s_hi, oh, h));
+      s_hi = h;
+    }
+    const float denom = __fadd_rn(s_hi, s_lo);
+    ws[n] = __fdiv_rn(exp_of_difference(vals[n], vmax), denom);
   }
 }
 

@@ -4,8 +4,9 @@ Tolerances (stated once, used by every parity test):
 
 * quantization, scales, top-k ids, permutation indices, counts, offsets:
   bit-exact;
-* routing weights: relative error <= 4e-6 (fp32 softmax on the device vs fp64
-  in the oracle: a few fp32 roundings of exp, sum and divide);
+* routing weights: relative error <= 1e-6 (the device keeps the softmax's
+  exponent arguments exact and its denominator compensated, so only the fp32
+  exp error and a final rounding or two remain against the oracle's fp64);
 * MXFP8 requant (gmm1 output): an element may differ from the oracle by at
   most one e4m3 grid step, on at most 0.1% of elements; a block whose scale
   byte differs counts as 32 mismatched elements;
@@ -20,7 +21,7 @@ from oracle import mx
 
 REQUANT_MAX_FRAC = 1e-3
 OUT_REL_FROB = 2e-3
-TOPK_W_RTOL = 4e-6
+TOPK_W_RTOL = 1e-6
 
 
 def bits16(t: torch.Tensor) -> np.ndarray:
