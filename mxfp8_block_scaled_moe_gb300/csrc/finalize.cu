@@ -5,6 +5,9 @@
 //   out[t] = sum_{j<k} topk_w[t, j] * y[src_to_sorted[t*k + j]]
 //
 // fp32 accumulation in slot order, one bf16 rounding (RNE) at the end.
+// Every index is checked against [0, T*k) before it is used: an index
+// outside records MXMOE_ERR_DEVICE_CHECK in the status word and its slot
+// contributes nothing (row 0 is read with weight 0).
 // One warp per token; each lane owns 16 consecutive columns (one 32 B load per
 // source row), two 512-column chunks in flight.  Roofline: HBM-bound,
 // k*H*2 B read + H*2 B written per token.
@@ -14,13 +17,15 @@
 namespace mxmoe {
 
 constexpr int kFinThreads = 256;
+constexpr int kErrDeviceCheck = 8;  // MXMOE_ERR_DEVICE_CHECK
 
 // Lane owns 16 consecutive columns (one 32-byte load per source row) of a
 // 512-column chunk; two chunks are in flight per iteration (2k loads).
 template <bool kV8>
 __global__ void __launch_bounds__(kFinThreads) finalize_kernel(
     const uint16_t* __restrict__ y, const float* __restrict__ topk_w,
-    const int32_t* __restrict__ src_to_sorted, int T, int k, int H, uint16_t* __restrict__ out) {
+    const int32_t* __restrict__ src_to_sorted, int T, int k, int H, uint16_t* __restrict__ out,
+    int* status) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (kFinThreads / 32) + (threadIdx.x >> 5);
   if (t >= T) return;  // warp-uniform
@@ -29,6 +34,11 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(
   if (lane < k) {
     my_row = src_to_sorted[(int64_t)t * k + lane];
     my_w = topk_w[(int64_t)t * k + lane];
+    if (my_row < 0 || my_row >= (int64_t)T * k) {
+      report_error(status, kErrDeviceCheck);
+      my_row = 0;
+      my_w = 0.f;
+    }
   }
   uint16_t* orow = out + (int64_t)t * H;
   for (int c0 = 0; c0 < H; c0 += 1024) {  // warp-uniform trip count
@@ -92,7 +102,8 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(
 // H % 16 != 0 (H % 8 == 0): lane owns 8 columns, one 16-byte load per row.
 __global__ void __launch_bounds__(kFinThreads) finalize_narrow_kernel(
     const uint16_t* __restrict__ y, const float* __restrict__ topk_w,
-    const int32_t* __restrict__ src_to_sorted, int T, int k, int H, uint16_t* __restrict__ out) {
+    const int32_t* __restrict__ src_to_sorted, int T, int k, int H, uint16_t* __restrict__ out,
+    int* status) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (kFinThreads / 32) + (threadIdx.x >> 5);
   if (t >= T) return;  // warp-uniform
@@ -101,6 +112,11 @@ __global__ void __launch_bounds__(kFinThreads) finalize_narrow_kernel(
   if (lane < k) {
     my_row = src_to_sorted[(int64_t)t * k + lane];
     my_w = topk_w[(int64_t)t * k + lane];
+    if (my_row < 0 || my_row >= (int64_t)T * k) {
+      report_error(status, kErrDeviceCheck);
+      my_row = 0;
+      my_w = 0.f;
+    }
   }
   uint16_t* orow = out + (int64_t)t * H;
   for (int c0 = 0; c0 < H; c0 += 256) {  // warp-uniform trip count
@@ -130,13 +146,14 @@ cudaError_t launch_finalize(const uint16_t* y, const float* topk_w, const int32_
                             int T, int k, int H, uint16_t* out, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   const int blocks = (int)ceil_div(T, kFinThreads / 32);
+  int* st = device_status_ptr();
   // 16-column lanes need H % 16 == 0; 32-byte accesses need 32-byte aligned rows
   if (H % 16 == 0 && ((uintptr_t)y & 31u) == 0 && ((uintptr_t)out & 31u) == 0)
-    finalize_kernel<true><<<blocks, kFinThreads, 0, stream>>>(y, topk_w, src_to_sorted, T, k, H, out);
+    finalize_kernel<true><<<blocks, kFinThreads, 0, stream>>>(y, topk_w, src_to_sorted, T, k, H, out, st);
   else if (H % 16 == 0)
-    finalize_kernel<false><<<blocks, kFinThreads, 0, stream>>>(y, topk_w, src_to_sorted, T, k, H, out);
+    finalize_kernel<false><<<blocks, kFinThreads, 0, stream>>>(y, topk_w, src_to_sorted, T, k, H, out, st);
   else
-    finalize_narrow_kernel<<<blocks, kFinThreads, 0, stream>>>(y, topk_w, src_to_sorted, T, k, H, out);
+    finalize_narrow_kernel<<<blocks, kFinThreads, 0, stream>>>(y, topk_w, src_to_sorted, T, k, H, out, st);
   return cudaGetLastError();
 }
 

@@ -91,15 +91,12 @@ __device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, 
                                                  int* status, volatile int* abort_flag) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
   const long long t0 = clock64();
-  uint32_t it = 0;
   while (!mbar_try_wait_cluster(bar, parity)) {
-    if ((++it & 63u) == 0) {
-      if (*abort_flag) return false;
-      if (clock64() - t0 > limit) {
-        report_error(status, ERR_TIMEOUT);
-        *abort_flag = 1;
-        return false;
-      }
+    if (*abort_flag) return false;
+    if (clock64() - t0 > limit) {
+      report_error(status, ERR_TIMEOUT);
+      *abort_flag = 1;
+      return false;
     }
   }
   return true;

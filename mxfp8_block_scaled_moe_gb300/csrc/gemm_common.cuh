@@ -31,6 +31,7 @@ constexpr int TMEM_COLS = 512;
 constexpr int SF_COL0 = 256;    // scale factors after the accumulator
 constexpr int SF_COLS_PER_STAGE = 16;
 constexpr int ERR_TIMEOUT = 7;  // MXMOE_ERR_DEVICE_TIMEOUT
+constexpr int ERR_CHECK = 8;    // MXMOE_ERR_DEVICE_CHECK
 
 struct Params {
   const uint8_t* sfa;        // [M, K/32], or tiled (tiled_scales.h)
@@ -216,15 +217,12 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, long lon
                                          int* status, volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  uint32_t it = 0;
   while (!mbar_try_wait(bar, parity)) {
-    if ((++it & 63u) == 0) {
-      if (*abort_flag) return false;
-      if (clock64() - t0 > limit) {
-        report_error(status, ERR_TIMEOUT);
-        *abort_flag = 1;
-        return false;
-      }
+    if (*abort_flag) return false;
+    if (clock64() - t0 > limit) {
+      report_error(status, ERR_TIMEOUT);
+      *abort_flag = 1;
+      return false;
     }
   }
   return true;
@@ -284,6 +282,11 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
 // row offsets, s_ts[e] the first work unit of expert e (a unit is CL
 // consecutive 128-row m-tiles x one n-tile), s_ts[E] the unit count, s_mtb[e]
 // the first 128-row block of expert e (tiled scale layout), s_mtb[E] total.
+//
+// The offsets are checked on the way: offsets[0] == 0, non-decreasing, and
+// offsets[E] == M.  Any other array would send tiles to rows outside
+// [0, M); instead the kernel records MXMOE_ERR_DEVICE_CHECK and schedules no
+// work (every CTA sees the same offsets, so every CTA stops).
 template <int CL>
 __device__ __forceinline__ void build_schedule(const Params& p, int lane, int64_t* s_off,
                                                int* s_ts, int* s_mtb) {
@@ -291,6 +294,7 @@ __device__ __forceinline__ void build_schedule(const Params& p, int lane, int64_
   const int E = p.E;
   int cnt[PER], mcnt[PER];
   int run = 0, mrun = 0;
+  bool bad = false;
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
     const int e = lane * PER + i;
@@ -299,13 +303,15 @@ __device__ __forceinline__ void build_schedule(const Params& p, int lane, int64_
       const int64_t o0 = p.offsets[e], o1 = p.offsets[e + 1];
       s_off[e] = o0;
       if (e == E - 1) s_off[E] = o1;
-      c = (int)((o1 - o0 + BM - 1) / BM);
+      bad |= o1 < o0 || (e == 0 && o0 != 0) || (e == E - 1 && o1 != p.M);
+      c = o1 < o0 ? 0 : (int)((o1 - o0 + BM - 1) / BM);
     }
     cnt[i] = run;
     mcnt[i] = mrun;
     run += (c + CL - 1) / CL * p.n_tiles_n;
     mrun += c;
   }
+  bad = __any_sync(0xffffffffu, bad);
   int incl = run, mincl = mrun;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -317,9 +323,10 @@ __device__ __forceinline__ void build_schedule(const Params& p, int lane, int64_
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
     const int e = lane * PER + i;
-    if (e < E) { s_ts[e] = excl + cnt[i]; s_mtb[e] = mexcl + mcnt[i]; }
+    if (e < E) { s_ts[e] = bad ? 0 : excl + cnt[i]; s_mtb[e] = bad ? 0 : mexcl + mcnt[i]; }
   }
-  if (lane == 31) { s_ts[E] = incl; s_mtb[E] = mincl; }
+  if (lane == 31) { s_ts[E] = bad ? 0 : incl; s_mtb[E] = bad ? 0 : mincl; }
+  if (bad && lane == 0) report_error(p.status, ERR_CHECK);
 }
 
 // ---------------------------------------------------------------- epilogue

@@ -6,8 +6,8 @@
   this pins the scale-factor mapping (row, 32-element block) -> element.
 * Ragged grouping: empty experts, one-row experts, experts spanning several
   128-row tiles with a ragged tail, the last tile past M.
-* Config shapes: full outputs for the small layers, sampled experts for the
-  16K-token prefill.
+* Config shapes: every expert of the small layers (the prefill sizes are in
+  test_gpu_full_oracle.py).
 """
 
 import numpy as np
@@ -101,7 +101,7 @@ def _layer_weights(mm, shape):
     return w13q, w13s, w2q, w2s
 
 
-@pytest.mark.parametrize("cfg", ["tiny", "qwen3_30b_decode", "qwen3_30b_prefill"])
+@pytest.mark.parametrize("cfg", ["tiny", "qwen3_30b_decode"])
 def test_gmm_chain_on_config(mm, cfg):
     shape = workloads.CONFIGS[cfg]
     inp = workloads.make_layer(shape, DEV, weights=False)
@@ -112,13 +112,7 @@ def test_gmm_chain_on_config(mm, cfg):
     torch.cuda.synchronize()
     assert mm.device_status() == 0
     offs = r["expert_offsets"].cpu().numpy()
-    if shape.E <= 8 or shape.T <= 64:
-        experts = list(range(shape.E))
-    else:   # sampled experts at full size: largest, smallest non-empty, a few others
-        cnt = np.diff(offs)
-        nz = np.flatnonzero(cnt)
-        experts = sorted(set([int(np.argmax(cnt)), int(nz[np.argmin(cnt[nz])]), 0, 37, 100,
-                              shape.E - 1]))
+    experts = list(range(shape.E))   # every expert (the prefill sizes: test_gpu_full_oracle)
     rows = np.concatenate([np.arange(offs[e], offs[e + 1]) for e in experts]).astype(np.int64)
     xq_h, xs_h = u8(r["xq"]), u8(r["xs"])
     w13q_h = {e: u8(w13q[e]) for e in experts}
@@ -182,27 +176,3 @@ def test_gemm_is_deterministic(mm):
     torch.cuda.synchronize()
     for a, b in zip(outs[0], outs[1]):
         assert torch.equal(a, b)
-
-
-def test_device_wait_timeout_reports_and_recovers(mm):
-    """A wait limit of one cycle makes a barrier wait run out: the kernel must
-    record MXMOE_ERR_DEVICE_TIMEOUT, free its resources and return; the next
-    call with the default limit is correct again."""
-    rng = np.random.default_rng(10)
-    M, E, I, H = 512, 2, 256, 256
-    offs = _offsets([300, 212])
-    aq, as_ = _int_mx(rng, (M, I))
-    w2q, w2s = _int_mx(rng, (E, H, I))
-    args = (_t(aq), _t(as_), _t(w2q), _t(w2s), _t(offs))
-    assert mm.device_status(clear=True) == 0
-    mm.set_wait_limit_cycles(1)
-    try:
-        mm.grouped_gemm_mxfp8(*args)
-        status = mm.device_status(clear=True)
-    finally:
-        mm.set_wait_limit_cycles(0)
-    assert status in (0, 7)   # 7 = MXMOE_ERR_DEVICE_TIMEOUT (0 if no wait ever blocked)
-    y = mm.grouped_gemm_mxfp8(*args)
-    torch.cuda.synchronize()
-    assert mm.device_status() == 0
-    assert np.array_equal(bits16(y), moe.gmm2(aq, as_, w2q, w2s, offs))
