@@ -124,7 +124,7 @@ def test_route_quant_bit_exact(mm, cfg):
     assert np.array_equal(u8(r["xq"]), xq)
 
 
-@pytest.mark.parametrize("T", [1, 8, 128, 1024, 16384])
+@pytest.mark.parametrize("T", workloads.SKEW_SWEEP_T)
 def test_route_quant_skewed_load(mm, T):
     shape = workloads.CONFIGS["qwen3_30b_skewed"].with_tokens(T)
     inp = workloads.make_layer(shape, DEV, weights=False)
