@@ -205,6 +205,28 @@ __device__ __forceinline__ bool aligned32(const void* p) {
   return (reinterpret_cast<uintptr_t>(p) & 31u) == 0;
 }
 
+// Programmatic dependent launch: a kernel launched with the
+// programmatic-serialization attribute may start before its predecessor on
+// the stream has finished; pdl_wait() blocks until that predecessor grid has
+// completed and its memory is visible (a no-op for an ordinary launch), and
+// pdl_launch_dependents() lets the next such kernel be scheduled.
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Bulk prefetch of [p, p + bytes) into L2 (p 16-byte aligned, bytes a
+// multiple of 16), issued in 64 KB pieces; nothing waits for it.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint64_t bytes) {
+  const char* c = static_cast<const char*>(p);
+  for (uint64_t off = 0; off < bytes; off += 65536) {
+    const uint32_t n = (uint32_t)(bytes - off < 65536 ? bytes - off : 65536);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(c + off), "r"(n) : "memory");
+  }
+}
+
 // Record the first device-side error in the library's status word.
 __device__ __forceinline__ void report_error(int* status, int code) {
   if (status) atomicCAS(status, 0, code);

@@ -13,6 +13,12 @@ constexpr int kRouteTokensPerBlock = 64;
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 int num_sms();                       // of the current device (cached)
+// Unique id of the calling thread's current CUDA context, 0 when none is
+// current yet.  Per-device caches (device addresses of the library's
+// globals, kernel attributes) record it: after cudaDeviceReset the device
+// gets a new primary context whose module globals and kernel attributes are
+// new, and no context ever reuses an id, so a changed id means "set up again".
+uint64_t context_id();
 int* device_status_ptr();            // library status word on the current device
 long long wait_limit_cycles();
 bool use_two_sm_gemm(bool swiglu, int64_t M, int E);  // 2-SM grouped GEMM kernel?
@@ -54,6 +60,25 @@ cudaError_t launch_mx_dequantize_bf16(const uint8_t* q, const uint8_t* s, int64_
                                       uint16_t* out, cudaStream_t stream);
 
 size_t route_workspace_bytes(int T, int E);
+
+// Launch with programmatic stream serialization: the kernel may begin while
+// its predecessor on the stream is still running and must call pdl_wait()
+// (common.cuh) before it reads anything that predecessor writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 cudaError_t launch_finalize(const uint16_t* y, const float* topk_w, const int32_t* src_to_sorted,
                             int T, int k, int H, uint16_t* out, cudaStream_t stream);

@@ -46,7 +46,8 @@ template <int EPL, int TPW = topk_tokens_per_warp<EPL>()>  // logits per lane: E
 __global__ void __launch_bounds__(32 * (kRouteTokensPerBlock / TPW)) route_topk_rank_kernel(
     const float* __restrict__ logits, int T, int E, int k, int renormalize,
     int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
-    int32_t* __restrict__ local_rank, int32_t* __restrict__ block_hist) {
+    int32_t* __restrict__ local_rank, int32_t* __restrict__ block_hist,
+    const uint16_t* __restrict__ x_prefetch, int H) {
   constexpr int WARPS = kRouteTokensPerBlock / TPW;
   // s_mask[e] bit tl: token tl of this block chose expert e.  A token's k
   // experts are distinct, so its rank among the block's rows of expert e in
@@ -55,6 +56,13 @@ __global__ void __launch_bounds__(32 * (kRouteTokensPerBlock / TPW)) route_topk_
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t0 = blockIdx.x * kRouteTokensPerBlock;
   const int nt = min(kRouteTokensPerBlock, T - t0);
+  // the scan and permute kernels may be scheduled now (they wait for this
+  // grid's results before reading them)
+  pdl_launch_dependents();
+  // the block's hidden-state rows (contiguous) head for L2 while the top-k
+  // runs, so the permutation reads them from L2 instead of HBM
+  if (x_prefetch && threadIdx.x == 0)
+    prefetch_l2_bulk(x_prefetch + (int64_t)t0 * H, (uint64_t)nt * H * 2);
 
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_mask[e] = 0ull;
   __syncthreads();
@@ -99,136 +107,96 @@ __global__ void __launch_bounds__(32 * (kRouteTokensPerBlock / TPW)) route_topk_
       local_rank[(int64_t)(t0 + tl) * k + lane] =
           __popcll(s_mask[chosen[it]] & ((1ull << tl) - 1ull));
   }
+  // expert-major histogram: row e holds expert e's count in every block
   for (int e = threadIdx.x; e < E; e += blockDim.x)
-    block_hist[(int64_t)blockIdx.x * E + e] = __popcll(s_mask[e]);
+    block_hist[(int64_t)e * gridDim.x + blockIdx.x] = __popcll(s_mask[e]);
 }
 
-// One block of 1024 threads.  G = 1024 / E thread groups split the routing
-// blocks; hist[b][e] becomes the exclusive prefix over blocks of expert e.
-__global__ void __launch_bounds__(1024) route_scan_kernel(int32_t* __restrict__ hist, int nb,
-                                                          int E, int64_t* __restrict__ counts,
-                                                          int64_t* __restrict__ offsets,
-                                                          int32_t* __restrict__ tile_base) {
-  extern __shared__ int smem_i[];
-  const int G = max(1, (int)(blockDim.x / E));
-  int* s_part = smem_i;          // [G][E]
-  int* s_tot = smem_i + G * E;   // [E]
-  const int g = threadIdx.x / E, e = threadIdx.x % E;
-  const int per = (nb + G - 1) / G;
-  const int b0 = g * per, b1 = min(nb, b0 + per);
-  const bool active = g < G;
-  constexpr int R = 8;  // independent loads in flight per thread
-  // up to RR blocks per thread: one round of loads, kept in registers for the
-  // second pass (the common case: nb <= RR * G)
-  constexpr int RR = 32;
-  const bool one_round = b1 - b0 <= RR;
-  int keep[RR];
-  if (active && one_round) {
-    int s = 0;
-#pragma unroll
-    for (int r = 0; r < RR; ++r) keep[r] = b0 + r < b1 ? hist[(int64_t)(b0 + r) * E + e] : 0;
-#pragma unroll
-    for (int r = 0; r < RR; ++r) s += keep[r];
-    s_part[g * E + e] = s;
-  } else if (active) {
-    int s = 0;
-    for (int c = b0; c < b1; c += R) {
-      int vals[R];
-#pragma unroll
-      for (int r = 0; r < R; ++r) vals[r] = c + r < b1 ? hist[(int64_t)(c + r) * E + e] : 0;
-#pragma unroll
-      for (int r = 0; r < R; ++r) s += vals[r];
-    }
-    s_part[g * E + e] = s;
-  }
-  __syncthreads();
-  if (threadIdx.x < E) {
-    int run = 0;
-    for (int gg = 0; gg < G; ++gg) {
-      const int v = s_part[gg * E + threadIdx.x];
-      s_part[gg * E + threadIdx.x] = run;
-      run += v;
-    }
-    s_tot[threadIdx.x] = run;
-  }
-  __syncthreads();
-  if (active && one_round) {
-    int run = s_part[g * E + e];
-#pragma unroll
-    for (int r = 0; r < RR; ++r) {
-      if (b0 + r < b1) hist[(int64_t)(b0 + r) * E + e] = run;
-      run += keep[r];
-    }
-  } else if (active) {
-    int run = s_part[g * E + e];
-    for (int c = b0; c < b1; c += R) {
-      int vals[R];
-#pragma unroll
-      for (int r = 0; r < R; ++r) vals[r] = c + r < b1 ? hist[(int64_t)(c + r) * E + e] : 0;
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        if (c + r < b1) hist[(int64_t)(c + r) * E + e] = run;
-        run += vals[r];
-      }
-    }
-  }
-  // exclusive scan of the expert totals (E <= 1024), warp-shuffle based
-  __shared__ int s_warp[32];
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  int v = tid < E ? s_tot[tid] : 0;
-  int incl = v;
+// One block of 1024 threads over the expert-major histogram hist[e][b] (nb
+// blocks per row).  Each warp takes whole expert rows (e = warp, warp + 32,
+// ...): 32 consecutive blocks per load, a shuffle scan per 32, and the row is
+// rewritten as its exclusive prefix (the block's base row inside expert e).
+// Then the expert totals are scanned into counts, offsets and the experts'
+// first 128-row blocks of the tiled scale layout.
+constexpr int kScanThreads = 1024;
+
+__device__ __forceinline__ int warp_incl_scan(int v, int lane) {
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
-    const int o = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += o;
+    const int o = __shfl_up_sync(0xffffffffu, v, off);
+    if (lane >= off) v += o;
   }
+  return v;
+}
+
+// Exclusive scan of one value per thread over the block (values of threads
+// >= n count as 0); *total receives the sum.  s_warp: 32 ints.
+__device__ __forceinline__ int block_excl_scan(int v, int* s_warp, int* total) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int incl = warp_incl_scan(v, lane);
   if (lane == 31) s_warp[w] = incl;
   __syncthreads();
   if (w == 0) {
-    int x = s_warp[lane];
-    int xi = x;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, xi, off);
-      if (lane >= off) xi += o;
-    }
-    s_warp[lane] = xi - x;  // exclusive prefix of warp totals
+    const int x = s_warp[lane];
+    const int xi = warp_incl_scan(x, lane);
+    s_warp[lane] = xi - x;
+    if (lane == 31) s_warp[32] = xi;
   }
   __syncthreads();
-  const int excl = incl - v + s_warp[w];
+  const int r = incl - v + s_warp[w];
+  *total = s_warp[32];
+  return r;
+}
+
+__global__ void __launch_bounds__(kScanThreads) route_scan_kernel(int32_t* __restrict__ hist,
+                                                                  int nb, int E,
+                                                                  int64_t* __restrict__ counts,
+                                                                  int64_t* __restrict__ offsets,
+                                                                  int32_t* __restrict__ tile_base) {
+  pdl_launch_dependents();
+  pdl_wait();  // the top-k kernel's histograms
+  __shared__ int s_tot[1024];
+  __shared__ int s_warp[33];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int U = 8;  // 32-block chunks loaded together
+  for (int e = warp; e < E; e += kScanThreads / 32) {
+    int32_t* row = hist + (int64_t)e * nb;
+    int run = 0;
+    for (int c0 = 0; c0 < nb; c0 += 32 * U) {
+      int v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int b = c0 + 32 * u + lane;
+        v[u] = b < nb ? row[b] : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int b = c0 + 32 * u + lane;
+        const int incl = warp_incl_scan(v[u], lane);
+        if (b < nb) row[b] = run + incl - v[u];
+        run += __shfl_sync(0xffffffffu, incl, 31);
+      }
+    }
+    if (lane == 0) s_tot[e] = run;
+  }
+  __syncthreads();
+  // expert totals -> counts and offsets (E <= 1024: one expert per thread)
+  const int v = tid < E ? s_tot[tid] : 0;
+  int sum = 0;
+  const int excl = block_excl_scan(v, s_warp, &sum);
   if (tid < E) {
     counts[tid] = v;
     offsets[tid] = excl;
-    if (tid == E - 1) offsets[E] = excl + v;
   }
+  if (tid == 0) offsets[E] = sum;
   if (tile_base == nullptr) return;
   // exclusive prefix of the experts' 128-row tile counts (tiled scale layout)
   __syncthreads();
   const int tv = (v + 127) / 128;
-  int tincl = tv;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int o = __shfl_up_sync(0xffffffffu, tincl, off);
-    if (lane >= off) tincl += o;
-  }
-  if (lane == 31) s_warp[w] = tincl;
-  __syncthreads();
-  if (w == 0) {
-    int x = s_warp[lane];
-    int xi = x;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, xi, off);
-      if (lane >= off) xi += o;
-    }
-    s_warp[lane] = xi - x;
-  }
-  __syncthreads();
-  const int texcl = tincl - tv + s_warp[w];
-  if (tid < E) {
-    tile_base[tid] = texcl;
-    if (tid == E - 1) tile_base[E] = texcl + tv;
-  }
+  int tsum = 0;
+  const int texcl = block_excl_scan(tv, s_warp, &tsum);
+  if (tid < E) tile_base[tid] = texcl;
+  if (tid == 0) tile_base[E] = tsum;
 }
 
 // kQ: 0 = bf16 rows to xp; 1 = MXFP8 (xq [M, H] e4m3); 2 = MXFP4 (xq [M, H/2]
@@ -244,14 +212,17 @@ __global__ void __launch_bounds__(kRouteThreads) route_permute_kernel(
     uint8_t* __restrict__ xq, uint8_t* __restrict__ xs, uint16_t* __restrict__ xp) {
   __shared__ int64_t s_dest[kRouteWarps][32];
   __shared__ int64_t s_sfrow[kRouteWarps][32];  // tiled layout: 128-row block and row
+  pdl_launch_dependents();
+  pdl_wait();  // ids, ranks, block bases and offsets of the two kernels before
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t = blockIdx.x * kRouteWarps + warp;
   if (t >= T) return;  // warp-uniform
   const int b = t / kRouteTokensPerBlock;
+  const int nbk = (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
   if (lane < k) {
     const int64_t f = (int64_t)t * k + lane;
     const int e = topk_ids[f];
-    const int64_t dest = offsets[e] + block_base[(int64_t)b * E + e] + src_to_sorted[f];
+    const int64_t dest = offsets[e] + block_base[(int64_t)e * nbk + b] + src_to_sorted[f];
     src_to_sorted[f] = (int32_t)dest;
     sorted_to_src[dest] = (int32_t)f;
     s_dest[warp][lane] = dest;
@@ -317,10 +288,10 @@ size_t route_workspace_bytes(int T, int E) {
 template <int EPL>
 static void launch_topk(int nb, size_t smem, cudaStream_t stream, const float* logits, int T,
                         int E, int k, int renorm, int32_t* ids, float* w, int32_t* rank,
-                        int32_t* hist) {
+                        int32_t* hist, const uint16_t* x, int H) {
   constexpr int threads = 32 * (kRouteTokensPerBlock / topk_tokens_per_warp<EPL>());
   route_topk_rank_kernel<EPL><<<nb, threads, smem, stream>>>(logits, T, E, k, renorm, ids,
-                                                                   w, rank, hist);
+                                                                   w, rank, hist, x, H);
 }
 
 cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, int E, int k,
@@ -343,26 +314,27 @@ cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, i
   // the fused router (router.cu) already wrote ids, weights, ranks and
   // histograms.
   if (topk_done) {
-  } else if (epl <= 1)       launch_topk<1>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist);
-  else if (epl <= 2)  launch_topk<2>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist);
-  else if (epl <= 4)  launch_topk<4>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist);
-  else if (epl <= 8)  launch_topk<8>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist);
-  else if (epl <= 16) launch_topk<16>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist);
-  else                launch_topk<32>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist);
+  } else if (epl <= 1)       launch_topk<1>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist, x, H);
+  else if (epl <= 2)  launch_topk<2>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist, x, H);
+  else if (epl <= 4)  launch_topk<4>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist, x, H);
+  else if (epl <= 8)  launch_topk<8>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist, x, H);
+  else if (epl <= 16) launch_topk<16>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist, x, H);
+  else                launch_topk<32>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist, x, H);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
 
-  const int G = E >= 1024 ? 1 : 1024 / E;
-  const size_t smem2 = sizeof(int) * ((size_t)G * E + E);
-  route_scan_kernel<<<1, 1024, smem2, stream>>>(block_hist, nb, E, counts, offsets, tile_base);
-  err = cudaGetLastError();
+  // the scan and the permutation start early (programmatic dependent
+  // launch) and wait on the device for their predecessor's results
+  err = launch_pdl(route_scan_kernel, dim3(1), dim3(kScanThreads), 0, stream, block_hist, nb, E,
+                   counts, offsets, tile_base);
   if (err != cudaSuccess) return err;
 
   const int nb3 = (int)ceil_div(T, kRouteWarps);
   const bool v8 = ((uintptr_t)x & 31u) == 0 && ((uintptr_t)(quant ? (const void*)xq : (const void*)xp) & 31u) == 0;
 #define MXMOE_PERMUTE(Q, TL, V)                                                                   \
-  route_permute_kernel<Q, TL, V><<<nb3, kRouteThreads, 0, stream>>>(                           \
-      x, T, H, E, k, topk_ids, block_hist, offsets, TL ? tile_base : nullptr, src_to_sorted,    \
+  err = launch_pdl(route_permute_kernel<Q, TL, V>, dim3(nb3), dim3(kRouteThreads), 0, stream,  \
+      x, T, H, E, k, (const int32_t*)topk_ids, (const int32_t*)block_hist,                     \
+      (const int64_t*)offsets, (const int32_t*)(TL ? tile_base : nullptr), src_to_sorted,     \
       sorted_to_src, Q ? xq : nullptr, Q ? xs : nullptr, Q ? nullptr : xp)
   if (quant == 2) {
     if (v8) MXMOE_PERMUTE(2, true, true); else MXMOE_PERMUTE(2, true, false);
@@ -374,7 +346,7 @@ cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, i
     if (v8) MXMOE_PERMUTE(0, false, true); else MXMOE_PERMUTE(0, false, false);
   }
 #undef MXMOE_PERMUTE
-  return cudaGetLastError();
+  return err;
 }
 
 }  // namespace mxmoe

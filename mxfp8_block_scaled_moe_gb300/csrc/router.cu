@@ -250,7 +250,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int i = threadIdx.x - 64; i < 2 * E; i += 32 * EPI) {
         const int half = i / E, e = i - half * E;
         const int b = 2 * blockIdx.x + half;
-        if (b < p.n_blocks) p.block_hist[(int64_t)b * E + e] = __popcll(s_mask[half * MAX_E + e]);
+        if (b < p.n_blocks)
+          p.block_hist[(int64_t)e * p.n_blocks + b] = __popcll(s_mask[half * MAX_E + e]);
       }
     }
   }
@@ -290,12 +291,13 @@ static cudaError_t launch_router_epl(const CUtensorMap& tmX, const CUtensorMap& 
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  static bool configured[64] = {};
-  if (!configured[dev]) {
+  static uint64_t configured[64] = {0};  // context id the attribute was set in
+  const uint64_t ctx = context_id();
+  if (ctx == 0 || configured[dev] != ctx) {
     const cudaError_t err = cudaFuncSetAttribute(router_gate_topk_kernel<EPL>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, ALLOC);
     if (err != cudaSuccess) return err;
-    configured[dev] = true;
+    configured[dev] = context_id();
   }
   router_gate_topk_kernel<EPL><<<grid, THREADS, ALLOC, stream>>>(tmX, tmG, p);
   return cudaGetLastError();

@@ -35,8 +35,14 @@ __device__ __forceinline__ float exp_of_difference(float v, float m) {
 // at token n's E fp32 logits (global or shared memory), or is null for no
 // token; lane l reads experts l, l + 32, ..., l + 32 (EPL - 1).  On lanes
 // j < k: ids[n] / vals[n] / ws[n] are token n's j-th chosen expert, its logit
-// and its weight.  The softmax sums run per lane in increasing expert order,
-// then over the lanes by an xor butterfly.
+// and its weight.
+//
+// Selection: k rounds of the warp's largest remaining key (redux max), ties
+// to the lowest expert id among the lanes holding it (redux min).  For
+// EPL <= 4 each lane first sorts its own EPL (key, id) pairs (descending key,
+// ties to the lower id, i.e. a stable sort of the lane's experts), so a round
+// reads the lane's head and, on a win, shifts the lane's list by one; wider
+// rows rescan the lane's live entries every round.
 template <int EPL, int NT>
 __device__ __forceinline__ void warp_topk_softmax(const float* const (&rows)[NT], int E, int k,
                                                   bool renormalize, int lane, int (&ids)[NT],
@@ -52,28 +58,70 @@ __device__ __forceinline__ void warp_topk_softmax(const float* const (&rows)[NT]
       v[n][i] = in ? rows[n][e] : 0.f;
       key[n][i] = in ? order_key(v[n][i]) : 0u;  // 0: below every finite key
     }
-  // k rounds: the warp's largest remaining key (redux max), ties to the
-  // lowest expert id among the lanes holding it (redux min); within a lane
-  // the lowest index wins a tie (strict compare in increasing i).
-  uint32_t taken[NT], my_key[NT];
+  uint32_t my_key[NT];
 #pragma unroll
-  for (int n = 0; n < NT; ++n) { taken[n] = 0; my_key[n] = 0; ids[n] = 0; }
-  for (int j = 0; j < k; ++j) {
+  for (int n = 0; n < NT; ++n) { my_key[n] = 0; ids[n] = 0; }
+  if constexpr (EPL <= 4) {
+    // the lane's sorted list: sk[n][0] is its current head
+    uint32_t sk[NT][EPL], si[NT][EPL];
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
-      uint32_t hk = 0u, hid = 0xFFFFFFFFu;
 #pragma unroll
       for (int i = 0; i < EPL; ++i) {
-        const bool live = lane + 32 * i < E && !((taken[n] >> i) & 1u);
-        if (live && (hid == 0xFFFFFFFFu || key[n][i] > hk)) {
-          hk = key[n][i];
-          hid = (uint32_t)(lane + 32 * i);
-        }
+        sk[n][i] = key[n][i];
+        si[n][i] = lane + 32 * i < E ? (uint32_t)(lane + 32 * i) : 0xFFFFFFFFu;
       }
-      const uint32_t m = __reduce_max_sync(0xffffffffu, hk);
-      const uint32_t id = __reduce_min_sync(0xffffffffu, hk == m ? hid : 0xFFFFFFFFu);
-      if (hid == id) taken[n] |= 1u << (id >> 5);
-      if (lane == j) { ids[n] = (int)id; my_key[n] = m; }
+      // stable bubble sort, descending (strict compare keeps the lower id first)
+#pragma unroll
+      for (int a = 0; a < EPL - 1; ++a)
+#pragma unroll
+        for (int b = 0; b < EPL - 1 - a; ++b) {
+          const bool sw = sk[n][b + 1] > sk[n][b];
+          const uint32_t k0 = sk[n][b], k1 = sk[n][b + 1], i0 = si[n][b], i1 = si[n][b + 1];
+          sk[n][b] = sw ? k1 : k0;
+          sk[n][b + 1] = sw ? k0 : k1;
+          si[n][b] = sw ? i1 : i0;
+          si[n][b + 1] = sw ? i0 : i1;
+        }
+    }
+    for (int j = 0; j < k; ++j) {
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        const uint32_t hk = sk[n][0], hid = si[n][0];
+        const uint32_t m = __reduce_max_sync(0xffffffffu, hk);
+        const uint32_t id = __reduce_min_sync(0xffffffffu, hk == m ? hid : 0xFFFFFFFFu);
+        const bool win = hid == id;
+#pragma unroll
+        for (int i = 0; i < EPL - 1; ++i) {
+          sk[n][i] = win ? sk[n][i + 1] : sk[n][i];
+          si[n][i] = win ? si[n][i + 1] : si[n][i];
+        }
+        if (win) { sk[n][EPL - 1] = 0u; si[n][EPL - 1] = 0xFFFFFFFFu; }
+        if (lane == j) { ids[n] = (int)id; my_key[n] = m; }
+      }
+    }
+  } else {
+    // within a lane the lowest index wins a tie (strict compare in increasing i)
+    uint32_t taken[NT];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) taken[n] = 0;
+    for (int j = 0; j < k; ++j) {
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        uint32_t hk = 0u, hid = 0xFFFFFFFFu;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+          const bool live = lane + 32 * i < E && !((taken[n] >> i) & 1u);
+          if (live && (hid == 0xFFFFFFFFu || key[n][i] > hk)) {
+            hk = key[n][i];
+            hid = (uint32_t)(lane + 32 * i);
+          }
+        }
+        const uint32_t m = __reduce_max_sync(0xffffffffu, hk);
+        const uint32_t id = __reduce_min_sync(0xffffffffu, hk == m ? hid : 0xFFFFFFFFu);
+        if (hid == id) taken[n] |= 1u << (id >> 5);
+        if (lane == j) { ids[n] = (int)id; my_key[n] = m; }
+      }
     }
   }
   // softmax weights of the chosen experts.  Every exponent argument
@@ -83,14 +131,18 @@ __device__ __forceinline__ void warp_topk_softmax(const float* const (&rows)[NT]
   // fp32 word), so the weights carry only the fp32 exp error and the final
   // roundings: a few 1e-7 relative to the exact softmax.  xor butterflies
   // leave the same bits on every lane (fp32 addition and the two-sum error
-  // are both symmetric in their operands).
+  // are both symmetric in their operands); renormalized sums run only the
+  // butterfly levels that lanes 0..k-1 need.
+  int kp = 1;
+  while (kp < k) kp <<= 1;
 #pragma unroll
   for (int n = 0; n < NT; ++n) {
     vals[n] = key_value(my_key[n]);
     const float vmax = __shfl_sync(0xffffffffu, vals[n], 0);
+    const float mine = lane < k ? exp_of_difference(vals[n], vmax) : 0.f;
     float s_hi = 0.f, s_lo = 0.f;
     if (renormalize) {
-      if (lane < k) s_hi = exp_of_difference(vals[n], vmax);
+      s_hi = mine;
     } else {
 #pragma unroll
       for (int i = 0; i < EPL; ++i) {
@@ -105,6 +157,7 @@ __device__ __forceinline__ void warp_topk_softmax(const float* const (&rows)[NT]
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
+      if (renormalize && off >= kp) continue;  // warp-uniform
       const float oh = __shfl_xor_sync(0xffffffffu, s_hi, off);
       const float ol = __shfl_xor_sync(0xffffffffu, s_lo, off);
       const float h = __fadd_rn(s_hi, oh);
@@ -112,7 +165,7 @@ __device__ __forceinline__ void warp_topk_softmax(const float* const (&rows)[NT]
       s_hi = h;
     }
     const float denom = __fadd_rn(s_hi, s_lo);
-    ws[n] = __fdiv_rn(exp_of_difference(vals[n], vmax), denom);
+    ws[n] = __fdiv_rn(mine, denom);
   }
 }
 
