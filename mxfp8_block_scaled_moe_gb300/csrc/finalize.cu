@@ -26,6 +26,7 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(
     const uint16_t* __restrict__ y, const float* __restrict__ topk_w,
     const int32_t* __restrict__ src_to_sorted, int T, int k, int H, uint16_t* __restrict__ out,
     int* status) {
+  pdl_wait();  // y of the GEMM before (programmatic serialization)
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (kFinThreads / 32) + (threadIdx.x >> 5);
   if (t >= T) return;  // warp-uniform
@@ -104,6 +105,7 @@ __global__ void __launch_bounds__(kFinThreads) finalize_narrow_kernel(
     const uint16_t* __restrict__ y, const float* __restrict__ topk_w,
     const int32_t* __restrict__ src_to_sorted, int T, int k, int H, uint16_t* __restrict__ out,
     int* status) {
+  pdl_wait();  // y of the GEMM before (programmatic serialization)
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (kFinThreads / 32) + (threadIdx.x >> 5);
   if (t >= T) return;  // warp-uniform
@@ -149,12 +151,14 @@ cudaError_t launch_finalize(const uint16_t* y, const float* topk_w, const int32_
   int* st = device_status_ptr();
   // 16-column lanes need H % 16 == 0; 32-byte accesses need 32-byte aligned rows
   if (H % 16 == 0 && ((uintptr_t)y & 31u) == 0 && ((uintptr_t)out & 31u) == 0)
-    finalize_kernel<true><<<blocks, kFinThreads, 0, stream>>>(y, topk_w, src_to_sorted, T, k, H, out, st);
+    return launch_pdl(finalize_kernel<true>, dim3(blocks), dim3(kFinThreads), 0, stream, y, topk_w,
+                      src_to_sorted, T, k, H, out, st);
   else if (H % 16 == 0)
-    finalize_kernel<false><<<blocks, kFinThreads, 0, stream>>>(y, topk_w, src_to_sorted, T, k, H, out, st);
+    return launch_pdl(finalize_kernel<false>, dim3(blocks), dim3(kFinThreads), 0, stream, y, topk_w,
+                      src_to_sorted, T, k, H, out, st);
   else
-    finalize_narrow_kernel<<<blocks, kFinThreads, 0, stream>>>(y, topk_w, src_to_sorted, T, k, H, out, st);
-  return cudaGetLastError();
+    return launch_pdl(finalize_narrow_kernel, dim3(blocks), dim3(kFinThreads), 0, stream, y, topk_w,
+                      src_to_sorted, T, k, H, out, st);
 }
 
 }  // namespace mxmoe

@@ -151,6 +151,11 @@ __global__ void __launch_bounds__(THREADS1, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+  // launched with programmatic serialization: everything above overlaps the
+  // previous kernel's tail; the offsets, operands and scales it (or an
+  // earlier kernel) wrote are read only after this wait
+  pdl_launch_dependents();
+  pdl_wait();
   if (warp == 2) build_schedule<1>(p, lane, s_off, s_ts, s_mtb);
   tc_fence_before();
   __syncthreads();
@@ -469,13 +474,14 @@ static cudaError_t launch_single(const uint8_t* a, const uint8_t* sfa, const uin
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  static bool configured[64] = {false};
+  static uint64_t configured[64] = {0};  // context id the attribute was set in
   auto kern = gemm1sm_kernel<BN, kSwiglu, kTiledSF, kFmt, kSplit>;
-  if (!configured[dev]) {
+  const uint64_t ctx = context_id();
+  if (ctx == 0 || configured[dev] != ctx) {
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (err != cudaSuccess) return err;
-    configured[dev] = true;
+    configured[dev] = context_id();
   }
   CUtensorMap tmA, tmB;
   const uint32_t b_box_rows = kSwiglu ? BN / 2 : BN;
@@ -503,8 +509,7 @@ static cudaError_t launch_single(const uint8_t* a, const uint8_t* sfa, const uin
   p.partial = kSplit ? partial : nullptr;
   const int64_t tiles_bound = (ceil_div(M, BM) + E) * (int64_t)p.n_tiles_n * ksplit;
   const int grid = (int)std::min<int64_t>(tiles_bound, num_sms());
-  kern<<<grid, THREADS1, L::ALLOC, stream>>>(tmA, tmB, p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(THREADS1), L::ALLOC, stream, tmA, tmB, p);
 }
 
 // Kernel choice (mxmoe_set_gemm_2sm): 256-wide tiles with MMA-layout scales go

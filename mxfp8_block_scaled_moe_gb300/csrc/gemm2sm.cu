@@ -204,6 +204,10 @@ __global__ void __launch_bounds__(THREADS1, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
+  // programmatic serialization: the set-up above overlaps the previous
+  // kernel's tail; its outputs are read only after this wait
+  pdl_launch_dependents();
+  pdl_wait();
   if (warp == 2) build_schedule<2>(p, lane, s_off, s_ts, s_mtb);
   tc_fence_before();
   __syncthreads();
@@ -487,20 +491,23 @@ cudaError_t launch_pair_impl(const uint8_t* a, const uint8_t* sfa, const uint8_t
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   static int max_clusters[64];
-  static bool configured[64] = {false};
+  static uint64_t configured[64] = {0};  // context id the attribute was set in
   auto kern = gemm2sm_kernel<kSwiglu, kFmt>;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(THREADS1, 1, 1);
   cfg.dynamicSmemBytes = L::ALLOC;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (!configured[dev]) {
+  const uint64_t ctx = context_id();
+  if (ctx == 0 || configured[dev] != ctx) {
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (err != cudaSuccess) return err;
     cfg.gridDim = dim3(2 * 64, 1, 1);
@@ -510,7 +517,7 @@ cudaError_t launch_pair_impl(const uint8_t* a, const uint8_t* sfa, const uint8_t
       n = 0;
     }
     max_clusters[dev] = n;
-    configured[dev] = true;
+    configured[dev] = context_id();
   }
   if (max_clusters[dev] <= 0) return cudaErrorNotSupported;
   CUtensorMap tmA, tmB;
@@ -539,6 +546,7 @@ cudaError_t launch_pair_impl(const uint8_t* a, const uint8_t* sfa, const uint8_t
   const int clusters = (int)std::min<int64_t>(
       {units_bound, (int64_t)max_clusters[dev], (int64_t)num_sms() / 2});
   cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cfg.numAttrs = 2;  // the cluster shape (as queried above) + programmatic serialization
   return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
 }
 
