@@ -160,7 +160,9 @@ mxmoe_status moe_route_quant_mxfp8(const uint16_t* x, const float* logits, int T
  *   - The call allocates nothing (no cudaMalloc / cudaFree, no allocating
  *     library routine).  Its first call on a device looks up the array's
  *     device address with that device current; make that first call before
- *     any stream capture.
+ *     any stream capture.  The address is kept per device and CUDA context:
+ *     after cudaDeviceReset the next call (the first in the new context)
+ *     looks it up again, and the array's contents start over.
  *   - Every call shares the one array.  Each call writes every scratch entry
  *     it later reads, so nothing has to start at zero, but calls that
  *     overlap on the GPU (other streams, other threads) race on it.
@@ -455,15 +457,19 @@ mxmoe_status moe_forward_mxfp8_host_plan(const uint16_t* x_host, const float* lo
 
 /*
  * Per-kernel timing of moe_forward_mxfp8 / moe_forward_mxfp8_mma_scales / mxfp8_linear*
- * (instrumentation, off by default; not part of the method).  While
- * enabled, each layer call records CUDA events on its stream between its
- * kernels; mxmoe_layer_profile_read then returns, for the last such call on
- * the current device, n <= 5 segment times in milliseconds:
+ * (instrumentation, off by default; not part of the method).  enable = 1:
+ * each layer call records CUDA events on its stream between its kernels;
+ * mxmoe_layer_profile_read then returns, for the last such call on the
+ * current device, n <= 5 segment times in milliseconds:
  *   [0] weight-scale re-layout (0 for the _mma_scales entry point),
  *   [1] route + fused quant, [2] gmm1, [3] gmm2, [4] finalize.
  * A dense-linear call (mxfp8_linear*) records [0] weight-scale re-layout,
  * [1] activation quant, [2] GEMM, and 0 for [3], [4].
- * The read synchronizes on the call's last event.  Not thread-safe.
+ * enable = 2: events only around gmm1 (the dense linear's GEMM), so the other
+ * kernel boundaries keep their overlapped (programmatic dependent) launches;
+ * the read returns [2] and 0 elsewhere.  enable = 0: off.  Other values:
+ * MXMOE_ERR_SHAPE.  The read synchronizes on the call's last event.  Not
+ * thread-safe.
  */
 mxmoe_status mxmoe_layer_profile_enable(int enable);
 mxmoe_status mxmoe_layer_profile_read(float* ms, int n);

@@ -338,9 +338,12 @@ def device_status(clear: bool = True) -> int:
     return int(v.value)
 
 
-def layer_profile_enable(enable: bool = True) -> None:
-    """Record CUDA events between the layer call's kernels (instrumentation)."""
-    _lib.check("mxmoe_layer_profile_enable", _lib.load().mxmoe_layer_profile_enable(int(enable)))
+def layer_profile_enable(enable=True) -> None:
+    """Record CUDA events between the layer call's kernels (instrumentation):
+    True / 1 = every boundary, "gemm1" / 2 = only around gmm1 (the other
+    boundaries keep their overlapped launches), False / 0 = off."""
+    mode = 2 if enable == "gemm1" else int(enable)
+    _lib.check("mxmoe_layer_profile_enable", _lib.load().mxmoe_layer_profile_enable(mode))
 
 
 def layer_profile_read() -> dict:

@@ -6,6 +6,8 @@
 #include <cstring>
 #include <mutex>
 
+#include <cuda.h>
+
 #include "internal.h"
 #include "mxmoe.h"
 
@@ -40,6 +42,7 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int g_sms[kMaxDevices] = {0};
 int* g_status_ptr[kMaxDevices] = {nullptr};
+uint64_t g_status_ctx[kMaxDevices] = {0};  // context id the cached address belongs to
 }  // namespace
 
 int num_sms() {
@@ -55,14 +58,43 @@ int num_sms() {
   return g_sms[dev];
 }
 
+uint64_t context_id() {
+  using GetCurrentFn = CUresult (*)(CUcontext*);
+  using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(f);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  unsigned long long id = 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return (uint64_t)id;
+}
+
 int* device_status_ptr() {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_status_ptr[dev]) {
+  const uint64_t ctx = context_id();
+  if (!g_status_ptr[dev] || ctx == 0 || ctx != g_status_ctx[dev]) {
+    // (the lookup makes the device's primary context current, so the id is
+    // taken again afterwards)
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_status) == cudaSuccess) g_status_ptr[dev] = (int*)p;
+    g_status_ptr[dev] = cudaGetSymbolAddress(&p, g_device_status) == cudaSuccess ? (int*)p : nullptr;
+    g_status_ctx[dev] = context_id();
   }
   return g_status_ptr[dev];
 }
@@ -295,31 +327,41 @@ constexpr int kProfEvents = 6;
 std::atomic<int> g_prof_enabled{0};
 cudaEvent_t g_prof_ev[kMaxDevices][kProfEvents] = {};
 bool g_prof_valid[kMaxDevices] = {false};
+int g_prof_mode[kMaxDevices] = {0};  // mode of the last profiled call
 
+// Mode 1 records an event at every kernel boundary; mode 2 only around the
+// dominant GEMM (events 2 and 3), so the other boundaries keep their
+// programmatic dependent launches (an event between two kernels makes the
+// second wait for the first to finish).
 struct LayerProfiler {
   int dev = -1;
-  bool on = false;
+  int mode = 0;
   cudaStream_t s;
   explicit LayerProfiler(cudaStream_t st) : s(st) {
-    if (!g_prof_enabled.load()) return;
+    const int m = g_prof_enabled.load();
+    if (!m) return;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return;
     std::lock_guard<std::mutex> lk(g_mu);
     for (int i = 0; i < kProfEvents; ++i)
       if (!g_prof_ev[dev][i] && cudaEventCreate(&g_prof_ev[dev][i]) != cudaSuccess) return;
     g_prof_valid[dev] = false;
-    on = true;
+    mode = m;
   }
   void mark(int i) {
-    if (on) cudaEventRecord(g_prof_ev[dev][i], s);
+    if (mode == 1 || (mode == 2 && (i == 2 || i == 3))) cudaEventRecord(g_prof_ev[dev][i], s);
   }
   void done() {
-    if (on) g_prof_valid[dev] = true;
+    if (mode) {
+      g_prof_valid[dev] = true;
+      g_prof_mode[dev] = mode;
+    }
   }
 };
 }  // namespace
 
 mxmoe_status mxmoe_layer_profile_enable(int enable) {
-  g_prof_enabled.store(enable ? 1 : 0);
+  if (enable < 0 || enable > 2) return MXMOE_ERR_SHAPE;
+  g_prof_enabled.store(enable);
   return MXMOE_OK;
 }
 
@@ -328,10 +370,13 @@ mxmoe_status mxmoe_layer_profile_read(float* ms, int n) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MXMOE_ERR_CUDA;
   if (!g_prof_valid[dev]) return MXMOE_ERR_UNSUPPORTED;
-  if (cudaEventSynchronize(g_prof_ev[dev][kProfEvents - 1]) != cudaSuccess) return MXMOE_ERR_CUDA;
+  const bool full = g_prof_mode[dev] == 1;
+  const int last = full ? kProfEvents - 1 : 3;
+  if (cudaEventSynchronize(g_prof_ev[dev][last]) != cudaSuccess) return MXMOE_ERR_CUDA;
   for (int i = 0; i < n && i < kProfEvents - 1; ++i) {
     float t = 0.f;
-    if (cudaEventElapsedTime(&t, g_prof_ev[dev][i], g_prof_ev[dev][i + 1]) != cudaSuccess)
+    if ((full || i == 2) &&
+        cudaEventElapsedTime(&t, g_prof_ev[dev][i], g_prof_ev[dev][i + 1]) != cudaSuccess)
       return MXMOE_ERR_CUDA;
     ms[i] = t;
   }

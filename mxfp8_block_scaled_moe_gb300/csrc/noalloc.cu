@@ -26,21 +26,26 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 int32_t* g_scratch_ptr[kMaxDevices] = {nullptr};
+uint64_t g_scratch_ctx[kMaxDevices] = {0};  // context id the cached address belongs to
 
 // Device address of g_route_scratch on the current device.  In host code the
 // array's name is only a host-side stand-in, never a device address, so the
-// address is looked up once per device with that device current.
+// address is looked up with that device current: once per device and
+// context (after cudaDeviceReset the device's new primary context holds a
+// new copy of the array, and the address is looked up again).
 cudaError_t scratch_address(int32_t** out) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  const uint64_t ctx = context_id();
+  if (!g_scratch_ptr[dev] || ctx == 0 || ctx != g_scratch_ctx[dev]) {
     void* p = nullptr;
     err = cudaGetSymbolAddress(&p, g_route_scratch);
     if (err != cudaSuccess) return err;
     g_scratch_ptr[dev] = static_cast<int32_t*>(p);
+    g_scratch_ctx[dev] = context_id();
   }
   *out = g_scratch_ptr[dev];
   return cudaSuccess;
