@@ -40,10 +40,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 FP8_OVER_BF16 = 2.0   # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 FP4_OVER_BF16 = 6.0   # nominal dense ratio (13.5 / 2.25 PFLOP/s): e2m1 x e2m1 MMAs
 
-# dram__bytes_read.sum + dram__bytes_write.sum of one grouped GEMM1 launch on
-# the bench workload (profiles/gemm1_swiglu_quant_qwen3_30b_prefill.md, the
-# DRAM-bytes capture at its end), keyed
-# by the hash of the sources it was captured from
+# DRAM traffic of one grouped GEMM1 launch on the bench workload: ncu's
+# dram__bytes_read.sum + dram__bytes_write.sum from a one-pass capture of the
+# profile_case layer run, keyed by the hash of the GEMM sources it was taken
+# on (a changed kernel reports no traffic until it is captured again)
 NCU_TRAFFIC = {"a9ec3d6a1d8bbad4": 786553600, "64d58b0d55536f8c": 786384128,
                "f21fe81032a4b103": 786399488, "afe529db44d76b76": 787179008}
 
@@ -73,6 +73,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-linear", action="store_true")
+    ap.add_argument("--no-configs", action="store_true")
     return ap.parse_args()
 
 
@@ -300,6 +301,114 @@ def dense_linear_bench(torch, mm, workloads, dev, flush, stream, peak, hbm, fp4=
     return out
 
 
+def gemm_algorithmic(T, H, E_touched, k, I):
+    """Flops and bytes of the two grouped GEMMs of one layer call: every
+    expanded row read once, every touched expert's weights (payload + e8m0
+    scales) read once, the outputs written once."""
+    M = T * k
+    sc = 1 + 1 / 32
+    g1 = dict(flops=2.0 * M * 2 * I * H,
+              bytes=M * H * sc + E_touched * 2 * I * H * sc + M * I * sc)
+    g2 = dict(flops=2.0 * M * H * I,
+              bytes=M * I * sc + E_touched * H * I * sc + 2.0 * M * H)
+    return g1, g2
+
+
+def kernel_roofline(ms, flops, nbytes, fp8_peak, hbm):
+    """TFLOP/s and GB/s of one launch, their fractions of the MXFP8 tensor
+    peak and of HBM, and the fraction of the launch's own roofline (the
+    larger of its tensor-bound and HBM-bound times over the measured one)."""
+    tf = flops / (ms / 1e3) / 1e12
+    gb = nbytes / (ms / 1e3) / 1e9
+    t_tensor = flops / (fp8_peak * 1e12) * 1e3
+    t_hbm = nbytes / (hbm * 1e9) * 1e3
+    return {"ms": round(ms, 4), "TFLOP/s": round(tf, 1), "frac_fp8_peak": round(tf / fp8_peak, 4),
+            "GB/s": round(gb, 1), "frac_hbm": round(gb / hbm, 4),
+            "bound": "tensor" if t_tensor >= t_hbm else "hbm",
+            "frac_roofline": round(max(t_tensor, t_hbm) / ms, 4)}
+
+
+CONFIG_BENCH = (("qwen3_30b_decode", None), ("qwen3_235b_prefill", None)) + tuple(
+    ("qwen3_30b_skewed", t) for t in (1, 8, 128, 1024, 4096, 16384))
+
+
+def layer_config_bench(torch, mm, workloads, dev, flush, stream, name, T, fp8_peak, hbm,
+                       steps=20):
+    """One layer configuration, timed like the headline step (L2 flushed,
+    CUDA events on the stream) with the library's per-kernel events: tokens/s
+    and each kernel against its roofline."""
+    shape = workloads.CONFIGS[name] if T is None else workloads.CONFIGS[name].with_tokens(T)
+    T, H, E, k, I = shape.T, shape.H, shape.E, shape.k, shape.I
+    inp = workloads.make_layer(shape, dev)
+    if shape.offline:
+        layer = mm.MXFP8MoELayer.from_quantized(inp["w13q"], inp["w13s"], inp["w2q"], inp["w2s"],
+                                                k)
+    else:
+        layer = mm.MXFP8MoELayer.from_bf16(inp["w13"], inp["w2"], k)
+    for key in ("w13", "w2", "w13q", "w13s", "w2q", "w2s"):
+        inp.pop(key, None)
+    x, logits = inp["x"], inp["logits"]
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    counts = mm.moe_route_quant_mxfp8(x, logits, k)["expert_counts"].cpu()
+    e_touched = int((counts > 0).sum())
+    for _ in range(3):
+        layer(x, logits, out=out)
+    torch.cuda.synchronize()
+    # eager calls (no instrumentation), then a pass with events at every
+    # kernel boundary for the per-kernel times
+    step_ms = statistics.mean(time_fn(torch, lambda: layer(x, logits, out=out), steps, flush,
+                                      stream))
+    mm.api.layer_profile_enable(True)
+    prof = []
+    for _ in range(steps):
+        flush.fill_(1)
+        layer(x, logits, out=out)
+        prof.append(mm.api.layer_profile_read())
+    mm.api.layer_profile_enable(False)
+    # the same call replayed from a CUDA graph (no host launch cost)
+    graph_ms = None
+    try:
+        gs = torch.cuda.Stream()
+        gs.wait_stream(stream)
+        with torch.cuda.stream(gs):
+            layer(x, logits, out=out)
+        stream.wait_stream(gs)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            layer(x, logits, out=out)
+        g.replay()
+        torch.cuda.synchronize()
+        graph_ms = statistics.mean(time_fn(torch, g.replay, steps, flush, stream))
+        del g
+    except Exception as exc:  # graph capture unavailable: report the eager time only
+        graph_ms = f"unavailable: {exc}"
+    if mm.device_status() != 0:
+        raise RuntimeError(f"device status error in the {shape.name} layer")
+
+    def km(key):
+        return statistics.mean(p_[key] for p_ in prof)
+    ab = algorithmic_bytes(T, H, E, k, I)
+    g1, g2 = gemm_algorithmic(T, H, e_touched, k, I)
+    r_ms, f_ms = km("route_quant"), km("finalize")
+    ent = {"T": T, "H": H, "E": E, "k": k, "I": I, "experts_touched": e_touched,
+           "max_expert_rows": int(counts.max()), "empty_experts": int((counts == 0).sum()),
+           "ms_per_step": round(step_ms, 4), "tokens_per_s": round(T / (step_ms / 1e3), 1),
+           "graph_ms_per_step": round(graph_ms, 4) if isinstance(graph_ms, float) else graph_ms,
+           "graph_tokens_per_s": (round(T / (graph_ms / 1e3), 1)
+                                  if isinstance(graph_ms, float) else None),
+           "route_quant": {"ms": round(r_ms, 4), "GB/s": round(ab["route"] / r_ms / 1e6, 1),
+                           "frac_hbm": round(ab["route"] / r_ms / 1e6 / hbm, 4)},
+           "gemm1_swiglu_quant": kernel_roofline(km("gemm1_swiglu_quant"), g1["flops"],
+                                                 g1["bytes"], fp8_peak, hbm),
+           "gemm2": kernel_roofline(km("gemm2"), g2["flops"], g2["bytes"], fp8_peak, hbm),
+           "finalize": {"ms": round(f_ms, 4), "GB/s": round(ab["finalize"] / f_ms / 1e6, 1),
+                        "frac_hbm": round(ab["finalize"] / f_ms / 1e6 / hbm, 4)},
+           "steps": steps}
+    del layer, inp, x, logits, out
+    torch.cuda.empty_cache()
+    return shape.name, ent
+
+
 def algorithmic_bytes(T, H, E, k, I):
     M = T * k
     route = 2 * T * H + M * H + M * H // 32 + 4 * T * E + M * 4 * 4
@@ -488,7 +597,9 @@ def main():
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    mm.api.layer_profile_enable(True)   # CUDA events between the layer's kernels
+    # CUDA events around gmm1 only (the roofline's kernel); the other kernel
+    # boundaries keep their overlapped launches
+    mm.api.layer_profile_enable("gemm1")
     step_ms, prof = [], []
     with ClockSampler(local_rank, enabled=not args.no_clocks) as clk:
         clk.mark_start()
@@ -510,11 +621,22 @@ def main():
     total_ms = max_over_ranks(torch, dist, sum(step_ms), world, dev)
     value = whole_job_rate(world, T, args.steps, total_ms)
 
-    # ---- per-kernel times inside the timed steps (library events on the stream)
+    # ---- gmm1 inside the timed steps (library events on the stream); the
+    # other kernels from a pass with events at every boundary, after the
+    # timed region
+    gemm1_ms = statistics.mean(p_["gemm1_swiglu_quant"] for p_ in prof)
+    reps_b = max(5, min(args.steps, 20))
+    mm.api.layer_profile_enable(True)
+    prof_all = []
+    for _ in range(reps_b):
+        flush.fill_(1)
+        step()
+        prof_all.append(mm.api.layer_profile_read())
+    mm.api.layer_profile_enable(False)
+
     def kmean(key):
-        return statistics.mean(p_[key] for p_ in prof)
-    route_ms, gemm1_ms = kmean("route_quant"), kmean("gemm1_swiglu_quant")
-    gemm2_ms, fin_ms = kmean("gemm2"), kmean("finalize")
+        return statistics.mean(p_[key] for p_ in prof_all)
+    route_ms, gemm2_ms, fin_ms = kmean("route_quant"), kmean("gemm2"), kmean("finalize")
     # the two-step comparator (bf16 permute, then a separate quant pass)
     reps = max(5, min(args.steps, 20))
 
@@ -527,6 +649,7 @@ def main():
         raise RuntimeError("device status error during timing")
 
     ab = algorithmic_bytes(T, H, E, k, I)
+    g1_alg, g2_alg = gemm_algorithmic(T, H, E, k, I)
     gemm1_flops = 2.0 * M * (2 * I) * H
     gemm2_flops = 2.0 * M * H * I
     gemm1_tflops = gemm1_flops / (gemm1_ms * 1e-3) / 1e12
@@ -546,9 +669,10 @@ def main():
         "route_quant": {"ms": route_ms, "GB/s": ab["route"] / route_ms / 1e6,
                         "frac_hbm": ab["route"] / route_ms / 1e6 / hbm},
         "two_step_route_then_quant": {"ms": twostep_ms, "GB/s": ab["twostep"] / twostep_ms / 1e6},
-        "gemm1_swiglu_quant": {"ms": gemm1_ms, "TFLOP/s": gemm1_tflops,
-                               "frac_fp8_peak": gemm1_tflops / fp8_peak},
-        "gemm2": {"ms": gemm2_ms, "TFLOP/s": gemm2_tflops, "frac_fp8_peak": gemm2_tflops / fp8_peak},
+        "gemm1_swiglu_quant": kernel_roofline(gemm1_ms, g1_alg["flops"], g1_alg["bytes"],
+                                              fp8_peak, peaks["hbm_gbs"]),
+        "gemm2": kernel_roofline(gemm2_ms, g2_alg["flops"], g2_alg["bytes"], fp8_peak,
+                                 peaks["hbm_gbs"]),
         "finalize": {"ms": fin_ms, "GB/s": ab["finalize"] / fin_ms / 1e6,
                      "frac_hbm": ab["finalize"] / fin_ms / 1e6 / hbm},
     }
@@ -557,7 +681,8 @@ def main():
                                              "frac_hbm": ab["weight_quant"] / wq_ms / 1e6 / hbm}
     for v in kernels.values():
         for kk in list(v):
-            v[kk] = round(v[kk], 4)
+            if isinstance(v[kk], float):
+                v[kk] = round(v[kk], 4)
 
     # ---- end to end through the public host-buffer call (copies overlapped with compute)
     x_h = x.cpu().pin_memory()
@@ -678,6 +803,16 @@ def main():
         dense["parity"] = ("tests/test_gpu_linear.py (row quant bit-exact incl. the partial block; "
                            "exact structured GEMM; sampled outputs of every shape vs oracle)")
 
+    # every other layer configuration: decode, the 235B offline prefill and
+    # the skewed-load sweep (each against its own roofline)
+    configs = None
+    if rank == 0 and not args.no_configs:
+        configs = {}
+        for cname, cT in CONFIG_BENCH:
+            key, ent = layer_config_bench(torch, mm, workloads, dev, flush, stream, cname, cT,
+                                          fp8_peak, hbm)
+            configs[key] = ent
+
     cpu_base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from oracle import mx as omx  # noqa: F401
@@ -701,6 +836,10 @@ def main():
                        "timing": "CUDA events per step on the launching stream"},
             "roofline": roofline,
             "kernels": kernels,
+            "kernels_timing": "gemm1_swiglu_quant: library CUDA events around it inside the "
+                              "timed steps; route_quant, gemm2, finalize: a separate pass of "
+                              f"{reps_b} steps with events at every kernel boundary (L2 "
+                              "flushed), after the timed region",
             "clocks": clk.summary(),
             "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,
@@ -713,6 +852,7 @@ def main():
             "router": router,
             "dense_linear": dense,
             "w4a4": w4a4,
+            "configs": configs,
             "peaks": {"hbm_gbs": hbm, "fp8_tflops": fp8_peak, "source": peaks["source"],
                       "library_dense_gemm": lib_rates},
             "gemm_src": src_hash,
