@@ -152,9 +152,10 @@ mxmoe_status moe_route_quant_mxfp8(const uint16_t* x, const float* logits, int T
  * framework owns device memory and offers no workspace hook.
  *
  * Same arguments, results and layouts as moe_route_quant_mxfp8, minus the
- * workspace: the routing scratch (per-block expert histograms) lives in a
- * 1 MiB array inside the library that every GPU loading the library keeps
- * until the process exits.  Inputs and outputs remain the caller's.
+ * workspace: the routing scratch (per-block expert histograms, expert totals
+ * and a counter) lives in a 1 MiB + 4.25 KiB array inside the library that
+ * every GPU loading the library keeps until the process exits.  Inputs and
+ * outputs remain the caller's.
  *   - Limit: ceil(T / 64) * E <= 262144 (e.g. T = 131072 tokens at E = 128);
  *     larger calls return MXMOE_ERR_WORKSPACE and launch nothing.
  *   - The call allocates nothing (no cudaMalloc / cudaFree, no allocating
@@ -164,8 +165,9 @@ mxmoe_status moe_route_quant_mxfp8(const uint16_t* x, const float* logits, int T
  *     after cudaDeviceReset the next call (the first in the new context)
  *     looks it up again, and the array's contents start over.
  *   - Every call shares the one array.  Each call writes every scratch entry
- *     it later reads, so nothing has to start at zero, but calls that
- *     overlap on the GPU (other streams, other threads) race on it.
+ *     before it reads it (the counter is zeroed by the call's first kernel),
+ *     so nothing has to start at zero, but calls that overlap on the GPU
+ *     (other streams, other threads) race on it.
  */
 mxmoe_status moe_route_quant_mxfp8_noalloc(const uint16_t* x, const float* logits, int T, int H,
                                            int E, int k, int renormalize, uint8_t* xq,

@@ -217,16 +217,6 @@ __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Bulk prefetch of [p, p + bytes) into L2 (p 16-byte aligned, bytes a
-// multiple of 16), issued in 64 KB pieces; nothing waits for it.
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint64_t bytes) {
-  const char* c = static_cast<const char*>(p);
-  for (uint64_t off = 0; off < bytes; off += 65536) {
-    const uint32_t n = (uint32_t)(bytes - off < 65536 ? bytes - off : 65536);
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(c + off), "r"(n) : "memory");
-  }
-}
-
 // Record the first device-side error in the library's status word.
 __device__ __forceinline__ void report_error(int* status, int code) {
   if (status) atomicCAS(status, 0, code);

@@ -8,9 +8,9 @@
 // Every index is checked against [0, T*k) before it is used: an index
 // outside records MXMOE_ERR_DEVICE_CHECK in the status word and its slot
 // contributes nothing (row 0 is read with weight 0).
-// One warp per token; each lane owns 16 consecutive columns (one 32 B load per
-// source row), two 512-column chunks in flight.  Roofline: HBM-bound,
-// k*H*2 B read + H*2 B written per token.
+// One warp per token and 512-column chunk; each lane owns 16 consecutive
+// columns (one 32 B load per source row), eight source rows in flight.
+// Roofline: HBM-bound, k*H*2 B read + H*2 B written per token.
 #include "common.cuh"
 #include "internal.h"
 
@@ -19,8 +19,30 @@ namespace mxmoe {
 constexpr int kFinThreads = 256;
 constexpr int kErrDeviceCheck = 8;  // MXMOE_ERR_DEVICE_CHECK
 
-// Lane owns 16 consecutive columns (one 32-byte load per source row) of a
-// 512-column chunk; two chunks are in flight per iteration (2k loads).
+// One warp per (token, 512-column chunk); a lane owns 16 consecutive columns
+// (one 32-byte load per source row).  The slots go eight at a time: the eight
+// rows' loads are all in flight before the first multiply-add, so a warp
+// waits for memory once per eight slots whatever the batch size.
+constexpr int kFinChunk = 512;
+constexpr int kFinGroup = 8;
+
+// Read-only 32-byte / 16-byte loads the compiler may schedule freely (y does
+// not change while the kernel runs).
+__device__ __forceinline__ void ld_ro_v8(const void* p, uint32_t (&r)[8]) {
+  asm("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7])
+      : "l"(p));
+}
+__device__ __forceinline__ void ld_ro_v4x2(const void* p, uint32_t (&r)[8]) {
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "l"(p));
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+      : "l"(static_cast<const char*>(p) + 16));
+}
+
 template <bool kV8>
 __global__ void __launch_bounds__(kFinThreads) finalize_kernel(
     const uint16_t* __restrict__ y, const float* __restrict__ topk_w,
@@ -28,7 +50,10 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(
     int* status) {
   pdl_wait();  // y of the GEMM before (programmatic serialization)
   const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (kFinThreads / 32) + (threadIdx.x >> 5);
+  const int nch = (H + kFinChunk - 1) / kFinChunk;
+  const int64_t wid = (int64_t)blockIdx.x * (kFinThreads / 32) + (threadIdx.x >> 5);
+  const int t = (int)(wid / nch);
+  const int c = (int)(wid - (int64_t)t * nch);
   if (t >= T) return;  // warp-uniform
   int64_t my_row = 0;
   float my_w = 0.f;
@@ -41,62 +66,44 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(
       my_w = 0.f;
     }
   }
-  uint16_t* orow = out + (int64_t)t * H;
-  for (int c0 = 0; c0 < H; c0 += 1024) {  // warp-uniform trip count
-    const int ca = c0 + lane * 16, cb = ca + 512;
-    const bool oka = ca < H, okb = cb < H;
-    float acc_a[16], acc_b[16];
+  const int col = c * kFinChunk + lane * 16;
+  const bool ok = col < H;
+  float acc[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) { acc_a[i] = 0.f; acc_b[i] = 0.f; }
-    for (int j = 0; j < k; ++j) {
-      const int64_t row = __shfl_sync(0xffffffffu, my_row, j);
-      const float w = __shfl_sync(0xffffffffu, my_w, j);
-      uint32_t va[8], vb[8];
-      if (kV8) {
-        if (oka) ld_nc_v8(y + row * H + ca, va);
-        if (okb) ld_nc_v8(y + row * H + cb, vb);
-      } else {
-        if (oka) {
-          const uint4 u0 = ld_nc_v4(y + row * H + ca), u1 = ld_nc_v4(y + row * H + ca + 8);
-          va[0] = u0.x; va[1] = u0.y; va[2] = u0.z; va[3] = u0.w;
-          va[4] = u1.x; va[5] = u1.y; va[6] = u1.z; va[7] = u1.w;
-        }
-        if (okb) {
-          const uint4 u0 = ld_nc_v4(y + row * H + cb), u1 = ld_nc_v4(y + row * H + cb + 8);
-          vb[0] = u0.x; vb[1] = u0.y; vb[2] = u0.z; vb[3] = u0.w;
-          vb[4] = u1.x; vb[5] = u1.y; vb[6] = u1.z; vb[7] = u1.w;
-        }
+  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+  for (int j0 = 0; j0 < k; j0 += kFinGroup) {  // warp-uniform
+    uint32_t v[kFinGroup][8];
+#pragma unroll
+    for (int u = 0; u < kFinGroup; ++u) {
+      const int64_t row = __shfl_sync(0xffffffffu, my_row, (j0 + u) & 31);
+      if (ok && j0 + u < k) {
+        if (kV8) ld_ro_v8(y + row * H + col, v[u]);
+        else ld_ro_v4x2(y + row * H + col, v[u]);
       }
-      if (oka) {
+    }
+    // fp32 multiply-adds in slot order j = 0, 1, ..., k - 1
+#pragma unroll
+    for (int u = 0; u < kFinGroup; ++u) {
+      const float w = __shfl_sync(0xffffffffu, my_w, (j0 + u) & 31);
+      if (ok && j0 + u < k) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          acc_a[2 * i] = fmaf(w, bf16_bits_to_float(va[i] & 0xFFFFu), acc_a[2 * i]);
-          acc_a[2 * i + 1] = fmaf(w, bf16_bits_to_float(va[i] >> 16), acc_a[2 * i + 1]);
-        }
-      }
-      if (okb) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          acc_b[2 * i] = fmaf(w, bf16_bits_to_float(vb[i] & 0xFFFFu), acc_b[2 * i]);
-          acc_b[2 * i + 1] = fmaf(w, bf16_bits_to_float(vb[i] >> 16), acc_b[2 * i + 1]);
+          acc[2 * i] = fmaf(w, bf16_bits_to_float(v[u][i] & 0xFFFFu), acc[2 * i]);
+          acc[2 * i + 1] = fmaf(w, bf16_bits_to_float(v[u][i] >> 16), acc[2 * i + 1]);
         }
       }
     }
-    uint32_t oa[8], ob[8];
+  }
+  if (!ok) return;
+  uint32_t o[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      oa[i] = cvt_bf16x2(acc_a[2 * i], acc_a[2 * i + 1]);
-      ob[i] = cvt_bf16x2(acc_b[2 * i], acc_b[2 * i + 1]);
-    }
-    if (kV8) {
-      if (oka) st_cs_v8(orow + ca, oa);
-      if (okb) st_cs_v8(orow + cb, ob);
-    } else {
-      if (oka) { st_cs_v4(orow + ca, make_uint4(oa[0], oa[1], oa[2], oa[3]));
-                 st_cs_v4(orow + ca + 8, make_uint4(oa[4], oa[5], oa[6], oa[7])); }
-      if (okb) { st_cs_v4(orow + cb, make_uint4(ob[0], ob[1], ob[2], ob[3]));
-                 st_cs_v4(orow + cb + 8, make_uint4(ob[4], ob[5], ob[6], ob[7])); }
-    }
+  for (int i = 0; i < 8; ++i) o[i] = cvt_bf16x2(acc[2 * i], acc[2 * i + 1]);
+  uint16_t* dst = out + (int64_t)t * H + col;
+  if (kV8) {
+    st_cs_v8(dst, o);
+  } else {
+    st_cs_v4(dst, make_uint4(o[0], o[1], o[2], o[3]));
+    st_cs_v4(dst + 8, make_uint4(o[4], o[5], o[6], o[7]));
   }
 }
 
@@ -148,14 +155,15 @@ cudaError_t launch_finalize(const uint16_t* y, const float* topk_w, const int32_
                             int T, int k, int H, uint16_t* out, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   const int blocks = (int)ceil_div(T, kFinThreads / 32);
+  const int64_t chunk_blocks = ceil_div((int64_t)T * ceil_div(H, kFinChunk), kFinThreads / 32);
   int* st = device_status_ptr();
   // 16-column lanes need H % 16 == 0; 32-byte accesses need 32-byte aligned rows
   if (H % 16 == 0 && ((uintptr_t)y & 31u) == 0 && ((uintptr_t)out & 31u) == 0)
-    return launch_pdl(finalize_kernel<true>, dim3(blocks), dim3(kFinThreads), 0, stream, y, topk_w,
-                      src_to_sorted, T, k, H, out, st);
+    return launch_pdl(finalize_kernel<true>, dim3((unsigned)chunk_blocks), dim3(kFinThreads), 0,
+                      stream, y, topk_w, src_to_sorted, T, k, H, out, st);
   else if (H % 16 == 0)
-    return launch_pdl(finalize_kernel<false>, dim3(blocks), dim3(kFinThreads), 0, stream, y, topk_w,
-                      src_to_sorted, T, k, H, out, st);
+    return launch_pdl(finalize_kernel<false>, dim3((unsigned)chunk_blocks), dim3(kFinThreads), 0,
+                      stream, y, topk_w, src_to_sorted, T, k, H, out, st);
   else
     return launch_pdl(finalize_narrow_kernel, dim3(blocks), dim3(kFinThreads), 0, stream, y, topk_w,
                       src_to_sorted, T, k, H, out, st);

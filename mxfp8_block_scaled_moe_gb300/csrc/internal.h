@@ -22,6 +22,7 @@ uint64_t context_id();
 int* device_status_ptr();            // library status word on the current device
 long long wait_limit_cycles();
 bool use_two_sm_gemm(bool swiglu, int64_t M, int E);  // 2-SM grouped GEMM kernel?
+bool use_weight_prefetch();  // small-batch GEMMs: L2 prefetch of the next tile's weights?
 
 cudaError_t launch_mx_quantize(const uint16_t* x, int64_t rows, int64_t K, uint8_t* q,
                                uint8_t* scale, cudaStream_t stream);
@@ -60,6 +61,9 @@ cudaError_t launch_mx_dequantize_bf16(const uint8_t* q, const uint8_t* s, int64_
                                       uint16_t* out, cudaStream_t stream);
 
 size_t route_workspace_bytes(int T, int E);
+// Bytes of the routing scratch's histogram part; the expert totals [E] and
+// the scan's completion counter follow it (the counter at int E of them).
+size_t route_hist_bytes(int T, int E);
 
 // Launch with programmatic stream serialization: the kernel may begin while
 // its predecessor on the stream is still running and must call pdl_wait()

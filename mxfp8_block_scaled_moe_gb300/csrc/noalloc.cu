@@ -18,8 +18,11 @@
 
 namespace mxmoe {
 
-// 1 MiB of scratch: room for ceil(T / 64) * E <= 262144 histogram entries.
-constexpr size_t kNoAllocScratchInts = 262144;
+// Scratch for ceil(T / 64) * E <= 262144 histogram entries (1 MiB) plus the
+// routing scan's expert totals and completion counter (E + 1 <= 1025 ints,
+// 256-byte aligned).
+constexpr int64_t kNoAllocHistInts = 262144;
+constexpr size_t kNoAllocScratchInts = kNoAllocHistInts + 1088;
 static __device__ __align__(256) int32_t g_route_scratch[kNoAllocScratchInts];
 
 namespace {
@@ -65,7 +68,7 @@ extern "C" mxmoe_status moe_route_quant_mxfp8_noalloc(
   if ((int64_t)T * k >= (1ll << 31)) return MXMOE_ERR_SHAPE;
   // the built-in scratch is the workspace: reject sizes it cannot hold
   const int64_t nb = ceil_div(T, kRouteTokensPerBlock);
-  if (nb * (int64_t)E > (int64_t)kNoAllocScratchInts) return MXMOE_ERR_WORKSPACE;
+  if (nb * (int64_t)E > kNoAllocHistInts) return MXMOE_ERR_WORKSPACE;
   int32_t* scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return MXMOE_ERR_CUDA;
   return moe_route_quant_mxfp8(x, logits, T, H, E, k, renormalize, xq, xs, topk_ids, topk_w,

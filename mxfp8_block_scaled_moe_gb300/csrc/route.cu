@@ -36,18 +36,20 @@ constexpr int kRouteThreads = 256;
 constexpr int kRouteWarps = kRouteThreads / 32;
 
 
-// TPW tokens per warp (kRouteTokensPerBlock / TPW warps per block): four for
-// narrow rows, whose warp reductions interleave; two for wide rows, where
-// more would not fit in the registers.
+// TPW tokens per warp (kRouteTokensPerBlock / TPW warps per block): two, so a
+// 64-token block runs 32 warps.  The selection is a chain of dependent warp
+// reductions per token; the two tokens of a warp interleave, and the block's
+// 32 warps keep the SM's schedulers busy (with four tokens per warp and 16
+// warps, each warp's ~1800-instruction chain set the kernel's length).
 template <int EPL>
-constexpr int topk_tokens_per_warp() { return EPL <= 4 ? 4 : 2; }
+constexpr int topk_tokens_per_warp() { return 2; }
 
 template <int EPL, int TPW = topk_tokens_per_warp<EPL>()>  // logits per lane: E <= 32 * EPL
 __global__ void __launch_bounds__(32 * (kRouteTokensPerBlock / TPW)) route_topk_rank_kernel(
     const float* __restrict__ logits, int T, int E, int k, int renormalize,
     int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
     int32_t* __restrict__ local_rank, int32_t* __restrict__ block_hist,
-    const uint16_t* __restrict__ x_prefetch, int H) {
+    int32_t* __restrict__ scan_counter) {
   constexpr int WARPS = kRouteTokensPerBlock / TPW;
   // s_mask[e] bit tl: token tl of this block chose expert e.  A token's k
   // experts are distinct, so its rank among the block's rows of expert e in
@@ -59,10 +61,9 @@ __global__ void __launch_bounds__(32 * (kRouteTokensPerBlock / TPW)) route_topk_
   // the scan and permute kernels may be scheduled now (they wait for this
   // grid's results before reading them)
   pdl_launch_dependents();
-  // the block's hidden-state rows (contiguous) head for L2 while the top-k
-  // runs, so the permutation reads them from L2 instead of HBM
-  if (x_prefetch && threadIdx.x == 0)
-    prefetch_l2_bulk(x_prefetch + (int64_t)t0 * H, (uint64_t)nt * H * 2);
+  // the scan's completion counter starts at zero (the scan reads it only
+  // after this grid has finished)
+  if (blockIdx.x == 0 && threadIdx.x == 0) scan_counter[0] = 0;
 
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_mask[e] = 0ull;
   __syncthreads();
@@ -112,13 +113,18 @@ __global__ void __launch_bounds__(32 * (kRouteTokensPerBlock / TPW)) route_topk_
     block_hist[(int64_t)e * gridDim.x + blockIdx.x] = __popcll(s_mask[e]);
 }
 
-// One block of 1024 threads over the expert-major histogram hist[e][b] (nb
-// blocks per row).  Each warp takes whole expert rows (e = warp, warp + 32,
-// ...): 32 consecutive blocks per load, a shuffle scan per 32, and the row is
-// rewritten as its exclusive prefix (the block's base row inside expert e).
-// Then the expert totals are scanned into counts, offsets and the experts'
-// first 128-row blocks of the tiled scale layout.
-constexpr int kScanThreads = 1024;
+// The scan, over the expert-major histogram hist[e][b] (nb blocks per row):
+// one warp per expert row, four per CTA.  A warp loads its row 256 blocks at a
+// time (lane l holds blocks l, l + 32, ..., l + 224: coalesced, all in
+// flight together), scans the eight 32-block chunks independently (their
+// shuffle chains interleave), joins them by the prefix of the chunk totals,
+// and rewrites the row as its exclusive prefix (each block's base row inside
+// expert e); the row total goes to totals[e].  The CTA that finishes last
+// (a ticket on a counter the top-k kernel zeroed; no CTA waits for another)
+// scans the totals into counts, offsets and the experts' first 128-row
+// blocks of the tiled scale layout.
+constexpr int kScanWarps = 4;
+constexpr int kScanThreads = 32 * kScanWarps;
 
 __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
 #pragma unroll
@@ -129,15 +135,15 @@ __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
   return v;
 }
 
-// Exclusive scan of one value per thread over the block (values of threads
-// >= n count as 0); *total receives the sum.  s_warp: 32 ints.
+// Exclusive scan of one value per thread over the block (blockDim.x a
+// multiple of 32, at most 1024); *total receives the sum.  s_warp: 33 ints.
 __device__ __forceinline__ int block_excl_scan(int v, int* s_warp, int* total) {
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int incl = warp_incl_scan(v, lane);
   if (lane == 31) s_warp[w] = incl;
   __syncthreads();
   if (w == 0) {
-    const int x = s_warp[lane];
+    const int x = lane < (int)(blockDim.x >> 5) ? s_warp[lane] : 0;
     const int xi = warp_incl_scan(x, lane);
     s_warp[lane] = xi - x;
     if (lane == 31) s_warp[32] = xi;
@@ -148,61 +154,156 @@ __device__ __forceinline__ int block_excl_scan(int v, int* s_warp, int* total) {
   return r;
 }
 
-__global__ void __launch_bounds__(kScanThreads) route_scan_kernel(int32_t* __restrict__ hist,
-                                                                  int nb, int E,
-                                                                  int64_t* __restrict__ counts,
-                                                                  int64_t* __restrict__ offsets,
-                                                                  int32_t* __restrict__ tile_base) {
+__global__ void __launch_bounds__(kScanThreads) route_scan_kernel(
+    int32_t* __restrict__ hist, int nb, int E, int32_t* __restrict__ totals,
+    int32_t* __restrict__ counter, int64_t* __restrict__ counts, int64_t* __restrict__ offsets,
+    int32_t* __restrict__ tile_base) {
   pdl_launch_dependents();
-  pdl_wait();  // the top-k kernel's histograms
-  __shared__ int s_tot[1024];
+  pdl_wait();  // the top-k kernel's histograms (and its zeroed counter)
   __shared__ int s_warp[33];
+  __shared__ int s_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  constexpr int U = 8;  // 32-block chunks loaded together
-  for (int e = warp; e < E; e += kScanThreads / 32) {
+  const int e = blockIdx.x * kScanWarps + warp;
+  if (e < E) {
+    constexpr int U = 8;
     int32_t* row = hist + (int64_t)e * nb;
     int run = 0;
     for (int c0 = 0; c0 < nb; c0 += 32 * U) {
-      int v[U];
+      int v[U], incl[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int b = c0 + 32 * u + lane;
         v[u] = b < nb ? row[b] : 0;
+        incl[u] = v[u];
+      }
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int o = __shfl_up_sync(0xffffffffu, incl[u], off);
+          if (lane >= off) incl[u] += o;
+        }
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int b = c0 + 32 * u + lane;
-        const int incl = warp_incl_scan(v[u], lane);
-        if (b < nb) row[b] = run + incl - v[u];
-        run += __shfl_sync(0xffffffffu, incl, 31);
+        if (b < nb) row[b] = run + incl[u] - v[u];
+        run += __shfl_sync(0xffffffffu, incl[u], 31);
       }
     }
-    if (lane == 0) s_tot[e] = run;
+    if (lane == 0) totals[e] = run;
+  }
+  // last CTA: every row total is written (each CTA fences before its ticket)
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    s_last = atomicAdd(counter, 1) == (int)gridDim.x - 1;
   }
   __syncthreads();
-  // expert totals -> counts and offsets (E <= 1024: one expert per thread)
-  const int v = tid < E ? s_tot[tid] : 0;
-  int sum = 0;
-  const int excl = block_excl_scan(v, s_warp, &sum);
-  if (tid < E) {
-    counts[tid] = v;
-    offsets[tid] = excl;
+  if (!s_last) return;
+  __threadfence();
+  // E <= 1024 totals, up to eight per thread in expert order
+  constexpr int PER = 1024 / kScanThreads;
+  int c[PER], tsum = 0, tl = 0;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int x = tid * PER + i;
+    c[i] = x < E ? __ldcg(totals + x) : 0;
+    tsum += c[i];
+    tl += (c[i] + 127) / 128;
   }
-  if (tid == 0) offsets[E] = sum;
-  if (tile_base == nullptr) return;
-  // exclusive prefix of the experts' 128-row tile counts (tiled scale layout)
+  int sum = 0, tiles = 0;
+  int run = block_excl_scan(tsum, s_warp, &sum);
   __syncthreads();
-  const int tv = (v + 127) / 128;
-  int tsum = 0;
-  const int texcl = block_excl_scan(tv, s_warp, &tsum);
-  if (tid < E) tile_base[tid] = texcl;
-  if (tid == 0) tile_base[E] = tsum;
+  int trun = block_excl_scan(tl, s_warp, &tiles);
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int x = tid * PER + i;
+    if (x < E) {
+      counts[x] = c[i];
+      offsets[x] = run;
+      if (tile_base) tile_base[x] = trun;
+    }
+    run += c[i];
+    trun += (c[i] + 127) / 128;
+  }
+  if (tid == 0) {
+    offsets[E] = sum;
+    if (tile_base) tile_base[E] = tiles;
+  }
 }
 
+// One token's row, by one warp: each lane takes 32-element blocks of the
+// row, quantizes a block once and writes its payload and scale byte to the k
+// destination rows dest[0..k) (sfrow: their tiled-layout rows), or copies
+// the bf16 block there (two-step mode).
 // kQ: 0 = bf16 rows to xp; 1 = MXFP8 (xq [M, H] e4m3); 2 = MXFP4 (xq [M, H/2]
 // packed e2m1, the W4A4 path).  kTiled: xs goes to the MMA-ready tiled scale
 // layout (tiled_scales.h) instead of [M, H/32]; requires H % 128 == 0 and the
 // experts' tile bases.
+template <int kQ, bool kTiled, bool kV8>
+__device__ __forceinline__ void permute_token_row(const uint16_t* __restrict__ xr, int H, int k,
+                                                  int lane, const int64_t* dest,
+                                                  const int64_t* sfrow, uint8_t* __restrict__ xq,
+                                                  uint8_t* __restrict__ xs,
+                                                  uint16_t* __restrict__ xp) {
+  const int H32 = H / 32;
+  // the scale bytes of four consecutive blocks are four consecutive bytes of
+  // a destination row (tiled layout: always; [M, H/32]: when H/32 is a
+  // multiple of 4), so lanes 4i..4i+3 pool them and lane 4i stores one word
+  const bool words = kTiled || (H32 & 3) == 0;
+  for (int j0 = 0; j0 < H32; j0 += 32) {  // warp-uniform
+    const int blk = j0 + lane;
+    const bool on = blk < H32;
+    uint32_t w[16];
+    if (on) load_block32_bf16<kV8>(xr + blk * 32, w);
+    if (kQ == 0) {
+      if (!on) continue;
+      for (int j = 0; j < k; ++j) {
+        uint16_t* dst = xp + dest[j] * H + blk * 32;
+        if (kV8) {
+          st_cs_v8(dst, *reinterpret_cast<const uint32_t(*)[8]>(&w[0]));
+          st_cs_v8(dst + 16, *reinterpret_cast<const uint32_t(*)[8]>(&w[8]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            st_cs_v4(dst + 8 * i, make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]));
+        }
+      }
+      continue;
+    }
+    uint32_t o[8], sb = 0;
+    if (on) {
+      if (kQ == 2) sb = quant_block32_bf16_fp4(w, *reinterpret_cast<uint32_t(*)[4]>(&o[0]));
+      else sb = quant_block32_bf16(w, o);
+    }
+    // scale word of blocks (blk & ~3) .. +3 on lanes with lane % 4 == 0
+    uint32_t sw = sb;
+    sw |= __shfl_down_sync(0xffffffffu, sb, 1) << 8;
+    sw |= __shfl_down_sync(0xffffffffu, sb, 2) << 16;
+    sw |= __shfl_down_sync(0xffffffffu, sb, 3) << 24;
+    if (!on) continue;
+    const bool lead = (lane & 3) == 0;
+    for (int j = 0; j < k; ++j) {
+      const int64_t d = dest[j];
+      if (kQ == 2)
+        st_cs_v4(xq + d * (H / 2) + blk * 16, make_uint4(o[0], o[1], o[2], o[3]));
+      else
+        store_block32_e4m3<kV8>(xq + d * H + blk * 32, o);
+      if (words) {
+        if (lead) {
+          const int64_t off = kTiled ? tiled_scale_offset(sfrow[j], blk, H / 128) : d * H32 + blk;
+          *reinterpret_cast<uint32_t*>(xs + off) = sw;
+        }
+      } else {
+        xs[d * H32 + blk] = (uint8_t)sb;
+      }
+    }
+  }
+}
+
+// The permutation: a warp per token computes its k destination rows (offset
+// + the block's base inside the expert + the in-block rank) and moves the row.
 template <int kQ, bool kTiled, bool kV8>
 __global__ void __launch_bounds__(kRouteThreads) route_permute_kernel(
     const uint16_t* __restrict__ x, int T, int H, int E, int k,
@@ -232,66 +333,120 @@ __global__ void __launch_bounds__(kRouteThreads) route_permute_kernel(
     }
   }
   __syncwarp();
-  // one lane = one 32-element block of the row: quantized once, written to
-  // the k destination rows (32 B of payload + 1 scale byte each)
-  const uint16_t* xr = x + (int64_t)t * H;
-  const int H32 = H / 32;
-  for (int j0 = 0; j0 < H32; j0 += 32) {
-    const int blk = j0 + lane;
-    if (blk >= H32) break;
-    uint32_t w[16];
-    load_block32_bf16<kV8>(xr + blk * 32, w);
-    if (kQ == 2) {
-      uint32_t o[4];
-      const uint32_t sb = quant_block32_bf16_fp4(w, o);
-      for (int j = 0; j < k; ++j) {
-        const int64_t d = s_dest[warp][j];
-        st_cs_v4(xq + d * (H / 2) + blk * 16, make_uint4(o[0], o[1], o[2], o[3]));
-        if (kTiled)
-          xs[tiled_scale_offset(s_sfrow[warp][j], blk, H / 128)] = (uint8_t)sb;
-        else
-          xs[d * H32 + blk] = (uint8_t)sb;
-      }
-    } else if (kQ == 1) {
-      uint32_t o[8];
-      const uint32_t sb = quant_block32_bf16(w, o);
-      for (int j = 0; j < k; ++j) {
-        const int64_t d = s_dest[warp][j];
-        store_block32_e4m3<kV8>(xq + d * H + blk * 32, o);
-        if (kTiled)
-          xs[tiled_scale_offset(s_sfrow[warp][j], blk, H / 128)] = (uint8_t)sb;
-        else
-          xs[d * H32 + blk] = (uint8_t)sb;
-      }
-    } else {
-      for (int j = 0; j < k; ++j) {
-        uint16_t* dst = xp + s_dest[warp][j] * H + blk * 32;
-        if (kV8) {
-          st_cs_v8(dst, *reinterpret_cast<const uint32_t(*)[8]>(&w[0]));
-          st_cs_v8(dst + 16, *reinterpret_cast<const uint32_t(*)[8]>(&w[8]));
-        } else {
+  permute_token_row<kQ, kTiled, kV8>(x + (int64_t)t * H, H, k, lane, s_dest[warp], s_sfrow[warp],
+                                     xq, xs, xp);
+}
+
+// Small batches (T <= one 64-token routing block): the whole routing step in
+// one kernel.  Each CTA of a small grid repeats the top-k of all T tokens and
+// the expert scan (latency only: T x E logits from L2), so no CTA waits for
+// another; CTA 0 alone writes ids, weights, counts, offsets and tile bases,
+// and CTA c permutes tokens 4c .. 4c + 3.  Same
+// selection, weights, in-block ranks and offsets as the three-kernel path.
+constexpr int kSmallThreads = 1024;
+constexpr int kSmallWarps = kSmallThreads / 32;
+// tokens each CTA permutes (one per warp): the payload and scale stores of
+// a token's k rows spread over T / 4 SMs instead of queueing on one
+constexpr int kSmallTokensPerCta = 4;
+
+template <int EPL, int kQ, bool kTiled, bool kV8>
+__global__ void __launch_bounds__(kSmallThreads) route_small_kernel(
+    const uint16_t* __restrict__ x, const float* __restrict__ logits, int T, int H, int E, int k,
+    int renormalize, int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
+    int32_t* __restrict__ src_to_sorted, int32_t* __restrict__ sorted_to_src,
+    int64_t* __restrict__ counts, int64_t* __restrict__ offsets, int32_t* __restrict__ tile_base,
+    uint8_t* __restrict__ xq, uint8_t* __restrict__ xs, uint16_t* __restrict__ xp) {
+  __shared__ unsigned long long s_mask[1024];  // s_mask[e] bit t: token t chose expert e
+  __shared__ int s_ids[kRouteTokensPerBlock][32];
+  __shared__ int s_off[1024];
+  __shared__ int s_tb[1024];
+  __shared__ int s_warp[33];
+  __shared__ int64_t s_dest[kSmallWarps][32];
+  __shared__ int64_t s_sfrow[kSmallWarps][32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int e = tid; e < E; e += kSmallThreads) s_mask[e] = 0ull;
+  __syncthreads();
+  // ---- top-k of every token (T <= 64: four per warp)
+  constexpr int TPW = kRouteTokensPerBlock / kSmallWarps;
+  constexpr int NT = EPL <= 4 ? TPW : 1;
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            st_cs_v4(dst + 8 * i, make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]));
+  for (int g = 0; g < TPW / NT; ++g) {
+    const float* rows[NT];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      const int tl = warp + kSmallWarps * (g * NT + n);
+      rows[n] = tl < T ? logits + (int64_t)tl * E : nullptr;
+    }
+    int c[NT];
+    float v[NT], w[NT];
+    warp_topk_softmax<EPL, NT>(rows, E, k, renormalize != 0, lane, c, v, w);
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      const int tl = warp + kSmallWarps * (g * NT + n);
+      if (tl < T && lane < k) {
+        s_ids[tl][lane] = c[n];
+        atomicOr(&s_mask[c[n]], 1ull << tl);
+        if (blockIdx.x == 0) {
+          topk_ids[(int64_t)tl * k + lane] = c[n];
+          topk_w[(int64_t)tl * k + lane] = w[n];
         }
       }
     }
   }
+  __syncthreads();
+  // ---- expert counts -> offsets and tiled-scale row-block bases (one
+  // expert per thread, E <= 1024)
+  const int c0 = tid < E ? __popcll(s_mask[tid]) : 0;
+  int sum = 0;
+  const int ex = block_excl_scan(c0, s_warp, &sum);
+  if (tid < E) s_off[tid] = ex;
+  __syncthreads();
+  const int t0c = (c0 + 127) / 128;
+  int tsum = 0;
+  const int tex = block_excl_scan(t0c, s_warp, &tsum);
+  if (tid < E) s_tb[tid] = tex;
+  if (blockIdx.x == 0) {
+    if (tid < E) { counts[tid] = c0; offsets[tid] = ex; if (tile_base) tile_base[tid] = tex; }
+    if (tid == 0) { offsets[E] = sum; if (tile_base) tile_base[E] = tsum; }
+  }
+  __syncthreads();
+  // ---- the permutation: token t = this CTA's first token + warp
+  const int t = blockIdx.x * kSmallTokensPerCta + warp;
+  if (warp >= kSmallTokensPerCta || t >= T) return;  // warp-uniform
+  if (lane < k) {
+    const int e = s_ids[t][lane];
+    const int64_t f = (int64_t)t * k + lane;
+    const int64_t rank = __popcll(s_mask[e] & ((1ull << t) - 1ull));
+    const int64_t dest = s_off[e] + rank;
+    src_to_sorted[f] = (int32_t)dest;
+    sorted_to_src[dest] = (int32_t)f;
+    s_dest[warp][lane] = dest;
+    if (kTiled) s_sfrow[warp][lane] = ((int64_t)s_tb[e] + rank / 128) * 128 + (rank % 128);
+  }
+  __syncwarp();
+  permute_token_row<kQ, kTiled, kV8>(x + (int64_t)t * H, H, k, lane, s_dest[warp], s_sfrow[warp],
+                                     xq, xs, xp);
 }
 
-size_t route_workspace_bytes(int T, int E) {
+// Routing scratch: the histograms [E][nb], then the expert totals [E] and
+// the scan's completion counter (one int), each piece 256-byte aligned.
+size_t route_hist_bytes(int T, int E) {
   const int64_t nb = ceil_div(T, kRouteTokensPerBlock);
   const size_t b = (size_t)(nb > 0 ? nb : 1) * (size_t)E * sizeof(int32_t);
   return (b + 255) & ~(size_t)255;
+}
+size_t route_workspace_bytes(int T, int E) {
+  return route_hist_bytes(T, E) + (((size_t)(E + 1) * sizeof(int32_t) + 255) & ~(size_t)255);
 }
 
 template <int EPL>
 static void launch_topk(int nb, size_t smem, cudaStream_t stream, const float* logits, int T,
                         int E, int k, int renorm, int32_t* ids, float* w, int32_t* rank,
-                        int32_t* hist, const uint16_t* x, int H) {
+                        int32_t* hist) {
   constexpr int threads = 32 * (kRouteTokensPerBlock / topk_tokens_per_warp<EPL>());
+  int32_t* counter = hist + route_hist_bytes(T, E) / sizeof(int32_t) + E;
   route_topk_rank_kernel<EPL><<<nb, threads, smem, stream>>>(logits, T, E, k, renorm, ids,
-                                                                   w, rank, hist, x, H);
+                                                                   w, rank, hist, counter);
 }
 
 cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, int E, int k,
@@ -307,6 +462,29 @@ cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, i
     return cudaMemsetAsync(offsets, 0, sizeof(int64_t) * (E + 1), stream);
   }
   const int nb = (int)ceil_div(T, kRouteTokensPerBlock);
+  if (!topk_done && nb == 1 && E <= 256) {
+    // one routing block: the single-kernel path
+    const int epl_s = (E + 31) / 32;
+    const int grid = (int)ceil_div(T, kSmallTokensPerCta);
+    const int rn_s = renormalize ? 1 : 0;
+    int32_t* tb = tile_base;
+#define MXMOE_SMALL(EPL, Q, TL)                                                                   \
+  route_small_kernel<EPL, Q, TL, false><<<grid, kSmallThreads, 0, stream>>>(                    \
+      x, logits, T, H, E, k, rn_s, topk_ids, topk_w, src_to_sorted, sorted_to_src, counts,    \
+      offsets, tb, Q ? xq : nullptr, Q ? xs : nullptr, Q ? nullptr : xp)
+#define MXMOE_SMALL_Q(EPL)                                                                        \
+  if (quant == 2) MXMOE_SMALL(EPL, 2, true);                                                      \
+  else if (quant && tile_base) MXMOE_SMALL(EPL, 1, true);                                         \
+  else if (quant) MXMOE_SMALL(EPL, 1, false);                                                     \
+  else MXMOE_SMALL(EPL, 0, false)
+    if (epl_s <= 1) { MXMOE_SMALL_Q(1); }
+    else if (epl_s <= 2) { MXMOE_SMALL_Q(2); }
+    else if (epl_s <= 4) { MXMOE_SMALL_Q(4); }
+    else { MXMOE_SMALL_Q(8); }
+#undef MXMOE_SMALL_Q
+#undef MXMOE_SMALL
+    return cudaGetLastError();
+  }
   const size_t smem1 = sizeof(unsigned long long) * (size_t)E;
   const int epl = (E + 31) / 32;
   const int rn = renormalize ? 1 : 0;
@@ -314,19 +492,20 @@ cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, i
   // the fused router (router.cu) already wrote ids, weights, ranks and
   // histograms.
   if (topk_done) {
-  } else if (epl <= 1)       launch_topk<1>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist, x, H);
-  else if (epl <= 2)  launch_topk<2>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist, x, H);
-  else if (epl <= 4)  launch_topk<4>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist, x, H);
-  else if (epl <= 8)  launch_topk<8>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist, x, H);
-  else if (epl <= 16) launch_topk<16>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist, x, H);
-  else                launch_topk<32>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist, x, H);
+  } else if (epl <= 1)       launch_topk<1>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist);
+  else if (epl <= 2)  launch_topk<2>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist);
+  else if (epl <= 4)  launch_topk<4>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist);
+  else if (epl <= 8)  launch_topk<8>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist);
+  else if (epl <= 16) launch_topk<16>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist);
+  else                launch_topk<32>(nb, smem1, stream, logits, T, E, k, rn, topk_ids, topk_w, src_to_sorted, block_hist);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
 
   // the scan and the permutation start early (programmatic dependent
   // launch) and wait on the device for their predecessor's results
-  err = launch_pdl(route_scan_kernel, dim3(1), dim3(kScanThreads), 0, stream, block_hist, nb, E,
-                   counts, offsets, tile_base);
+  int32_t* totals = block_hist + route_hist_bytes(T, E) / sizeof(int32_t);
+  err = launch_pdl(route_scan_kernel, dim3((unsigned)ceil_div(E, kScanWarps)), dim3(kScanThreads),
+                   0, stream, block_hist, nb, E, totals, totals + E, counts, offsets, tile_base);
   if (err != cudaSuccess) return err;
 
   const int nb3 = (int)ceil_div(T, kRouteWarps);

@@ -135,6 +135,34 @@ __device__ __forceinline__ void warp_topk_softmax(const float* const (&rows)[NT]
   // butterfly levels that lanes 0..k-1 need.
   int kp = 1;
   while (kp < k) kp <<= 1;
+  if (NT == 2 && renormalize && k <= 16) {
+    // both tokens in one pass: token n's slot j on lane 16 n + j (the
+    // butterfly's levels below kp <= 16 stay inside each half, so every
+    // weight gets the bits of the one-token pass)
+    const int j = lane & 15;
+    const float a = __shfl_sync(0xffffffffu, key_value(my_key[0]), j);
+    const float b = __shfl_sync(0xffffffffu, key_value(my_key[NT - 1]), j);
+    const float val = lane < 16 ? a : b;
+    const float vmax = __shfl_sync(0xffffffffu, val, lane & 16);
+    const float mine = j < k ? exp_of_difference(val, vmax) : 0.f;
+    float s_hi = mine, s_lo = 0.f;
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) {
+      if (off >= kp) continue;  // warp-uniform
+      const float oh = __shfl_xor_sync(0xffffffffu, s_hi, off);
+      const float ol = __shfl_xor_sync(0xffffffffu, s_lo, off);
+      const float h = __fadd_rn(s_hi, oh);
+      s_lo = __fadd_rn(__fadd_rn(s_lo, ol), two_sum_err(s_hi, oh, h));
+      s_hi = h;
+    }
+    const float w = __fdiv_rn(mine, __fadd_rn(s_hi, s_lo));
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      vals[n] = key_value(my_key[n]);
+      ws[n] = __shfl_sync(0xffffffffu, w, 16 * n + j);
+    }
+    return;
+  }
 #pragma unroll
   for (int n = 0; n < NT; ++n) {
     vals[n] = key_value(my_key[n]);
