@@ -20,11 +20,12 @@ constexpr int kFinThreads = 256;
 constexpr int kErrDeviceCheck = 8;  // MXMOE_ERR_DEVICE_CHECK
 
 // One warp per (token, 512-column chunk); a lane owns 16 consecutive columns
-// (one 32-byte load per source row).  The slots go eight at a time: the eight
-// rows' loads are all in flight before the first multiply-add, so a warp
-// waits for memory once per eight slots whatever the batch size.
+// (one 32-byte load per source row).  The slots go G at a time: the G rows'
+// loads are all in flight before the first multiply-add.  Small batches take
+// G = 8, so a warp waits for memory once per eight slots (there are too few
+// warps to hide a chain of k dependent loads); large batches take G = 2,
+// whose smaller register footprint keeps more warps per SM in flight.
 constexpr int kFinChunk = 512;
-constexpr int kFinGroup = 8;
 
 // Read-only 32-byte / 16-byte loads the compiler may schedule freely (y does
 // not change while the kernel runs).
@@ -43,7 +44,7 @@ __device__ __forceinline__ void ld_ro_v4x2(const void* p, uint32_t (&r)[8]) {
       : "l"(static_cast<const char*>(p) + 16));
 }
 
-template <bool kV8>
+template <bool kV8, int kFinGroup>
 __global__ void __launch_bounds__(kFinThreads) finalize_kernel(
     const uint16_t* __restrict__ y, const float* __restrict__ topk_w,
     const int32_t* __restrict__ src_to_sorted, int T, int k, int H, uint16_t* __restrict__ out,
@@ -157,16 +158,18 @@ cudaError_t launch_finalize(const uint16_t* y, const float* topk_w, const int32_
   const int blocks = (int)ceil_div(T, kFinThreads / 32);
   const int64_t chunk_blocks = ceil_div((int64_t)T * ceil_div(H, kFinChunk), kFinThreads / 32);
   int* st = device_status_ptr();
-  // 16-column lanes need H % 16 == 0; 32-byte accesses need 32-byte aligned rows
-  if (H % 16 == 0 && ((uintptr_t)y & 31u) == 0 && ((uintptr_t)out & 31u) == 0)
-    return launch_pdl(finalize_kernel<true>, dim3((unsigned)chunk_blocks), dim3(kFinThreads), 0,
-                      stream, y, topk_w, src_to_sorted, T, k, H, out, st);
-  else if (H % 16 == 0)
-    return launch_pdl(finalize_kernel<false>, dim3((unsigned)chunk_blocks), dim3(kFinThreads), 0,
-                      stream, y, topk_w, src_to_sorted, T, k, H, out, st);
-  else
-    return launch_pdl(finalize_narrow_kernel, dim3(blocks), dim3(kFinThreads), 0, stream, y, topk_w,
-                      src_to_sorted, T, k, H, out, st);
+  // 16-column lanes need H % 16 == 0; 32-byte accesses need 32-byte aligned
+  // rows; a few warps per SM take deep per-warp load groups, many take shallow ones
+  const bool deep = chunk_blocks <= 4 * (int64_t)num_sms();
+  const bool v8 = ((uintptr_t)y & 31u) == 0 && ((uintptr_t)out & 31u) == 0;
+  if (H % 16 == 0) {
+    auto kern = v8 ? (deep ? finalize_kernel<true, 8> : finalize_kernel<true, 2>)
+                   : (deep ? finalize_kernel<false, 8> : finalize_kernel<false, 2>);
+    return launch_pdl(kern, dim3((unsigned)chunk_blocks), dim3(kFinThreads), 0, stream, y,
+                      topk_w, src_to_sorted, T, k, H, out, st);
+  }
+  return launch_pdl(finalize_narrow_kernel, dim3(blocks), dim3(kFinThreads), 0, stream, y, topk_w,
+                    src_to_sorted, T, k, H, out, st);
 }
 
 }  // namespace mxmoe

@@ -22,7 +22,6 @@ uint64_t context_id();
 int* device_status_ptr();            // library status word on the current device
 long long wait_limit_cycles();
 bool use_two_sm_gemm(bool swiglu, int64_t M, int E);  // 2-SM grouped GEMM kernel?
-bool use_weight_prefetch();  // small-batch GEMMs: L2 prefetch of the next tile's weights?
 
 cudaError_t launch_mx_quantize(const uint16_t* x, int64_t rows, int64_t K, uint8_t* q,
                                uint8_t* scale, cudaStream_t stream);
