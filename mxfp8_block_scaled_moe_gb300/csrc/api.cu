@@ -448,10 +448,11 @@ static mxmoe_status forward_impl(const uint16_t* x, const float* logits, const u
                    w, s2s, src2s, counts, offs, (int32_t*)(b + L.hist), s, tbase, gate != nullptr);
   if (e != cudaSuccess) return MXMOE_ERR_CUDA;
   prof.mark(2);
-  e = launch_gemm_swiglu_quant(xq, xs, w13q, w13s_t, offs, M, E, H, I, aq, as, s, true, fmt);
+  // an expert's rows are at most T (the k experts of a token are distinct)
+  e = launch_gemm_swiglu_quant(xq, xs, w13q, w13s_t, offs, M, E, H, I, aq, as, s, true, fmt, T);
   if (e != cudaSuccess) return MXMOE_ERR_CUDA;
   prof.mark(3);
-  e = launch_gemm_bf16(aq, as, w2q, w2s_t, offs, M, E, I, H, y, s, true, fmt);
+  e = launch_gemm_bf16(aq, as, w2q, w2s_t, offs, M, E, I, H, y, s, true, fmt, 1, nullptr, T);
   if (e != cudaSuccess) return MXMOE_ERR_CUDA;
   prof.mark(4);
   e = launch_finalize(y, w, src2s, T, k, H, out, s);

@@ -53,11 +53,20 @@ constexpr int STAGES1 = 4;
 constexpr int SEG = 8;           // k-slices per scale segment
 constexpr int SEG_COLS = 128;    // TMEM columns per segment buffer (16 per k-slice)
 
-template <int BN_>
+// BMA: A rows staged per stage (the TMA box).  128 = the whole m-tile.  When
+// every group has at most BMA_SMALL rows (small batches: an expert's rows
+// are at most the token count), only the first BMA_SMALL rows of each tile
+// are loaded; the MMA still reads 128 rows from the stage's address on, the
+// rows past BMA_SMALL are whatever shared memory holds there and only ever
+// reach accumulator rows past the group's end, which the epilogue masks.
+// The 12 KB saved per stage buy a fifth stage: more weight bytes in flight.
+constexpr int BMA_SMALL = 32;
+
+template <int BN_, int BMA = BM>
 struct Layout1 {
   static constexpr int BN = BN_;
-  static constexpr int S = STAGES1;
-  static constexpr int A_BYTES = BM * BK;
+  static constexpr int S = BMA == BM ? STAGES1 : STAGES1 + 1;
+  static constexpr int A_BYTES = BMA * BK;
   static constexpr int B_BYTES = BN * BK;
   static constexpr int SFA_SEG = SEG * 512;               // one 512-byte chunk per k-slice
   static constexpr int SFB_SEG = (BN / 128) * SEG * 512;  // per 128-row block of B
@@ -85,11 +94,12 @@ struct Layout1 {
 // the same staging layout by cp.async.
 // kSplit: split-K tiles (Params::ksplit); the other instantiations fold the
 // split arithmetic away.
-template <int BN, bool kSwiglu, bool kTiledSF, int kFmt, bool kSplit>
+template <int BN, bool kSwiglu, bool kTiledSF, int kFmt, bool kSplit, int BMA = BM>
 __global__ void __launch_bounds__(THREADS1, 1)
     gemm1sm_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, const Params p) {
-  using L = Layout1<BN>;
+  using L = Layout1<BN, BMA>;
+  static_assert(BMA == BM || kTiledSF, "short A boxes take tiled scales");
   constexpr int STAGES = L::S;
   constexpr bool kFp4B = kFmt != FMT_W8A8, kFp4A = kFmt == FMT_W4A4;
   // W4A4: kind::mxf4 on packed operands, so a 128-byte k-slice holds 256
@@ -464,18 +474,18 @@ __global__ void __launch_bounds__(THREADS1, 1)
 
 // ---------------------------------------------------------------- host side
 
-template <int BN, bool kSwiglu, bool kTiledSF, int kFmt, bool kSplit = false>
+template <int BN, bool kSwiglu, bool kTiledSF, int kFmt, bool kSplit = false, int BMA = BM>
 static cudaError_t launch_single(const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
                                  const uint8_t* sfb, const int64_t* offsets, int64_t M, int E,
                                  int K, int Nw, int n_out, void* out, uint8_t* out_scale,
                                  cudaStream_t stream, int ksplit = 1, float* partial = nullptr) {
-  using L = Layout1<BN>;
+  using L = Layout1<BN, BMA>;
   if (M == 0) return cudaSuccess;
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   static uint64_t configured[64] = {0};  // context id the attribute was set in
-  auto kern = gemm1sm_kernel<BN, kSwiglu, kTiledSF, kFmt, kSplit>;
+  auto kern = gemm1sm_kernel<BN, kSwiglu, kTiledSF, kFmt, kSplit, BMA>;
   const uint64_t ctx = context_id();
   if (ctx == 0 || configured[dev] != ctx) {
     cudaError_t err =
@@ -487,7 +497,7 @@ static cudaError_t launch_single(const uint8_t* a, const uint8_t* sfa, const uin
   const uint32_t b_box_rows = kSwiglu ? BN / 2 : BN;
   // W4A4: packed bytes as they are (K / 2 per row); W4A8: B unpacked
   const uint64_t inner = kFmt == FMT_W4A4 ? (uint64_t)K / 2 : (uint64_t)K;
-  if (!make_map(&tmA, a, inner, (uint64_t)M, BK, BM))
+  if (!make_map(&tmA, a, inner, (uint64_t)M, BK, BMA))
     return cudaErrorInvalidValue;
   if (!make_map(&tmB, b, inner, (uint64_t)E * Nw, BK, b_box_rows, kFmt == FMT_W4A8))
     return cudaErrorInvalidValue;
@@ -516,12 +526,14 @@ static cudaError_t launch_single(const uint8_t* a, const uint8_t* sfa, const uin
 // to the 2-SM kernel when selected for this GEMM and the device can
 // co-schedule CTA pairs; both kernels give the same bytes.  By default gmm2
 // (bf16 out) takes the 2-SM kernel when experts average at least 4 m-tiles,
-// everything else the 1-SM kernel.
+// everything else the 1-SM kernel.  group_rows_max > 0 bounds every group's
+// row count (the caller's guarantee); at most BMA_SMALL rows select the 1-SM
+// kernel's short A boxes (MXFP8, MMA-layout scales, 256-wide tiles).
 template <int BN, bool kSwiglu, bool kTiledSF, int kFmt>
 static cudaError_t launch(const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
                           const uint8_t* sfb, const int64_t* offsets, int64_t M, int E, int K,
                           int Nw, int n_out, void* out, uint8_t* out_scale, cudaStream_t stream,
-                          int ksplit = 1, float* partial = nullptr) {
+                          int ksplit = 1, float* partial = nullptr, int64_t group_rows_max = 0) {
   if (ksplit > 1) {
     if constexpr (kSwiglu) {
       return cudaErrorNotSupported;
@@ -536,6 +548,11 @@ static cudaError_t launch(const uint8_t* a, const uint8_t* sfa, const uint8_t* b
                                                            n_out, out, out_scale, stream);
     if (err != cudaErrorNotSupported) return err;
   }
+  if constexpr (BN == 256 && kTiledSF && kFmt == FMT_W8A8) {
+    if (group_rows_max > 0 && group_rows_max <= BMA_SMALL)
+      return launch_single<BN, kSwiglu, kTiledSF, kFmt, false, BMA_SMALL>(
+          a, sfa, b, sfb, offsets, M, E, K, Nw, n_out, out, out_scale, stream);
+  }
   return launch_single<BN, kSwiglu, kTiledSF, kFmt>(a, sfa, b, sfb, offsets, M, E, K, Nw, n_out, out,
                                               out_scale, stream);
 }
@@ -545,7 +562,8 @@ static cudaError_t launch(const uint8_t* a, const uint8_t* sfa, const uint8_t* b
 cudaError_t launch_gemm_swiglu_quant(const uint8_t* xq, const uint8_t* xs, const uint8_t* w13q,
                                      const uint8_t* w13s, const int64_t* offsets, int64_t M,
                                      int E, int H, int I, uint8_t* aq, uint8_t* as,
-                                     cudaStream_t stream, bool tiled_scales, int fmt) {
+                                     cudaStream_t stream, bool tiled_scales, int fmt,
+                                     int64_t group_rows_max) {
   if (fmt == gemm::FMT_W4A8 || fmt == gemm::FMT_W4A4) {
     if (!tiled_scales) return cudaErrorNotSupported;
     if (fmt == gemm::FMT_W4A8)
@@ -557,7 +575,7 @@ cudaError_t launch_gemm_swiglu_quant(const uint8_t* xq, const uint8_t* xs, const
   if (fmt != gemm::FMT_W8A8) return cudaErrorNotSupported;
   if (tiled_scales)
     return gemm::launch<256, true, true, gemm::FMT_W8A8>(xq, xs, w13q, w13s, offsets, M, E, H, 2 * I,
-                                                   I, aq, as, stream);
+                                                   I, aq, as, stream, 1, nullptr, group_rows_max);
   return gemm::launch<256, true, false, gemm::FMT_W8A8>(xq, xs, w13q, w13s, offsets, M, E, H, 2 * I,
                                                   I, aq, as, stream);
 }
@@ -588,11 +606,11 @@ template <int kFmt>
 static cudaError_t launch_bf16_fmt(const uint8_t* aq, const uint8_t* as, const uint8_t* w2q,
                                    const uint8_t* w2s, const int64_t* offsets, int64_t M, int E,
                                    int I, int H, uint16_t* y, cudaStream_t stream, int ksplit,
-                                   float* partial) {
+                                   float* partial, int64_t group_rows_max) {
   cudaError_t err;
   if (ceil_div(H, 128) % 2 == 0)
     err = gemm::launch<256, false, true, kFmt>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y,
-                                               nullptr, stream, ksplit, partial);
+                                               nullptr, stream, ksplit, partial, group_rows_max);
   else
     err = gemm::launch<128, false, true, kFmt>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y,
                                                nullptr, stream, ksplit, partial);
@@ -620,20 +638,20 @@ int gemm_bf16_ksplit(int64_t M, int N, int K, bool packed_fp4) {
 cudaError_t launch_gemm_bf16(const uint8_t* aq, const uint8_t* as, const uint8_t* w2q,
                              const uint8_t* w2s, const int64_t* offsets, int64_t M, int E,
                              int I, int H, uint16_t* y, cudaStream_t stream, bool tiled_scales,
-                             int fmt, int ksplit, float* partial) {
+                             int fmt, int ksplit, float* partial, int64_t group_rows_max) {
   if (ksplit > 1 && (E != 1 || !tiled_scales || !partial)) return cudaErrorNotSupported;
   if (fmt == gemm::FMT_W4A8 || fmt == gemm::FMT_W4A4) {
     if (!tiled_scales) return cudaErrorNotSupported;
     return fmt == gemm::FMT_W4A8
                ? launch_bf16_fmt<gemm::FMT_W4A8>(aq, as, w2q, w2s, offsets, M, E, I, H, y, stream,
-                                                 ksplit, partial)
+                                                 ksplit, partial, group_rows_max)
                : launch_bf16_fmt<gemm::FMT_W4A4>(aq, as, w2q, w2s, offsets, M, E, I, H, y, stream,
-                                                 ksplit, partial);
+                                                 ksplit, partial, group_rows_max);
   }
   if (fmt != gemm::FMT_W8A8) return cudaErrorNotSupported;
   if (tiled_scales)
     return launch_bf16_fmt<gemm::FMT_W8A8>(aq, as, w2q, w2s, offsets, M, E, I, H, y, stream,
-                                           ksplit, partial);
+                                           ksplit, partial, group_rows_max);
   if (ceil_div(H, 128) % 2 == 0)
     return gemm::launch<256, false, false, gemm::FMT_W8A8>(aq, as, w2q, w2s, offsets, M, E, I, H, H, y,
                                                      nullptr, stream);

@@ -89,6 +89,9 @@ cudaError_t launch_finalize(const uint16_t* y, const float* topk_w, const int32_
 // Grouped GEMMs.  Return cudaErrorInvalidValue when a tensor map can't be built.
 // tiled_scales: every scale array (inputs and gmm1's output scales) is in the
 // tiled layout of tiled_scales.h instead of [rows, K/32].
+// group_rows_max > 0: the caller guarantees that no group has more rows (the
+// layer passes its token count: a token picks an expert at most once), which
+// lets small batches load only the first rows of each m-tile.
 // fmt: 0 = W8A8; 1 = W4A8 (w13q / w2q packed MXFP4, e2m1 [rows, K/2]); 2 =
 // W4A4 (the activations packed MXFP4 too, and gmm1's output aq [M, I/2]); 1
 // and 2 require tiled_scales.
@@ -96,7 +99,7 @@ cudaError_t launch_gemm_swiglu_quant(const uint8_t* xq, const uint8_t* xs, const
                                      const uint8_t* w13s, const int64_t* offsets, int64_t M,
                                      int E, int H, int I, uint8_t* aq, uint8_t* as,
                                      cudaStream_t stream, bool tiled_scales = false,
-                                     int fmt = 0);
+                                     int fmt = 0, int64_t group_rows_max = 0);
 // ksplit > 1 (E == 1, tiled scales): split-K over ksplit K ranges whose fp32
 // partial sums go to partial [ksplit][M][H], then one reduce kernel rounds
 // their in-order sum to bf16.
@@ -104,7 +107,7 @@ cudaError_t launch_gemm_bf16(const uint8_t* aq, const uint8_t* as, const uint8_t
                              const uint8_t* w2s, const int64_t* offsets, int64_t M, int E,
                              int I, int H, uint16_t* y, cudaStream_t stream,
                              bool tiled_scales = false, int fmt = 0, int ksplit = 1,
-                             float* partial = nullptr);
+                             float* partial = nullptr, int64_t group_rows_max = 0);
 // Split count the dense linear uses for an [M, K] x [N, K]^T product on the
 // current device (1 when the tiles alone fill the GPU).  packed_fp4: the W4A4
 // kernel, whose k-slices hold 256 K elements instead of 128 (never more splits

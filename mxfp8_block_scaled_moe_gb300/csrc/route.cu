@@ -233,32 +233,82 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(
   }
 }
 
-// One token's row, by one warp: each lane takes 32-element blocks of the
-// row, quantizes a block once and writes its payload and scale byte to the k
-// destination rows dest[0..k) (sfrow: their tiled-layout rows), or copies
-// the bf16 block there (two-step mode).
+// One token's row, by one warp, in chunks of 32 MX blocks: lane l of chunk c
+// takes the row's 32-element block 32 c + l, quantizes it once and writes its
+// payload and scale byte to the k destination rows dest[0..k) (sfrow: their
+// tiled-layout rows), or copies the bf16 block there (two-step mode).
 // kQ: 0 = bf16 rows to xp; 1 = MXFP8 (xq [M, H] e4m3); 2 = MXFP4 (xq [M, H/2]
 // packed e2m1, the W4A4 path).  kTiled: xs goes to the MMA-ready tiled scale
 // layout (tiled_scales.h) instead of [M, H/32]; requires H % 128 == 0 and the
 // experts' tile bases.
+//
+// A quantized chunk: the lane's payload words (4 for MXFP4), its scale byte,
+// and on lanes 4i the scale word of blocks 4i .. 4i + 3 (the scale bytes of
+// four consecutive blocks are four consecutive bytes of a destination row:
+// tiled layout always, [M, H/32] when H/32 is a multiple of 4, so one lane
+// stores the four as one word).
+struct QuantChunk {
+  uint32_t o[8];
+  uint32_t sb, sw;
+};
+
+template <int kQ, bool kV8>
+__device__ __forceinline__ void quant_chunk(const uint16_t* __restrict__ xr, int H32, int j0,
+                                            int lane, QuantChunk& q) {
+  const int blk = j0 + lane;
+  q.sb = 0;
+  if (blk < H32) {
+    uint32_t w[16];
+    load_block32_bf16<kV8>(xr + blk * 32, w);
+    if (kQ == 2) q.sb = quant_block32_bf16_fp4(w, *reinterpret_cast<uint32_t(*)[4]>(&q.o[0]));
+    else q.sb = quant_block32_bf16(w, q.o);
+  }
+  q.sw = q.sb;
+  q.sw |= __shfl_down_sync(0xffffffffu, q.sb, 1) << 8;
+  q.sw |= __shfl_down_sync(0xffffffffu, q.sb, 2) << 16;
+  q.sw |= __shfl_down_sync(0xffffffffu, q.sb, 3) << 24;
+}
+
+template <int kQ, bool kTiled, bool kV8>
+__device__ __forceinline__ void store_chunk(const QuantChunk& q, int H, int k, int j0, int lane,
+                                            const int64_t* dest, const int64_t* sfrow,
+                                            uint8_t* __restrict__ xq, uint8_t* __restrict__ xs) {
+  const int H32 = H / 32;
+  const int blk = j0 + lane;
+  if (blk >= H32) return;
+  const bool words = kTiled || (H32 & 3) == 0;
+  const bool lead = (lane & 3) == 0;
+  for (int j = 0; j < k; ++j) {
+    const int64_t d = dest[j];
+    if (kQ == 2)
+      st_cs_v4(xq + d * (H / 2) + blk * 16, make_uint4(q.o[0], q.o[1], q.o[2], q.o[3]));
+    else
+      store_block32_e4m3<kV8>(xq + d * H + blk * 32, q.o);
+    if (words) {
+      if (lead) {
+        const int64_t off = kTiled ? tiled_scale_offset(sfrow[j], blk, H / 128) : d * H32 + blk;
+        *reinterpret_cast<uint32_t*>(xs + off) = q.sw;
+      }
+    } else {
+      xs[d * H32 + blk] = (uint8_t)q.sb;
+    }
+  }
+}
+
+// Chunks [c0, ...) of the row: load, quantize (or copy) and store.
 template <int kQ, bool kTiled, bool kV8>
 __device__ __forceinline__ void permute_token_row(const uint16_t* __restrict__ xr, int H, int k,
                                                   int lane, const int64_t* dest,
                                                   const int64_t* sfrow, uint8_t* __restrict__ xq,
                                                   uint8_t* __restrict__ xs,
-                                                  uint16_t* __restrict__ xp) {
+                                                  uint16_t* __restrict__ xp, int c0 = 0) {
   const int H32 = H / 32;
-  // the scale bytes of four consecutive blocks are four consecutive bytes of
-  // a destination row (tiled layout: always; [M, H/32]: when H/32 is a
-  // multiple of 4), so lanes 4i..4i+3 pool them and lane 4i stores one word
-  const bool words = kTiled || (H32 & 3) == 0;
-  for (int j0 = 0; j0 < H32; j0 += 32) {  // warp-uniform
-    const int blk = j0 + lane;
-    const bool on = blk < H32;
-    uint32_t w[16];
-    if (on) load_block32_bf16<kV8>(xr + blk * 32, w);
+  for (int j0 = 32 * c0; j0 < H32; j0 += 32) {  // warp-uniform
     if (kQ == 0) {
-      if (!on) continue;
+      const int blk = j0 + lane;
+      if (blk >= H32) continue;
+      uint32_t w[16];
+      load_block32_bf16<kV8>(xr + blk * 32, w);
       for (int j = 0; j < k; ++j) {
         uint16_t* dst = xp + dest[j] * H + blk * 32;
         if (kV8) {
@@ -272,38 +322,20 @@ __device__ __forceinline__ void permute_token_row(const uint16_t* __restrict__ x
       }
       continue;
     }
-    uint32_t o[8], sb = 0;
-    if (on) {
-      if (kQ == 2) sb = quant_block32_bf16_fp4(w, *reinterpret_cast<uint32_t(*)[4]>(&o[0]));
-      else sb = quant_block32_bf16(w, o);
-    }
-    // scale word of blocks (blk & ~3) .. +3 on lanes with lane % 4 == 0
-    uint32_t sw = sb;
-    sw |= __shfl_down_sync(0xffffffffu, sb, 1) << 8;
-    sw |= __shfl_down_sync(0xffffffffu, sb, 2) << 16;
-    sw |= __shfl_down_sync(0xffffffffu, sb, 3) << 24;
-    if (!on) continue;
-    const bool lead = (lane & 3) == 0;
-    for (int j = 0; j < k; ++j) {
-      const int64_t d = dest[j];
-      if (kQ == 2)
-        st_cs_v4(xq + d * (H / 2) + blk * 16, make_uint4(o[0], o[1], o[2], o[3]));
-      else
-        store_block32_e4m3<kV8>(xq + d * H + blk * 32, o);
-      if (words) {
-        if (lead) {
-          const int64_t off = kTiled ? tiled_scale_offset(sfrow[j], blk, H / 128) : d * H32 + blk;
-          *reinterpret_cast<uint32_t*>(xs + off) = sw;
-        }
-      } else {
-        xs[d * H32 + blk] = (uint8_t)sb;
-      }
-    }
+    QuantChunk q;
+    quant_chunk<kQ, kV8>(xr, H32, j0, lane, q);
+    store_chunk<kQ, kTiled, kV8>(q, H, k, j0, lane, dest, sfrow, xq, xs);
   }
 }
 
 // The permutation: a warp per token computes its k destination rows (offset
 // + the block's base inside the expert + the in-block rank) and moves the row.
+// The row x[t] is an input of the routing step, complete before its first
+// kernel (an ordinary launch) started, and this kernel starts only after that
+// one did: so the first kPermPre chunks of the row are loaded and quantized
+// before the wait for the routing results, while the kernels before finish.
+constexpr int kPermPre = 1;
+
 template <int kQ, bool kTiled, bool kV8>
 __global__ void __launch_bounds__(kRouteThreads) route_permute_kernel(
     const uint16_t* __restrict__ x, int T, int H, int E, int k,
@@ -314,10 +346,18 @@ __global__ void __launch_bounds__(kRouteThreads) route_permute_kernel(
   __shared__ int64_t s_dest[kRouteWarps][32];
   __shared__ int64_t s_sfrow[kRouteWarps][32];  // tiled layout: 128-row block and row
   pdl_launch_dependents();
-  pdl_wait();  // ids, ranks, block bases and offsets of the two kernels before
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t = blockIdx.x * kRouteWarps + warp;
   if (t >= T) return;  // warp-uniform
+  const uint16_t* xr = x + (int64_t)t * H;
+  const int H32 = H / 32;
+  QuantChunk pre[kPermPre];
+  if constexpr (kQ != 0) {
+#pragma unroll
+    for (int c = 0; c < kPermPre; ++c)
+      if (32 * c < H32) quant_chunk<kQ, kV8>(xr, H32, 32 * c, lane, pre[c]);  // warp-uniform
+  }
+  pdl_wait();  // ids, ranks, block bases and offsets of the two kernels before
   const int b = t / kRouteTokensPerBlock;
   const int nbk = (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
   if (lane < k) {
@@ -333,8 +373,15 @@ __global__ void __launch_bounds__(kRouteThreads) route_permute_kernel(
     }
   }
   __syncwarp();
-  permute_token_row<kQ, kTiled, kV8>(x + (int64_t)t * H, H, k, lane, s_dest[warp], s_sfrow[warp],
-                                     xq, xs, xp);
+  if constexpr (kQ != 0) {
+#pragma unroll
+    for (int c = 0; c < kPermPre; ++c)
+      if (32 * c < H32)
+        store_chunk<kQ, kTiled, kV8>(pre[c], H, k, 32 * c, lane, s_dest[warp], s_sfrow[warp], xq,
+                                     xs);
+  }
+  permute_token_row<kQ, kTiled, kV8>(xr, H, k, lane, s_dest[warp], s_sfrow[warp], xq, xs, xp,
+                                     kQ != 0 ? kPermPre : 0);
 }
 
 // Small batches (T <= one 64-token routing block): the whole routing step in

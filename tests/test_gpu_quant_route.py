@@ -144,8 +144,11 @@ def test_route_quant_skewed_load(mm, T):
                                              (130, 512, 40, 8, True), (7, 2048, 128, 8, False),
                                              (300, 64, 256, 32, True), (64, 256, 8, 8, True),
                                              (200, 64, 600, 32, True), (130, 96, 1000, 4, False),
-                                             (70, 64, 1024, 8, True)])
+                                             (70, 64, 1024, 8, True), (20001, 64, 128, 8, True),
+                                             (9800, 32, 256, 6, False)])
 def test_route_quant_edge_shapes(mm, T, H, E, k, renorm):
+    """Odd E, E up to 256 at 313 routing blocks with a ragged last one (20001
+    tokens) and at 154 (9800), wide E (8+ logits per lane), ties."""
     g = torch.Generator(device=DEV).manual_seed(T * 7 + E)
     x = torch.randn(T, H, generator=g, device=DEV).to(torch.bfloat16)
     logits = torch.randn(T, E, generator=g, device=DEV)
@@ -178,6 +181,20 @@ def test_route_16_byte_aligned_input(mm, quant):
         torch.cuda.synchronize()
         ref = moe.permute_rows(xb, r["sorted_to_src"].cpu().numpy(), k)
         assert np.array_equal(bits16(r["xp"]), ref)
+
+
+def test_route_logits_not_16_byte_aligned_is_rejected(mm):
+    """Every input pointer of the routing call must be 16-byte aligned: logits
+    at a 4-byte aligned address return MXMOE_ERR_ALIGN before any launch."""
+    from mxfp8_block_scaled_moe_gb300._lib import MXMoEError
+    T, H, E, k = 100, 128, 128, 8
+    x = torch.zeros(T, H, dtype=torch.bfloat16, device=DEV)
+    logits = torch.zeros(T * E + 1, device=DEV)[1:].view(T, E)
+    assert logits.data_ptr() % 16 == 4
+    with pytest.raises(MXMoEError, match="MXMOE_ERR_ALIGN"):
+        mm.moe_route_quant_mxfp8(x, logits, k)
+    torch.cuda.synchronize()
+    assert mm.device_status() == 0
 
 
 def test_route_empty_batch(mm):
