@@ -117,6 +117,9 @@ EXACT_SHAPES = [
     (300, 1152, 4304),   # K = 4304: 135 scales, ragged last K slice
     (257, 272, 208),     # N = 272: odd row blocks (BN 128), 16-column tail
     (640, 512, 4304),    # enough rows for the 2-SM kernel
+    (32, 4096, 1152),    # decode-sized M: split-K over 2 K ranges
+    (20, 512, 4304),     # split-K over 7 K ranges, ragged last K slice
+    (31, 8192, 256),     # 32 tiles of one partial m-tile, no split
 ]
 
 
