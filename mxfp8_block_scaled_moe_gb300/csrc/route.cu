@@ -411,6 +411,11 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(
   __shared__ int64_t s_dest[kSmallWarps][32];
   __shared__ int64_t s_sfrow[kSmallWarps][32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the rows this CTA permutes start their way into L2 now, so the DRAM
+  // latency of their loads hides behind the top-k and the scan
+  if (lane == 0 && warp < kSmallTokensPerCta && blockIdx.x * kSmallTokensPerCta + warp < T)
+    prefetch_l2_bulk(x + (int64_t)(blockIdx.x * kSmallTokensPerCta + warp) * H,
+                     (uint32_t)H * 2u);
   for (int e = tid; e < E; e += kSmallThreads) s_mask[e] = 0ull;
   __syncthreads();
   // ---- top-k of every token (T <= 64: four per warp)
