@@ -217,12 +217,6 @@ __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Ask the L2 to fetch [p, p + bytes) (16-byte aligned, a multiple of 16
-// bytes); nothing waits for it.
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 // Record the first device-side error in the library's status word.
 __device__ __forceinline__ void report_error(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
