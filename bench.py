@@ -46,7 +46,7 @@ FP4_OVER_BF16 = 6.0   # nominal dense ratio (13.5 / 2.25 PFLOP/s): e2m1 x e2m1 M
 # on (a changed kernel reports no traffic until it is captured again)
 NCU_TRAFFIC = {"a9ec3d6a1d8bbad4": 786553600, "64d58b0d55536f8c": 786384128,
                "f21fe81032a4b103": 786399488, "afe529db44d76b76": 787179008,
-               "318d8521ea941ed5": 786471936}
+               "318d8521ea941ed5": 786471936, "7ede47c7a46a5cfc": 787526144}
 
 
 def max_over_ranks(torch, dist, ms, world, device):
@@ -97,12 +97,14 @@ def load_peaks():
     return dict(FALLBACK_PEAKS, source="fallback")
 
 
-GEMM_SOURCES = ("gemm.cu", "gemm_common.cuh", "tiled_scales.h", "common.cuh")
+GEMM_SOURCES = ("gemm.cu", "gemm2sm.cu", "gemm_common.cuh", "tiled_scales.h", "common.cuh",
+                "api.cu")
 
 
 def gemm_src_hash():
-    """Hash of the sources the 1-SM grouped GEMM kernel is compiled from; the
-    stored ncu traffic is only reported while it matches."""
+    """Hash of the sources the grouped GEMM kernels and their 1-SM / 2-SM
+    choice (api.cu) are compiled from; the stored ncu traffic is only
+    reported while it matches."""
     h = hashlib.sha256()
     for name in GEMM_SOURCES:
         with open(os.path.join(ROOT, "mxfp8_block_scaled_moe_gb300", "csrc", name), "rb") as f:

@@ -497,8 +497,9 @@ void mxmoe_set_wait_limit_cycles(long long cycles);
  * run the 2-SM kernel (tcgen05 cta_group::2 over CTA pairs) when the device
  * can co-schedule pairs.  mode 2 (the default): the 2-SM kernel for the
  * bf16-output GEMM (grouped GEMM2) when its rows average at least 512 per
- * expert (M >= 512 * E), the 1-SM kernel otherwise.  Other values select
- * mode 2.
+ * expert (M >= 512 * E) and for the SwiGLU GEMM (grouped GEMM1) when they
+ * average at least 1024 (M >= 1024 * E), the 1-SM kernel otherwise.  Other
+ * values select mode 2.
  */
 void mxmoe_set_gemm_2sm(int mode);
 

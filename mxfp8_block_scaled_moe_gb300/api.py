@@ -365,7 +365,7 @@ def set_gemm_2sm(mode="auto") -> None:
     """Grouped-GEMM kernel choice: False/0 = 1-SM kernel, True/1 = 2-SM kernel
     (cta_group::2) for the layer's 256-wide tiles, "auto"/2 (the default) =
     2-SM for grouped GEMM2 when it has at least 512 rows per expert on
-    average.  Both kernels give the same bytes."""
+    average and for grouped GEMM1 at 1024.  Both kernels give the same bytes."""
     m = 2 if mode == "auto" else int(mode)
     _lib.load().mxmoe_set_gemm_2sm(m)
 

@@ -19,16 +19,19 @@ __device__ int g_device_status = 0;
 
 static std::atomic<long long> g_wait_limit{0};
 // grouped GEMM kernel choice: 0 = 1-SM, 1 = 2-SM, 2 (default) = 2-SM for the
-// bf16-output GEMM when experts average at least 4 m-tiles.  A CTA pair
-// computes two m-tiles of one expert, so an expert with an odd m-tile count
-// pays a padded tile; with few m-tiles per expert that outweighs the pair's
-// third less L2 traffic (measured on GB300: the 16K-token Qwen3-30B-A3B and
-// 8K-token Qwen3-235B-A22B prefills gain, decode loses; gmm1 is even).
+// bf16-output GEMM when experts average at least 4 m-tiles, and for the SwiGLU
+// GEMM when they average at least 8.  A CTA pair computes two m-tiles of one
+// expert, so an expert with an odd m-tile count pays a padded tile; with few
+// m-tiles per expert that outweighs the pair's third less L2 traffic
+// (measured on GB300: gmm2 gains on the 16K-token Qwen3-30B-A3B and 8K-token
+// Qwen3-235B-A22B prefills and loses at decode; gmm1 gains 1-3% at 16K
+// tokens, plain or skewed, is even on the 235B prefill and loses 12% at 4K
+// skewed tokens).
 static std::atomic<int> g_use_2sm{2};
 
 bool use_two_sm_gemm(bool swiglu, int64_t M, int E) {
   const int m = g_use_2sm.load();
-  return m == 1 || (m == 2 && !swiglu && M >= 512 * (int64_t)E);
+  return m == 1 || (m == 2 && M >= (swiglu ? 1024 : 512) * (int64_t)E);
 }
 constexpr long long kDefaultWaitLimit = 1ll << 32;  // ~2 s at 2 GHz
 
