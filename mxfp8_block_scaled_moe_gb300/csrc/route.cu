@@ -307,9 +307,10 @@ __device__ __forceinline__ void permute_token_row(const uint16_t* __restrict__ x
                                                   int lane, const int64_t* dest,
                                                   const int64_t* sfrow, uint8_t* __restrict__ xq,
                                                   uint8_t* __restrict__ xs,
-                                                  uint16_t* __restrict__ xp, int c0 = 0) {
+                                                  uint16_t* __restrict__ xp, int c0 = 0,
+                                                  int cstep = 1) {
   const int H32 = H / 32;
-  for (int j0 = 32 * c0; j0 < H32; j0 += 32) {  // warp-uniform
+  for (int j0 = 32 * c0; j0 < H32; j0 += 32 * cstep) {  // warp-uniform
     if (kQ == 0) {
       const int blk = j0 + lane;
       if (blk >= H32) continue;
@@ -394,21 +395,27 @@ __global__ void __launch_bounds__(kRouteThreads) route_permute_kernel(
 // one kernel.  Each CTA of a small grid repeats the top-k of all T tokens and
 // the expert scan (latency only: T x E logits from L2), so no CTA waits for
 // another; CTA 0 alone writes ids, weights, counts, offsets and tile bases,
-// and CTA c permutes tokens 4c .. 4c + 3.  Same
-// selection, weights, in-block ranks and offsets as the three-kernel path.
+// and CTA c permutes tokens 4c .. 4c + 3, each row split over kSplit warps
+// (32-block chunks p, p + kSplit, ...).  Same selection, weights, in-block
+// ranks and offsets as the three-kernel path.  TPW tokens per warp in the
+// top-k: 1 for T <= 32 (a warp's instruction stream carries no empty token),
+// else 2.
 constexpr int kSmallThreads = 1024;
 constexpr int kSmallWarps = kSmallThreads / 32;
 // tokens each CTA permutes (one per warp): the payload and scale stores of
 // a token's k rows spread over T / 4 SMs instead of queueing on one
 constexpr int kSmallTokensPerCta = 4;
 
-template <int EPL, int kQ, bool kTiled, bool kV8>
+constexpr int kSmallMaxSplit = kSmallWarps / kSmallTokensPerCta;
+
+template <int EPL, int kQ, bool kTiled, bool kV8, int TPW>
 __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(
     const uint16_t* __restrict__ x, const float* __restrict__ logits, int T, int H, int E, int k,
     int renormalize, int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
     int32_t* __restrict__ src_to_sorted, int32_t* __restrict__ sorted_to_src,
     int64_t* __restrict__ counts, int64_t* __restrict__ offsets, int32_t* __restrict__ tile_base,
-    uint8_t* __restrict__ xq, uint8_t* __restrict__ xs, uint16_t* __restrict__ xp) {
+    uint8_t* __restrict__ xq, uint8_t* __restrict__ xs, uint16_t* __restrict__ xp, int kSplit) {
+  static_assert(TPW * kSmallWarps <= kRouteTokensPerBlock, "tokens per warp");
   __shared__ unsigned long long s_mask[1024];  // s_mask[e] bit t: token t chose expert e
   __shared__ int s_ids[kRouteTokensPerBlock][32];
   __shared__ int s_off[1024];
@@ -417,6 +424,9 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(
   __shared__ int64_t s_dest[kSmallWarps][32];
   __shared__ int64_t s_sfrow[kSmallWarps][32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the grouped GEMM after the routing may be scheduled now (its CTAs set
+  // up on the free SMs and wait for this grid's results before reading them)
+  pdl_launch_dependents();
   // the rows this CTA permutes start their way into L2 now, so the DRAM
   // latency of their loads hides behind the top-k and the scan
   if (lane == 0 && warp < kSmallTokensPerCta && blockIdx.x * kSmallTokensPerCta + warp < T)
@@ -424,11 +434,11 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(
                      (uint32_t)H * 2u);
   for (int e = tid; e < E; e += kSmallThreads) s_mask[e] = 0ull;
   __syncthreads();
-  // ---- top-k of every token (T <= 64: four per warp)
-  constexpr int TPW = kRouteTokensPerBlock / kSmallWarps;
+  // ---- top-k of every token (T <= TPW x 32: TPW per warp)
   constexpr int NT = EPL <= 4 ? TPW : 1;
 #pragma unroll
   for (int g = 0; g < TPW / NT; ++g) {
+    if (warp + kSmallWarps * g * NT >= T) break;  // warp-uniform: no token left
     const float* rows[NT];
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
@@ -468,22 +478,27 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(
     if (tid == 0) { offsets[E] = sum; if (tile_base) tile_base[E] = tsum; }
   }
   __syncthreads();
-  // ---- the permutation: token t = this CTA's first token + warp
-  const int t = blockIdx.x * kSmallTokensPerCta + warp;
-  if (warp >= kSmallTokensPerCta || t >= T) return;  // warp-uniform
+  // ---- the permutation: token t = this CTA's first token + warp % 4, row
+  // part warp / 4 of kSplit (every part's warp computes the destinations;
+  // part 0 writes the index maps)
+  const int part = warp / kSmallTokensPerCta;
+  const int t = blockIdx.x * kSmallTokensPerCta + warp % kSmallTokensPerCta;
+  if (part >= kSplit || t >= T) return;  // warp-uniform
   if (lane < k) {
     const int e = s_ids[t][lane];
     const int64_t f = (int64_t)t * k + lane;
     const int64_t rank = __popcll(s_mask[e] & ((1ull << t) - 1ull));
     const int64_t dest = s_off[e] + rank;
-    src_to_sorted[f] = (int32_t)dest;
-    sorted_to_src[dest] = (int32_t)f;
+    if (part == 0) {
+      src_to_sorted[f] = (int32_t)dest;
+      sorted_to_src[dest] = (int32_t)f;
+    }
     s_dest[warp][lane] = dest;
     if (kTiled) s_sfrow[warp][lane] = ((int64_t)s_tb[e] + rank / 128) * 128 + (rank % 128);
   }
   __syncwarp();
   permute_token_row<kQ, kTiled, kV8>(x + (int64_t)t * H, H, k, lane, s_dest[warp], s_sfrow[warp],
-                                     xq, xs, xp);
+                                     xq, xs, xp, part, kSplit);
 }
 
 // Routing scratch: the histograms [E][nb], then the expert totals [E] and
@@ -526,10 +541,17 @@ cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, i
     const int grid = (int)ceil_div(T, kSmallTokensPerCta);
     const int rn_s = renormalize ? 1 : 0;
     int32_t* tb = tile_base;
-#define MXMOE_SMALL(EPL, Q, TL)                                                                   \
-  route_small_kernel<EPL, Q, TL, false><<<grid, kSmallThreads, 0, stream>>>(                    \
+    // warps per token row in the permutation: one per 32-block chunk, up to 8
+    const int split = (int)std::min<int64_t>(kSmallMaxSplit, ceil_div(H / 32, 32));
+#define MXMOE_SMALL_T(EPL, Q, TL, TPW)                                                            \
+  route_small_kernel<EPL, Q, TL, false, TPW><<<grid, kSmallThreads, 0, stream>>>(               \
       x, logits, T, H, E, k, rn_s, topk_ids, topk_w, src_to_sorted, sorted_to_src, counts,    \
-      offsets, tb, Q ? xq : nullptr, Q ? xs : nullptr, Q ? nullptr : xp)
+      offsets, tb, Q ? xq : nullptr, Q ? xs : nullptr, Q ? nullptr : xp, split)
+#define MXMOE_SMALL(EPL, Q, TL)                                                                   \
+  do {                                                                                            \
+    if (T <= kSmallWarps) MXMOE_SMALL_T(EPL, Q, TL, 1);                                           \
+    else MXMOE_SMALL_T(EPL, Q, TL, 2);                                                            \
+  } while (0)
 #define MXMOE_SMALL_Q(EPL)                                                                        \
   if (quant == 2) MXMOE_SMALL(EPL, 2, true);                                                      \
   else if (quant && tile_base) MXMOE_SMALL(EPL, 1, true);                                         \
@@ -541,6 +563,7 @@ cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, i
     else { MXMOE_SMALL_Q(8); }
 #undef MXMOE_SMALL_Q
 #undef MXMOE_SMALL
+#undef MXMOE_SMALL_T
     return cudaGetLastError();
   }
   const size_t smem1 = sizeof(unsigned long long) * (size_t)E;
