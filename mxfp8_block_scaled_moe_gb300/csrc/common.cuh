@@ -69,6 +69,13 @@ __device__ __forceinline__ uint32_t bf16x2_absmax_bits(uint32_t w) {
 }
 
 // Streaming 16-byte global accesses.
+// Ask the L2 to fetch [p, p + bytes) (16-byte aligned, a multiple of 16
+// bytes); the issuing thread does not wait for the data, but the SM's bulk
+// copy unit moves the bytes one request after another.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   uint4 r;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"

@@ -44,6 +44,8 @@
 // Every mbarrier wait has a clock-based limit; when it runs out the kernel
 // records a timeout in the library status word, every role stops, in-flight
 // copies and MMAs are drained with bounded waits, and tensor memory is freed.
+#include <cmath>
+
 #include "gemm_common.cuh"
 
 namespace mxmoe {
@@ -160,6 +162,36 @@ __global__ void __launch_bounds__(THREADS1, 1)
                  "r"(TMEM_COLS)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  // small batches: before the routing results exist, guess this CTA's first
+  // unit (unit blockIdx.x with one m-tile per expert: expert u / n-tiles,
+  // n-tile u % n-tiles) and start its weight rows and their tiled scales into
+  // L2; the weights are inputs of the layer call, written before its first
+  // kernel started.  Lane i takes 64 KB piece i.
+  if (p.pf_b != nullptr && kTiledSF && warp == 0) {
+    const int e = (int)blockIdx.x / p.n_tiles_n, nt = (int)blockIdx.x % p.n_tiles_n;
+    const int64_t brow = (int64_t)e * p.Nw;
+    const int64_t r0 = kSwiglu ? brow + (int64_t)nt * (BN / 2) : brow + (int64_t)nt * BN;
+    const int64_t r1 = brow + p.n_out + (int64_t)nt * (BN / 2);
+    const int64_t nrows = kSwiglu ? BN / 2 : BN;  // per block
+    const int64_t rows_all = (int64_t)E * p.Nw;
+    const int KTCp = (p.K + BK - 1) / BK;
+    if (e < E && r0 + nrows <= rows_all && (!kSwiglu || r1 + nrows <= rows_all)) {
+      constexpr int64_t kPiece = 64 << 10;
+      const int64_t blk_bytes = nrows * p.pf_row_bytes;
+      const int64_t per_blk = (blk_bytes + kPiece - 1) / kPiece;
+      const int nblk = kSwiglu ? 2 : 1;
+      for (int64_t i = lane; i < nblk * per_blk; i += 32) {
+        const int64_t bi = i / per_blk, o = (i - bi * per_blk) * kPiece;
+        const uint8_t* src = p.pf_b + (bi == 0 ? r0 : r1) * p.pf_row_bytes + o;
+        prefetch_l2_bulk(src, (uint32_t)min(kPiece, blk_bytes - o));
+      }
+      // the tiled scales of the 128-row blocks (KTC chunks of 512 bytes each)
+      if (lane == 31)
+        prefetch_l2_bulk(p.sfb + (r0 >> 7) * KTCp * 512, (uint32_t)((nrows / 128) * KTCp * 512));
+      if (kSwiglu && lane == 30)
+        prefetch_l2_bulk(p.sfb + (r1 >> 7) * KTCp * 512, (uint32_t)(KTCp * 512));
+    }
   }
   // launched with programmatic serialization: everything above overlaps the
   // previous kernel's tail; the offsets, operands and scales it (or an
@@ -478,7 +510,8 @@ template <int BN, bool kSwiglu, bool kTiledSF, int kFmt, bool kSplit = false, in
 static cudaError_t launch_single(const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
                                  const uint8_t* sfb, const int64_t* offsets, int64_t M, int E,
                                  int K, int Nw, int n_out, void* out, uint8_t* out_scale,
-                                 cudaStream_t stream, int ksplit = 1, float* partial = nullptr) {
+                                 cudaStream_t stream, int ksplit = 1, float* partial = nullptr,
+                                 bool prefetch_first = false) {
   using L = Layout1<BN, BMA>;
   if (M == 0) return cudaSuccess;
   int dev = 0;
@@ -517,6 +550,11 @@ static cudaError_t launch_single(const uint8_t* a, const uint8_t* sfa, const uin
   p.wait_limit = wait_limit_cycles();
   p.ksplit = kSplit ? ksplit : 1;
   p.partial = kSplit ? partial : nullptr;
+  // 16-byte aligned rows and pieces for the bulk prefetch
+  const bool pf_ok = prefetch_first && kTiledSF && ((uintptr_t)b & 15u) == 0 &&
+                     ((uintptr_t)sfb & 15u) == 0 && inner % 16 == 0;
+  p.pf_b = pf_ok ? b : nullptr;
+  p.pf_row_bytes = (int64_t)(kFmt == FMT_W8A8 ? K : K / 2);  // global bytes per weight row
   const int64_t tiles_bound = (ceil_div(M, BM) + E) * (int64_t)p.n_tiles_n * ksplit;
   const int grid = (int)std::min<int64_t>(tiles_bound, num_sms());
   return launch_pdl(kern, dim3(grid), dim3(THREADS1), L::ALLOC, stream, tmA, tmB, p);
@@ -549,9 +587,17 @@ static cudaError_t launch(const uint8_t* a, const uint8_t* sfa, const uint8_t* b
     if (err != cudaErrorNotSupported) return err;
   }
   if constexpr (BN == 256 && kTiledSF && kFmt == FMT_W8A8) {
-    if (group_rows_max > 0 && group_rows_max <= BMA_SMALL)
+    if (group_rows_max > 0 && group_rows_max <= BMA_SMALL) {
+      // gmm1 (which follows the routing) prefetches its guessed first unit;
+      // the guess assumes every expert has rows, so only when uniform routing
+      // of T = group_rows_max tokens to k = M / T of the E experts would leave
+      // at most a fifth of them empty.  (gmm2's weights gain nothing from it.)
+      const double T = (double)group_rows_max, k = (double)M / T;
+      const bool guess = kSwiglu && k < E && 1.0 - std::pow(1.0 - k / E, T) >= 0.8;
       return launch_single<BN, kSwiglu, kTiledSF, kFmt, false, BMA_SMALL>(
-          a, sfa, b, sfb, offsets, M, E, K, Nw, n_out, out, out_scale, stream);
+          a, sfa, b, sfb, offsets, M, E, K, Nw, n_out, out, out_scale, stream, 1, nullptr,
+          guess);
+    }
   }
   return launch_single<BN, kSwiglu, kTiledSF, kFmt>(a, sfa, b, sfb, offsets, M, E, K, Nw, n_out, out,
                                               out_scale, stream);

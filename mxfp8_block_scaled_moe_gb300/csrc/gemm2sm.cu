@@ -540,6 +540,8 @@ cudaError_t launch_pair_impl(const uint8_t* a, const uint8_t* sfa, const uint8_t
   p.n_tiles_n = kSwiglu ? n_out / 128 : (int)ceil_div(n_out, 256);
   p.ksplit = 1;
   p.partial = nullptr;
+  p.pf_b = nullptr;
+  p.pf_row_bytes = 0;
   p.status = device_status_ptr();
   p.wait_limit = wait_limit_cycles();
   const int64_t units_bound = (ceil_div(M, BM) / 2 + E) * (int64_t)p.n_tiles_n;

@@ -48,6 +48,12 @@ struct Params {
   // fp32 partial sums to partial [ksplit][M][n_out]; ksplit = 1 otherwise
   int ksplit;
   float* partial;
+  // small batches (1-SM kernel, gmm1): the raw weight array [E * Nw, row
+  // bytes], whose rows the CTA's first unit would read if every expert had
+  // one m-tile, prefetched into L2 before the wait for the previous kernel (a
+  // guess, made while the routing runs); null: no prefetch
+  const uint8_t* pf_b;
+  int64_t pf_row_bytes;
 };
 
 // ---------------------------------------------------------------- PTX wrappers

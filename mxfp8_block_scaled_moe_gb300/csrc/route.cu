@@ -32,12 +32,6 @@
 
 namespace mxmoe {
 
-// Ask the L2 to fetch [p, p + bytes) (16-byte aligned, a multiple of 16
-// bytes); nothing waits for it.
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 constexpr int kRouteThreads = 256;
 constexpr int kRouteWarps = kRouteThreads / 32;
 
