@@ -386,78 +386,90 @@ __global__ void __launch_bounds__(kRouteThreads) route_permute_kernel(
 }
 
 // Small batches (T <= one 64-token routing block): the whole routing step in
-// one kernel.  Each CTA of a small grid repeats the top-k of all T tokens and
-// the expert scan (latency only: T x E logits from L2), so no CTA waits for
-// another; CTA 0 alone writes ids, weights, counts, offsets and tile bases,
-// and CTA c permutes tokens 4c .. 4c + 3, each row split over kSplit warps
-// (32-block chunks p, p + kSplit, ...).  Same selection, weights, in-block
-// ranks and offsets as the three-kernel path.  TPW tokens per warp in the
-// top-k: 1 for T <= 32 (a warp's instruction stream carries no empty token),
-// else 2.
-constexpr int kSmallThreads = 1024;
+// one kernel, launched as one cluster of G = ceil(T / TPC) <= 8 CTAs with
+// TPC = ceil(T / 8) tokens each.  CTA c takes the top-k of its tokens
+// c TPC, c TPC + 1, ... (a warp per token), writes their ids and weights and
+// marks them in its expert masks; after a cluster barrier every CTA ORs the G
+// masks (distributed shared memory) into the expert counts, offsets and
+// tiled-scale row-block bases, and permutes its own tokens, each row split
+// over kSplit warps by 32-block chunk (p, p + kSplit, ...).  CTA 0 writes the
+// counts, offsets and tile bases.  Same selection, weights, in-block ranks
+// and offsets as the three-kernel path.
+constexpr int kSmallThreads = 256;
 constexpr int kSmallWarps = kSmallThreads / 32;
-// tokens each CTA permutes (one per warp): the payload and scale stores of
-// a token's k rows spread over T / 4 SMs instead of queueing on one
-constexpr int kSmallTokensPerCta = 4;
+constexpr int kSmallMaxCtas = 8;  // portable cluster size
+constexpr int kSmallMaxE = 256;
 
-constexpr int kSmallMaxSplit = kSmallWarps / kSmallTokensPerCta;
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// 64-bit load from the shared memory of CTA `rank` of the cluster, at the
+// offset of this CTA's `p`
+__device__ __forceinline__ unsigned long long ld_peer_u64(const void* p, uint32_t rank) {
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+  uint32_t ra;
+  unsigned long long v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(ra) : "memory");
+  return v;
+}
 
-template <int EPL, int kQ, bool kTiled, bool kV8, int TPW>
+template <int EPL, int kQ, bool kTiled, bool kV8>
 __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(
     const uint16_t* __restrict__ x, const float* __restrict__ logits, int T, int H, int E, int k,
     int renormalize, int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
     int32_t* __restrict__ src_to_sorted, int32_t* __restrict__ sorted_to_src,
     int64_t* __restrict__ counts, int64_t* __restrict__ offsets, int32_t* __restrict__ tile_base,
-    uint8_t* __restrict__ xq, uint8_t* __restrict__ xs, uint16_t* __restrict__ xp, int kSplit) {
-  static_assert(TPW * kSmallWarps <= kRouteTokensPerBlock, "tokens per warp");
-  __shared__ unsigned long long s_mask[1024];  // s_mask[e] bit t: token t chose expert e
-  __shared__ int s_ids[kRouteTokensPerBlock][32];
-  __shared__ int s_off[1024];
-  __shared__ int s_tb[1024];
+    uint8_t* __restrict__ xq, uint8_t* __restrict__ xs, uint16_t* __restrict__ xp, int tpc,
+    int kSplit) {
+  __shared__ unsigned long long s_mine[kSmallMaxE];  // bit t: this CTA's token t chose e
+  __shared__ unsigned long long s_mask[kSmallMaxE];  // bit t: token t chose e (all CTAs)
+  __shared__ int s_ids[kSmallWarps][32];             // this CTA's tokens' experts
+  __shared__ int s_off[kSmallMaxE];
+  __shared__ int s_tb[kSmallMaxE];
   __shared__ int s_warp[33];
   __shared__ int64_t s_dest[kSmallWarps][32];
   __shared__ int64_t s_sfrow[kSmallWarps][32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t_first = (int)blockIdx.x * tpc;
   // the grouped GEMM after the routing may be scheduled now (its CTAs set
   // up on the free SMs and wait for this grid's results before reading them)
   pdl_launch_dependents();
-  // the rows this CTA permutes start their way into L2 now, so the DRAM
-  // latency of their loads hides behind the top-k and the scan
-  if (lane == 0 && warp < kSmallTokensPerCta && blockIdx.x * kSmallTokensPerCta + warp < T)
-    prefetch_l2_bulk(x + (int64_t)(blockIdx.x * kSmallTokensPerCta + warp) * H,
-                     (uint32_t)H * 2u);
-  for (int e = tid; e < E; e += kSmallThreads) s_mask[e] = 0ull;
+  // this CTA's rows start their way into L2 now, so the DRAM latency of
+  // their loads hides behind the top-k and the scan
+  if (lane == 0 && warp < tpc && t_first + warp < T)
+    prefetch_l2_bulk(x + (int64_t)(t_first + warp) * H, (uint32_t)H * 2u);
+  if (tid < E) s_mine[tid] = 0ull;
   __syncthreads();
-  // ---- top-k of every token (T <= TPW x 32: TPW per warp)
-  constexpr int NT = EPL <= 4 ? TPW : 1;
-#pragma unroll
-  for (int g = 0; g < TPW / NT; ++g) {
-    if (warp + kSmallWarps * g * NT >= T) break;  // warp-uniform: no token left
-    const float* rows[NT];
-#pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      const int tl = warp + kSmallWarps * (g * NT + n);
-      rows[n] = tl < T ? logits + (int64_t)tl * E : nullptr;
-    }
-    int c[NT];
-    float v[NT], w[NT];
-    warp_topk_softmax<EPL, NT>(rows, E, k, renormalize != 0, lane, c, v, w);
-#pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      const int tl = warp + kSmallWarps * (g * NT + n);
-      if (tl < T && lane < k) {
-        s_ids[tl][lane] = c[n];
-        atomicOr(&s_mask[c[n]], 1ull << tl);
-        if (blockIdx.x == 0) {
-          topk_ids[(int64_t)tl * k + lane] = c[n];
-          topk_w[(int64_t)tl * k + lane] = w[n];
-        }
-      }
+  // ---- top-k of this CTA's tokens, a warp per token
+  if (warp < tpc && t_first + warp < T) {  // warp-uniform
+    const int t = t_first + warp;
+    const float* rows[1] = {logits + (int64_t)t * E};
+    int c[1];
+    float v[1], w[1];
+    warp_topk_softmax<EPL, 1>(rows, E, k, renormalize != 0, lane, c, v, w);
+    if (lane < k) {
+      s_ids[warp][lane] = c[0];
+      atomicOr(&s_mine[c[0]], 1ull << t);
+      topk_ids[(int64_t)t * k + lane] = c[0];
+      topk_w[(int64_t)t * k + lane] = w[0];
     }
   }
-  __syncthreads();
+  // every CTA's masks are complete; OR them together, then a second barrier
+  // keeps each CTA's masks alive until all the others have read them
+  __syncwarp();
+  cluster_barrier();
+  if (tid < E) {
+    unsigned long long m = 0ull;
+    for (uint32_t r = 0; r < gridDim.x; ++r) m |= ld_peer_u64(&s_mine[tid], r);
+    s_mask[tid] = m;
+  }
+  __syncwarp();
+  cluster_barrier();
   // ---- expert counts -> offsets and tiled-scale row-block bases (one
-  // expert per thread, E <= 1024)
+  // expert per thread, E <= 256)
   const int c0 = tid < E ? __popcll(s_mask[tid]) : 0;
   int sum = 0;
   const int ex = block_excl_scan(c0, s_warp, &sum);
@@ -472,14 +484,14 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(
     if (tid == 0) { offsets[E] = sum; if (tile_base) tile_base[E] = tsum; }
   }
   __syncthreads();
-  // ---- the permutation: token t = this CTA's first token + warp % 4, row
-  // part warp / 4 of kSplit (every part's warp computes the destinations;
-  // part 0 writes the index maps)
-  const int part = warp / kSmallTokensPerCta;
-  const int t = blockIdx.x * kSmallTokensPerCta + warp % kSmallTokensPerCta;
+  // ---- the permutation: token t = this CTA's token warp % tpc, row part
+  // warp / tpc of kSplit (every part's warp computes the destinations; part
+  // 0 writes the index maps)
+  const int part = warp / tpc, tl = warp % tpc;
+  const int t = t_first + tl;
   if (part >= kSplit || t >= T) return;  // warp-uniform
   if (lane < k) {
-    const int e = s_ids[t][lane];
+    const int e = s_ids[tl][lane];
     const int64_t f = (int64_t)t * k + lane;
     const int64_t rank = __popcll(s_mask[e] & ((1ull << t) - 1ull));
     const int64_t dest = s_off[e] + rank;
@@ -493,6 +505,29 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(
   __syncwarp();
   permute_token_row<kQ, kTiled, kV8>(x + (int64_t)t * H, H, k, lane, s_dest[warp], s_sfrow[warp],
                                      xq, xs, xp, part, kSplit);
+}
+
+template <int EPL, int kQ, bool kTiled>
+static cudaError_t launch_small(int grid, int tpc, int split, cudaStream_t stream,
+                                const uint16_t* x, const float* logits, int T, int H, int E,
+                                int k, int rn, int32_t* ids, float* w, int32_t* s2s,
+                                int32_t* src2s, int64_t* counts, int64_t* offsets, int32_t* tb,
+                                uint8_t* xq, uint8_t* xs, uint16_t* xp) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)grid;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kSmallThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, route_small_kernel<EPL, kQ, kTiled, false>, x, logits, T, H, E,
+                            k, rn, ids, w, s2s, src2s, counts, offsets, tb, xq, xs, xp, tpc,
+                            split);
 }
 
 // Routing scratch: the histograms [E][nb], then the expert totals [E] and
@@ -529,23 +564,20 @@ cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, i
     return cudaMemsetAsync(offsets, 0, sizeof(int64_t) * (E + 1), stream);
   }
   const int nb = (int)ceil_div(T, kRouteTokensPerBlock);
-  if (!topk_done && nb == 1 && E <= 256) {
-    // one routing block: the single-kernel path
+  if (!topk_done && nb == 1 && E <= kSmallMaxE) {
+    // one routing block: the single-kernel path (one cluster)
     const int epl_s = (E + 31) / 32;
-    const int grid = (int)ceil_div(T, kSmallTokensPerCta);
+    const int tpc = (int)ceil_div(T, kSmallMaxCtas);
+    const int grid = (int)ceil_div(T, tpc);
     const int rn_s = renormalize ? 1 : 0;
-    int32_t* tb = tile_base;
-    // warps per token row in the permutation: one per 32-block chunk, up to 8
-    const int split = (int)std::min<int64_t>(kSmallMaxSplit, ceil_div(H / 32, 32));
-#define MXMOE_SMALL_T(EPL, Q, TL, TPW)                                                            \
-  route_small_kernel<EPL, Q, TL, false, TPW><<<grid, kSmallThreads, 0, stream>>>(               \
-      x, logits, T, H, E, k, rn_s, topk_ids, topk_w, src_to_sorted, sorted_to_src, counts,    \
-      offsets, tb, Q ? xq : nullptr, Q ? xs : nullptr, Q ? nullptr : xp, split)
+    // warps per token row in the permutation: one per 32-block chunk
+    const int split = (int)std::min<int64_t>(kSmallWarps / tpc, ceil_div(H / 32, 32));
+    cudaError_t err;
 #define MXMOE_SMALL(EPL, Q, TL)                                                                   \
-  do {                                                                                            \
-    if (T <= kSmallWarps) MXMOE_SMALL_T(EPL, Q, TL, 1);                                           \
-    else MXMOE_SMALL_T(EPL, Q, TL, 2);                                                            \
-  } while (0)
+  err = launch_small<EPL, Q, TL>(grid, tpc, split, stream, x, logits, T, H, E, k, rn_s, topk_ids, \
+                                 topk_w, src_to_sorted, sorted_to_src, counts, offsets,           \
+                                 tile_base, Q ? xq : nullptr, Q ? xs : nullptr,                   \
+                                 Q ? nullptr : xp)
 #define MXMOE_SMALL_Q(EPL)                                                                        \
   if (quant == 2) MXMOE_SMALL(EPL, 2, true);                                                      \
   else if (quant && tile_base) MXMOE_SMALL(EPL, 1, true);                                         \
@@ -557,8 +589,7 @@ cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, i
     else { MXMOE_SMALL_Q(8); }
 #undef MXMOE_SMALL_Q
 #undef MXMOE_SMALL
-#undef MXMOE_SMALL_T
-    return cudaGetLastError();
+    return err;
   }
   const size_t smem1 = sizeof(unsigned long long) * (size_t)E;
   const int epl = (E + 31) / 32;

@@ -145,10 +145,14 @@ def test_route_quant_skewed_load(mm, T):
                                              (300, 64, 256, 32, True), (64, 256, 8, 8, True),
                                              (200, 64, 600, 32, True), (130, 96, 1000, 4, False),
                                              (70, 64, 1024, 8, True), (20001, 64, 128, 8, True),
-                                             (9800, 32, 256, 6, False)])
+                                             (9800, 32, 256, 6, False), (9, 4096, 256, 8, True),
+                                             (17, 96, 64, 6, False), (33, 2048, 200, 8, True),
+                                             (57, 128, 160, 4, True)])
 def test_route_quant_edge_shapes(mm, T, H, E, k, renorm):
     """Odd E, E up to 256 at 313 routing blocks with a ragged last one (20001
-    tokens) and at 154 (9800), wide E (8+ logits per lane), ties."""
+    tokens) and at 154 (9800), wide E (8+ logits per lane), ties; the
+    single-cluster small-batch path at 1, 7, 9, 17, 33, 57 and 64 tokens (one
+    to eight tokens per CTA, one to eight CTAs, rows of 1 to 4 chunks)."""
     g = torch.Generator(device=DEV).manual_seed(T * 7 + E)
     x = torch.randn(T, H, generator=g, device=DEV).to(torch.bfloat16)
     logits = torch.randn(T, E, generator=g, device=DEV)
