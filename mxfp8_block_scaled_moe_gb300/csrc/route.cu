@@ -507,7 +507,7 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(
                                      xq, xs, xp, part, kSplit);
 }
 
-template <int EPL, int kQ, bool kTiled>
+template <int EPL, int kQ, bool kTiled, bool kV8>
 static cudaError_t launch_small(int grid, int tpc, int split, cudaStream_t stream,
                                 const uint16_t* x, const float* logits, int T, int H, int E,
                                 int k, int rn, int32_t* ids, float* w, int32_t* s2s,
@@ -525,7 +525,7 @@ static cudaError_t launch_small(int grid, int tpc, int split, cudaStream_t strea
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, route_small_kernel<EPL, kQ, kTiled, false>, x, logits, T, H, E,
+  return cudaLaunchKernelEx(&cfg, route_small_kernel<EPL, kQ, kTiled, kV8>, x, logits, T, H, E,
                             k, rn, ids, w, s2s, src2s, counts, offsets, tb, xq, xs, xp, tpc,
                             split);
 }
@@ -572,12 +572,21 @@ cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, i
     const int rn_s = renormalize ? 1 : 0;
     // warps per token row in the permutation: one per 32-block chunk
     const int split = (int)std::min<int64_t>(kSmallWarps / tpc, ceil_div(H / 32, 32));
+    // 32-byte loads and stores (half the store instructions, which bound the
+    // permutation here) when the rows allow them
+    const bool v8s = ((uintptr_t)x & 31u) == 0 &&
+                     ((uintptr_t)(quant ? (const void*)xq : (const void*)xp) & 31u) == 0;
     cudaError_t err;
+#define MXMOE_SMALL_V(EPL, Q, TL, V)                                                              \
+  err = launch_small<EPL, Q, TL, V>(grid, tpc, split, stream, x, logits, T, H, E, k, rn_s,       \
+                                    topk_ids, topk_w, src_to_sorted, sorted_to_src, counts,      \
+                                    offsets, tile_base, Q ? xq : nullptr, Q ? xs : nullptr,      \
+                                    Q ? nullptr : xp)
 #define MXMOE_SMALL(EPL, Q, TL)                                                                   \
-  err = launch_small<EPL, Q, TL>(grid, tpc, split, stream, x, logits, T, H, E, k, rn_s, topk_ids, \
-                                 topk_w, src_to_sorted, sorted_to_src, counts, offsets,           \
-                                 tile_base, Q ? xq : nullptr, Q ? xs : nullptr,                   \
-                                 Q ? nullptr : xp)
+  do {                                                                                            \
+    if (v8s) MXMOE_SMALL_V(EPL, Q, TL, true);                                                     \
+    else MXMOE_SMALL_V(EPL, Q, TL, false);                                                        \
+  } while (0)
 #define MXMOE_SMALL_Q(EPL)                                                                        \
   if (quant == 2) MXMOE_SMALL(EPL, 2, true);                                                      \
   else if (quant && tile_base) MXMOE_SMALL(EPL, 1, true);                                         \
@@ -589,6 +598,7 @@ cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, i
     else { MXMOE_SMALL_Q(8); }
 #undef MXMOE_SMALL_Q
 #undef MXMOE_SMALL
+#undef MXMOE_SMALL_V
     return err;
   }
   const size_t smem1 = sizeof(unsigned long long) * (size_t)E;
