@@ -566,7 +566,7 @@ static cudaError_t launch_single(const uint8_t* a, const uint8_t* sfa, const uin
 // (bf16 out) takes the 2-SM kernel when experts average at least 4 m-tiles,
 // everything else the 1-SM kernel.  group_rows_max > 0 bounds every group's
 // row count (the caller's guarantee); at most BMA_SMALL rows select the 1-SM
-// kernel's short A boxes (MXFP8, MMA-layout scales, 256-wide tiles).
+// kernel's short A boxes (MMA-layout scales, 256-wide tiles, every format).
 template <int BN, bool kSwiglu, bool kTiledSF, int kFmt>
 static cudaError_t launch(const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
                           const uint8_t* sfb, const int64_t* offsets, int64_t M, int E, int K,
@@ -586,7 +586,7 @@ static cudaError_t launch(const uint8_t* a, const uint8_t* sfa, const uint8_t* b
                                                            n_out, out, out_scale, stream);
     if (err != cudaErrorNotSupported) return err;
   }
-  if constexpr (BN == 256 && kTiledSF && kFmt == FMT_W8A8) {
+  if constexpr (BN == 256 && kTiledSF) {
     if (group_rows_max > 0 && group_rows_max <= BMA_SMALL) {
       // gmm1 (which follows the routing) prefetches its guessed first unit;
       // the guess assumes every expert has rows, so only when uniform routing
@@ -614,9 +614,9 @@ cudaError_t launch_gemm_swiglu_quant(const uint8_t* xq, const uint8_t* xs, const
     if (!tiled_scales) return cudaErrorNotSupported;
     if (fmt == gemm::FMT_W4A8)
       return gemm::launch<256, true, true, gemm::FMT_W4A8>(xq, xs, w13q, w13s, offsets, M, E, H, 2 * I,
-                                                     I, aq, as, stream);
+                                                     I, aq, as, stream, 1, nullptr, group_rows_max);
     return gemm::launch<256, true, true, gemm::FMT_W4A4>(xq, xs, w13q, w13s, offsets, M, E, H, 2 * I, I,
-                                                   aq, as, stream);
+                                                   aq, as, stream, 1, nullptr, group_rows_max);
   }
   if (fmt != gemm::FMT_W8A8) return cudaErrorNotSupported;
   if (tiled_scales)
