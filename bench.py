@@ -408,6 +408,13 @@ def layer_config_bench(torch, mm, workloads, dev, flush, stream, name, T, fp8_pe
            "finalize": {"ms": round(f_ms, 4), "GB/s": round(ab["finalize"] / f_ms / 1e6, 1),
                         "frac_hbm": round(ab["finalize"] / f_ms / 1e6 / hbm, 4)},
            "steps": steps}
+    if T <= 32 and H % 256 == 0 and I % 128 == 0:
+        # the library runs both grouped GEMMs as one kernel here (its profile
+        # gives the pair's time as gmm1's): one roofline over both GEMMs' work
+        pair_ms = km("gemm1_swiglu_quant") + km("gemm2")
+        ent["gemms_one_kernel"] = kernel_roofline(pair_ms, g1["flops"] + g2["flops"],
+                                                  g1["bytes"] + g2["bytes"], fp8_peak, hbm)
+        ent["gemm1_swiglu_quant"] = ent["gemm2"] = "in gemms_one_kernel"
     del layer, inp, x, logits, out
     torch.cuda.empty_cache()
     return shape.name, ent

@@ -503,6 +503,18 @@ void mxmoe_set_wait_limit_cycles(long long cycles);
  */
 void mxmoe_set_gemm_2sm(int mode);
 
+/*
+ * Small-batch grouped GEMMs (not part of the method; process-wide).  enable
+ * != 0 (the default): an MXFP8 layer call whose token count is at most 32
+ * (so no expert has more than 32 rows), with H % 256 == 0 and logits given,
+ * runs both grouped GEMMs in one persistent kernel, gmm2's work of an expert
+ * starting once that expert's gmm1 output is stored; 0: one kernel per GEMM.
+ * Both give the same bytes.  With the one-kernel form the layer profile
+ * (mxmoe_layer_profile_read) reports the pair's time as gmm1's and 0 for
+ * gmm2.
+ */
+void mxmoe_set_gemm_chain(int enable);
+
 /* Library version string. */
 const char* mxmoe_version(void);
 

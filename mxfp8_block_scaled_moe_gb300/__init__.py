@@ -15,7 +15,7 @@ from .api import (  # noqa: F401
     moe_forward_mxfp8_mma_scales, moe_route_permute_bf16, moe_route_quant_mxfp8, mx_quantize_3d,
     mx_scales_to_mma_layout, set_wait_limit_cycles, W4A8MoELayer, mx_quantize_fp4_3d,
     moe_forward_w4a8_mma_scales, MXFP8Linear, mxfp8_linear, mxfp8_linear_mma_scales,
-    mxfp8_linear_workspace_size, set_gemm_2sm, W4A4MoELayer, moe_forward_w4a4_mma_scales,
+    mxfp8_linear_workspace_size, set_gemm_2sm, set_gemm_chain, W4A4MoELayer, moe_forward_w4a4_mma_scales,
     MXFP4Linear, mxfp4_linear, mxfp4_linear_mma_scales, moe_router_gate_topk,
     mx_dequantize_bf16_2d, moe_forward_mxfp8_gated_mma_scales,
 )

@@ -20,7 +20,7 @@ EXPORTS = (
     "grouped_gemm_mxfp8", "moe_finalize_routing", "moe_forward_mxfp8_workspace_size",
     "moe_forward_mxfp8", "moe_route_quant_mxfp8_noalloc", "mx_scales_to_mma_layout",
     "moe_forward_mxfp8_mma_scales", "mxmoe_layer_profile_enable", "mxmoe_layer_profile_read",
-    "mxmoe_set_gemm_2sm", "moe_forward_mxfp8_host", "moe_forward_mxfp8_host_workspace_size",
+    "mxmoe_set_gemm_2sm", "mxmoe_set_gemm_chain", "moe_forward_mxfp8_host", "moe_forward_mxfp8_host_workspace_size",
     "moe_forward_mxfp8_host_plan", "mx_quantize_fp4_3d", "moe_forward_w4a8_mma_scales",
     "mxfp8_linear_workspace_size", "mxfp8_linear", "mxfp8_linear_mma_scales",
     "moe_forward_w4a4_mma_scales", "mxfp4_linear", "mxfp4_linear_mma_scales",
@@ -57,6 +57,7 @@ _PROTOS = {
     "mx_scales_to_mma_layout": (_I, [_P, _I64, _I64, _I64, _P, _P]),
     "mxmoe_layer_profile_enable": (_I, [_I]),
     "mxmoe_set_gemm_2sm": (None, [_I]),
+    "mxmoe_set_gemm_chain": (None, [_I]),
     "moe_forward_mxfp8_host_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "moe_forward_mxfp8_host": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _I, _P,
                                     _SZ, _P]),

@@ -370,6 +370,14 @@ def set_gemm_2sm(mode="auto") -> None:
     _lib.load().mxmoe_set_gemm_2sm(m)
 
 
+def set_gemm_chain(enable: bool = True) -> None:
+    """Small MXFP8 batches (at most 32 tokens): both grouped GEMMs in one
+    persistent kernel (True, the default) or one kernel each (False).  Both
+    give the same bytes; with one kernel the layer profile reports the pair's
+    time as gmm1's and 0 for gmm2."""
+    _lib.load().mxmoe_set_gemm_chain(1 if enable else 0)
+
+
 def set_wait_limit_cycles(cycles: int) -> None:
     _lib.load().mxmoe_set_wait_limit_cycles(int(cycles))
 

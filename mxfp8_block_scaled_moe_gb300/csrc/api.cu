@@ -28,6 +28,9 @@ static std::atomic<long long> g_wait_limit{0};
 // tokens, plain or skewed, is even on the 235B prefill and loses 12% at 4K
 // skewed tokens).
 static std::atomic<int> g_use_2sm{2};
+// small batches: both grouped GEMMs of an MXFP8 layer in one kernel (1, the
+// default) or one kernel each (0); both give the same bytes
+static std::atomic<int> g_use_chain{1};
 
 bool use_two_sm_gemm(bool swiglu, int64_t M, int E) {
   const int m = g_use_2sm.load();
@@ -139,6 +142,8 @@ const char* mxmoe_version(void) { return "mxmoe 0.1.0 (sm_103a)"; }
 void mxmoe_set_wait_limit_cycles(long long cycles) { g_wait_limit.store(cycles > 0 ? cycles : 0); }
 
 void mxmoe_set_gemm_2sm(int mode) { g_use_2sm.store(mode < 0 || mode > 2 ? 2 : mode); }
+
+void mxmoe_set_gemm_chain(int enable) { g_use_chain.store(enable ? 1 : 0); }
 
 mxmoe_status mxmoe_get_device_status(int32_t* status_out, int clear) {
   if (!status_out) return MXMOE_ERR_NULL;
@@ -280,7 +285,7 @@ mxmoe_status moe_finalize_routing(const uint16_t* y, const float* topk_w,
 // route histograms | aq [M,I] | as tiled | y [M,H] bf16 | w13s tiled | w2s tiled.
 // Tiled activation scales hold at most ceil(M/128) + E row blocks.
 struct FwdLayout {
-  size_t xq, xs, ids, w, s2s, src2s, counts, offs, tbase, hist, aq, as, y, w13s, w2s, total;
+  size_t xq, xs, ids, w, s2s, src2s, counts, offs, tbase, hist, aq, as, y, w13s, w2s, done, total;
 };
 
 static FwdLayout fwd_layout(int T, int H, int E, int k, int I) {
@@ -304,6 +309,7 @@ static FwdLayout fwd_layout(int T, int H, int E, int k, int I) {
   L.y = take(M * H * 2);
   L.w13s = take((size_t)E * 2 * I * (H / 32));
   L.w2s = take((size_t)E * H * (I / 32));
+  L.done = take((size_t)E * 4);
   L.total = o;
   return L;
 }
@@ -447,17 +453,32 @@ static mxmoe_status forward_impl(const uint16_t* x, const float* logits, const u
                                 (int32_t*)(b + L.hist), s);
     if (e != cudaSuccess) return MXMOE_ERR_CUDA;
   }
+  // small MXFP8 batches: both grouped GEMMs in one kernel, whose per-expert
+  // completion counters the routing kernel zeroes
+  const bool chain = fmt == 0 && !gate && g_use_chain.load() != 0 &&
+                     T <= kRouteTokensPerBlock && E <= 256 && gemm_chain_supported(T, H, I);
+  int* done = chain ? (int*)(b + L.done) : nullptr;
   e = launch_route(x, logits, T, H, E, k, renormalize != 0, fmt == 2 ? 2 : 1, xq, xs, nullptr, ids,
-                   w, s2s, src2s, counts, offs, (int32_t*)(b + L.hist), s, tbase, gate != nullptr);
+                   w, s2s, src2s, counts, offs, (int32_t*)(b + L.hist), s, tbase, gate != nullptr,
+                   done);
   if (e != cudaSuccess) return MXMOE_ERR_CUDA;
   prof.mark(2);
   // an expert's rows are at most T (the k experts of a token are distinct)
-  e = launch_gemm_swiglu_quant(xq, xs, w13q, w13s_t, offs, M, E, H, I, aq, as, s, true, fmt, T);
-  if (e != cudaSuccess) return MXMOE_ERR_CUDA;
-  prof.mark(3);
-  e = launch_gemm_bf16(aq, as, w2q, w2s_t, offs, M, E, I, H, y, s, true, fmt, 1, nullptr, T);
-  if (e != cudaSuccess) return MXMOE_ERR_CUDA;
-  prof.mark(4);
+  if (chain) {
+    // one kernel: its time is reported as gmm1's, gmm2's as zero
+    e = launch_gemm_chain(xq, xs, w13q, w13s_t, w2q, w2s_t, offs, M, E, H, I, aq, as, y, done, s,
+                          T);
+    if (e != cudaSuccess) return MXMOE_ERR_CUDA;
+    prof.mark(3);
+    prof.mark(4);
+  } else {
+    e = launch_gemm_swiglu_quant(xq, xs, w13q, w13s_t, offs, M, E, H, I, aq, as, s, true, fmt, T);
+    if (e != cudaSuccess) return MXMOE_ERR_CUDA;
+    prof.mark(3);
+    e = launch_gemm_bf16(aq, as, w2q, w2s_t, offs, M, E, I, H, y, s, true, fmt, 1, nullptr, T);
+    if (e != cudaSuccess) return MXMOE_ERR_CUDA;
+    prof.mark(4);
+  }
   e = launch_finalize(y, w, src2s, T, k, H, out, s);
   if (e != cudaSuccess) return MXMOE_ERR_CUDA;
   prof.mark(5);

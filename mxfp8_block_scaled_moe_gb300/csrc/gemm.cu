@@ -504,6 +504,411 @@ __global__ void __launch_bounds__(THREADS1, 1)
   }
 }
 
+// ---------------------------------------------------------------- both GEMMs in one kernel
+//
+// Small batches (every group at most BMA_SMALL rows, MXFP8, MMA-layout
+// scales): the layer's two grouped GEMMs run as one persistent kernel.  CTA b
+// takes units b, b + grid, ... of one list holding gmm1's U1 units (expert by
+// expert, n-tile fastest) and then gmm2's U2 units, so gmm2 fills the SMs
+// that gmm1's last partial round leaves idle and needs no launch of its own.
+// A gmm2 unit of expert e reads gmm1's output rows of e (payload by TMA, tiled
+// scales by bulk copy): every epilogue warp of a gmm1 unit, once its stores
+// are done, fences them for the async proxy and adds one to done[e] (after a
+// gpu-scope fence); the producer of a gmm2 unit reads done[e] with acquire
+// until it holds EPI_WARPS x the expert's gmm1 units, then fences for the
+// async proxy before its loads.  That wait is bounded and happens only at the
+// unit's first load, where every earlier unit of the CTA can finish without
+// the producer; the scale request made one segment ahead only polls, and a
+// gmm2 unit whose expert is not done yet gets its first scale segment
+// requested at its start instead.  gmm1 units wait for nothing, and the grid
+// (at most one CTA per SM) is co-resident, so every wait ends.  done[] is
+// zeroed by the layer's routing kernel before this kernel's wait returns.
+struct ChainParams {
+  Params g[2];  // [0] gmm1 (SwiGLU + requant), [1] gmm2 (bf16 out)
+  int* done;    // [E]
+};
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(THREADS1, 1)
+    gemm_chain_kernel(const __grid_constant__ CUtensorMap tmA1,
+                      const __grid_constant__ CUtensorMap tmB1,
+                      const __grid_constant__ CUtensorMap tmA2,
+                      const __grid_constant__ CUtensorMap tmB2, const ChainParams cp) {
+  constexpr int BN = 256;
+  using L = Layout1<BN, BMA_SMALL>;
+  constexpr int STAGES = L::S;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~(uintptr_t)1023);
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Params& p = cp.g[0];  // the fields both GEMMs share: E, M, offsets, status, limit
+
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+  int64_t* s_off = reinterpret_cast<int64_t*>(smem + L::OFF_OFFS);
+  int* s_ts = reinterpret_cast<int*>(smem + L::OFF_TS);
+  int* s_mtb = reinterpret_cast<int*>(smem + L::OFF_MTB);
+  auto bar_full = [&](int s) { return sbase + L::OFF_BAR + 8u * s; };
+  auto bar_empty = [&](int s) { return sbase + L::OFF_BAR + 8u * (STAGES + s); };
+  const uint32_t bar_acc_full = sbase + L::OFF_BAR + 8u * (2 * STAGES);
+  const uint32_t bar_acc_empty = bar_acc_full + 8;
+  const uint32_t bar_drain = bar_acc_full + 16;
+  auto bar_sfs_full = [&](int b) { return bar_acc_full + 24 + 8u * b; };
+  auto bar_sfs_free = [&](int b) { return bar_acc_full + 40 + 8u * b; };
+  auto bar_sft_ready = [&](int b) { return bar_acc_full + 56 + 8u * b; };
+  auto bar_sft_free = [&](int b) { return bar_acc_full + 72 + 8u * b; };
+
+  const int E = p.E;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    mbar_init(bar_acc_full, 1);
+    mbar_init(bar_acc_empty, EPI_WARPS);
+    mbar_init(bar_drain, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_sfs_full(b), 1);
+      mbar_init(bar_sfs_free(b), SF_WARPS);
+      mbar_init(bar_sft_ready(b), SF_WARPS);
+      mbar_init(bar_sft_free(b), 1);
+    }
+    *s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(s_tmem)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  // the guessed first unit's gate and up rows into L2 while the routing runs
+  // (as in the single-GEMM kernel; unit blockIdx.x with one m-tile per expert)
+  if (p.pf_b != nullptr && warp == 0) {
+    const int e = (int)blockIdx.x / p.n_tiles_n, nt = (int)blockIdx.x % p.n_tiles_n;
+    const int64_t r0 = (int64_t)e * p.Nw + (int64_t)nt * (BN / 2);
+    const int64_t r1 = (int64_t)e * p.Nw + p.n_out + (int64_t)nt * (BN / 2);
+    const int KTCp = (p.K + BK - 1) / BK;
+    if (e < E && r1 + BN / 2 <= (int64_t)E * p.Nw) {
+      constexpr int64_t kPiece = 64 << 10;
+      const int64_t blk_bytes = (BN / 2) * p.pf_row_bytes;
+      const int64_t per_blk = (blk_bytes + kPiece - 1) / kPiece;
+      for (int64_t i = lane; i < 2 * per_blk; i += 32) {
+        const int64_t bi = i / per_blk, o = (i - bi * per_blk) * kPiece;
+        prefetch_l2_bulk(p.pf_b + (bi == 0 ? r0 : r1) * p.pf_row_bytes + o,
+                         (uint32_t)min(kPiece, blk_bytes - o));
+      }
+      if (lane == 31) prefetch_l2_bulk(p.sfb + (r0 >> 7) * KTCp * 512, (uint32_t)(KTCp * 512));
+      if (lane == 30) prefetch_l2_bulk(p.sfb + (r1 >> 7) * KTCp * 512, (uint32_t)(KTCp * 512));
+    }
+  }
+  pdl_launch_dependents();
+  pdl_wait();
+  if (warp == 2) build_schedule<1>(p, lane, s_off, s_ts, s_mtb);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const int U1 = s_ts[E];                          // gmm1 units (n_tiles_n of gmm1)
+  const int total = U1 + s_mtb[E] * cp.g[1].n_tiles_n;
+  const int KT[2] = {(cp.g[0].K + BK - 1) / BK, (cp.g[1].K + BK - 1) / BK};
+  // unit -> (GEMM gi, expert, m-tile, n-tile)
+  auto unit_at = [&](int u, int& gi, int& e, int& mt, int& nt) {
+    gi = u >= U1 ? 1 : 0;
+    const int lu = gi ? u - U1 : u;
+    const int ntn = cp.g[gi].n_tiles_n;
+    const int m = lu / ntn;
+    nt = lu - m * ntn;
+    int unused;
+    decode_tile(m, s_mtb, E, 1, e, mt, unused);
+  };
+  // gmm1 epilogue-warp completions that make expert e's gmm2 inputs whole
+  auto done_need = [&](int e) { return EPI_WARPS * (s_mtb[e + 1] - s_mtb[e]) * cp.g[0].n_tiles_n; };
+
+  if (warp == 0) {
+    // ================= producer
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t armed = 0, armed_parity = 0;
+    int g = 0;
+    bool ok = true;
+    int deferred = -1;  // a gmm2 unit whose first scale segment waits for its start
+    auto load_scales = [&](int gseg, int u, int sg) -> bool {
+      const int b = gseg & 1;
+      const uint32_t par = ((uint32_t)(gseg >> 1) & 1u) ^ 1u;
+      const bool got = wait_bar(bar_sfs_free(b), par, p.wait_limit, p.status, s_abort);
+      if (!__all_sync(0xffffffffu, got)) return false;
+      int gi, e, mt, nt;
+      unit_at(u, gi, e, mt, nt);
+      const Params& q = cp.g[gi];
+      const int64_t brow = (int64_t)e * q.Nw;
+      const int64_t bh0 = gi == 0 ? brow + (int64_t)nt * (BN / 2) : brow + (int64_t)nt * BN;
+      const int64_t bh1 = gi == 0 ? brow + q.n_out + (int64_t)nt * (BN / 2) : bh0 + 128;
+      const int kt0 = sg * SEG, len = min(SEG, KT[gi] - kt0);
+      const uint32_t sA = sbase + L::OFF_SFA + b * L::SFA_SEG;
+      const uint32_t sB = sbase + L::OFF_SFB + b * L::SFB_SEG;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar_sfs_full(b), (uint32_t)(3 * len * 512));
+        bulk_copy_g2s(sA, q.sfa + ((int64_t)(s_mtb[e] + mt) * KT[gi] + kt0) * 512,
+                      (uint32_t)(len * 512), bar_sfs_full(b));
+        bulk_copy_g2s(sB, q.sfb + ((bh0 >> 7) * KT[gi] + kt0) * 512, (uint32_t)(len * 512),
+                      bar_sfs_full(b));
+        bulk_copy_g2s(sB + SEG * 512, q.sfb + ((bh1 >> 7) * KT[gi] + kt0) * 512,
+                      (uint32_t)(len * 512), bar_sfs_full(b));
+      }
+      __syncwarp();
+      return true;
+    };
+    // expert e's gmm1 outputs all stored (lane 0 reads; the whole warp agrees)
+    auto expert_done = [&](int e) -> bool {
+      int ready = 0;
+      if (lane == 0) ready = ld_acquire_gpu(cp.done + e) >= done_need(e);
+      return __shfl_sync(0xffffffffu, ready, 0) != 0;
+    };
+    auto wait_expert = [&](int e) -> bool {
+      bool ready = expert_done(e);
+      const long long t0 = clock64();
+      while (!ready) {
+        if (*s_abort) return false;
+        if (clock64() - t0 > p.wait_limit) {
+          if (lane == 0) report_error(p.status, ERR_TIMEOUT);
+          *s_abort = 1;
+          return false;
+        }
+        __nanosleep(200);
+        ready = expert_done(e);
+      }
+      fence_proxy_async_global();
+      return true;
+    };
+    // request segment 0 (the first unit's first), or defer it
+    if ((int)blockIdx.x < total) {
+      int gi, e, mt, nt;
+      unit_at(blockIdx.x, gi, e, mt, nt);
+      if (gi == 1 && !expert_done(e)) deferred = blockIdx.x;
+      else ok = load_scales(0, blockIdx.x, 0);
+    }
+    for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
+      int gi, e, mt, nt;
+      unit_at(u, gi, e, mt, nt);
+      if (gi == 1) {
+        // gmm1's rows of this expert (and their scales) are stored
+        if (!wait_expert(e)) { ok = false; break; }
+        if (deferred == u) {
+          deferred = -1;
+          if (!load_scales(g, u, 0)) { ok = false; break; }
+        }
+      }
+      const Params& q = cp.g[gi];
+      const CUtensorMap* mA = gi ? &tmA2 : &tmA1;
+      const CUtensorMap* mB = gi ? &tmB2 : &tmB1;
+      const int kt_n = KT[gi];
+      const int nseg = (kt_n + SEG - 1) / SEG;
+      const int64_t row0 = s_off[e] + (int64_t)mt * BM;
+      const int64_t brow = (int64_t)e * q.Nw;
+      const int64_t bh0 = gi == 0 ? brow + (int64_t)nt * (BN / 2) : brow + (int64_t)nt * BN;
+      const int64_t bh1 = brow + q.n_out + (int64_t)nt * (BN / 2);
+      for (int kt = 0; kt < kt_n; ++kt) {
+        if (kt % SEG == 0) {
+          // the next segment: later in this unit, or the next unit's first
+          const int sg = kt / SEG;
+          const int nu = sg + 1 < nseg ? u : u + (int)gridDim.x;
+          if (nu < total) {
+            int ngi, ne, nmt, nnt;
+            unit_at(nu, ngi, ne, nmt, nnt);
+            if (nu != u && ngi == 1 && !expert_done(ne)) {
+              deferred = nu;
+            } else if (!load_scales(g + 1, nu, sg + 1 < nseg ? sg + 1 : 0)) {
+              ok = false;
+              break;
+            }
+          }
+          ++g;
+        }
+        const bool got = wait_bar(bar_empty(stage), phase ^ 1, p.wait_limit, p.status, s_abort);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sA = sbase + L::OFF_A + stage * L::A_BYTES;
+        const uint32_t sB = sbase + L::OFF_B + stage * L::B_BYTES;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar_full(stage), L::A_BYTES + L::B_BYTES);
+          tma_load_2d(sA, mA, kt * BK, (int)row0, bar_full(stage));
+          if (gi == 0) {
+            tma_load_2d(sB, mB, kt * BK, (int)bh0, bar_full(stage));
+            tma_load_2d(sB + (BN / 2) * BK, mB, kt * BK, (int)bh1, bar_full(stage));
+          } else {
+            tma_load_2d(sB, mB, kt * BK, (int)bh0, bar_full(stage));
+          }
+        }
+        armed |= 1u << stage;
+        if (phase) armed_parity |= 1u << stage; else armed_parity &= ~(1u << stage);
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+      }
+    }
+    if (!ok) {
+      for (int s = 0; s < STAGES; ++s)
+        if ((armed >> s) & 1u) {
+          volatile int no_abort = 0;
+          wait_bar(bar_full(s), (armed_parity >> s) & 1u, 1ll << 32, nullptr, &no_abort);
+        }
+    }
+  } else if (warp == 1) {
+    // ================= MMA issuer (one thread)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      int g = 0;
+      bool ok = true;
+      bool issued = false;
+      constexpr uint32_t IDESC = make_idesc(BM, BN, false);
+      for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
+        int gi, e, mt, nt;
+        unit_at(u, gi, e, mt, nt);
+        const int kt_n = KT[gi];
+        if (!wait_bar(bar_acc_empty, acc_phase ^ 1, p.wait_limit, p.status, s_abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int kt = 0; kt < kt_n; ++kt) {
+          const int i = kt % SEG;
+          const int b = g & 1;
+          if (i == 0 && !wait_bar(bar_sft_ready(b), (uint32_t)(g >> 1) & 1u, p.wait_limit,
+                                  p.status, s_abort)) {
+            ok = false;
+            break;
+          }
+          if (!wait_bar(bar_full(stage), phase, p.wait_limit, p.status, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sA = sbase + L::OFF_A + stage * L::A_BYTES;
+          const uint32_t sB = sbase + L::OFF_B + stage * L::B_BYTES;
+          const uint32_t t_sf = tmem + SF_COL0 + b * SEG_COLS + i * SF_COLS_PER_STAGE;
+          const uint64_t adesc = make_sdesc(sA, 16, 1024, 2);
+          const uint64_t bdesc = make_sdesc(sB, 16, 1024, 2);
+#pragma unroll
+          for (int kk = 0; kk < BK / 32; ++kk) {
+            const uint32_t sfid = (uint32_t)kk;
+            const uint32_t idesc = IDESC | (sfid << 29) | (sfid << 4);
+            const uint32_t acc = (kt | kk) != 0 ? 1u : 0u;
+            tc_mma_mxf8(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, t_sf, t_sf + 4, acc);
+          }
+          issued = true;
+          tc_commit(bar_empty(stage));
+          if (i == SEG - 1 || kt == kt_n - 1) {
+            tc_commit(bar_sft_free(b));
+            ++g;
+          }
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        tc_commit(bar_acc_full);
+        acc_phase ^= 1;
+      }
+      if (!ok && issued) {
+        tc_commit(bar_drain);
+        volatile int no_abort = 0;
+        wait_bar(bar_drain, 0, 1ll << 32, nullptr, &no_abort);
+      }
+    }
+    __syncwarp();
+  } else if (warp < EPI_WARP0) {
+    // ================= scale-factor writers (as in the single-GEMM kernel)
+    const uint32_t t_q = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    int g = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
+      int gi, e, mt, nt;
+      unit_at(u, gi, e, mt, nt);
+      const int nseg = (KT[gi] + SEG - 1) / SEG;
+      for (int sg = 0; sg < nseg; ++sg, ++g) {
+        const int b = g & 1;
+        const uint32_t par = (uint32_t)(g >> 1) & 1u;
+        const bool got = wait_bar(bar_sfs_full(b), par, p.wait_limit, p.status, s_abort) &&
+                         wait_bar(bar_sft_free(b), par ^ 1u, p.wait_limit, p.status, s_abort);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        const int len = min(SEG, KT[gi] - sg * SEG);
+        const uint8_t* sfa_s = smem + L::OFF_SFA + b * L::SFA_SEG;
+        const uint8_t* sfb_s = smem + L::OFF_SFB + b * L::SFB_SEG;
+        for (int i = 0; i < len; ++i) {
+          const uint32_t col = SF_COL0 + b * SEG_COLS + i * SF_COLS_PER_STAGE;
+          tmem_st_4(t_q + col, *reinterpret_cast<const uint4*>(sfa_s + i * 512 + lane * 16));
+          tmem_st_4(t_q + col + 4, *reinterpret_cast<const uint4*>(sfb_s + i * 512 + lane * 16));
+          tmem_st_4(t_q + col + 8,
+                    *reinterpret_cast<const uint4*>(sfb_s + SEG * 512 + i * 512 + lane * 16));
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar_sft_ready(b));
+          mbar_arrive(bar_sfs_free(b));
+        }
+      }
+    }
+  } else {
+    // ================= epilogue
+    const int q = warp & 3;
+    const int grp = (warp - EPI_WARP0) >> 2;
+    const int row = q * 32 + lane;
+    const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
+    uint32_t acc_phase = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      int gi, e, mt, nt;
+      unit_at(u, gi, e, mt, nt);
+      const int64_t grow = s_off[e] + (int64_t)mt * BM + row;
+      const bool valid = grow < s_off[e + 1];
+      const bool got = wait_bar(bar_acc_full, acc_phase, p.wait_limit, p.status, s_abort);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      auto release = [&] { if (lane == 0) mbar_arrive(bar_acc_empty); };
+      const int64_t tiled_row = (int64_t)(s_mtb[e] + mt) * BM + row;
+      if (gi == 0) {
+        epilogue_tile<BN, true, true, false, false>(cp.g[0], t_row, grp, row, lane, grow, valid,
+                                                    nt, tiled_row, release);
+        // this warp's rows of expert e are stored: visible to the async
+        // proxy, then counted (gpu-scope fence before the count)
+        fence_proxy_async_global();
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(cp.done + e, 1);
+      } else {
+        epilogue_tile<BN, false, true, false, false>(cp.g[1], t_row, grp, row, lane, grow, valid,
+                                                     nt, tiled_row, release);
+      }
+      acc_phase ^= 1;
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
 // ---------------------------------------------------------------- host side
 
 template <int BN, bool kSwiglu, bool kTiledSF, int kFmt, bool kSplit = false, int BMA = BM>
@@ -604,6 +1009,80 @@ static cudaError_t launch(const uint8_t* a, const uint8_t* sfa, const uint8_t* b
 }
 
 }  // namespace gemm
+
+bool gemm_chain_supported(int64_t group_rows_max, int H, int I) {
+  return group_rows_max > 0 && group_rows_max <= gemm::BMA_SMALL && H % 256 == 0 && I % 128 == 0;
+}
+
+cudaError_t launch_gemm_chain(const uint8_t* xq, const uint8_t* xs, const uint8_t* w13q,
+                              const uint8_t* w13s, const uint8_t* w2q, const uint8_t* w2s,
+                              const int64_t* offsets, int64_t M, int E, int H, int I, uint8_t* aq,
+                              uint8_t* as, uint16_t* y, int* done, cudaStream_t stream,
+                              int64_t group_rows_max) {
+  using namespace gemm;
+  using L = Layout1<256, BMA_SMALL>;
+  if (!gemm_chain_supported(group_rows_max, H, I) || !done || E > MAX_E)
+    return cudaErrorNotSupported;
+  if (M == 0) return cudaSuccess;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  static uint64_t configured[64] = {0};
+  const uint64_t ctx = context_id();
+  if (ctx == 0 || configured[dev] != ctx) {
+    cudaError_t err = cudaFuncSetAttribute(gemm_chain_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+    if (err != cudaSuccess) return err;
+    configured[dev] = context_id();
+  }
+  CUtensorMap tmA1, tmB1, tmA2, tmB2;
+  if (!make_map(&tmA1, xq, (uint64_t)H, (uint64_t)M, BK, BMA_SMALL) ||
+      !make_map(&tmB1, w13q, (uint64_t)H, (uint64_t)E * 2 * I, BK, 128) ||
+      !make_map(&tmA2, aq, (uint64_t)I, (uint64_t)M, BK, BMA_SMALL) ||
+      !make_map(&tmB2, w2q, (uint64_t)I, (uint64_t)E * H, BK, 256))
+    return cudaErrorInvalidValue;
+  ChainParams cp;
+  for (int gi = 0; gi < 2; ++gi) {
+    Params& p = cp.g[gi];
+    p.offsets = offsets;
+    p.M = M;
+    p.E = E;
+    p.status = device_status_ptr();
+    p.wait_limit = wait_limit_cycles();
+    p.ksplit = 1;
+    p.partial = nullptr;
+    p.pf_b = nullptr;
+    p.pf_row_bytes = 0;
+  }
+  cp.g[0].sfa = xs;
+  cp.g[0].sfb = w13s;
+  cp.g[0].out = aq;
+  cp.g[0].out_scale = as;
+  cp.g[0].K = H;
+  cp.g[0].Nw = 2 * I;
+  cp.g[0].n_out = I;
+  cp.g[0].n_tiles_n = I / 128;
+  cp.g[1].sfa = as;
+  cp.g[1].sfb = w2s;
+  cp.g[1].out = y;
+  cp.g[1].out_scale = nullptr;
+  cp.g[1].K = I;
+  cp.g[1].Nw = H;
+  cp.g[1].n_out = H;
+  cp.g[1].n_tiles_n = H / 256;
+  cp.done = done;
+  // gmm1's first-unit guess, under the same condition as the single-GEMM launch
+  const double T = (double)group_rows_max, k = (double)M / T;
+  if (k < E && 1.0 - std::pow(1.0 - k / E, T) >= 0.8 && ((uintptr_t)w13q & 15u) == 0 &&
+      ((uintptr_t)w13s & 15u) == 0) {
+    cp.g[0].pf_b = w13q;
+    cp.g[0].pf_row_bytes = H;
+  }
+  const int64_t units_bound = (ceil_div(M, BM) + E) * (int64_t)(I / 128 + H / 256);
+  const int grid = (int)std::min<int64_t>(units_bound, num_sms());
+  return launch_pdl(gemm_chain_kernel, dim3(grid), dim3(THREADS1), L::ALLOC, stream, tmA1, tmB1,
+                    tmA2, tmB2, cp);
+}
 
 cudaError_t launch_gemm_swiglu_quant(const uint8_t* xq, const uint8_t* xs, const uint8_t* w13q,
                                      const uint8_t* w13s, const int64_t* offsets, int64_t M,

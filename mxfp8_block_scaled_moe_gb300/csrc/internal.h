@@ -36,13 +36,15 @@ cudaError_t launch_mx_quantize_fp4(const uint16_t* x, int64_t rows, int64_t K, u
                                    uint8_t* scale, cudaStream_t stream);
 
 // Routing + permutation.  quant 1: MXFP8 xq [M, H] / xs outputs; 2: MXFP4 xq
-// [M, H/2] / xs (tiled scales only); 0: bf16 xp output.
+// [M, H/2] / xs (tiled scales only); 0: bf16 xp output.  zero_e (nullable): E
+// ints the routing step sets to zero (the chained GEMMs' counters).
 cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, int E, int k,
                          bool renormalize, int quant, uint8_t* xq, uint8_t* xs, uint16_t* xp,
                          int32_t* topk_ids, float* topk_w, int32_t* sorted_to_src,
                          int32_t* src_to_sorted, int64_t* counts, int64_t* offsets,
                          int32_t* block_hist, cudaStream_t stream,
-                         int32_t* tile_base = nullptr, bool topk_done = false);
+                         int32_t* tile_base = nullptr, bool topk_done = false,
+                         int32_t* zero_e = nullptr);
 
 // Router gate GEMM (bf16 x [T, H] . bf16 gate [E, H]^T, fp32 accumulate on the
 // tensor cores) fused with softmax top-k.  logits (nullable) receives the fp32
@@ -108,6 +110,18 @@ cudaError_t launch_gemm_bf16(const uint8_t* aq, const uint8_t* as, const uint8_t
                              int I, int H, uint16_t* y, cudaStream_t stream,
                              bool tiled_scales = false, int fmt = 0, int ksplit = 1,
                              float* partial = nullptr, int64_t group_rows_max = 0);
+// Both grouped GEMMs of an MXFP8 layer (MMA-layout scales) in one persistent
+// kernel, for small batches: gemm_chain_supported(group_rows_max, H, I) says
+// when it applies (every group at most 32 rows, H % 256 == 0).  done: E ints of
+// scratch that are zero when the kernel starts (the layer's routing kernel
+// zeroes them).  Same outputs, byte for byte, as launch_gemm_swiglu_quant then
+// launch_gemm_bf16.
+bool gemm_chain_supported(int64_t group_rows_max, int H, int I);
+cudaError_t launch_gemm_chain(const uint8_t* xq, const uint8_t* xs, const uint8_t* w13q,
+                              const uint8_t* w13s, const uint8_t* w2q, const uint8_t* w2s,
+                              const int64_t* offsets, int64_t M, int E, int H, int I, uint8_t* aq,
+                              uint8_t* as, uint16_t* y, int* done, cudaStream_t stream,
+                              int64_t group_rows_max);
 // Split count the dense linear uses for an [M, K] x [N, K]^T product on the
 // current device (1 when the tiles alone fill the GPU).  packed_fp4: the W4A4
 // kernel, whose k-slices hold 256 K elements instead of 128 (never more splits

@@ -423,7 +423,7 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(
     int32_t* __restrict__ src_to_sorted, int32_t* __restrict__ sorted_to_src,
     int64_t* __restrict__ counts, int64_t* __restrict__ offsets, int32_t* __restrict__ tile_base,
     uint8_t* __restrict__ xq, uint8_t* __restrict__ xs, uint16_t* __restrict__ xp, int tpc,
-    int kSplit) {
+    int kSplit, int32_t* __restrict__ zero_e) {
   __shared__ unsigned long long s_mine[kSmallMaxE];  // bit t: this CTA's token t chose e
   __shared__ unsigned long long s_mask[kSmallMaxE];  // bit t: token t chose e (all CTAs)
   __shared__ int s_ids[kSmallWarps][32];             // this CTA's tokens' experts
@@ -482,6 +482,7 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(
   if (blockIdx.x == 0) {
     if (tid < E) { counts[tid] = c0; offsets[tid] = ex; if (tile_base) tile_base[tid] = tex; }
     if (tid == 0) { offsets[E] = sum; if (tile_base) tile_base[E] = tsum; }
+    if (zero_e != nullptr && tid < E) zero_e[tid] = 0;
   }
   __syncthreads();
   // ---- the permutation: token t = this CTA's token warp % tpc, row part
@@ -512,7 +513,7 @@ static cudaError_t launch_small(int grid, int tpc, int split, cudaStream_t strea
                                 const uint16_t* x, const float* logits, int T, int H, int E,
                                 int k, int rn, int32_t* ids, float* w, int32_t* s2s,
                                 int32_t* src2s, int64_t* counts, int64_t* offsets, int32_t* tb,
-                                uint8_t* xq, uint8_t* xs, uint16_t* xp) {
+                                uint8_t* xq, uint8_t* xs, uint16_t* xp, int32_t* zero_e) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -527,7 +528,7 @@ static cudaError_t launch_small(int grid, int tpc, int split, cudaStream_t strea
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, route_small_kernel<EPL, kQ, kTiled, kV8>, x, logits, T, H, E,
                             k, rn, ids, w, s2s, src2s, counts, offsets, tb, xq, xs, xp, tpc,
-                            split);
+                            split, zero_e);
 }
 
 // Routing scratch: the histograms [E][nb], then the expert totals [E] and
@@ -556,7 +557,7 @@ cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, i
                          int32_t* topk_ids, float* topk_w, int32_t* sorted_to_src,
                          int32_t* src_to_sorted, int64_t* counts, int64_t* offsets,
                          int32_t* block_hist, cudaStream_t stream, int32_t* tile_base,
-                         bool topk_done) {
+                         bool topk_done, int32_t* zero_e) {
   if (quant == 2 && !tile_base) return cudaErrorNotSupported;  // MXFP4 rows: tiled scales only
   if (T == 0) {
     cudaError_t err = cudaMemsetAsync(counts, 0, sizeof(int64_t) * E, stream);
@@ -581,7 +582,7 @@ cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, i
   err = launch_small<EPL, Q, TL, V>(grid, tpc, split, stream, x, logits, T, H, E, k, rn_s,       \
                                     topk_ids, topk_w, src_to_sorted, sorted_to_src, counts,      \
                                     offsets, tile_base, Q ? xq : nullptr, Q ? xs : nullptr,      \
-                                    Q ? nullptr : xp)
+                                    Q ? nullptr : xp, zero_e)
 #define MXMOE_SMALL(EPL, Q, TL)                                                                   \
   do {                                                                                            \
     if (v8s) MXMOE_SMALL_V(EPL, Q, TL, true);                                                     \
@@ -600,6 +601,10 @@ cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, i
 #undef MXMOE_SMALL
 #undef MXMOE_SMALL_V
     return err;
+  }
+  if (zero_e) {
+    const cudaError_t zerr = cudaMemsetAsync(zero_e, 0, sizeof(int32_t) * (size_t)E, stream);
+    if (zerr != cudaSuccess) return zerr;
   }
   const size_t smem1 = sizeof(unsigned long long) * (size_t)E;
   const int epl = (E + 31) / 32;

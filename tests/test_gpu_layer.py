@@ -148,6 +148,32 @@ def test_two_sm_and_one_sm_gemm_kernels_agree(mm, cfg):
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
 
 
+@pytest.mark.parametrize("shape", [
+    workloads.CONFIGS["qwen3_30b_decode"],                       # 32 tokens, ~110 of 128 experts
+    workloads.CONFIGS["qwen3_30b_decode"].with_tokens(1),        # 8 experts, one row each
+    workloads.CONFIGS["qwen3_30b_decode"].with_tokens(7),
+    workloads.CONFIGS["qwen3_30b_skewed"].with_tokens(32),       # Zipf routing: crowded experts
+    workloads.LayerShape("chain_e8", T=32, H=512, E=8, k=2, I=256, seed=5, gate_std=0.05),
+], ids=lambda s: s.name)
+def test_small_batch_gemm_chain_equals_two_kernels(mm, shape):
+    """At most 32 tokens: both grouped GEMMs in one persistent kernel (gmm2's
+    units of an expert wait for that expert's gmm1 units) give the bytes of one
+    kernel per GEMM, on uniform, single-token, skewed and few-expert routing
+    (up to 32 rows per expert, gmm2 units waiting on gmm1 units of other CTAs)."""
+    inp = workloads.make_layer(shape, DEV)
+    layer = mm.MXFP8MoELayer.from_bf16(inp["w13"], inp["w2"], shape.k)
+    outs = []
+    try:
+        for chain in (False, True, True):
+            mm.api.set_gemm_chain(chain)
+            outs.append(layer(inp["x"], inp["logits"]).clone())
+    finally:
+        mm.api.set_gemm_chain(True)
+    torch.cuda.synchronize()
+    assert mm.device_status() == 0
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
 @pytest.mark.parametrize("cfg,n_chunks", [("tiny", 3), ("qwen3_30b_decode", 0),
                                           ("qwen3_30b_prefill", 0), ("qwen3_30b_prefill", 5)])
 def test_host_buffer_layer_matches_device_layer(mm, cfg, n_chunks):
