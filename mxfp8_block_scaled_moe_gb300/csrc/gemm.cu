@@ -644,11 +644,13 @@ __global__ void __launch_bounds__(THREADS1, 1)
     int g = 0;
     bool ok = true;
     int deferred = -1;  // a gmm2 unit whose first scale segment waits for its start
+    int req_hi = -1;    // the last scale segment requested
     auto load_scales = [&](int gseg, int u, int sg) -> bool {
       const int b = gseg & 1;
       const uint32_t par = ((uint32_t)(gseg >> 1) & 1u) ^ 1u;
       const bool got = wait_bar(bar_sfs_free(b), par, p.wait_limit, p.status, s_abort);
       if (!__all_sync(0xffffffffu, got)) return false;
+      req_hi = gseg;
       int gi, e, mt, nt;
       unit_at(u, gi, e, mt, nt);
       const Params& q = cp.g[gi];
@@ -759,11 +761,15 @@ __global__ void __launch_bounds__(THREADS1, 1)
       }
     }
     if (!ok) {
+      // abort: every copy into this CTA's shared memory lands before it exits
+      // (the armed operand stages and the last two scale segments requested)
+      volatile int no_abort = 0;
       for (int s = 0; s < STAGES; ++s)
-        if ((armed >> s) & 1u) {
-          volatile int no_abort = 0;
+        if ((armed >> s) & 1u)
           wait_bar(bar_full(s), (armed_parity >> s) & 1u, 1ll << 32, nullptr, &no_abort);
-        }
+      for (int sg = req_hi - 1; sg <= req_hi; ++sg)
+        if (sg >= 0)
+          wait_bar(bar_sfs_full(sg & 1), (uint32_t)(sg >> 1) & 1u, 1ll << 32, nullptr, &no_abort);
     }
   } else if (warp == 1) {
     // ================= MMA issuer (one thread)

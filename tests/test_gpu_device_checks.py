@@ -19,6 +19,7 @@ import pytest
 import torch
 
 from oracle import moe, mx
+from mxfp8_block_scaled_moe_gb300 import workloads
 
 from _util import REQUANT_MAX_FRAC, bits16, finalize_bound_ok, requant_mismatch, u8
 
@@ -180,3 +181,27 @@ def test_device_wait_timeout_reports_and_recovers(mm):
     torch.cuda.synchronize()
     assert mm.device_status() == 0
     assert np.array_equal(bits16(y), moe.gmm2(aq, as_, w2q, w2s, offs))
+
+
+def test_small_batch_gemm_chain_wait_timeout_reports_and_recovers(mm):
+    """The 32-token layer runs both grouped GEMMs as one kernel whose producer
+    waits on other CTAs' gmm1 units; with a wait limit of one cycle its waits
+    run out, the layer reports MXMOE_ERR_DEVICE_TIMEOUT, and the next call with
+    the default limit gives the bytes of a call that never timed out."""
+    shape = workloads.CONFIGS["qwen3_30b_decode"]
+    inp = workloads.make_layer(shape, "cuda")
+    layer = mm.MXFP8MoELayer.from_bf16(inp["w13"], inp["w2"], shape.k)
+    ref = layer(inp["x"], inp["logits"]).clone()
+    torch.cuda.synchronize()
+    assert mm.device_status(clear=True) == 0
+    mm.set_wait_limit_cycles(1)
+    try:
+        layer(inp["x"], inp["logits"])
+        status = mm.device_status(clear=True)
+    finally:
+        mm.set_wait_limit_cycles(0)
+    assert status == ERR_DEVICE_TIMEOUT
+    out = layer(inp["x"], inp["logits"])
+    torch.cuda.synchronize()
+    assert mm.device_status() == 0
+    assert torch.equal(out, ref)
