@@ -228,12 +228,14 @@ __global__ void __launch_bounds__(THREADS1, 1)
     uint32_t armed = 0, armed_parity = 0;  // per-stage bit masks, for the abort drain
     int g = 0;                             // global segment index of the operand loads
     bool ok = true;
+    int req_hi = -1;                       // the last scale segment requested
     // request the scales of segment (tile, sg) into buffer gseg & 1
     auto load_scales = [&](int gseg, int tile, int sg) -> bool {
       const int b = gseg & 1;
       const uint32_t par = ((uint32_t)(gseg >> 1) & 1u) ^ 1u;
       const bool got = wait_bar(bar_sfs_free(b), par, p.wait_limit, p.status, s_abort);
       if (!__all_sync(0xffffffffu, got)) return false;
+      req_hi = gseg;
       int e, mt, nt, ks, k0, k1;
       tile_at(tile, e, mt, nt, ks, k0, k1);
       const int64_t row0 = s_off[e] + (int64_t)mt * BM;
@@ -330,13 +332,18 @@ __global__ void __launch_bounds__(THREADS1, 1)
       }
     }
     if (!ok) {
-      // drain: wait for this thread's cp.async and every armed stage's copies
+      // drain: wait for this thread's cp.async, every armed stage's copies and
+      // the last two scale segments requested (bulk copies into this CTA)
       cp_async_wait_all();
+      volatile int no_abort = 0;
       for (int s = 0; s < STAGES; ++s)
-        if ((armed >> s) & 1u) {
-          volatile int no_abort = 0;
+        if ((armed >> s) & 1u)
           wait_bar(bar_full(s), (armed_parity >> s) & 1u, 1ll << 32, nullptr, &no_abort);
-        }
+      if (kTiledSF)
+        for (int sg = req_hi - 1; sg <= req_hi; ++sg)
+          if (sg >= 0)
+            wait_bar(bar_sfs_full(sg & 1), (uint32_t)(sg >> 1) & 1u, 1ll << 32, nullptr,
+                     &no_abort);
     }
     // every requested scale segment is consumed by the scale writers, which
     // wait for its copies; this thread's own cp.async complete here

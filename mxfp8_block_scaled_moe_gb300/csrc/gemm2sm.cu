@@ -240,11 +240,13 @@ __global__ void __launch_bounds__(THREADS1, 1)
     uint32_t phase = 0;
     int g = 0;
     bool ok = true;
+    int req_hi = -1;  // the last scale segment requested
     auto load_scales = [&](int gseg, int unit, int sg) -> bool {
       const int b = gseg & 1;
       const uint32_t par = ((uint32_t)(gseg >> 1) & 1u) ^ 1u;
       const bool got = wait_bar(bar_sfs_free(b), par, p.wait_limit, p.status, s_abort);
       if (!__all_sync(0xffffffffu, got)) return false;
+      req_hi = gseg;
       if (lane == 0) {
         int e, mt, nt;
         int64_t bh0, bh1;
@@ -313,8 +315,15 @@ __global__ void __launch_bounds__(THREADS1, 1)
         if (++stage == STAGES) { stage = 0; phase ^= 1; }
       }
     } else {
-      // abort: loads already issued complete on the leader's barriers; give
-      // them a bounded moment to land before the CTA pair tears down
+      // abort: this CTA's scale copies land on its own barriers (wait for the
+      // last two segments requested); its operand loads complete on the
+      // leader's barriers, so give them a bounded moment to land before the
+      // CTA pair tears down
+      volatile int no_abort = 0;
+      for (int sg = req_hi - 1; sg <= req_hi; ++sg)
+        if (sg >= 0)
+          wait_bar(bar_sfs_full(sg & 1), (uint32_t)(sg >> 1) & 1u, 1ll << 32, nullptr,
+                   &no_abort);
       const long long t0 = clock64();
       while (clock64() - t0 < 200000) __nanosleep(1000);
     }
