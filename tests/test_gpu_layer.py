@@ -174,6 +174,27 @@ def test_small_batch_gemm_chain_equals_two_kernels(mm, shape):
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
 
 
+def test_small_batch_gemm_chain_token_sweep(mm):
+    """One set of Qwen3-30B-A3B-shaped weights, token counts 2..31 in turn (the
+    per-expert counters are zeroed by every routing step): the one-kernel GEMMs
+    give the bytes of one kernel per GEMM at every size."""
+    shape = workloads.CONFIGS["qwen3_30b_decode"]
+    inp = workloads.make_layer(shape.with_tokens(31), DEV)
+    layer = mm.MXFP8MoELayer.from_bf16(inp["w13"], inp["w2"], shape.k)
+    try:
+        for T in (2, 3, 9, 16, 24, 31):
+            x, logits = inp["x"][:T].contiguous(), inp["logits"][:T].contiguous()
+            mm.api.set_gemm_chain(False)
+            ref = layer(x, logits).clone()
+            mm.api.set_gemm_chain(True)
+            out = layer(x, logits)
+            torch.cuda.synchronize()
+            assert torch.equal(out, ref), T
+    finally:
+        mm.api.set_gemm_chain(True)
+    assert mm.device_status() == 0
+
+
 @pytest.mark.parametrize("cfg,n_chunks", [("tiny", 3), ("qwen3_30b_decode", 0),
                                           ("qwen3_30b_prefill", 0), ("qwen3_30b_prefill", 5)])
 def test_host_buffer_layer_matches_device_layer(mm, cfg, n_chunks):
