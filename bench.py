@@ -48,7 +48,8 @@ NCU_TRAFFIC = {"a9ec3d6a1d8bbad4": 786553600, "64d58b0d55536f8c": 786384128,
                "f21fe81032a4b103": 786399488, "afe529db44d76b76": 787179008,
                "318d8521ea941ed5": 786471936, "7ede47c7a46a5cfc": 787526144,
                "1c20b020eb8a1633": 787512064, "cc23eb524901ee20": 787625984,
-               "5238fc07798b52b4": 787269376, "16b1bf2dc0156978": 787060736}
+               "5238fc07798b52b4": 787269376, "16b1bf2dc0156978": 787060736,
+               "0fd02ef804c608ce": 787518976}
 
 
 def max_over_ranks(torch, dist, ms, world, device):

@@ -90,6 +90,37 @@ struct Layout1 {
   static_assert(SF_COL0 + 2 * SEG_COLS <= TMEM_COLS, "tensor memory");
 };
 
+// Small batches: before the routing results exist, guess this CTA's first
+// unit (unit blockIdx.x with one m-tile per expert: expert u / n-tiles,
+// n-tile u % n-tiles) and start its weight rows (gmm1: the gate and the up
+// block) and their tiled scales into L2, one 64 KB piece per lane of the
+// calling warp.  The weights are inputs of the layer call, written before
+// its first kernel started; rows outside [0, E * Nw) are never touched.
+template <int BN, bool kSwiglu>
+__device__ __forceinline__ void prefetch_first_unit(const Params& p, int lane) {
+  const int e = (int)blockIdx.x / p.n_tiles_n, nt = (int)blockIdx.x % p.n_tiles_n;
+  const int64_t brow = (int64_t)e * p.Nw;
+  const int64_t r0 = kSwiglu ? brow + (int64_t)nt * (BN / 2) : brow + (int64_t)nt * BN;
+  const int64_t r1 = brow + p.n_out + (int64_t)nt * (BN / 2);
+  const int64_t nrows = kSwiglu ? BN / 2 : BN;  // per block
+  const int64_t rows_all = (int64_t)p.E * p.Nw;
+  const int KTC = (p.K + BK - 1) / BK;
+  if (e >= p.E || r0 + nrows > rows_all || (kSwiglu && r1 + nrows > rows_all)) return;
+  constexpr int64_t kPiece = 64 << 10;
+  const int64_t blk_bytes = nrows * p.pf_row_bytes;
+  const int64_t per_blk = (blk_bytes + kPiece - 1) / kPiece;
+  const int nblk = kSwiglu ? 2 : 1;
+  for (int64_t i = lane; i < nblk * per_blk; i += 32) {
+    const int64_t bi = i / per_blk, o = (i - bi * per_blk) * kPiece;
+    prefetch_l2_bulk(p.pf_b + (bi == 0 ? r0 : r1) * p.pf_row_bytes + o,
+                     (uint32_t)min(kPiece, blk_bytes - o));
+  }
+  // the tiled scales of the 128-row blocks (KTC chunks of 512 bytes each)
+  if (lane == 31)
+    prefetch_l2_bulk(p.sfb + (r0 >> 7) * KTC * 512, (uint32_t)((nrows / 128) * KTC * 512));
+  if (kSwiglu && lane == 30) prefetch_l2_bulk(p.sfb + (r1 >> 7) * KTC * 512, (uint32_t)(KTC * 512));
+}
+
 // kTiledSF: all scales (A, B and gmm1's output scales) use the tiled layout
 // of tiled_scales.h (a segment's chunks are contiguous: one bulk copy per 128
 // rows); otherwise they are the row-major [rows, K/32] arrays, gathered into
@@ -163,36 +194,7 @@ __global__ void __launch_bounds__(THREADS1, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  // small batches: before the routing results exist, guess this CTA's first
-  // unit (unit blockIdx.x with one m-tile per expert: expert u / n-tiles,
-  // n-tile u % n-tiles) and start its weight rows and their tiled scales into
-  // L2; the weights are inputs of the layer call, written before its first
-  // kernel started.  Lane i takes 64 KB piece i.
-  if (p.pf_b != nullptr && kTiledSF && warp == 0) {
-    const int e = (int)blockIdx.x / p.n_tiles_n, nt = (int)blockIdx.x % p.n_tiles_n;
-    const int64_t brow = (int64_t)e * p.Nw;
-    const int64_t r0 = kSwiglu ? brow + (int64_t)nt * (BN / 2) : brow + (int64_t)nt * BN;
-    const int64_t r1 = brow + p.n_out + (int64_t)nt * (BN / 2);
-    const int64_t nrows = kSwiglu ? BN / 2 : BN;  // per block
-    const int64_t rows_all = (int64_t)E * p.Nw;
-    const int KTCp = (p.K + BK - 1) / BK;
-    if (e < E && r0 + nrows <= rows_all && (!kSwiglu || r1 + nrows <= rows_all)) {
-      constexpr int64_t kPiece = 64 << 10;
-      const int64_t blk_bytes = nrows * p.pf_row_bytes;
-      const int64_t per_blk = (blk_bytes + kPiece - 1) / kPiece;
-      const int nblk = kSwiglu ? 2 : 1;
-      for (int64_t i = lane; i < nblk * per_blk; i += 32) {
-        const int64_t bi = i / per_blk, o = (i - bi * per_blk) * kPiece;
-        const uint8_t* src = p.pf_b + (bi == 0 ? r0 : r1) * p.pf_row_bytes + o;
-        prefetch_l2_bulk(src, (uint32_t)min(kPiece, blk_bytes - o));
-      }
-      // the tiled scales of the 128-row blocks (KTC chunks of 512 bytes each)
-      if (lane == 31)
-        prefetch_l2_bulk(p.sfb + (r0 >> 7) * KTCp * 512, (uint32_t)((nrows / 128) * KTCp * 512));
-      if (kSwiglu && lane == 30)
-        prefetch_l2_bulk(p.sfb + (r1 >> 7) * KTCp * 512, (uint32_t)(KTCp * 512));
-    }
-  }
+  if (p.pf_b != nullptr && kTiledSF && warp == 0) prefetch_first_unit<BN, kSwiglu>(p, lane);
   // launched with programmatic serialization: everything above overlaps the
   // previous kernel's tail; the offsets, operands and scales it (or an
   // earlier kernel) wrote are read only after this wait
@@ -600,26 +602,7 @@ __global__ void __launch_bounds__(THREADS1, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  // the guessed first unit's gate and up rows into L2 while the routing runs
-  // (as in the single-GEMM kernel; unit blockIdx.x with one m-tile per expert)
-  if (p.pf_b != nullptr && warp == 0) {
-    const int e = (int)blockIdx.x / p.n_tiles_n, nt = (int)blockIdx.x % p.n_tiles_n;
-    const int64_t r0 = (int64_t)e * p.Nw + (int64_t)nt * (BN / 2);
-    const int64_t r1 = (int64_t)e * p.Nw + p.n_out + (int64_t)nt * (BN / 2);
-    const int KTCp = (p.K + BK - 1) / BK;
-    if (e < E && r1 + BN / 2 <= (int64_t)E * p.Nw) {
-      constexpr int64_t kPiece = 64 << 10;
-      const int64_t blk_bytes = (BN / 2) * p.pf_row_bytes;
-      const int64_t per_blk = (blk_bytes + kPiece - 1) / kPiece;
-      for (int64_t i = lane; i < 2 * per_blk; i += 32) {
-        const int64_t bi = i / per_blk, o = (i - bi * per_blk) * kPiece;
-        prefetch_l2_bulk(p.pf_b + (bi == 0 ? r0 : r1) * p.pf_row_bytes + o,
-                         (uint32_t)min(kPiece, blk_bytes - o));
-      }
-      if (lane == 31) prefetch_l2_bulk(p.sfb + (r0 >> 7) * KTCp * 512, (uint32_t)(KTCp * 512));
-      if (lane == 30) prefetch_l2_bulk(p.sfb + (r1 >> 7) * KTCp * 512, (uint32_t)(KTCp * 512));
-    }
-  }
+  if (p.pf_b != nullptr && warp == 0) prefetch_first_unit<BN, true>(p, lane);
   pdl_launch_dependents();
   pdl_wait();
   if (warp == 2) build_schedule<1>(p, lane, s_off, s_ts, s_mtb);
