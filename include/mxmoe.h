@@ -152,8 +152,8 @@ mxmoe_status moe_route_quant_mxfp8(const uint16_t* x, const float* logits, int T
  * framework owns device memory and offers no workspace hook.
  *
  * Same arguments, results and layouts as moe_route_quant_mxfp8, minus the
- * workspace: the routing scratch (per-block expert histograms, expert totals
- * and a counter) lives in a 1 MiB + 4.25 KiB array inside the library that
+ * workspace: the routing scratch (per-block expert histograms and their
+ * scanned block bases) lives in a 2 MiB array inside the library that
  * every GPU loading the library keeps until the process exits.  Inputs and
  * outputs remain the caller's.
  *   - Limit: ceil(T / 64) * E <= 262144 (e.g. T = 131072 tokens at E = 128);

@@ -62,8 +62,8 @@ cudaError_t launch_mx_dequantize_bf16(const uint8_t* q, const uint8_t* s, int64_
                                       uint16_t* out, cudaStream_t stream);
 
 size_t route_workspace_bytes(int T, int E);
-// Bytes of the routing scratch's histogram part; the expert totals [E] and
-// the scan's completion counter follow it (the counter at int E of them).
+// Bytes of the routing scratch's histogram part [E][nb]; the scan's block
+// bases (as many bytes) follow it.
 size_t route_hist_bytes(int T, int E);
 
 // Launch with programmatic stream serialization: the kernel may begin while

@@ -8,7 +8,8 @@
 // framework owns device memory and offers no workspace hook, or a
 // latency-critical path that must not pay cudaMalloc's cost.  They still own
 // their inputs and outputs, but not a scratch buffer.  For them the routing
-// step's only scratch -- the per-block expert histograms -- lives in the
+// step's only scratch -- the per-block expert histograms and their scanned
+// block bases -- lives in the
 // file-scope device array below, which every GPU that loads this library
 // holds until the process exits.
 #include <mutex>
@@ -18,11 +19,10 @@
 
 namespace mxmoe {
 
-// Scratch for ceil(T / 64) * E <= 262144 histogram entries (1 MiB) plus the
-// routing scan's expert totals and completion counter (E + 1 <= 1025 ints,
-// 256-byte aligned).
+// Scratch for ceil(T / 64) * E <= 262144 histogram entries (1 MiB) and as
+// many block bases.
 constexpr int64_t kNoAllocHistInts = 262144;
-constexpr size_t kNoAllocScratchInts = kNoAllocHistInts + 1088;
+constexpr size_t kNoAllocScratchInts = 2 * kNoAllocHistInts;
 static __device__ __align__(256) int32_t g_route_scratch[kNoAllocScratchInts];
 
 namespace {

@@ -15,7 +15,8 @@
 //      assignment's rank inside the block (flat order) and the block's
 //      per-expert histogram are popcounts.
 //   2. route_scan: per-expert exclusive prefix of the block histograms (the
-//      block's base row inside each expert) and of the expert totals (offsets).
+//      block's base row inside each expert, into a second array) and, in one
+//      more CTA beside them, of the expert totals (offsets).
 //   3. route_permute_quant: one warp per token computes its k destination rows
 //      (offset + block base + rank); each lane quantizes one 32-element block
 //      of the hidden row once and writes its 32 payload bytes and scale byte
@@ -48,8 +49,7 @@ template <int EPL, int TPW = topk_tokens_per_warp<EPL>()>  // logits per lane: E
 __global__ void __launch_bounds__(32 * (kRouteTokensPerBlock / TPW)) route_topk_rank_kernel(
     const float* __restrict__ logits, int T, int E, int k, int renormalize,
     int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
-    int32_t* __restrict__ local_rank, int32_t* __restrict__ block_hist,
-    int32_t* __restrict__ scan_counter) {
+    int32_t* __restrict__ local_rank, int32_t* __restrict__ block_hist) {
   constexpr int WARPS = kRouteTokensPerBlock / TPW;
   // s_mask[e] bit tl: token tl of this block chose expert e.  A token's k
   // experts are distinct, so its rank among the block's rows of expert e in
@@ -61,9 +61,6 @@ __global__ void __launch_bounds__(32 * (kRouteTokensPerBlock / TPW)) route_topk_
   // the scan and permute kernels may be scheduled now (they wait for this
   // grid's results before reading them)
   pdl_launch_dependents();
-  // the scan's completion counter starts at zero (the scan reads it only
-  // after this grid has finished)
-  if (blockIdx.x == 0 && threadIdx.x == 0) scan_counter[0] = 0;
 
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_mask[e] = 0ull;
   __syncthreads();
@@ -113,17 +110,20 @@ __global__ void __launch_bounds__(32 * (kRouteTokensPerBlock / TPW)) route_topk_
     block_hist[(int64_t)e * gridDim.x + blockIdx.x] = __popcll(s_mask[e]);
 }
 
-// The scan, over the expert-major histogram hist[e][b] (nb blocks per row):
-// one warp per expert row, four per CTA.  A warp loads its row 256 blocks at a
-// time (lane l holds blocks l, l + 32, ..., l + 224: coalesced, all in
-// flight together), scans the eight 32-block chunks independently (their
-// shuffle chains interleave), joins them by the prefix of the chunk totals,
-// and rewrites the row as its exclusive prefix (each block's base row inside
-// expert e); the row total goes to totals[e].  The CTA that finishes last
-// (a ticket on a counter the top-k kernel zeroed; no CTA waits for another)
-// scans the totals into counts, offsets and the experts' first 128-row
-// blocks of the tiled scale layout.
-constexpr int kScanWarps = 4;
+// The scan, over the expert-major histogram hist[e][b] (nb blocks per row),
+// by ceil(E / kScanWarps) row CTAs and one totals CTA that all start
+// together; no CTA waits for another.  A row CTA's warp takes one expert row:
+// it loads the row 256 blocks at a time (lane l holds blocks l, l + 32, ...,
+// l + 224: coalesced, all in flight together), scans the eight 32-block
+// chunks independently (their shuffle chains interleave), joins them by the
+// prefix of the chunk totals, and writes the row's exclusive prefix (each
+// block's base row inside expert e) to base[e][b].  The totals CTA (the last)
+// sums every row itself, eight rows per warp with all their loads in flight,
+// and scans the E totals into counts, offsets and the experts' first 128-row
+// blocks of the tiled scale layout.  (Before, the row CTAs wrote the totals
+// and the last of them to take a ticket scanned them: two more dependent
+// round trips to memory.)
+constexpr int kScanWarps = 16;
 constexpr int kScanThreads = 32 * kScanWarps;
 
 __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
@@ -155,18 +155,19 @@ __device__ __forceinline__ int block_excl_scan(int v, int* s_warp, int* total) {
 }
 
 __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(
-    int32_t* __restrict__ hist, int nb, int E, int32_t* __restrict__ totals,
-    int32_t* __restrict__ counter, int64_t* __restrict__ counts, int64_t* __restrict__ offsets,
+    const int32_t* __restrict__ hist, int nb, int E, int32_t* __restrict__ base,
+    int64_t* __restrict__ counts, int64_t* __restrict__ offsets,
     int32_t* __restrict__ tile_base) {
   pdl_launch_dependents();
-  pdl_wait();  // the top-k kernel's histograms (and its zeroed counter)
-  __shared__ int s_warp[33];
-  __shared__ int s_last;
+  pdl_wait();  // the top-k kernel's histograms
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int e = blockIdx.x * kScanWarps + warp;
-  if (e < E) {
-    constexpr int U = 8;
-    int32_t* row = hist + (int64_t)e * nb;
+  constexpr int U = 8;
+  if (blockIdx.x + 1 < gridDim.x) {
+    // ----- a row CTA
+    const int e = blockIdx.x * kScanWarps + warp;
+    if (e >= E) return;  // warp-uniform; no block-wide barrier follows
+    const int32_t* row = hist + (int64_t)e * nb;
+    int32_t* out = base + (int64_t)e * nb;
     int run = 0;
     for (int c0 = 0; c0 < nb; c0 += 32 * U) {
       int v[U], incl[U];
@@ -187,28 +188,51 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int b = c0 + 32 * u + lane;
-        if (b < nb) row[b] = run + incl[u] - v[u];
+        if (b < nb) out[b] = run + incl[u] - v[u];
         run += __shfl_sync(0xffffffffu, incl[u], 31);
       }
     }
-    if (lane == 0) totals[e] = run;
+    return;
   }
-  // last CTA: every row total is written (each CTA fences before its ticket)
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    s_last = atomicAdd(counter, 1) == (int)gridDim.x - 1;
+  // ----- the totals CTA: every row's sum, R rows per warp at a time
+  __shared__ int s_tot[1024];
+  __shared__ int s_warp[33];
+  constexpr int R = 8;
+  for (int e0 = warp; e0 < E; e0 += kScanWarps * R) {
+    int sum[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) sum[r] = 0;
+    for (int c0 = 0; c0 < nb; c0 += 32 * U) {
+      int v[R][U];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int e = e0 + kScanWarps * r;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int b = c0 + 32 * u + lane;
+          v[r][u] = e < E && b < nb ? hist[(int64_t)e * nb + b] : 0;
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int u = 0; u < U; ++u) sum[r] += v[r][u];
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int e = e0 + kScanWarps * r;
+      const int t = __reduce_add_sync(0xffffffffu, sum[r]);
+      if (lane == 0 && e < E) s_tot[e] = t;
+    }
   }
   __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  // E <= 1024 totals, up to eight per thread in expert order
+  // E <= 1024 totals, PER per thread in expert order
   constexpr int PER = 1024 / kScanThreads;
   int c[PER], tsum = 0, tl = 0;
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
     const int x = tid * PER + i;
-    c[i] = x < E ? __ldcg(totals + x) : 0;
+    c[i] = x < E ? s_tot[x] : 0;
     tsum += c[i];
     tl += (c[i] + 127) / 128;
   }
@@ -531,25 +555,22 @@ static cudaError_t launch_small(int grid, int tpc, int split, cudaStream_t strea
                             split, zero_e);
 }
 
-// Routing scratch: the histograms [E][nb], then the expert totals [E] and
-// the scan's completion counter (one int), each piece 256-byte aligned.
+// Routing scratch: the histograms [E][nb], then the scan's block bases
+// [E][nb], each piece 256-byte aligned.
 size_t route_hist_bytes(int T, int E) {
   const int64_t nb = ceil_div(T, kRouteTokensPerBlock);
   const size_t b = (size_t)(nb > 0 ? nb : 1) * (size_t)E * sizeof(int32_t);
   return (b + 255) & ~(size_t)255;
 }
-size_t route_workspace_bytes(int T, int E) {
-  return route_hist_bytes(T, E) + (((size_t)(E + 1) * sizeof(int32_t) + 255) & ~(size_t)255);
-}
+size_t route_workspace_bytes(int T, int E) { return 2 * route_hist_bytes(T, E); }
 
 template <int EPL>
 static void launch_topk(int nb, size_t smem, cudaStream_t stream, const float* logits, int T,
                         int E, int k, int renorm, int32_t* ids, float* w, int32_t* rank,
                         int32_t* hist) {
   constexpr int threads = 32 * (kRouteTokensPerBlock / topk_tokens_per_warp<EPL>());
-  int32_t* counter = hist + route_hist_bytes(T, E) / sizeof(int32_t) + E;
   route_topk_rank_kernel<EPL><<<nb, threads, smem, stream>>>(logits, T, E, k, renorm, ids,
-                                                                   w, rank, hist, counter);
+                                                                   w, rank, hist);
 }
 
 cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, int E, int k,
@@ -624,16 +645,17 @@ cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, i
 
   // the scan and the permutation start early (programmatic dependent
   // launch) and wait on the device for their predecessor's results
-  int32_t* totals = block_hist + route_hist_bytes(T, E) / sizeof(int32_t);
-  err = launch_pdl(route_scan_kernel, dim3((unsigned)ceil_div(E, kScanWarps)), dim3(kScanThreads),
-                   0, stream, block_hist, nb, E, totals, totals + E, counts, offsets, tile_base);
+  int32_t* block_base = block_hist + route_hist_bytes(T, E) / sizeof(int32_t);
+  err = launch_pdl(route_scan_kernel, dim3((unsigned)ceil_div(E, kScanWarps) + 1u),
+                   dim3(kScanThreads), 0, stream, (const int32_t*)block_hist, nb, E, block_base,
+                   counts, offsets, tile_base);
   if (err != cudaSuccess) return err;
 
   const int nb3 = (int)ceil_div(T, kRouteWarps);
   const bool v8 = ((uintptr_t)x & 31u) == 0 && ((uintptr_t)(quant ? (const void*)xq : (const void*)xp) & 31u) == 0;
 #define MXMOE_PERMUTE(Q, TL, V)                                                                   \
   err = launch_pdl(route_permute_kernel<Q, TL, V>, dim3(nb3), dim3(kRouteThreads), 0, stream,  \
-      x, T, H, E, k, (const int32_t*)topk_ids, (const int32_t*)block_hist,                     \
+      x, T, H, E, k, (const int32_t*)topk_ids, (const int32_t*)block_base,                     \
       (const int64_t*)offsets, (const int32_t*)(TL ? tile_base : nullptr), src_to_sorted,     \
       sorted_to_src, Q ? xq : nullptr, Q ? xs : nullptr, Q ? nullptr : xp)
   if (quant == 2) {

@@ -59,7 +59,6 @@ struct Params {
   float* topk_w;
   int32_t* local_rank;
   int32_t* block_hist;
-  int32_t* scan_counter;  // the routing scan's completion counter, zeroed here
   int* status;
   long long wait_limit;
 };
@@ -107,8 +106,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(bar_acc, 1);
     *s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    // the routing scan (next kernel) counts its finished CTAs from zero
-    if (blockIdx.x == 0 && p.scan_counter) p.scan_counter[0] = 0;
   }
   for (int i = threadIdx.x; i < 2 * MAX_E; i += THREADS) s_mask[i] = 0ull;
   if (warp == 1) {
@@ -330,8 +327,6 @@ cudaError_t launch_router_gate_topk(const uint16_t* x, const uint16_t* gate, int
   p.topk_w = topk_w;
   p.local_rank = local_rank;
   p.block_hist = block_hist;
-  p.scan_counter =
-      block_hist ? block_hist + route_hist_bytes(T, E) / sizeof(int32_t) + E : nullptr;
   p.status = device_status_ptr();
   p.wait_limit = wait_limit_cycles();
   const int grid = (int)ceil_div(T, TOK);

@@ -3,7 +3,7 @@
 moe_route_quant_mxfp8_noalloc serves callers that own their inputs and
 outputs but may not cudaMalloc a workspace (for instance a serving runtime
 that has split all device memory into its own pool).  Its scratch is a fixed
-1 MiB array inside the library, shared by every call.  These tests call it
+2 MiB array inside the library, shared by every call.  These tests call it
 through the C ABI and check that its results equal those of
 moe_route_quant_mxfp8 (which takes a caller-provided workspace), bit for bit,
 on two calls in a row with different inputs -- the second call must not see
