@@ -166,8 +166,7 @@ mxmoe_status moe_route_quant_mxfp8(const uint16_t* x, const float* logits, int T
  *     looks it up again, and the array's contents start over.
  *   - Every call shares the one array.  Each call writes every scratch entry
  *     before it reads it, so nothing has to start at zero, but calls that
- *     overlap on the GPU
- *     (other streams, other threads) race on it.
+ *     overlap on the GPU (other streams, other threads) race on it.
  */
 mxmoe_status moe_route_quant_mxfp8_noalloc(const uint16_t* x, const float* logits, int T, int H,
                                            int E, int k, int renormalize, uint8_t* xq,
