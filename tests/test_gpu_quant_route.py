@@ -147,12 +147,15 @@ def test_route_quant_skewed_load(mm, T):
                                              (70, 64, 1024, 8, True), (20001, 64, 128, 8, True),
                                              (9800, 32, 256, 6, False), (9, 4096, 256, 8, True),
                                              (17, 96, 64, 6, False), (33, 2048, 200, 8, True),
-                                             (57, 128, 160, 4, True)])
+                                             (57, 128, 160, 4, True), (40, 64, 300, 8, True),
+                                             (64, 96, 1024, 2, False)])
 def test_route_quant_edge_shapes(mm, T, H, E, k, renorm):
     """Odd E, E up to 256 at 313 routing blocks with a ragged last one (20001
     tokens) and at 154 (9800), wide E (8+ logits per lane), ties; the
     single-cluster small-batch path at 1, 7, 9, 17, 33, 57 and 64 tokens (one
-    to eight tokens per CTA, one to eight CTAs, rows of 1 to 4 chunks)."""
+    to eight tokens per CTA, one to eight CTAs, rows of 1 to 4 chunks); one
+    routing block through the three-kernel path (E above the cluster path's
+    256: the scan's row and totals CTAs over a single block)."""
     g = torch.Generator(device=DEV).manual_seed(T * 7 + E)
     x = torch.randn(T, H, generator=g, device=DEV).to(torch.bfloat16)
     logits = torch.randn(T, E, generator=g, device=DEV)
