@@ -45,7 +45,8 @@ constexpr int kRouteWarps = kRouteThreads / 32;
 template <int EPL>
 constexpr int topk_tokens_per_warp() { return 2; }
 
-template <int EPL, int TPW = topk_tokens_per_warp<EPL>()>  // logits per lane: E <= 32 * EPL
+// KC > 0: k == KC (the selection rounds unrolled)
+template <int EPL, int TPW = topk_tokens_per_warp<EPL>(), int KC = 0>  // logits per lane: E <= 32 * EPL
 __global__ void __launch_bounds__(32 * (kRouteTokensPerBlock / TPW)) route_topk_rank_kernel(
     const float* __restrict__ logits, int T, int E, int k, int renormalize,
     int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
@@ -80,7 +81,7 @@ __global__ void __launch_bounds__(32 * (kRouteTokensPerBlock / TPW)) route_topk_
     }
     int c[NT];
     float v[NT], w[NT];
-    warp_topk_softmax<EPL, NT>(rows, E, k, renormalize != 0, lane, c, v, w);
+    warp_topk_softmax<EPL, NT, KC>(rows, E, k, renormalize != 0, lane, c, v, w);
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
       chosen[g * NT + n] = c[n];
@@ -569,8 +570,12 @@ static void launch_topk(int nb, size_t smem, cudaStream_t stream, const float* l
                         int E, int k, int renorm, int32_t* ids, float* w, int32_t* rank,
                         int32_t* hist) {
   constexpr int threads = 32 * (kRouteTokensPerBlock / topk_tokens_per_warp<EPL>());
-  route_topk_rank_kernel<EPL><<<nb, threads, smem, stream>>>(logits, T, E, k, renorm, ids,
-                                                                   w, rank, hist);
+  if (k == 8)  // the common top-8: its selection rounds unrolled
+    route_topk_rank_kernel<EPL, topk_tokens_per_warp<EPL>(), 8>
+        <<<nb, threads, smem, stream>>>(logits, T, E, k, renorm, ids, w, rank, hist);
+  else
+    route_topk_rank_kernel<EPL><<<nb, threads, smem, stream>>>(logits, T, E, k, renorm, ids, w,
+                                                               rank, hist);
 }
 
 cudaError_t launch_route(const uint16_t* x, const float* logits, int T, int H, int E, int k,
