@@ -46,9 +46,10 @@ __device__ __forceinline__ float exp_of_difference(float v, float m) {
 // guarantees k == KC, and the EPL <= 4 rounds are unrolled (measured on
 // GB300 with k = 8: the 16K-token route+quant 76.3 against 77.2-78.0 us).
 template <int EPL, int NT, int KC = 0>
-__device__ __forceinline__ void warp_topk_softmax(const float* const (&rows)[NT], int E, int k,
+__device__ __forceinline__ void warp_topk_softmax(const float* const (&rows)[NT], int E, int k_rt,
                                                   bool renormalize, int lane, int (&ids)[NT],
                                                   float (&vals)[NT], float (&ws)[NT]) {
+  const int k = KC > 0 ? KC : k_rt;  // a compile-time constant when KC > 0
   float v[NT][EPL];
   uint32_t key[NT][EPL];
 #pragma unroll
@@ -87,7 +88,7 @@ __device__ __forceinline__ void warp_topk_softmax(const float* const (&rows)[NT]
         }
     }
 #pragma unroll
-    for (int j = 0; j < (KC > 0 ? KC : k); ++j) {
+    for (int j = 0; j < k; ++j) {
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
         const uint32_t hk = sk[n][0], hid = si[n][0];
