@@ -79,7 +79,8 @@ __device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t adesc, uint64_t bd
       : "memory");
 }
 
-template <int EPL>
+// KC > 0: k == KC (the top-k selection rounds unrolled)
+template <int EPL, int KC = 0>
 __global__ void __launch_bounds__(THREADS, 1)
     router_gate_topk_kernel(const __grid_constant__ CUtensorMap tmX,
                             const __grid_constant__ CUtensorMap tmG, const Params p) {
@@ -220,7 +221,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         int ids[NT];
         float vals[NT], ws[NT];
-        warp_topk_softmax<EPL, NT>(rows, E, k, p.renormalize != 0, lane, ids, vals, ws);
+        warp_topk_softmax<EPL, NT, KC>(rows, E, k, p.renormalize != 0, lane, ids, vals, ws);
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
           const int tl = ew + EPI * (g * NT + n);
@@ -284,7 +285,7 @@ static bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint
 
 }  // namespace router
 
-template <int EPL>
+template <int EPL, int KC = 0>
 static cudaError_t launch_router_epl(const CUtensorMap& tmX, const CUtensorMap& tmG,
                                      const router::Params& p, int grid, cudaStream_t stream) {
   using namespace router;
@@ -294,12 +295,12 @@ static cudaError_t launch_router_epl(const CUtensorMap& tmX, const CUtensorMap& 
   static uint64_t configured[64] = {0};  // context id the attribute was set in
   const uint64_t ctx = context_id();
   if (ctx == 0 || configured[dev] != ctx) {
-    const cudaError_t err = cudaFuncSetAttribute(router_gate_topk_kernel<EPL>,
+    const cudaError_t err = cudaFuncSetAttribute(router_gate_topk_kernel<EPL, KC>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, ALLOC);
     if (err != cudaSuccess) return err;
     configured[dev] = context_id();
   }
-  router_gate_topk_kernel<EPL><<<grid, THREADS, ALLOC, stream>>>(tmX, tmG, p);
+  router_gate_topk_kernel<EPL, KC><<<grid, THREADS, ALLOC, stream>>>(tmX, tmG, p);
   return cudaGetLastError();
 }
 
@@ -333,6 +334,7 @@ cudaError_t launch_router_gate_topk(const uint16_t* x, const uint16_t* gate, int
   const int epl = (E + 31) / 32;
   if (epl <= 1) return launch_router_epl<1>(tmX, tmG, p, grid, stream);
   if (epl <= 2) return launch_router_epl<2>(tmX, tmG, p, grid, stream);
+  if (epl <= 4 && k == 8) return launch_router_epl<4, 8>(tmX, tmG, p, grid, stream);  // top-8
   if (epl <= 4) return launch_router_epl<4>(tmX, tmG, p, grid, stream);
   return launch_router_epl<8>(tmX, tmG, p, grid, stream);
 }
